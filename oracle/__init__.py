@@ -1,0 +1,52 @@
+"""Plain, slow fp64 CPU oracle for the MLA latent-KV hot path.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline / reference arm of ``bench.py`` may import or run anything in this
+package.  The CUDA library never calls it and shares no code with it.
+
+Sources, cited by page title and section:
+
+* [MLA-KV] the page "MLA 注意力与 KV 缓存" (colibri-analysis 06):
+  §1 "压缩 KV-cache 的核心思想" (latent cache Lc + shared rotated key Rc),
+  §2 "attention 的数据流" (dims qh, kvb_dim, Tk = pos_base + S),
+  §2.1 (interleaved partial RoPE ``rope_interleave`` on the qk_rope tail),
+  §2.2 "DSA lightning indexer" (ReLU-gated head-weighted scores, causal
+  top-2048 keys, the keep-all check),
+  §2.3 "两条注意力路径：吸收 vs 非吸收" (absorbed decode via qabs and clat;
+  non-absorbed prefill via one kv_b GEMM).
+* [FDSA] the page "第 7 章 · 03 token 精确前向验证与 faithful DSA", §二 (the
+  indexer key cache Ic holds index_hd fp32 values per token).
+
+Every function takes numpy arrays, widens them to float64 and computes the
+plain definition; none of them blocks, fuses or reorders beyond what the
+definition states.  Readings of points the pages leave open are stated in
+each docstring.
+
+Parity status of each function (what pins it, see tests/test_oracle_pins.py):
+
+* rope_interleave       - complex-multiply brute force, textbook cos/sin values,
+                          pos=0 identity, relative-position invariance.
+* attend_dense          - brute-force Python loops; T=1 and uniform closed forms;
+                          hand-derived two-token example.
+* attend_absorbed       - equals attend_dense (associativity, [MLA-KV] §2.3).
+* prefill_nonabsorbed   - equals dense decode at every query position.
+* index_scores          - hand-worked integer example; brute-force loops.
+* topk_select           - brute-force full sort with the (score desc, index asc)
+                          comparator; keep-all; -0.0 == +0.0 tie case.
+* sparse_decode         - keep-all equals dense; a subset equals dense attention
+                          over the gathered rows.
+"""
+from .mla import (  # noqa: F401
+    rope_interleave,
+    split_kv_b,
+    attend_dense,
+    attend_absorbed,
+    softmax_probs,
+    decode_dense,
+    decode_absorbed,
+    prefill_nonabsorbed,
+    index_scores,
+    topk_select,
+    sparse_decode,
+    query_positions,
+)

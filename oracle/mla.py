@@ -1,0 +1,262 @@
+"""fp64 CPU oracle: definitions of every step of the MLA latent-KV hot path.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring for who may call it).
+
+Notation (the page "MLA 注意力与 KV 缓存", §2): H heads; per head a query of
+qk_head = qk_nope + qk_rope values; the cache holds per token a latent
+``Lc[t]`` of kv_lora values and a rotated key ``Rc[t]`` of qk_rope values
+shared by all heads; ``kv_b [H, qk_nope + v_head, kv_lora]`` reconstructs the
+per-head key part ``W_UK[h] = kv_b[h, :qk_nope]`` and value ``W_UV[h] =
+kv_b[h, qk_nope:]``.
+
+Readings of points the pages leave open:
+
+* kv_b packing: per head, the qk_nope key rows first, then the v_head value
+  rows (from kvb_dim = H*(qk_nope+v_head), §2).
+* RoPE: pair j of the rope part is (x[2j], x[2j+1]); it rotates by
+  pos * base^(-2j/qk_rope); the results go to y[j] and y[qk_rope/2 + j]
+  (§2.1, rope_interleave).  Rc arrives already rotated.
+* A call holds S new tokens whose cache rows are already written, so the
+  query s of sequence b sits at pos = T[b] - S + s (Tk = pos_base + S, §2) and
+  attends to keys t <= pos (causal, self included).
+* softmax scale: 1/sqrt(qk_nope + qk_rope) unless given; plain softmax, no sink.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+NEG_INF = -np.inf
+
+
+def _f64(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+# ---------------------------------------------------------------------------
+# RoPE ([MLA-KV] §2.1: only the qk_rope tail rotates; even/odd pair (a, b)
+# becomes v[j] = a*cs - b*sn, v[half+j] = b*cs + a*sn)
+# ---------------------------------------------------------------------------
+def rope_interleave(x, pos, base: float = 10000.0):
+    """Rotate the last axis of ``x`` (length qk_rope, even) to position ``pos``.
+
+    ``pos`` broadcasts against ``x[..., 0]``.  Angle of pair j:
+    pos * base ** (-2j / qk_rope).
+    """
+    x = _f64(x)
+    d = x.shape[-1]
+    assert d % 2 == 0
+    half = d // 2
+    j = np.arange(half, dtype=np.float64)
+    theta = base ** (-2.0 * j / d)
+    ang = _f64(pos)[..., None] * theta
+    cs, sn = np.cos(ang), np.sin(ang)
+    a = x[..., 0::2]
+    b = x[..., 1::2]
+    y = np.empty_like(x)
+    y[..., :half] = a * cs - b * sn
+    y[..., half:] = b * cs + a * sn
+    return y
+
+
+def split_kv_b(kv_b, qk_nope: int):
+    """kv_b [H, qk_nope+v_head, kv_lora] -> (W_UK [H,qk_nope,kv_lora], W_UV [H,v_head,kv_lora])."""
+    kv_b = _f64(kv_b)
+    return kv_b[:, :qk_nope, :], kv_b[:, qk_nope:, :]
+
+
+def softmax_probs(scores):
+    """Plain softmax over the last axis with max subtraction; -inf entries get 0."""
+    s = _f64(scores)
+    m = np.max(s, axis=-1, keepdims=True)
+    e = np.exp(s - m)
+    return e / np.sum(e, axis=-1, keepdims=True)
+
+
+def query_positions(T_b: int, S: int):
+    """Positions of the S new query tokens of a sequence whose cache holds T_b rows."""
+    return [T_b - S + s for s in range(S)]
+
+
+# ---------------------------------------------------------------------------
+# One query token against a set of cached rows (all given rows are attended)
+# ---------------------------------------------------------------------------
+def attend_dense(q, Lc_rows, Rc_rows, kv_b, qk_nope: int, pos, scale: float,
+                 rope_base: float = 10000.0):
+    """Definition: plain multi-head attention over keys/values rebuilt from the latent.
+
+    q [H, qk_nope+qk_rope] (pre-RoPE), Lc_rows [n, kv_lora], Rc_rows [n, qk_rope].
+    k[t,h] = [W_UK[h] Lc[t] ; Rc[t]], v[t,h] = W_UV[h] Lc[t] ([MLA-KV] §1: k_nope
+    and value are rebuilt from the latent through kv_b at attention time).
+    Returns out [H, v_head].
+    """
+    q = _f64(q)
+    L = _f64(Lc_rows)
+    R = _f64(Rc_rows)
+    W_UK, W_UV = split_kv_b(kv_b, qk_nope)
+    k_nope = np.einsum("hil,tl->thi", W_UK, L)          # [n, H, qk_nope]
+    v = np.einsum("hjl,tl->thj", W_UV, L)               # [n, H, v_head]
+    q_nope = q[:, :qk_nope]
+    q_rot = rope_interleave(q[:, qk_nope:], pos, rope_base)
+    scores = scale * (np.einsum("hi,thi->ht", q_nope, k_nope) + np.einsum("hr,tr->ht", q_rot, R))
+    p = softmax_probs(scores)                            # [H, n]
+    return np.einsum("ht,thj->hj", p, v)
+
+
+def attend_absorbed(q, Lc_rows, Rc_rows, kv_b, qk_nope: int, pos, scale: float,
+                    rope_base: float = 10000.0, return_probs: bool = False):
+    """Weight-absorbed attention ([MLA-KV] §2.3, absorbed path).
+
+    qabs[h] = sum_i q_nope[h,i] W_UK[h,i,:] (qt_addrow); score_t =
+    scale*(qabs . Lc[t] + q_rot . Rc[t]); clat = sum_t p_t Lc[t];
+    out[h] = W_UV[h] clat (qt_matvec_rows).
+    """
+    q = _f64(q)
+    L = _f64(Lc_rows)
+    R = _f64(Rc_rows)
+    W_UK, W_UV = split_kv_b(kv_b, qk_nope)
+    qabs = np.einsum("hi,hil->hl", q[:, :qk_nope], W_UK)      # [H, kv_lora]
+    q_rot = rope_interleave(q[:, qk_nope:], pos, rope_base)    # [H, qk_rope]
+    scores = scale * (qabs @ L.T + q_rot @ R.T)                # [H, n]
+    p = softmax_probs(scores)
+    clat = p @ L                                               # [H, kv_lora]
+    out = np.einsum("hjl,hl->hj", W_UV, clat)
+    if return_probs:
+        return out, p
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Batched decode: causal rule applied per query
+# ---------------------------------------------------------------------------
+def _decode(attend, q, Lc, Rc, T, kv_b, qk_nope, scale, rope_base, rows=None):
+    q = np.asarray(q)
+    B, S, H = q.shape[0], q.shape[1], q.shape[2]
+    v_head = np.asarray(kv_b).shape[1] - qk_nope
+    out = np.full((B, S, H, v_head), np.nan)
+    for b in range(B):
+        for s, pos in enumerate(query_positions(int(T[b]), S)):
+            if rows is not None and (b, s) not in rows:
+                continue
+            out[b, s] = attend(q[b, s], Lc[b, :pos + 1], Rc[b, :pos + 1], kv_b, qk_nope,
+                               pos, scale, rope_base)
+    return out
+
+
+def decode_dense(q, Lc, Rc, T, kv_b, qk_nope, scale, rope_base=10000.0, rows=None):
+    """Dense MHA decode for q [B,S,H,qk_head], caches [B,T_cap,.], T [B]."""
+    return _decode(attend_dense, q, Lc, Rc, T, kv_b, qk_nope, scale, rope_base, rows)
+
+
+def decode_absorbed(q, Lc, Rc, T, kv_b, qk_nope, scale, rope_base=10000.0, rows=None):
+    """Absorbed decode for q [B,S,H,qk_head]; ``rows`` optionally limits the (b, s) pairs."""
+    return _decode(attend_absorbed, q, Lc, Rc, T, kv_b, qk_nope, scale, rope_base, rows)
+
+
+# ---------------------------------------------------------------------------
+# Non-absorbed prefill ([MLA-KV] §2.3, non-absorbed path)
+# ---------------------------------------------------------------------------
+def prefill_nonabsorbed(q, Lc, Rc, kv_b, qk_nope, scale, pos_base, rope_base=10000.0,
+                        queries=None, heads=None):
+    """q [S,H,qk_head] at positions pos_base+s against Lc/Rc [Tk,.], Tk = pos_base+S.
+
+    Step 1 (one kv_b matrix product for all Tk keys): KV[t,h,:] = kv_b[h] Lc[t],
+    giving k_nope = KV[..., :qk_nope] and value = KV[..., qk_nope:].
+    Step 2 (causal attention): score = scale*(q_pass . k_nope[t] + q_rot . Rc[t]) for
+    t <= pos, softmax, sum of p * value.
+    ``queries``/``heads`` optionally restrict which outputs are computed (the
+    rest stay NaN).  Returns out [S,H,v_head].
+    """
+    q = _f64(q)
+    S, H = q.shape[0], q.shape[1]
+    kvb = _f64(kv_b)
+    Tk = pos_base + S
+    L = _f64(Lc)[:Tk]
+    R = _f64(Rc)[:Tk]
+    heads = list(range(H)) if heads is None else list(heads)
+    queries = list(range(S)) if queries is None else list(queries)
+    KV = np.einsum("hjl,tl->thj", kvb[heads], L)          # [Tk, |heads|, qk_nope+v_head]
+    k_nope = KV[..., :qk_nope]
+    value = KV[..., qk_nope:]
+    v_head = kvb.shape[1] - qk_nope
+    out = np.full((S, H, v_head), np.nan)
+    for s in queries:
+        pos = pos_base + s
+        q_pass = q[s, heads, :qk_nope]
+        q_rot = rope_interleave(q[s, heads, qk_nope:], pos, rope_base)
+        sc = scale * (np.einsum("hi,thi->ht", q_pass, k_nope[:pos + 1])
+                      + q_rot @ R[:pos + 1].T)
+        p = softmax_probs(sc)
+        out[s, heads] = np.einsum("ht,thj->hj", p, value[:pos + 1])
+    return out
+
+
+# ---------------------------------------------------------------------------
+# DSA lightning indexer and causal top-k ([MLA-KV] §2.2)
+# ---------------------------------------------------------------------------
+def index_scores(q_idx, w, Ic, T, S_positions=None):
+    """I[b,s,t] = sum_h w[b,s,h] * max(0, q_idx[b,s,h] . Ic[b,t]) for t <= pos, else -inf.
+
+    q_idx [B,S,n_ih,index_hd], w [B,S,n_ih], Ic [B,T_cap,index_hd] (fp32 per
+    token, [FDSA] §二), T [B].  No extra scale (none is printed).
+    Returns [B,S,T_cap] float64.
+    """
+    qi = _f64(q_idx)
+    ww = _f64(w)
+    B, S = qi.shape[0], qi.shape[1]
+    T_cap = np.asarray(Ic).shape[1]
+    out = np.full((B, S, T_cap), NEG_INF)
+    for b in range(B):
+        for s, pos in enumerate(query_positions(int(T[b]), S)):
+            K = _f64(np.asarray(Ic)[b, :pos + 1])                  # [n, hd]
+            dots = qi[b, s] @ K.T                                   # [n_ih, n]
+            out[b, s, :pos + 1] = ww[b, s] @ np.maximum(dots, 0.0)
+    return out
+
+
+def topk_select(scores, T, S: int, k: int):
+    """Causal top-k key selection for every (b, s).
+
+    Candidates are t in [0, pos]; with at most k of them all are kept (the
+    indexer only prunes once the context exceeds index_topk).  Otherwise keys
+    are ordered by (score descending, index ascending) -- the lower index wins
+    ties, and -0.0 equals +0.0 -- and the first k are kept.  Output indices are
+    ascending, padded with -1: sel [B,S,k] int64, nsel [B,S] int64.
+    """
+    sc = np.asarray(scores)
+    B = sc.shape[0]
+    sel = np.full((B, S, k), -1, dtype=np.int64)
+    nsel = np.zeros((B, S), dtype=np.int64)
+    for b in range(B):
+        for s, pos in enumerate(query_positions(int(T[b]), S)):
+            n = pos + 1
+            idx = np.arange(n)
+            if n <= k:
+                keep = idx
+            else:
+                vals = _f64(sc[b, s, :n])
+                order = np.lexsort((idx, -vals))   # primary: -score asc; secondary: index asc
+                keep = np.sort(order[:k])
+            sel[b, s, :len(keep)] = keep
+            nsel[b, s] = len(keep)
+    return sel, nsel
+
+
+def sparse_decode(q, Lc, Rc, T, kv_b, sel, nsel, qk_nope, scale, rope_base=10000.0, rows=None):
+    """Absorbed decode restricted to the selected keys sel[b,s,:nsel[b,s]].
+
+    The selection of a query is shared by all heads ([MLA-KV] §2.2: later layers
+    reuse ``dsa_sel``).  Selected indices must be <= pos.
+    """
+    q = np.asarray(q)
+    B, S, H = q.shape[0], q.shape[1], q.shape[2]
+    v_head = np.asarray(kv_b).shape[1] - qk_nope
+    out = np.full((B, S, H, v_head), np.nan)
+    for b in range(B):
+        for s, pos in enumerate(query_positions(int(T[b]), S)):
+            if rows is not None and (b, s) not in rows:
+                continue
+            idx = np.asarray(sel[b, s, :int(nsel[b, s])], dtype=np.int64)
+            assert idx.size > 0 and idx.max() <= pos and idx.min() >= 0
+            out[b, s] = attend_absorbed(q[b, s], np.asarray(Lc)[b, idx], np.asarray(Rc)[b, idx],
+                                        kv_b, qk_nope, pos, scale, rope_base)
+    return out
