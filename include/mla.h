@@ -1,0 +1,188 @@
+/*
+ * mla.h -- C ABI of the GB300 MLA latent-KV hot path.
+ *
+ * Operations follow two web pages, cited by title and section:
+ *   [MLA-KV] "MLA 注意力与 KV 缓存" (colibri-analysis 06)
+ *   [FDSA]   "第 7 章 · 03 token 精确前向验证与 faithful DSA"
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every tensor pointer is a DEVICE pointer owned by the caller; the library
+ *   never frees or keeps it.  Tensors are dense, row-major, innermost dimension
+ *   contiguous, with the shapes written beside each argument.
+ * - Calls only enqueue work on `stream` (a cudaStream_t; NULL = legacy default
+ *   stream) and return at once.  They never synchronise and never allocate
+ *   device memory: scratch space is the caller's `workspace` of at least
+ *   `*_workspace_size()` bytes (256-byte aligned).  Calls that share a
+ *   workspace must be ordered on one stream.
+ * - Return value: MLA_OK, or a negative mla_status.  Argument errors are found
+ *   on the host before anything is enqueued; the reason is in mla_last_error()
+ *   (thread-local).  Bad values that live in device memory (sequence lengths,
+ *   selected indices) are found by the kernels, which write NaN for the
+ *   offending rows and raise a flag read by mla_device_status().
+ * - Query positions: a call holds S new tokens per sequence whose cache rows
+ *   are already written, so query s of sequence b sits at
+ *   pos = T[b] - S + s and attends to keys t <= pos ([MLA-KV] §2: Tk = pos_base + S).
+ * - dtype MLA_F32: q, Lc, Rc, kv_b are float; every kernel computes in fp32.
+ *   dtype MLA_BF16: q, Lc, Rc, kv_b are bf16; products run on the tensor cores
+ *   with fp32 accumulation.  Outputs are always float.
+ */
+#ifndef MLA_H
+#define MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Head geometry of one attention layer ([MLA-KV] §2: qh = qk_nope + qk_rope,
+ * kvb_dim = H * (qk_nope + v_head)). */
+typedef struct mla_dims {
+  int H;           /* attention heads                                        */
+  int qk_nope;     /* non-rotary query/key width per head                    */
+  int qk_rope;     /* rotary width (even); the rotated key is shared by heads */
+  int kv_lora;     /* latent width of the cache                              */
+  int v_head;      /* value width per head                                   */
+  float scale;     /* softmax scale; <= 0 selects 1/sqrt(qk_nope + qk_rope)  */
+  float rope_base; /* RoPE base; <= 0 selects 10000                          */
+} mla_dims;
+
+enum mla_dtype { MLA_F32 = 0, MLA_BF16 = 1 };
+
+enum mla_status {
+  MLA_OK = 0,
+  MLA_ERR_INVALID = -1,     /* null pointer, bad size, misaligned pointer, short workspace */
+  MLA_ERR_UNSUPPORTED = -2, /* valid request this build does not implement (shape/dtype)   */
+  MLA_ERR_CUDA = -3,        /* a CUDA runtime call or a launch failed                       */
+  MLA_ERR_DEVICE = -4       /* a kernel flagged bad device data or a wait that ran out      */
+};
+
+/* Device status flags (bits of the word returned by mla_device_status). */
+enum mla_device_flag {
+  MLA_DEV_BAD_LENGTH = 1,   /* some T[b] outside [S, T_cap]: that sequence was skipped      */
+  MLA_DEV_BAD_INDEX = 2,    /* a selected index < 0 or > pos, or nsel outside [1, topk]     */
+  MLA_DEV_TIMEOUT = 4       /* a bounded wait inside a kernel ran out; the kernel returned  */
+};
+
+/* Message of the last failing call on this thread ("" if none). */
+const char* mla_last_error(void);
+
+/* ABI version (incremented on any signature change). */
+int mla_abi_version(void);
+
+/* Waits on `stream`, then returns in *flags (may be NULL) the OR of the
+ * mla_device_flag bits raised on the current device since the last call, and
+ * clears them.  Returns MLA_OK, MLA_ERR_DEVICE if any flag was set, or
+ * MLA_ERR_CUDA. */
+int mla_device_status(void* stream, int* flags);
+
+/* Limit of every bounded wait inside the kernels, in nanoseconds of
+ * %globaltimer (default 2e9).  Host-side setting, read at each launch. */
+void mla_set_wait_limit_ns(long long ns);
+
+/* ---------------------------------------------------------------------------
+ * Weight-absorbed decode ([MLA-KV] §2.3, absorbed path)
+ *
+ *   qabs[h]   = sum_i q_nope[h,i] * W_UK[h,i,:]              (qt_addrow)
+ *   q_rot[h]  = RoPE(q_rope[h], pos)                          ([MLA-KV] §2.1)
+ *   score[t]  = scale * (qabs[h] . Lc[t] + q_rot[h] . Rc[t]), t <= pos
+ *   clat[h]   = sum_t softmax(score)[t] * Lc[t]
+ *   out[h]    = W_UV[h] * clat[h]                              (qt_matvec_rows)
+ * with W_UK[h] = kv_b[h, 0:qk_nope, :], W_UV[h] = kv_b[h, qk_nope:, :].
+ * RoPE pairs (x[2j], x[2j+1]) rotate by pos * rope_base^(-2j/qk_rope) into
+ * (y[j], y[qk_rope/2 + j]).
+ *
+ *   q    [B, S, H, qk_nope+qk_rope]  query before RoPE
+ *   Lc   [B, T_cap, kv_lora]         latent cache (after the cache writer's RMSNorm)
+ *   Rc   [B, T_cap, qk_rope]         rotated key cache (already rotated)
+ *   T    [B] int32                   cached rows per sequence, S <= T[b] <= T_cap
+ *   kv_b [H, qk_nope+v_head, kv_lora]
+ *   out  [B, S, H, v_head] float
+ * The tensor-core path takes BF16 with H == 64, kv_lora == 512, qk_rope == 64,
+ * qk_nope % 16 == 0, v_head % 16 == 0 and 16-byte aligned pointers; every
+ * other valid request runs on the CUDA-core path.
+ * ------------------------------------------------------------------------- */
+size_t mla_decode_absorbed_workspace_size(const mla_dims* d, int dtype, int B, int S, int T_cap);
+int mla_decode_absorbed(const mla_dims* d, int dtype, int B, int S,
+                        const void* q, const void* Lc, const void* Rc, int T_cap,
+                        const int32_t* T, const void* kv_b, float* out,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* Number of kernels one mla_decode_absorbed (sparse = 0) or mla_sparse_decode
+ * (sparse = 1) call launches for this geometry and dtype (host-only query). */
+int mla_decode_launch_count(const mla_dims* d, int dtype, int sparse);
+
+/* ---------------------------------------------------------------------------
+ * Sparse decode over DSA-selected keys ([MLA-KV] §2.2: the top-k keys chosen
+ * by the indexer are reused by the attention of the shared layers)
+ *
+ * Same as mla_decode_absorbed, but query (b,s) attends only to the keys
+ * sel[b,s,0:nsel[b,s]] (one selection shared by all heads).
+ *   sel  [B, S, topk] int32, entries in [0, pos] (any order)
+ *   nsel [B, S] int32 in [1, topk]
+ * ------------------------------------------------------------------------- */
+size_t mla_sparse_decode_workspace_size(const mla_dims* d, int dtype, int B, int S, int topk);
+int mla_sparse_decode(const mla_dims* d, int dtype, int B, int S,
+                      const void* q, const void* Lc, const void* Rc, int T_cap,
+                      const int32_t* T, const void* kv_b,
+                      const int32_t* sel, const int32_t* nsel, int topk, float* out,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Non-absorbed prefill ([MLA-KV] §2.3, non-absorbed path)
+ *
+ * Step 1: one kv_b product rebuilds, for every key t < Tk = pos_base + S,
+ *         KV[b,t,h,:] = kv_b[h] * Lc[b,t]  (k_nope = first qk_nope, value = rest).
+ * Step 2: causal attention of query s (pos = pos_base + s):
+ *         score = scale * (q_pass . k_nope[t] + q_rot . Rc[t]), t <= pos,
+ *         softmax, out = sum_t p_t * value[t].
+ *   q    [B, S, H, qk_nope+qk_rope]
+ *   Lc   [B, Tk, kv_lora], Rc [B, Tk, qk_rope]
+ *   kv_b [H, qk_nope+v_head, kv_lora]
+ *   out  [B, S, H, v_head] float
+ * The rebuilt KV lives in the workspace (dtype of the inputs).
+ * ------------------------------------------------------------------------- */
+size_t mla_prefill_naive_workspace_size(const mla_dims* d, int dtype, int B, int S, int pos_base);
+int mla_prefill_naive(const mla_dims* d, int dtype, int B, int S, int pos_base,
+                      const void* q, const void* Lc, const void* Rc, const void* kv_b,
+                      float* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * DSA lightning-indexer scores ([MLA-KV] §2.2 "ReLU-gated" scores; the key
+ * cache Ic holds index_hd fp32 values per token, [FDSA] §二)
+ *
+ *   scores[b,s,t] = sum_h w[b,s,h] * max(0, q_idx[b,s,h,:] . Ic[b,t,:])   t <= pos
+ *                 = -inf                                                   pos < t < T_cap
+ *   q_idx  [B, S, n_ih, index_hd] float (after the indexer's RoPE)
+ *   w      [B, S, n_ih] float
+ *   Ic     [B, T_cap, index_hd] float
+ *   scores [B, S, T_cap] float
+ * Products and sums are fp32 (integer-valued inputs give exact scores).
+ * ------------------------------------------------------------------------- */
+int dsa_index_scores(int B, int S, int n_ih, int index_hd,
+                     const float* q_idx, const float* w, const float* Ic, int T_cap,
+                     const int32_t* T, float* scores, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Causal top-k key selection ([MLA-KV] §2.2: "top-keep" selection into
+ * dsa_sel / dsa_nsel; the indexer only prunes once the context exceeds topk)
+ *
+ * For each (b,s) with pos + 1 <= topk all keys 0..pos are kept; otherwise the
+ * topk keys with the largest scores[b,s,t], t <= pos, where the lower index
+ * wins a tie and -0.0 equals +0.0.  Scores must not be NaN.
+ *   scores [B, S, T_cap] float (entries past pos are ignored)
+ *   sel    [B, S, topk] int32: kept indices in ascending order, then -1
+ *   nsel   [B, S] int32: number kept (min(pos + 1, topk))
+ * ------------------------------------------------------------------------- */
+size_t dsa_topk_select_workspace_size(int B, int S, int T_cap, int topk);
+int dsa_topk_select(int B, int S, const float* scores, int T_cap, const int32_t* T, int topk,
+                    int32_t* sel, int32_t* nsel, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H */

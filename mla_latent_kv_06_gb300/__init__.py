@@ -1,0 +1,246 @@
+"""Thin Python binding of libmla.so (the C ABI in include/mla.h).
+
+Argument marshalling only: every step of the hot path runs in the library's
+CUDA kernels.  PyTorch provides device memory and streams.  Functions take
+CUDA tensors, check dtype/shape/contiguity, allocate outputs and workspace
+with torch when the caller gives none, and enqueue on the current stream.
+There is no CPU fallback: without the built library every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmla.so")
+
+MLA_F32, MLA_BF16 = 0, 1
+MLA_OK, MLA_ERR_INVALID, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA, MLA_ERR_DEVICE = 0, -1, -2, -3, -4
+MLA_DEV_BAD_LENGTH, MLA_DEV_BAD_INDEX, MLA_DEV_TIMEOUT = 1, 2, 4
+
+# Every symbol declared in include/mla.h.
+EXPORTS = (
+    "mla_last_error", "mla_abi_version", "mla_device_status", "mla_set_wait_limit_ns",
+    "mla_decode_absorbed_workspace_size", "mla_decode_absorbed", "mla_decode_launch_count",
+    "mla_sparse_decode_workspace_size", "mla_sparse_decode",
+    "mla_prefill_naive_workspace_size", "mla_prefill_naive",
+    "dsa_index_scores", "dsa_topk_select_workspace_size", "dsa_topk_select",
+)
+
+
+class MlaDims(ctypes.Structure):
+    _fields_ = [("H", ctypes.c_int), ("qk_nope", ctypes.c_int), ("qk_rope", ctypes.c_int),
+                ("kv_lora", ctypes.c_int), ("v_head", ctypes.c_int), ("scale", ctypes.c_float),
+                ("rope_base", ctypes.c_float)]
+
+
+class MlaError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"libmla status {code}: {msg}")
+        self.code = code
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+_DP = ctypes.POINTER(MlaDims)
+
+
+def _declare(lib: ctypes.CDLL) -> None:
+    sig = {
+        "mla_last_error": (ctypes.c_char_p, []),
+        "mla_abi_version": (_I, []),
+        "mla_device_status": (_I, [_P, ctypes.POINTER(_I)]),
+        "mla_set_wait_limit_ns": (None, [ctypes.c_longlong]),
+        "mla_decode_absorbed_workspace_size": (_SZ, [_DP, _I, _I, _I, _I]),
+        "mla_decode_launch_count": (_I, [_DP, _I, _I]),
+        "mla_decode_absorbed": (_I, [_DP, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _P, _SZ, _P]),
+        "mla_sparse_decode_workspace_size": (_SZ, [_DP, _I, _I, _I, _I]),
+        "mla_sparse_decode": (_I, [_DP, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _P, _I, _P, _P,
+                                   _SZ, _P]),
+        "mla_prefill_naive_workspace_size": (_SZ, [_DP, _I, _I, _I, _I]),
+        "mla_prefill_naive": (_I, [_DP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+        "dsa_index_scores": (_I, [_I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P]),
+        "dsa_topk_select_workspace_size": (_SZ, [_I, _I, _I, _I]),
+        "dsa_topk_select": (_I, [_I, _I, _P, _I, _P, _I, _P, _P, _P, _SZ, _P]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libmla.so (built by __graft_entry__.build()); raises if it is missing."""
+    global _lib
+    if _lib is None:
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(p)
+        _declare(lib)
+        _lib = lib
+    return _lib
+
+
+def lib() -> ctypes.CDLL:
+    return load()
+
+
+def _check(rc: int) -> None:
+    if rc != MLA_OK:
+        raise MlaError(rc, lib().mla_last_error().decode(errors="replace"))
+
+
+def make_dims(dims) -> MlaDims:
+    """Accepts workload.Dims or any object with the same fields."""
+    scale = getattr(dims, "scale", None)
+    return MlaDims(dims.H, dims.qk_nope, dims.qk_rope, dims.kv_lora, dims.v_head,
+                   float(scale) if scale else 0.0, float(getattr(dims, "rope_base", 10000.0)))
+
+
+# ------------------------------------------------------------------ helpers
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return MLA_F32
+    if t.dtype == torch.bfloat16:
+        return MLA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors must live on the GPU")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _workspace(nbytes: int, device, ws):
+    torch = _torch()
+    if nbytes == 0:
+        return ws, 0
+    if ws is None or ws.numel() * ws.element_size() < nbytes:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return ws, ws.numel() * ws.element_size()
+
+
+def device_status(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device flag word."""
+    flags = _I(0)
+    rc = lib().mla_device_status(_stream(stream), ctypes.byref(flags))
+    if rc not in (MLA_OK, MLA_ERR_DEVICE):
+        _check(rc)
+    return flags.value
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    lib().mla_set_wait_limit_ns(int(ns))
+
+
+# ------------------------------------------------------------------ ops
+def kernels_per_call(kind: str, dims, dtype: int = MLA_BF16) -> int:
+    """Kernels one decode ("decode") or sparse-decode ("sparse") call launches."""
+    d = make_dims(dims)
+    return lib().mla_decode_launch_count(ctypes.byref(d), dtype, 1 if kind == "sparse" else 0)
+
+
+def decode_workspace_size(dims, dtype: int, B: int, S: int, T_cap: int) -> int:
+    d = make_dims(dims)
+    return lib().mla_decode_absorbed_workspace_size(ctypes.byref(d), dtype, B, S, T_cap)
+
+
+def decode_absorbed(q, Lc, Rc, T, kv_b, dims, out=None, workspace=None, stream=None):
+    """Weight-absorbed decode; q [B,S,H,qk], Lc [B,T_cap,kv_lora], Rc [B,T_cap,qk_rope]."""
+    torch = _torch()
+    B, S, H = q.shape[0], q.shape[1], q.shape[2]
+    T_cap = Lc.shape[1]
+    code = _dtype_code(q)
+    if out is None:
+        out = torch.empty(B, S, H, dims.v_head, dtype=torch.float32, device=q.device)
+    d = make_dims(dims)
+    need = lib().mla_decode_absorbed_workspace_size(ctypes.byref(d), code, B, S, T_cap)
+    workspace, wsb = _workspace(need, q.device, workspace)
+    _check(lib().mla_decode_absorbed(ctypes.byref(d), code, B, S, _ptr(q), _ptr(Lc), _ptr(Rc), T_cap,
+                                     _ptr(T), _ptr(kv_b), _ptr(out), _ptr(workspace), wsb,
+                                     _stream(stream)))
+    return out
+
+
+def sparse_decode(q, Lc, Rc, T, kv_b, sel, nsel, dims, out=None, workspace=None, stream=None):
+    """Absorbed decode over the keys sel[b,s,:nsel[b,s]] (sel [B,S,topk] int32)."""
+    torch = _torch()
+    B, S, H = q.shape[0], q.shape[1], q.shape[2]
+    T_cap = Lc.shape[1]
+    topk = sel.shape[2]
+    code = _dtype_code(q)
+    if out is None:
+        out = torch.empty(B, S, H, dims.v_head, dtype=torch.float32, device=q.device)
+    d = make_dims(dims)
+    need = lib().mla_sparse_decode_workspace_size(ctypes.byref(d), code, B, S, topk)
+    workspace, wsb = _workspace(need, q.device, workspace)
+    _check(lib().mla_sparse_decode(ctypes.byref(d), code, B, S, _ptr(q), _ptr(Lc), _ptr(Rc), T_cap,
+                                   _ptr(T), _ptr(kv_b), _ptr(sel), _ptr(nsel), topk, _ptr(out),
+                                   _ptr(workspace), wsb, _stream(stream)))
+    return out
+
+
+def prefill_naive(q, Lc, Rc, kv_b, dims, pos_base: int, out=None, workspace=None, stream=None):
+    """Non-absorbed prefill of S new tokens at pos_base; Lc/Rc hold Tk = pos_base + S rows."""
+    torch = _torch()
+    B, S, H = q.shape[0], q.shape[1], q.shape[2]
+    code = _dtype_code(q)
+    if out is None:
+        out = torch.empty(B, S, H, dims.v_head, dtype=torch.float32, device=q.device)
+    d = make_dims(dims)
+    need = lib().mla_prefill_naive_workspace_size(ctypes.byref(d), code, B, S, pos_base)
+    workspace, wsb = _workspace(need, q.device, workspace)
+    _check(lib().mla_prefill_naive(ctypes.byref(d), code, B, S, pos_base, _ptr(q), _ptr(Lc), _ptr(Rc),
+                                   _ptr(kv_b), _ptr(out), _ptr(workspace), wsb, _stream(stream)))
+    return out
+
+
+def index_scores(q_idx, w, Ic, T, out=None, stream=None):
+    """DSA indexer scores [B,S,T_cap] (fp32; -inf past each query's position)."""
+    torch = _torch()
+    B, S, n_ih, hd = q_idx.shape
+    T_cap = Ic.shape[1]
+    if out is None:
+        out = torch.empty(B, S, T_cap, dtype=torch.float32, device=q_idx.device)
+    _check(lib().dsa_index_scores(B, S, n_ih, hd, _ptr(q_idx), _ptr(w), _ptr(Ic), T_cap, _ptr(T),
+                                  _ptr(out), _stream(stream)))
+    return out
+
+
+def topk_select(scores, T, topk: int, S: Optional[int] = None, sel=None, nsel=None,
+                workspace=None, stream=None) -> Tuple[object, object]:
+    """Causal top-k selection: (sel [B,S,topk] ascending then -1, nsel [B,S])."""
+    torch = _torch()
+    B, S_, T_cap = scores.shape
+    S = S_ if S is None else S
+    if sel is None:
+        sel = torch.empty(B, S, topk, dtype=torch.int32, device=scores.device)
+    if nsel is None:
+        nsel = torch.empty(B, S, dtype=torch.int32, device=scores.device)
+    need = lib().dsa_topk_select_workspace_size(B, S, T_cap, topk)
+    workspace, wsb = _workspace(need, scores.device, workspace)
+    _check(lib().dsa_topk_select(B, S, _ptr(scores), T_cap, _ptr(T), topk, _ptr(sel), _ptr(nsel),
+                                 _ptr(workspace), wsb, _stream(stream)))
+    return sel, nsel

@@ -1,0 +1,295 @@
+// api.cu -- the C ABI declared in include/mla.h: argument checks, workspace
+// sizing, choice of kernel path, and the device status word.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+#include "decode_tc.h"
+#include "internal.h"
+
+#define MLA_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+thread_local std::string g_err;
+std::atomic<long long> g_wait_limit_ns{2000000000LL};
+
+// Flags raised by kernels on this device (see mla_device_flag).
+__device__ unsigned int g_dev_flags;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int* g_flag_ptr[kMaxDevices] = {};
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+  return fail(MLA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+// Device address of g_dev_flags for the current device (looked up once).
+unsigned int* flags_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_flag_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dev_flags) != cudaSuccess) return nullptr;
+    g_flag_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  return g_flag_ptr[dev];
+}
+
+bool resolve(const mla_dims* d, mla::Geometry* g) {
+  if (!d) return false;
+  if (d->H < 1 || d->qk_nope < 0 || d->qk_rope < 0 || d->kv_lora < 1 || d->v_head < 1) return false;
+  if (d->qk_rope % 2 != 0 || d->qk_nope + d->qk_rope < 1) return false;
+  g->H = d->H;
+  g->Dn = d->qk_nope;
+  g->Dr = d->qk_rope;
+  g->Dl = d->kv_lora;
+  g->Dv = d->v_head;
+  g->scale = d->scale > 0.f ? d->scale : (float)(1.0 / std::sqrt((double)(d->qk_nope + d->qk_rope)));
+  g->rope_base = d->rope_base > 0.f ? (double)d->rope_base : 10000.0;
+  return true;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_common(const mla_dims* d, int dtype, int B, int S, mla::Geometry* g) {
+  if (!resolve(d, g)) return fail(MLA_ERR_INVALID, "invalid mla_dims (null, non-positive size or odd qk_rope)");
+  if (dtype != MLA_F32 && dtype != MLA_BF16) return fail(MLA_ERR_INVALID, "unknown dtype %d", dtype);
+  if (B < 1 || S < 1) return fail(MLA_ERR_INVALID, "B=%d and S=%d must be >= 1", B, S);
+  return MLA_OK;
+}
+
+// The tensor-core decode covers the GLM-5.2 head geometry with bf16 inputs.
+bool tc_decode_ok(const mla::Geometry& g, int dtype, const void* q, const void* Lc, const void* Rc,
+                  const void* kv_b) {
+  return dtype == MLA_BF16 && mla::tc_decode_geometry_ok(g) && aligned16(q) && aligned16(Lc) &&
+         aligned16(Rc) && aligned16(kv_b);
+}
+
+}  // namespace
+
+MLA_EXPORT const char* mla_last_error(void) { return g_err.c_str(); }
+
+MLA_EXPORT int mla_abi_version(void) { return 1; }
+
+MLA_EXPORT void mla_set_wait_limit_ns(long long ns) { g_wait_limit_ns.store(ns > 0 ? ns : 1); }
+
+MLA_EXPORT int mla_device_status(void* stream, int* flags) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mla_device_status: stream synchronize");
+  unsigned int v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_dev_flags, sizeof(v));
+  if (e != cudaSuccess) return cuda_fail(e, "mla_device_status: read flags");
+  const unsigned int zero = 0;
+  e = cudaMemcpyToSymbol(g_dev_flags, &zero, sizeof(zero));
+  if (e != cudaSuccess) return cuda_fail(e, "mla_device_status: clear flags");
+  if (flags) *flags = (int)v;
+  if (v) return fail(MLA_ERR_DEVICE, "device flags 0x%x raised", v);
+  return MLA_OK;
+}
+
+// ---------------------------------------------------------------- decode
+MLA_EXPORT size_t mla_decode_absorbed_workspace_size(const mla_dims* d, int dtype, int B, int S,
+                                                      int T_cap) {
+  mla::Geometry g;
+  if (!resolve(d, &g) || B < 1 || S < 1 || T_cap < S) return 0;
+  if (dtype == MLA_BF16 && mla::tc_decode_geometry_ok(g))
+    return round256(mla::tc_decode_workspace_bytes(g, B, S, T_cap, /*sparse_topk=*/0));
+  return 0;
+}
+
+MLA_EXPORT int mla_decode_absorbed(const mla_dims* d, int dtype, int B, int S, const void* q,
+                                   const void* Lc, const void* Rc, int T_cap, const int32_t* T,
+                                   const void* kv_b, float* out, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  mla::Geometry g;
+  int rc = check_common(d, dtype, B, S, &g);
+  if (rc) return rc;
+  if (T_cap < S) return fail(MLA_ERR_INVALID, "T_cap=%d < S=%d", T_cap, S);
+  if (!q || !Lc || !Rc || !T || !kv_b || !out) return fail(MLA_ERR_INVALID, "null tensor pointer");
+  mla::DecodeArgs a{};
+  a.g = g;
+  a.B = B;
+  a.S = S;
+  a.T_cap = T_cap;
+  a.q = q;
+  a.Lc = Lc;
+  a.Rc = Rc;
+  a.T = T;
+  a.kv_b = kv_b;
+  a.out = out;
+  a.flags = flags_ptr();
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  if (!a.flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (tc_decode_ok(g, dtype, q, Lc, Rc, kv_b)) {
+    size_t need = mla::tc_decode_workspace_bytes(g, B, S, T_cap, 0);
+    if (need && (!workspace || workspace_bytes < need))
+      return fail(MLA_ERR_INVALID, "workspace of %zu bytes < %zu required", workspace_bytes, need);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+      return fail(MLA_ERR_INVALID, "workspace must be 256-byte aligned");
+    e = mla::launch_decode_tc(a, workspace, workspace_bytes, st);
+  } else {
+    e = mla::launch_decode_simt(a, dtype, /*sparse=*/false, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "mla_decode_absorbed launch");
+  return MLA_OK;
+}
+
+MLA_EXPORT int mla_decode_launch_count(const mla_dims* d, int dtype, int sparse) {
+  mla::Geometry g;
+  if (!resolve(d, &g)) return 0;
+  if (dtype == MLA_BF16 && mla::tc_decode_geometry_ok(g)) return mla::tc_decode_launch_count(sparse != 0);
+  return 1;
+}
+
+// ---------------------------------------------------------------- sparse decode
+MLA_EXPORT size_t mla_sparse_decode_workspace_size(const mla_dims* d, int dtype, int B, int S,
+                                                    int topk) {
+  mla::Geometry g;
+  if (!resolve(d, &g) || B < 1 || S < 1 || topk < 1) return 0;
+  if (dtype == MLA_BF16 && mla::tc_decode_geometry_ok(g))
+    return round256(mla::tc_decode_workspace_bytes(g, B, S, topk, topk));
+  return 0;
+}
+
+MLA_EXPORT int mla_sparse_decode(const mla_dims* d, int dtype, int B, int S, const void* q,
+                                 const void* Lc, const void* Rc, int T_cap, const int32_t* T,
+                                 const void* kv_b, const int32_t* sel, const int32_t* nsel, int topk,
+                                 float* out, void* workspace, size_t workspace_bytes, void* stream) {
+  mla::Geometry g;
+  int rc = check_common(d, dtype, B, S, &g);
+  if (rc) return rc;
+  if (T_cap < S) return fail(MLA_ERR_INVALID, "T_cap=%d < S=%d", T_cap, S);
+  if (topk < 1) return fail(MLA_ERR_INVALID, "topk=%d must be >= 1", topk);
+  if (!q || !Lc || !Rc || !T || !kv_b || !out || !sel || !nsel)
+    return fail(MLA_ERR_INVALID, "null tensor pointer");
+  mla::DecodeArgs a{};
+  a.g = g;
+  a.B = B;
+  a.S = S;
+  a.T_cap = T_cap;
+  a.q = q;
+  a.Lc = Lc;
+  a.Rc = Rc;
+  a.T = T;
+  a.kv_b = kv_b;
+  a.out = out;
+  a.sel = sel;
+  a.nsel = nsel;
+  a.topk = topk;
+  a.flags = flags_ptr();
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  if (!a.flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (tc_decode_ok(g, dtype, q, Lc, Rc, kv_b)) {
+    size_t need = mla::tc_decode_workspace_bytes(g, B, S, topk, topk);
+    if (need && (!workspace || workspace_bytes < need))
+      return fail(MLA_ERR_INVALID, "workspace of %zu bytes < %zu required", workspace_bytes, need);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+      return fail(MLA_ERR_INVALID, "workspace must be 256-byte aligned");
+    e = mla::launch_sparse_decode_tc(a, workspace, workspace_bytes, st);
+  } else {
+    e = mla::launch_decode_simt(a, dtype, /*sparse=*/true, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "mla_sparse_decode launch");
+  return MLA_OK;
+}
+
+// ---------------------------------------------------------------- prefill
+MLA_EXPORT size_t mla_prefill_naive_workspace_size(const mla_dims* d, int dtype, int B, int S,
+                                                    int pos_base) {
+  mla::Geometry g;
+  if (!resolve(d, &g) || B < 1 || S < 1 || pos_base < 0) return 0;
+  size_t el = dtype == MLA_F32 ? 4 : 2;
+  size_t Tk = (size_t)pos_base + S;
+  return round256((size_t)B * Tk * g.H * (g.Dn + g.Dv) * el);
+}
+
+MLA_EXPORT int mla_prefill_naive(const mla_dims* d, int dtype, int B, int S, int pos_base,
+                                 const void* q, const void* Lc, const void* Rc, const void* kv_b,
+                                 float* out, void* workspace, size_t workspace_bytes, void* stream) {
+  mla::Geometry g;
+  int rc = check_common(d, dtype, B, S, &g);
+  if (rc) return rc;
+  if (pos_base < 0) return fail(MLA_ERR_INVALID, "pos_base=%d must be >= 0", pos_base);
+  if (!q || !Lc || !Rc || !kv_b || !out) return fail(MLA_ERR_INVALID, "null tensor pointer");
+  size_t need = mla_prefill_naive_workspace_size(d, dtype, B, S, pos_base);
+  if (!workspace || workspace_bytes < need)
+    return fail(MLA_ERR_INVALID, "workspace of %zu bytes < %zu required", workspace_bytes, need);
+  mla::PrefillArgs a{};
+  a.g = g;
+  a.B = B;
+  a.S = S;
+  a.pos_base = pos_base;
+  a.q = q;
+  a.Lc = Lc;
+  a.Rc = Rc;
+  a.kv_b = kv_b;
+  a.kv = workspace;
+  a.out = out;
+  cudaError_t e = mla::launch_prefill_simt(a, dtype, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mla_prefill_naive launch");
+  return MLA_OK;
+}
+
+// ---------------------------------------------------------------- DSA
+MLA_EXPORT int dsa_index_scores(int B, int S, int n_ih, int index_hd, const float* q_idx,
+                                const float* w, const float* Ic, int T_cap, const int32_t* T,
+                                float* scores, void* stream) {
+  if (B < 1 || S < 1 || n_ih < 1 || index_hd < 1 || T_cap < S)
+    return fail(MLA_ERR_INVALID, "bad sizes B=%d S=%d n_ih=%d index_hd=%d T_cap=%d", B, S, n_ih,
+                index_hd, T_cap);
+  if (!q_idx || !w || !Ic || !T || !scores) return fail(MLA_ERR_INVALID, "null tensor pointer");
+  size_t smem = sizeof(float) * ((size_t)n_ih * index_hd + n_ih + 128 * (size_t)(index_hd + 1) + 256);
+  if (smem > 220 * 1024)
+    return fail(MLA_ERR_UNSUPPORTED, "n_ih*index_hd too large for one CTA (%zu bytes)", smem);
+  mla::IndexArgs a{B, S, n_ih, index_hd, T_cap, q_idx, w, Ic, T, scores, flags_ptr()};
+  if (!a.flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
+  cudaError_t e = mla::launch_index_scores(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_index_scores launch");
+  return MLA_OK;
+}
+
+MLA_EXPORT size_t dsa_topk_select_workspace_size(int B, int S, int T_cap, int topk) {
+  (void)B;
+  (void)S;
+  (void)T_cap;
+  (void)topk;
+  return 0;
+}
+
+MLA_EXPORT int dsa_topk_select(int B, int S, const float* scores, int T_cap, const int32_t* T,
+                               int topk, int32_t* sel, int32_t* nsel, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (B < 1 || S < 1 || T_cap < S || topk < 1)
+    return fail(MLA_ERR_INVALID, "bad sizes B=%d S=%d T_cap=%d topk=%d", B, S, T_cap, topk);
+  if (!scores || !T || !sel || !nsel) return fail(MLA_ERR_INVALID, "null tensor pointer");
+  mla::TopkArgs a{B, S, T_cap, topk, scores, T, sel, nsel, flags_ptr()};
+  if (!a.flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
+  cudaError_t e = mla::launch_topk_select(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_topk_select launch");
+  return MLA_OK;
+}

@@ -1,0 +1,60 @@
+// common.cuh -- small device helpers shared by the library's kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+// Raise a device status flag (see mla_device_flag in mla.h).
+__device__ __forceinline__ void raise_flag(unsigned int* flags, unsigned int bit) {
+  if (flags) atomicOr(flags, bit);
+}
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Rotary angle pos * base^(-2j/d) and its cos/sin, taken in double: a float
+// product pos*theta loses ~1e-3 rad at pos ~ 6.5e4, far above fp32 tolerance.
+__device__ __forceinline__ void rope_cos_sin(int pos, int j, int d, double base, float* c,
+                                             float* s) {
+  double theta = pow(base, -2.0 * (double)j / (double)d);
+  double sn, cs;
+  sincos((double)pos * theta, &sn, &cs);
+  *c = (float)cs;
+  *s = (float)sn;
+}
+
+// %globaltimer in nanoseconds.
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Float -> uint32 key whose unsigned order equals the float order; -0.0 is
+// first turned into +0.0 so that the two compare equal.
+__device__ __forceinline__ uint32_t ordered_key(float x) {
+  x = x + 0.0f;
+  uint32_t u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float qnan() { return __int_as_float(0x7fc00000); }
+
+}  // namespace mla

@@ -1,0 +1,72 @@
+// internal.h -- launchers shared between the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+struct Geometry {
+  int H, Dn, Dr, Dl, Dv;  // heads, qk_nope, qk_rope, kv_lora, v_head
+  float scale;            // resolved softmax scale
+  double rope_base;       // resolved RoPE base
+};
+
+// Arguments common to the decode kernels (dense and sparse).
+struct DecodeArgs {
+  Geometry g;
+  int B, S, T_cap;
+  const void* q;
+  const void* Lc;
+  const void* Rc;
+  const int32_t* T;
+  const void* kv_b;
+  float* out;
+  const int32_t* sel;   // sparse only: [B,S,topk]
+  const int32_t* nsel;  // sparse only: [B,S]
+  int topk;
+  unsigned int* flags;
+  long long wait_limit_ns;
+};
+
+cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, bool sparse, cudaStream_t st);
+
+struct PrefillArgs {
+  Geometry g;
+  int B, S, pos_base;
+  const void* q;
+  const void* Lc;
+  const void* Rc;
+  const void* kv_b;
+  void* kv;  // rebuilt [B, Tk, H, Dn+Dv], input dtype
+  float* out;
+};
+
+cudaError_t launch_prefill_simt(const PrefillArgs& a, int dtype, cudaStream_t st);
+
+struct IndexArgs {
+  int B, S, n_ih, hd, T_cap;
+  const float* q_idx;
+  const float* w;
+  const float* Ic;
+  const int32_t* T;
+  float* scores;
+  unsigned int* flags;
+};
+
+cudaError_t launch_index_scores(const IndexArgs& a, cudaStream_t st);
+
+struct TopkArgs {
+  int B, S, T_cap, topk;
+  const float* scores;
+  const int32_t* T;
+  int32_t* sel;
+  int32_t* nsel;
+  unsigned int* flags;
+};
+
+cudaError_t launch_topk_select(const TopkArgs& a, cudaStream_t st);
+
+}  // namespace mla

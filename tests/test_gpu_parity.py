@@ -1,0 +1,209 @@
+"""GPU parity of every C ABI entry point against the fp64 oracle.
+
+Tolerances (normwise max relative error, max|gpu - oracle| / max|oracle|):
+fp32 inputs 1e-5, bf16 inputs 2e-2.  DSA scores and the selected index sets
+are compared bit for bit.  Inputs come from workload/ (NaN past each
+sequence's end, so a read out of range shows up as a NaN output).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests._np import max_rel_err, to_np
+from workload import GLM, TINY, WORKLOADS, dsa_inputs, mla_inputs, workload_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-5, "bf16": 2e-2}
+DEV = "cuda:0"
+
+
+def _dev(x):
+    return {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+
+
+def _np_inputs(x):
+    return {k: to_np(x[k]) for k in ("q", "Lc", "Rc", "kv_b")}
+
+
+# --------------------------------------------------------------- absorbed decode
+def test_tiny_workload_decode(cuda_lib):
+    x = workload_inputs("tiny", "cpu")
+    g = _dev(x)
+    out = cuda_lib.decode_absorbed(g["q"], g["Lc"], g["Rc"], g["T"], g["kv_b"], TINY)
+    n = _np_inputs(x)
+    ref = oracle.decode_dense(n["q"], n["Lc"], n["Rc"], x["T_list"], n["kv_b"], TINY.qk_nope,
+                              TINY.softmax_scale)
+    assert max_rel_err(to_np(out), ref) < TOL["f32"]
+
+
+@pytest.mark.parametrize("dtype,dims", [("f32", TINY), ("bf16", GLM), ("f32", GLM)])
+@pytest.mark.parametrize("T,S", [([1], 1), ([6], 6), ([129, 300, 64], 1), ([130, 257, 6], 6),
+                                 ([1000], 2)])
+def test_decode_ragged(cuda_lib, dtype, dims, T, S):
+    T_cap = max(T) + 37
+    x = mla_inputs(dims, len(T), S, T, T_cap, dtype, 100 + sum(T) + S, "cpu")
+    g = _dev(x)
+    out = cuda_lib.decode_absorbed(g["q"], g["Lc"], g["Rc"], g["T"], g["kv_b"], dims)
+    n = _np_inputs(x)
+    ref = oracle.decode_absorbed(n["q"], n["Lc"], n["Rc"], T, n["kv_b"], dims.qk_nope, dims.softmax_scale)
+    got = to_np(out)
+    assert np.all(np.isfinite(got))
+    assert max_rel_err(got, ref) < TOL[dtype]
+    assert cuda_lib.device_status() == 0
+
+
+def test_decode_glm_t4096_full(cuda_lib):
+    """The GLM-5.2 single-sequence workload at full size (B=1, S=1, T=4096), every output."""
+    x = workload_inputs("glm_decode_t4096", DEV)
+    out = cuda_lib.decode_absorbed(x["q"], x["Lc"], x["Rc"], x["T"], x["kv_b"], GLM)
+    n = _np_inputs(x)
+    ref = oracle.decode_absorbed(n["q"], n["Lc"], n["Rc"], x["T_list"], n["kv_b"], GLM.qk_nope,
+                                 GLM.softmax_scale)
+    assert max_rel_err(to_np(out), ref) < TOL["bf16"]
+
+
+@pytest.mark.parametrize("S", [1, 6])
+def test_decode_batched_b32_sampled(cuda_lib, S):
+    """B=32, T_b ~ U{1024..32768}: all outputs computed, sampled (b, s) rows checked."""
+    x = workload_inputs("glm_batched_b32", DEV, S=S)
+    out = to_np(cuda_lib.decode_absorbed(x["q"], x["Lc"], x["Rc"], x["T"], x["kv_b"], GLM))
+    assert np.all(np.isfinite(out))
+    T = x["T_list"]
+    rows = [(0, 0), (7, S - 1), (int(np.argmax(T)), S - 1), (int(np.argmin(T)), 0), (31, S // 2)]
+    kvb = to_np(x["kv_b"])
+    for b, s in rows:
+        Tb = T[b]
+        pos = Tb - S + s
+        q = to_np(x["q"][b, s])
+        L = to_np(x["Lc"][b, :pos + 1])
+        R = to_np(x["Rc"][b, :pos + 1])
+        ref = oracle.attend_absorbed(q, L, R, kvb, GLM.qk_nope, pos, GLM.softmax_scale)
+        assert max_rel_err(out[b, s], ref) < TOL["bf16"], (b, s)
+
+
+def test_decode_flags_bad_length(cuda_lib):
+    T = [40, 10]
+    x = mla_inputs(GLM, 2, 1, T, 40, "bf16", 5, "cpu")
+    g = _dev(x)
+    g["T"] = torch.tensor([40, 41], dtype=torch.int32, device=DEV)  # 41 > T_cap
+    out = cuda_lib.decode_absorbed(g["q"], g["Lc"], g["Rc"], g["T"], g["kv_b"], GLM)
+    flags = cuda_lib.device_status()
+    assert flags & cuda_lib.MLA_DEV_BAD_LENGTH
+    got = to_np(out)
+    assert np.all(np.isnan(got[1])) and np.all(np.isfinite(got[0]))
+    assert cuda_lib.device_status() == 0  # cleared by the previous read
+
+
+# --------------------------------------------------------------- DSA
+@pytest.mark.parametrize("T,S,nh,hd,k", [([64], 1, 2, 8, 16), ([300, 17, 1000], 2, 4, 32, 64),
+                                         ([2048, 2049, 5000], 1, 32, 128, 2048)])
+def test_index_and_topk_bit_exact(cuda_lib, T, S, nh, hd, k):
+    T_cap = max(T) + 5
+    d = dsa_inputs(len(T), S, T, T_cap, nh, hd, 40 + sum(T), "cpu")
+    g = _dev(d)
+    Tt = torch.tensor(T, dtype=torch.int32, device=DEV)
+    sc = cuda_lib.index_scores(g["q_idx"], g["w"], g["Ic"], Tt)
+    ref = oracle.index_scores(to_np(d["q_idx"]), to_np(d["w"]), to_np(d["Ic"]), T)
+    got = to_np(sc)
+    assert np.array_equal(got, ref)
+    sel, nsel = cuda_lib.topk_select(sc, Tt, k)
+    rsel, rn = oracle.topk_select(ref, T, S, k)
+    assert np.array_equal(nsel.cpu().numpy(), rn)
+    assert np.array_equal(sel.cpu().numpy(), rsel)
+
+
+def test_topk_ties_and_negative_zero(cuda_lib):
+    """Many equal scores, +0.0 and -0.0 mixed: the lower index wins."""
+    r = np.random.default_rng(3)
+    B, S, T_cap, k = 2, 1, 5000, 700
+    sc = r.integers(-2, 3, (B, S, T_cap)).astype(np.float32)
+    sc[sc == 0] = np.where(r.random(np.sum(sc == 0)) < 0.5, -0.0, 0.0).astype(np.float32)
+    T = [5000, 3001]
+    g = torch.from_numpy(sc).to(DEV)
+    sel, nsel = cuda_lib.topk_select(g, torch.tensor(T, dtype=torch.int32, device=DEV), k)
+    rsel, rn = oracle.topk_select(sc.astype(np.float64), T, S, k)
+    assert np.array_equal(sel.cpu().numpy(), rsel) and np.array_equal(nsel.cpu().numpy(), rn)
+
+
+def test_dsa_glm_t65536_pipeline(cuda_lib):
+    """B=4, T=65536: indexer and top-2048 bit-exact, sparse decode within 2e-2 on every output."""
+    x = workload_inputs("glm_dsa_t65536", DEV)
+    sc = cuda_lib.index_scores(x["q_idx"], x["w"], x["Ic"], x["T"])
+    T = x["T_list"]
+    ref_sc = oracle.index_scores(to_np(x["q_idx"]), to_np(x["w"]), to_np(x["Ic"]), T)
+    assert np.array_equal(to_np(sc), ref_sc)
+    sel, nsel = cuda_lib.topk_select(sc, x["T"], x["topk"])
+    rsel, rn = oracle.topk_select(ref_sc, T, 1, x["topk"])
+    assert np.array_equal(sel.cpu().numpy(), rsel) and np.array_equal(nsel.cpu().numpy(), rn)
+    out = to_np(cuda_lib.sparse_decode(x["q"], x["Lc"], x["Rc"], x["T"], x["kv_b"], sel, nsel, GLM))
+    kvb = to_np(x["kv_b"])
+    for b in range(4):
+        idx = rsel[b, 0]
+        pos = T[b] - 1
+        ref = oracle.attend_absorbed(to_np(x["q"][b, 0]), to_np(x["Lc"][b, idx]), to_np(x["Rc"][b, idx]),
+                                     kvb, GLM.qk_nope, pos, GLM.softmax_scale)
+        assert max_rel_err(out[b, 0], ref) < TOL["bf16"], b
+
+
+@pytest.mark.parametrize("dtype,dims", [("f32", TINY), ("bf16", GLM)])
+def test_sparse_decode_keep_all_and_subset(cuda_lib, dtype, dims):
+    T = [50, 300]
+    S, k = 2, 256
+    x = mla_inputs(dims, 2, S, T, 320, dtype, 77, "cpu")
+    g = _dev(x)
+    n = _np_inputs(x)
+    r = np.random.default_rng(5)
+    sel = np.full((2, S, k), -1, dtype=np.int32)
+    nsel = np.zeros((2, S), dtype=np.int32)
+    for b in range(2):
+        for s in range(S):
+            pos = T[b] - S + s
+            cnt = min(pos + 1, k)
+            sel[b, s, :cnt] = np.sort(r.choice(pos + 1, cnt, replace=False))
+            nsel[b, s] = cnt
+    out = cuda_lib.sparse_decode(g["q"], g["Lc"], g["Rc"], g["T"], g["kv_b"],
+                                 torch.from_numpy(sel).to(DEV), torch.from_numpy(nsel).to(DEV), dims)
+    ref = oracle.sparse_decode(n["q"], n["Lc"], n["Rc"], T, n["kv_b"], sel, nsel, dims.qk_nope,
+                               dims.softmax_scale)
+    assert max_rel_err(to_np(out), ref) < TOL[dtype]
+    # keep-all selection reproduces dense decode
+    dense = oracle.decode_absorbed(n["q"], n["Lc"], n["Rc"], [50, 300], n["kv_b"], dims.qk_nope,
+                                   dims.softmax_scale)
+    assert max_rel_err(ref[0], dense[0]) < 1e-12
+
+
+def test_sparse_decode_flags_future_index(cuda_lib):
+    T = [100]
+    x = mla_inputs(GLM, 1, 1, T, 100, "bf16", 8, "cpu")
+    g = _dev(x)
+    sel = torch.tensor([[[0, 5, 100, -1]]], dtype=torch.int32, device=DEV)  # 100 > pos=99
+    nsel = torch.tensor([[3]], dtype=torch.int32, device=DEV)
+    out = cuda_lib.sparse_decode(g["q"], g["Lc"], g["Rc"], g["T"], g["kv_b"], sel, nsel, GLM)
+    assert cuda_lib.device_status() & cuda_lib.MLA_DEV_BAD_INDEX
+    assert np.all(np.isnan(to_np(out)))
+
+
+# --------------------------------------------------------------- prefill
+@pytest.mark.parametrize("dtype,dims,S,pos_base", [("f32", TINY, 6, 10), ("f32", TINY, 16, 0),
+                                                   ("bf16", GLM, 16, 200), ("bf16", GLM, 130, 77)])
+def test_prefill_naive(cuda_lib, dtype, dims, S, pos_base):
+    Tk = pos_base + S
+    x = mla_inputs(dims, 1, S, [Tk], Tk, dtype, 60 + S, "cpu")
+    g = _dev(x)
+    out = cuda_lib.prefill_naive(g["q"], g["Lc"], g["Rc"], g["kv_b"], dims, pos_base)
+    n = _np_inputs(x)
+    ref = oracle.prefill_nonabsorbed(n["q"][0], n["Lc"][0], n["Rc"][0], n["kv_b"], dims.qk_nope,
+                                     dims.softmax_scale, pos_base)
+    assert max_rel_err(to_np(out[0]), ref) < TOL[dtype]
+
+
+def test_prefill_equals_decode_on_gpu(cuda_lib):
+    """Absorbed decode and non-absorbed prefill of the same block agree ([MLA-KV] §2.3)."""
+    S, pos_base = 6, 500
+    x = mla_inputs(GLM, 1, S, [pos_base + S], pos_base + S, "bf16", 61, "cpu")
+    g = _dev(x)
+    a = to_np(cuda_lib.prefill_naive(g["q"], g["Lc"], g["Rc"], g["kv_b"], GLM, pos_base))
+    b = to_np(cuda_lib.decode_absorbed(g["q"], g["Lc"], g["Rc"], g["T"], g["kv_b"], GLM))
+    assert max_rel_err(a, b) < 2 * TOL["bf16"]
