@@ -150,6 +150,30 @@ int mla_prefill_naive(const mla_dims* d, int dtype, int B, int S, int pos_base,
                       float* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Non-absorbed prefill without caller workspace.  The pages have no
+ * counterpart of this entry point; it exists for callers that cannot allocate
+ * device memory: code whose GPU memory belongs to a host framework's pool
+ * that forbids third-party cudaMalloc, code on a latency-critical path that
+ * cannot afford the device-wide synchronisation cudaMalloc/cudaFree may
+ * cause, and plain C callers with no allocator at hand.
+ *
+ * Same arguments and results as mla_prefill_naive minus the workspace: the
+ * rebuilt KV lives in a 32 MiB static device array of the library, held by
+ * every GPU that loads it until the process exits.  Calls needing more
+ * (B * (pos_base+S) * H * (qk_nope+v_head) * sizeof(input dtype) > 32 MiB)
+ * return MLA_ERR_INVALID with the sizes in mla_last_error().  The first call
+ * on a device looks up the array's device address (cudaGetSymbolAddress, with
+ * that device current); make that first call before any stream capture.
+ * The call allocates nothing.  All calls share the one array, which keeps the
+ * last call's contents (every entry is rewritten before it is read, so
+ * nothing needs clearing); calls whose executions overlap on the GPU race on
+ * it, so order them on one stream.
+ * ------------------------------------------------------------------------- */
+int mla_prefill_naive_noalloc(const mla_dims* d, int dtype, int B, int S, int pos_base,
+                              const void* q, const void* Lc, const void* Rc, const void* kv_b,
+                              float* out, void* stream);
+
+/* ---------------------------------------------------------------------------
  * DSA lightning-indexer scores ([MLA-KV] §2.2 "ReLU-gated" scores; the key
  * cache Ic holds index_hd fp32 values per token, [FDSA] §二)
  *

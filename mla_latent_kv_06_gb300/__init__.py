@@ -24,7 +24,7 @@ EXPORTS = (
     "mla_last_error", "mla_abi_version", "mla_device_status", "mla_set_wait_limit_ns",
     "mla_decode_absorbed_workspace_size", "mla_decode_absorbed", "mla_decode_launch_count",
     "mla_sparse_decode_workspace_size", "mla_sparse_decode",
-    "mla_prefill_naive_workspace_size", "mla_prefill_naive",
+    "mla_prefill_naive_workspace_size", "mla_prefill_naive", "mla_prefill_naive_noalloc",
     "dsa_index_scores", "dsa_topk_select_workspace_size", "dsa_topk_select",
 )
 
@@ -63,6 +63,7 @@ def _declare(lib: ctypes.CDLL) -> None:
                                    _SZ, _P]),
         "mla_prefill_naive_workspace_size": (_SZ, [_DP, _I, _I, _I, _I]),
         "mla_prefill_naive": (_I, [_DP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+        "mla_prefill_naive_noalloc": (_I, [_DP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
         "dsa_index_scores": (_I, [_I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P]),
         "dsa_topk_select_workspace_size": (_SZ, [_I, _I, _I, _I]),
         "dsa_topk_select": (_I, [_I, _I, _P, _I, _P, _I, _P, _P, _P, _SZ, _P]),

@@ -86,6 +86,8 @@ bool tc_decode_ok(const mla::Geometry& g, int dtype, const void* q, const void* 
 
 }  // namespace
 
+void mla::set_last_error(const char* msg) { g_err = msg ? msg : ""; }
+
 MLA_EXPORT const char* mla_last_error(void) { return g_err.c_str(); }
 
 MLA_EXPORT int mla_abi_version(void) { return 1; }

@@ -69,4 +69,7 @@ struct TopkArgs {
 
 cudaError_t launch_topk_select(const TopkArgs& a, cudaStream_t st);
 
+// Sets the thread-local message returned by mla_last_error().
+void set_last_error(const char* msg);
+
 }  // namespace mla
