@@ -49,7 +49,8 @@ constexpr uint32_t kTmemS = 0;    // S^T: 64 columns
 constexpr uint32_t kTmemO = 128;  // O^T: 4 M-tiles x 64 columns
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kTau = 8.f;  // lazy rescale threshold (log2 units)
-constexpr int kPlanMax = 1024;  // tile-list rows whose plan the attention CTA builds itself
+constexpr int kPlanMax = 1024;
+constexpr int kPrefetchTiles = 2;  // key tiles pulled into L2 ahead of the tile loads  // tile-list rows whose plan the attention CTA builds itself
 // Waits that drain in-flight copies / MMAs before a CTA exits use at least
 // this limit, whatever the caller's wait limit.
 constexpr long long kDrainNs = 1000000000LL;
@@ -280,12 +281,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     for (int a = 0; a < kSlots; ++a) last_it[a] = -1;
     int last_q = -1;
     bool waited = !local_plan;
+    // L2 prefetch cursor, kPrefetchTiles key tiles ahead of the tile loads:
+    // HBM keeps streaming while a tile's score product, softmax and value
+    // product run, and the tile loads then hit L2.
+    int pf_row = row0, pf_lo = 0, pf_hi = 0, pf_k = 0;
+    bool pf_live = true;
+    auto prefetch_next = [&]() {
+      if (!pf_live) return;
+      if (pf_k >= pf_hi) {
+        if (pf_hi > 0) ++pf_row;
+        if (!next_piece<kSparse>(p, ts, NR, N, g, s, &pf_row, &pf_lo, &pf_hi)) {
+          pf_live = false;
+          return;
+        }
+        pf_k = pf_lo;
+      }
+      const int y = (kSparse ? pf_row : pf_row) * p.kv_rows + pf_k * kTile;
+      for (int a = 0; a < 8; ++a) tma_prefetch_l2_2d(&p.mL, 64 * a, y);
+      tma_prefetch_l2_2d(&p.mR, 0, y);
+      ++pf_k;
+    };
+    if (lane == 0)
+      for (int i = 0; i <= kPrefetchTiles; ++i) prefetch_next();
     while (ok && next_piece<kSparse>(p, ts, NR, N, g, s, &row, &lo, &hi)) {
       const int qrow = kSparse ? row : row * S + s;
       const int b = kSparse ? row / S : row;
       const int kvrow = kSparse ? row : b;
       for (int k = lo; ok && k < hi; ++k, ++it) {
         const uint32_t par = (it & 1) ^ 1;
+        if (lane == 0 && it > 0) prefetch_next();
         if (lane == 0) {
           const int y = kvrow * p.kv_rows + k * kTile;
           for (int a = 0; a < kSlots && ok; ++a) {

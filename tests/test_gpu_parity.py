@@ -54,6 +54,23 @@ def test_decode_ragged(cuda_lib, dtype, dims, T, S):
     assert cuda_lib.device_status() == 0
 
 
+@pytest.mark.parametrize("T,S", [([128 * 152 * 2], 1), ([128 * 152 * 2 + 77], 1), ([40000], 1),
+                                 ([3000, 5000, 129, 7000], 2)])
+def test_decode_several_tiles_per_cta(cuda_lib, T, S):
+    """Long sequences: every persistent CTA runs several key tiles and, for B > 1,
+    several sequences, so the split pipeline crosses tile and sequence borders."""
+    x = mla_inputs(GLM, len(T), S, T, max(T), "bf16", 11, DEV)
+    out = to_np(cuda_lib.decode_absorbed(x["q"], x["Lc"], x["Rc"], x["T"], x["kv_b"], GLM))
+    assert cuda_lib.device_status() == 0
+    kvb = to_np(x["kv_b"])
+    for b in range(len(T)):
+        for s in range(S):
+            pos = T[b] - S + s
+            ref = oracle.attend_absorbed(to_np(x["q"][b, s]), to_np(x["Lc"][b, :pos + 1]),
+                                         to_np(x["Rc"][b, :pos + 1]), kvb, GLM.qk_nope, pos, GLM.softmax_scale)
+            assert max_rel_err(out[b, s], ref) < TOL["bf16"], (b, s)
+
+
 def test_decode_glm_t4096_full(cuda_lib):
     """The GLM-5.2 single-sequence workload at full size (B=1, S=1, T=4096), every output."""
     x = workload_inputs("glm_decode_t4096", DEV)
