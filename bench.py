@@ -97,7 +97,7 @@ def build_workload(name, device):
                     flops=2 * dims.H * sum(sum(T - S + s + 1 for s in range(S)) * (dims.kv_lora * 2 + dims.qk_rope)
                                            for T in T_list)
                     + 2 * dims.H * B * S * (dims.qk_nope + dims.v_head) * dims.kv_lora,
-                    bound="hbm", kernels_per_step=mla_kernels_per_call("decode", dims))
+                    bound="hbm", kernels_per_step=mla_kernels_per_call("decode", dims, B, S))
         e2e = dict(inputs=[x["q"], x["T"]], run=lambda q, T: mla.decode_absorbed(
             q, x["Lc"], x["Rc"], T, x["kv_b"], dims, out=out, workspace=ws), out=out)
     elif kind == "dsa":
@@ -119,7 +119,7 @@ def build_workload(name, device):
         gathered = row * B * S * k
         acct.update(cache_bytes=gathered, alg_bytes=ic_bytes + 2 * 4 * B * S * x["T_cap"] + gathered + w_bytes
                     + q_bytes + out_bytes, flops=0, bound="hbm",
-                    kernels_per_step=2 + mla_kernels_per_call("sparse", dims))
+                    kernels_per_step=2 + mla_kernels_per_call("sparse", dims, B, S))
         e2e = dict(inputs=[x["q"], x["q_idx"], x["w"], x["T"]], run=None, out=out)
     else:
         pos_base = x["pos_base"]
@@ -140,10 +140,10 @@ def build_workload(name, device):
     return x, step, acct, e2e
 
 
-def mla_kernels_per_call(kind, dims):
-    """Kernels one API call launches (the tensor-core decode path is three, the CUDA-core one)."""
+def mla_kernels_per_call(kind, dims, B, S):
+    """Kernels one API call launches (queried from the library)."""
     import mla_latent_kv_06_gb300 as mla
-    return mla.kernels_per_call(kind, dims)
+    return mla.kernels_per_call(kind, dims, B, S)
 
 
 # ------------------------------------------------------------------ clocks

@@ -101,8 +101,8 @@ void mla_set_wait_limit_ns(long long ns);
  *   kv_b [H, qk_nope+v_head, kv_lora]
  *   out  [B, S, H, v_head] float
  * The tensor-core path takes BF16 with H == 64, kv_lora == 512, qk_rope == 64,
- * qk_nope % 16 == 0, v_head % 16 == 0 and 16-byte aligned pointers; every
- * other valid request runs on the CUDA-core path.
+ * qk_nope % 64 == 0 (<= 256), v_head % 64 == 0 and 16-byte aligned pointers;
+ * every other valid request runs on the CUDA-core path.
  * ------------------------------------------------------------------------- */
 size_t mla_decode_absorbed_workspace_size(const mla_dims* d, int dtype, int B, int S, int T_cap);
 int mla_decode_absorbed(const mla_dims* d, int dtype, int B, int S,
@@ -111,8 +111,8 @@ int mla_decode_absorbed(const mla_dims* d, int dtype, int B, int S,
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /* Number of kernels one mla_decode_absorbed (sparse = 0) or mla_sparse_decode
- * (sparse = 1) call launches for this geometry and dtype (host-only query). */
-int mla_decode_launch_count(const mla_dims* d, int dtype, int sparse);
+ * (sparse = 1) call launches for this geometry, dtype and batch (host-only query). */
+int mla_decode_launch_count(const mla_dims* d, int dtype, int B, int S, int sparse);
 
 /* ---------------------------------------------------------------------------
  * Sparse decode over DSA-selected keys ([MLA-KV] §2.2: the top-k keys chosen

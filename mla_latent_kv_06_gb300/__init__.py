@@ -56,7 +56,7 @@ def _declare(lib: ctypes.CDLL) -> None:
         "mla_device_status": (_I, [_P, ctypes.POINTER(_I)]),
         "mla_set_wait_limit_ns": (None, [ctypes.c_longlong]),
         "mla_decode_absorbed_workspace_size": (_SZ, [_DP, _I, _I, _I, _I]),
-        "mla_decode_launch_count": (_I, [_DP, _I, _I]),
+        "mla_decode_launch_count": (_I, [_DP, _I, _I, _I, _I]),
         "mla_decode_absorbed": (_I, [_DP, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _P, _SZ, _P]),
         "mla_sparse_decode_workspace_size": (_SZ, [_DP, _I, _I, _I, _I]),
         "mla_sparse_decode": (_I, [_DP, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _P, _I, _P, _P,
@@ -157,10 +157,10 @@ def set_wait_limit_ns(ns: int) -> None:
 
 
 # ------------------------------------------------------------------ ops
-def kernels_per_call(kind: str, dims, dtype: int = MLA_BF16) -> int:
+def kernels_per_call(kind: str, dims, B: int = 1, S: int = 1, dtype: int = MLA_BF16) -> int:
     """Kernels one decode ("decode") or sparse-decode ("sparse") call launches."""
     d = make_dims(dims)
-    return lib().mla_decode_launch_count(ctypes.byref(d), dtype, 1 if kind == "sparse" else 0)
+    return lib().mla_decode_launch_count(ctypes.byref(d), dtype, B, S, 1 if kind == "sparse" else 0)
 
 
 def decode_workspace_size(dims, dtype: int, B: int, S: int, T_cap: int) -> int:

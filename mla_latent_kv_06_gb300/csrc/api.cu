@@ -157,10 +157,10 @@ MLA_EXPORT int mla_decode_absorbed(const mla_dims* d, int dtype, int B, int S, c
   return MLA_OK;
 }
 
-MLA_EXPORT int mla_decode_launch_count(const mla_dims* d, int dtype, int sparse) {
+MLA_EXPORT int mla_decode_launch_count(const mla_dims* d, int dtype, int B, int S, int sparse) {
   mla::Geometry g;
-  if (!resolve(d, &g)) return 0;
-  if (dtype == MLA_BF16 && mla::tc_decode_geometry_ok(g)) return mla::tc_decode_launch_count(sparse != 0);
+  if (!resolve(d, &g) || B < 1 || S < 1) return 0;
+  if (dtype == MLA_BF16 && mla::tc_decode_geometry_ok(g)) return mla::tc_decode_launch_count(sparse != 0, B, S);
   return 1;
 }
 

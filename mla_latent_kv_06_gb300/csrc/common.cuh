@@ -57,4 +57,10 @@ __device__ __forceinline__ uint32_t ordered_key(float x) {
 
 __device__ __forceinline__ float qnan() { return __int_as_float(0x7fc00000); }
 
+// Two floats -> packed bf16x2 (round to nearest even).
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&t);
+}
+
 }  // namespace mla

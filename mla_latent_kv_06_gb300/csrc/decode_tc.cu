@@ -27,6 +27,7 @@
 #include <cmath>
 
 #include "decode_tc.h"
+#include "gemm_tc.h"
 #include "sm100.cuh"
 #include "tmap.h"
 
@@ -592,6 +593,7 @@ struct AbsorbParams {
   int32_t* tile_start;  // [NR + 1]
   int32_t* bad;         // [NR]
   int B, S, T_cap, Dn, Dv, topk, sparse;
+  int do_qabs;            // 0: plan and rotary part only (qabs comes from the GEMM kernel)
   double theta[kDr / 2];  // RoPE frequencies rope_base^(-2j/qk_rope), from the host
   unsigned int* flags;
 };
@@ -628,7 +630,7 @@ __global__ void __launch_bounds__(kAbsThreads) absorb_kernel(const AbsorbParams 
   // W_UK[h][:, cb*128 : cb*128+128] -> smem: every 16-byte load is issued
   // before the first store so that the whole tile is in flight at once.
   const __nv_bfloat16* W = p.kv_b + (size_t)h * (Dn + p.Dv) * kDl + cb * kAbsCols;
-  const int nvec = Dn * kAbsCols / 8;
+  const int nvec = p.do_qabs ? Dn * kAbsCols / 8 : 0;
   constexpr int kMaxVec = 256 * kAbsCols / 8 / kAbsThreads;  // qk_nope <= 256
   uint4 wv[kMaxVec];
 #pragma unroll
@@ -703,12 +705,13 @@ __global__ void __launch_bounds__(kAbsThreads) absorb_kernel(const AbsorbParams 
       qn[rr * Dn + i] = __bfloat162float(p.q[((size_t)(r0 + rr) * kH + h) * Dq + i]);
     }
     __syncthreads();
-    if (nr == 1) absorb_rows<1>(Ws, qn, Dn, col, i0, i1, part, half);
+    if (!p.do_qabs) {
+    } else if (nr == 1) absorb_rows<1>(Ws, qn, Dn, col, i0, i1, part, half);
     else if (nr <= 4) absorb_rows<4>(Ws, qn, Dn, col, i0, i1, part, half);
     else if (nr <= 8) absorb_rows<8>(Ws, qn, Dn, col, i0, i1, part, half);
     else absorb_rows<kAbsRows>(Ws, qn, Dn, col, i0, i1, part, half);
     __syncthreads();
-    for (int e = tid; e < nr * kAbsCols; e += kAbsThreads) {
+    for (int e = tid; e < (p.do_qabs ? nr * kAbsCols : 0); e += kAbsThreads) {
       const int u = e / kAbsCols, c = e % kAbsCols;
       const float v = part[u * kAbsCols + c] + part[(kAbsRows + u) * kAbsCols + c];
       p.qcat[((size_t)(r0 + u) * kH + h) * kDc + cb * kAbsCols + c] = __float2bfloat16_rn(v);
@@ -923,6 +926,91 @@ __global__ void __launch_bounds__(kCmbThreads) combine_kernel(const CombineParam
 }
 
 // ===========================================================================
+// Merge kernel (batches with more than kSmallRows query rows): one warp per
+// (row, head) forms the normalised latent context clat = sum_i w_i O_i / L
+// (bf16) for the W_UV GEMM; inv_l is 1, or NaN for a flagged row.
+// ===========================================================================
+struct MergeParams {
+  const float* o_part;
+  const float* ml_part;
+  const int32_t* tile_start;
+  const int32_t* T;
+  const int32_t* bad;
+  __nv_bfloat16* clat;  // [R, 64, 512]
+  float* inv_l;         // [R, 64]
+  int B, S, G, sparse;
+};
+
+__global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int R = p.B * p.S;
+  const int gw = blockIdx.x * 8 + warp;
+  if (gw >= R * kH) return;
+  const int r = gw / kH, h = gw % kH, b = r / p.S, s = r % p.S;
+  const int row = p.sparse ? r : b;
+  const int NR = p.sparse ? R : p.B;
+  const long long N = p.tile_start[NR];
+  __nv_bfloat16* dst = p.clat + ((size_t)r * kH + h) * kDl + 16 * lane;
+  if (p.bad[row] || N <= 0) {
+    *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(dst + 8) = make_uint4(0, 0, 0, 0);
+    if (lane == 0) p.inv_l[(size_t)r * kH + h] = qnan();
+    return;
+  }
+  const long long a = p.tile_start[row], e = p.tile_start[row + 1];
+  const int glo = chunk_of(a, N, p.G), ghi = chunk_of(e - 1, N, p.G);
+  float M = -INFINITY;
+  for (int gg = glo + lane; gg <= ghi; gg += 32) {
+    int lo, hi;
+    if (p.sparse) piece_range<true>(p.tile_start, p.T, p.S, s, row, gg, p.G, N, &lo, &hi);
+    else piece_range<false>(p.tile_start, p.T, p.S, s, row, gg, p.G, N, &lo, &hi);
+    if (lo < hi) {
+      const int slot = p.sparse ? gg + row : (gg + row) * p.S + s;
+      M = fmaxf(M, p.ml_part[((size_t)slot * kH + h) * 2]);
+    }
+  }
+  M = warp_max(M);
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  float L = 0.f;
+  for (int gg = glo; gg <= ghi; ++gg) {
+    int lo, hi;
+    if (p.sparse) piece_range<true>(p.tile_start, p.T, p.S, s, row, gg, p.G, N, &lo, &hi);
+    else piece_range<false>(p.tile_start, p.T, p.S, s, row, gg, p.G, N, &lo, &hi);
+    if (lo >= hi) continue;
+    const int slot = p.sparse ? gg + row : (gg + row) * p.S + s;
+    const float2 ml = *reinterpret_cast<const float2*>(p.ml_part + ((size_t)slot * kH + h) * 2);
+    const float wgt = exp2f(ml.x - M);
+    L = fmaf(wgt, ml.y, L);
+    const float4* op = reinterpret_cast<const float4*>(p.o_part + ((size_t)slot * kH + h) * kDl + 16 * lane);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 o = op[i];
+      acc[4 * i] = fmaf(wgt, o.x, acc[4 * i]);
+      acc[4 * i + 1] = fmaf(wgt, o.y, acc[4 * i + 1]);
+      acc[4 * i + 2] = fmaf(wgt, o.z, acc[4 * i + 2]);
+      acc[4 * i + 3] = fmaf(wgt, o.w, acc[4 * i + 3]);
+    }
+  }
+  const float il = 1.f / L;
+  uint4 w0, w1;
+  w0.x = pack2(acc[0] * il, acc[1] * il);
+  w0.y = pack2(acc[2] * il, acc[3] * il);
+  w0.z = pack2(acc[4] * il, acc[5] * il);
+  w0.w = pack2(acc[6] * il, acc[7] * il);
+  w1.x = pack2(acc[8] * il, acc[9] * il);
+  w1.y = pack2(acc[10] * il, acc[11] * il);
+  w1.z = pack2(acc[12] * il, acc[13] * il);
+  w1.w = pack2(acc[14] * il, acc[15] * il);
+  *reinterpret_cast<uint4*>(dst) = w0;
+  *reinterpret_cast<uint4*>(dst + 8) = w1;
+  if (lane == 0) p.inv_l[(size_t)r * kH + h] = (L == L) ? 1.f : qnan();
+}
+
+// ===========================================================================
 // Gather kernel (sparse only): staging[r, j, 0:512 | 512:576] = Lc | Rc of key
 // sel[r, j] for j < nsel[r]; zero rows past nsel or for an index outside
 // [0, pos] (flagged).  CTA = (32 keys, row r); one warp per key row.
@@ -971,8 +1059,12 @@ __global__ void __launch_bounds__(256) gather_kernel(const GatherParams p) {
 // ===========================================================================
 struct Plan {
   int G, NR, P, R, Kpad;
-  size_t off_q, off_ts, off_bad, off_o, off_ml, off_stage, total;
+  size_t off_q, off_ts, off_bad, off_o, off_ml, off_stage, off_clat, off_invl, total;
 };
+
+// Query rows above which the weight products run as tcgen05 GEMMs; below it
+// they are weight-bandwidth-bound GEMVs on the CUDA cores.
+constexpr int kSmallRows = 8;
 
 int sm_count() {
   int dev = 0, n = 0;
@@ -1034,6 +1126,10 @@ Plan make_plan(int B, int S, int T_cap, int sparse_topk) {
   pl.Kpad = sparse_topk ? (sparse_topk + kTile - 1) / kTile * kTile : 0;
   pl.off_stage = off;
   off = align256(off + (size_t)pl.R * pl.Kpad * kDc * 2);
+  pl.off_clat = off;
+  off = align256(off + (pl.R > kSmallRows ? (size_t)pl.R * kH * kDl * 2 : 0));
+  pl.off_invl = off;
+  off = align256(off + (pl.R > kSmallRows ? (size_t)pl.R * kH * 4 : 0));
   pl.total = off;
   return pl;
 }
@@ -1104,14 +1200,42 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   ap.Dv = g.Dv;
   ap.topk = a.topk;
   ap.sparse = sparse ? 1 : 0;
+  const bool big = pl.R > kSmallRows;
+  ap.do_qabs = big ? 0 : 1;
   for (int j = 0; j < kDr / 2; ++j) ap.theta[j] = std::pow(g.rope_base, -2.0 * j / kDr);
   ap.flags = a.flags;
   const size_t abs_smem = (size_t)g.Dn * kAbsCols * 2 + (size_t)kAbsRows * g.Dn * 4 +
                           (size_t)2 * kAbsRows * kAbsCols * 4;
   e = set_smem_once(absorb_kernel, 200 * 1024, &g_abs_attr);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(absorb_kernel, dim3(kDl / kAbsCols, kH), dim3(kAbsThreads), abs_smem, st, ap);
+  e = launch_pdl(absorb_kernel, dim3(big ? 1 : kDl / kAbsCols, kH), dim3(kAbsThreads), abs_smem, st, ap);
   if (e != cudaSuccess) return e;
+  if (big) {  // qabs for many rows: per-head GEMM [R x qk_nope] x W_UK[h] on the tensor cores
+    GemmArgs ga{};
+    ga.a_base = a.q;
+    ga.a_ld_z = g.Dn + kDr;
+    ga.a_ld_m = (long long)kH * (g.Dn + kDr);
+    ga.b_base = a.kv_b;
+    ga.b_rows = (long long)kH * (g.Dn + g.Dv);
+    ga.b_cols = kDl;
+    ga.b_ld = kDl;
+    ga.b_mn_major = 1;
+    ga.b_row0 = 0;
+    ga.b_rows_per_z = g.Dn + g.Dv;
+    ga.b_col0 = 0;
+    ga.c_base = qcat;
+    ga.c_ld_m = (long long)kH * kDc;
+    ga.c_ld_z = kDc;
+    ga.out_kind = kGemmOutBf16;
+    ga.M = pl.R;
+    ga.N = kDl;
+    ga.K = g.Dn;
+    ga.Z = kH;
+    ga.flags = a.flags;
+    ga.wait_ns = a.wait_limit_ns;
+    e = launch_gemm_tc(ga, true, st);
+    if (e != cudaSuccess) return e;
+  }
 
   // 2. attention
   AttnParams tp{};
@@ -1149,7 +1273,47 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   e = launch_pdl(kern, dim3(nblk), dim3(kAttnThreads), kAttnDynSmem, st, tp);
   if (e != cudaSuccess) return e;
 
-  // 3. combine + W_UV
+  // 3. merge of the splits and the W_UV lift
+  if (big) {
+    MergeParams mp{};
+    mp.o_part = o_part;
+    mp.ml_part = ml_part;
+    mp.tile_start = ts;
+    mp.T = a.T;
+    mp.bad = bad;
+    mp.clat = reinterpret_cast<__nv_bfloat16*>(w + pl.off_clat);
+    mp.inv_l = reinterpret_cast<float*>(w + pl.off_invl);
+    mp.B = B;
+    mp.S = S;
+    mp.G = pl.G;
+    mp.sparse = sparse ? 1 : 0;
+    e = launch_pdl(merge_kernel, dim3((pl.R * kH + 7) / 8), dim3(256), 0, st, mp);
+    if (e != cudaSuccess) return e;
+    GemmArgs gu{};
+    gu.a_base = mp.clat;
+    gu.a_ld_z = kDl;
+    gu.a_ld_m = (long long)kH * kDl;
+    gu.b_base = a.kv_b;
+    gu.b_rows = (long long)kH * (g.Dn + g.Dv);
+    gu.b_cols = kDl;
+    gu.b_ld = kDl;
+    gu.b_mn_major = 0;
+    gu.b_row0 = g.Dn;
+    gu.b_rows_per_z = g.Dn + g.Dv;
+    gu.b_col0 = 0;
+    gu.c_base = a.out;
+    gu.c_ld_m = (long long)kH * g.Dv;
+    gu.c_ld_z = g.Dv;
+    gu.out_kind = kGemmOutF32Scaled;
+    gu.scale = mp.inv_l;
+    gu.M = pl.R;
+    gu.N = g.Dv;
+    gu.K = kDl;
+    gu.Z = kH;
+    gu.flags = a.flags;
+    gu.wait_ns = a.wait_limit_ns;
+    return launch_gemm_tc(gu, true, st);
+  }
   CombineParams cp{};
   cp.kv_b = static_cast<const __nv_bfloat16*>(a.kv_b);
   cp.o_part = o_part;
@@ -1175,11 +1339,13 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
 }  // namespace
 
 bool tc_decode_geometry_ok(const Geometry& g) {
-  return g.H == kH && g.Dl == kDl && g.Dr == kDr && g.Dn >= 16 && g.Dn % 16 == 0 && g.Dn <= 256 &&
+  return g.H == kH && g.Dl == kDl && g.Dr == kDr && g.Dn >= 64 && g.Dn % 64 == 0 && g.Dn <= 256 &&
          g.Dv >= kCmbJ && g.Dv % kCmbJ == 0;
 }
 
-int tc_decode_launch_count(bool sparse) { return sparse ? 4 : 3; }
+int tc_decode_launch_count(bool sparse, int B, int S) {
+  return (sparse ? 1 : 0) + ((long long)B * S > kSmallRows ? 5 : 3);
+}
 
 size_t tc_decode_workspace_bytes(const Geometry&, int B, int S, int T_cap, int sparse_topk) {
   return make_plan(B, S, T_cap, sparse_topk).total;

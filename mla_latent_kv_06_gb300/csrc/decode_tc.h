@@ -17,7 +17,7 @@ bool tc_decode_geometry_ok(const Geometry& g);
 size_t tc_decode_workspace_bytes(const Geometry& g, int B, int S, int T_cap, int sparse_topk);
 
 // Kernels launched by one tensor-core decode call.
-int tc_decode_launch_count(bool sparse);
+int tc_decode_launch_count(bool sparse, int B, int S);
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);
 cudaError_t launch_sparse_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);

@@ -44,4 +44,21 @@ inline bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows,
   return r == CUDA_SUCCESS;
 }
 
+// 3D bf16 tensor: dims[0] contiguous (element count), strides (bytes) of
+// dims 1 and 2, box sizes per dim.  Out-of-range elements read as zero.
+inline bool make_tmap_3d_bf16(CUtensorMap* map, const void* base, const uint64_t dims[3],
+                              const uint64_t stride_bytes[2], const uint32_t box[3],
+                              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  cuuint64_t st[2] = {stride_bytes[0], stride_bytes[1]};
+  cuuint32_t bx[3] = {box[0], box[1], box[2]};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), d, st, bx, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace mla
