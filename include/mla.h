@@ -142,7 +142,10 @@ int mla_sparse_decode(const mla_dims* d, int dtype, int B, int S,
  *   Lc   [B, Tk, kv_lora], Rc [B, Tk, qk_rope]
  *   kv_b [H, qk_nope+v_head, kv_lora]
  *   out  [B, S, H, v_head] float
- * The rebuilt KV lives in the workspace (dtype of the inputs).
+ * The rebuilt KV lives in the workspace (dtype of the inputs).  BF16 with the
+ * GLM-5.2 geometry (H 64, qk_nope 192, qk_rope 64, v_head 256) runs on the
+ * tensor cores (kv_b GEMM + causal flash attention); other requests run on
+ * the CUDA cores.
  * ------------------------------------------------------------------------- */
 size_t mla_prefill_naive_workspace_size(const mla_dims* d, int dtype, int B, int S, int pos_base);
 int mla_prefill_naive(const mla_dims* d, int dtype, int B, int S, int pos_base,

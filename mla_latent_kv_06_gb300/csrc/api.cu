@@ -10,6 +10,7 @@
 #include "common.cuh"
 #include "decode_tc.h"
 #include "internal.h"
+#include "prefill_tc.h"
 
 #define MLA_EXPORT extern "C" __attribute__((visibility("default")))
 
@@ -250,7 +251,16 @@ MLA_EXPORT int mla_prefill_naive(const mla_dims* d, int dtype, int B, int S, int
   a.kv_b = kv_b;
   a.kv = workspace;
   a.out = out;
-  cudaError_t e = mla::launch_prefill_simt(a, dtype, static_cast<cudaStream_t>(stream));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (dtype == MLA_BF16 && mla::tc_prefill_geometry_ok(g) && aligned16(q) && aligned16(Lc) && aligned16(Rc) &&
+      aligned16(kv_b) && aligned16(workspace)) {
+    unsigned int* flags = flags_ptr();
+    if (!flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
+    e = mla::launch_prefill_tc(a, flags, g_wait_limit_ns.load(), st);
+  } else {
+    e = mla::launch_prefill_simt(a, dtype, st);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "mla_prefill_naive launch");
   return MLA_OK;
 }

@@ -426,8 +426,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       bool bad_idx = false;
       for (int k = lo; ok && k < hi; ++k, ++it) {
         const bool first = (k == lo);
-        ok = mbar_wait(&s_full, it & 1, abort, p.flags, p.wait_ns);
-        if (!ok) break;
+        // A failed wait is decided jointly by the 128 softmax threads (bar.red
+        // below), so that no thread is left waiting at a barrier the others quit.
+        bool fail = !mbar_wait(&s_full, it & 1, abort, p.flags, p.wait_ns);
+        if (bar_red_or(1, 128, fail)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         float v[kH];
         tmem_ld64(tmem + t_lane + kTmemS, v);
@@ -512,8 +517,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           }
         }
         if (rescale) {  // O^T columns scaled by alpha once the previous value product retired
-          ok = mbar_wait(&o_done, (it - 1) & 1, abort, p.flags, p.wait_ns);
-          if (!ok) break;
+          fail = !mbar_wait(&o_done, (it - 1) & 1, abort, p.flags, p.wait_ns);
+          if (bar_red_or(2, 128, fail)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
 #pragma unroll 1
           for (int m = 0; m < 4; ++m) {
@@ -539,8 +547,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       if (!ok) break;
       // ---- end of piece: write the split's partials
       const int slot = kSparse ? g + row : (g + row) * S + s;
-      ok = mbar_wait(&o_done, (it - 1) & 1, abort, p.flags, p.wait_ns);
-      if (!ok) break;
+      const bool fail_end = !mbar_wait(&o_done, (it - 1) & 1, abort, p.flags, p.wait_ns);
+      if (bar_red_or(1, 128, fail_end)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       float* op = p.o_part + (size_t)slot * kH * kDl;
 #pragma unroll 1

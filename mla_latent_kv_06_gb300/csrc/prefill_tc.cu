@@ -1,0 +1,398 @@
+// prefill_tc.cu -- tensor-core non-absorbed prefill for the GLM-5.2 shape
+// (64 heads, qk_nope 192 + qk_rope 64, v_head 256).
+//
+// The non-absorbed path of the page "MLA 注意力与 KV 缓存", §2.3:
+//   1. one kv_b product rebuilds k_nope and the value of every key,
+//      KV[t, h, :] = kv_b[h] Lc[t]  -> the batched tcgen05 GEMM (gemm_tc.cu);
+//   2. causal attention per head with score = q_pass . k_nope + q_rot . k_rot,
+//      k_rot = Rc[t] shared by all heads, softmax, and a value sum.
+//
+// Step 2 is a flash-attention forward on tcgen05.  CTA = (128 queries, head,
+// sequence).  Query rows live in the 128 TMEM lanes, so every softmax thread
+// owns one query row and its max / sum / rescale stay in registers.  Per
+// 64-key tile j:
+//   S(j)  = Q K(j)^T       M=128, N=64,  K=256  (Q and K K-major)
+//   O    += P(j-1) V(j-1)  M=128, N=256, K=64   (P K-major, V MN-major)
+// with K/V double-buffered in shared memory (TMA), S and P double-buffered.
+#include <atomic>
+#include <cmath>
+
+#include "common.cuh"
+#include "gemm_tc.h"
+#include "internal.h"
+#include "prefill_tc.h"
+#include "sm100.cuh"
+#include "tmap.h"
+
+namespace mla {
+namespace {
+
+using namespace sm100;
+
+constexpr int kH = 64, kDn = 192, kDr = 64, kDq = 256, kDv = 256, kDkv = kDn + kDv;  // kDkv = 448
+constexpr int kQT = 128;                    // queries per CTA
+constexpr int kKT = 64;                     // keys per tile
+constexpr uint32_t kQAtom = kQT * 128;      // 16 KB: 128 rows x 64 bf16
+constexpr uint32_t kKAtom = kKT * 128;      // 8 KB:  64 rows x 64 bf16
+constexpr uint32_t kQBytes = 4 * kQAtom;    // 64 KB
+constexpr uint32_t kKBytes = 4 * kKAtom;    // 32 KB (192 k_nope + 64 k_rot dims)
+constexpr uint32_t kVBytes = 4 * kKAtom;    // 32 KB (256 value dims as 4 MN atoms)
+constexpr uint32_t kPBytes = kQT * 128;     // 16 KB: 128 queries x 64 keys bf16
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffKV = kQBytes;                        // 2 stages of K | V
+constexpr uint32_t kOffP = kOffKV + 2 * (kKBytes + kVBytes);
+constexpr uint32_t kPrefillSmem = kOffP + 2 * kPBytes + 1024;
+constexpr int kPThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS = 0;    // two S buffers of 64 columns
+constexpr uint32_t kTmemO = 128;  // O: 256 columns
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kTau = 8.f;
+constexpr long long kDrainNs = 1000000000LL;
+
+struct FlashParams {
+  CUtensorMap mQ;   // q as 3D {256 dims, 64 heads, B*S tokens}, box {64, 1, 128}
+  CUtensorMap mKV;  // KV as 2D [B*Tk rows, 64*448 cols], box {64 cols, 64 rows}
+  CUtensorMap mR;   // Rc as 2D [B*Tk rows, 64 cols], box {64, 64 rows}
+  const __nv_bfloat16* q;
+  float* out;
+  int B, S, Tk, pos_base;
+  float c;                // softmax scale * log2(e)
+  double theta[kDr / 2];  // RoPE frequencies
+  unsigned int* flags;
+  long long wait_ns;
+};
+
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_constant__ FlashParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                         ~static_cast<uintptr_t>(1023));
+  unsigned char* sQ = smem + kOffQ;
+  unsigned char* sKV = smem + kOffKV;
+  unsigned char* sP = smem + kOffP;
+  // o_done[j & 1] completes its (j >> 1)-th phase when O += P(j) V(j) retires;
+  // the product for tile j + 2 needs P(j + 2), so parity waits never alias.
+  __shared__ uint64_t q_full, q_rope, kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full[2], o_done[2], mma_done;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int s0 = qt * kQT;
+  const int s_end = min(s0 + kQT, p.S);
+  const int nkt = (p.pos_base + s_end + kKT - 1) / kKT;  // key tiles holding keys <= the last query
+
+  if (threadIdx.x == 0) {
+    mbar_init(&q_full, 1);
+    mbar_init(&q_rope, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 128);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&o_done[i], 1);
+    }
+    mbar_init(&mma_done, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&p.mQ);
+    prefetch_tensormap(&p.mKV);
+    prefetch_tensormap(&p.mR);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  volatile int* abort = &abort_flag;
+  grid_dep_wait();  // KV comes from the kv_b GEMM
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      bool ok = true;
+      mbar_arrive_expect_tx(&q_full, 3 * kQAtom);
+      for (int a = 0; a < 3; ++a) tma_load_3d(sQ + a * kQAtom, &p.mQ, 64 * a, h, b * p.S + s0, &q_full);
+      int last = -1;
+      for (int j = 0; j < nkt && ok; ++j) {
+        const int st = j & 1;
+        ok = mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1, abort, p.flags, p.wait_ns);
+        if (!ok) break;
+        unsigned char* sK = sKV + st * (kKBytes + kVBytes);
+        unsigned char* sV = sK + kKBytes;
+        const int y = b * p.Tk + j * kKT;
+        mbar_arrive_expect_tx(&kv_full[st], kKBytes + kVBytes);
+        for (int a = 0; a < 3; ++a) tma_load_2d(sK + a * kKAtom, &p.mKV, h * kDkv + 64 * a, y, &kv_full[st]);
+        tma_load_2d(sK + 3 * kKAtom, &p.mR, 0, y, &kv_full[st]);
+        for (int a = 0; a < 4; ++a) tma_load_2d(sV + a * kKAtom, &p.mKV, h * kDkv + kDn + 64 * a, y, &kv_full[st]);
+        last = j;
+      }
+      volatile int no_abort = 0;
+      const long long dn = p.wait_ns > kDrainNs ? p.wait_ns : kDrainNs;
+      mbar_wait(&q_full, 0, &no_abort, p.flags, dn);
+      for (int j = last - 1; j <= last; ++j)
+        if (j >= 0) mbar_wait(&kv_full[j & 1], (j >> 1) & 1, &no_abort, p.flags, dn);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_bf16_f32(128, kKT, 0, 0);
+      const uint32_t idesc_o = idesc_bf16_f32(128, kDv, 0, 1);
+      const uint32_t q0 = smem_u32(sQ), kv0 = smem_u32(sKV), p0 = smem_u32(sP);
+      bool ok = mbar_wait(&q_full, 0, abort, p.flags, p.wait_ns) && mbar_wait(&q_rope, 0, abort, p.flags, p.wait_ns);
+      bool issued = false;
+      auto pv = [&](int j) -> bool {  // O += P(j) V(j)
+        if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1, abort, p.flags, p.wait_ns)) return false;
+        tc_fence_after();
+        const uint32_t v0 = kv0 + (j & 1) * (kKBytes + kVBytes) + kKBytes;
+        const uint32_t pp = p0 + (j & 1) * kPBytes;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t da = smem_desc_sw128(pp + kk * 32, 16, 1024);
+          const uint64_t db = smem_desc_sw128(v0 + kk * 2048, kKAtom, 1024);
+          mma_bf16(tmem + kTmemO, da, db, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&kv_empty[j & 1]);
+        mma_commit(&o_done[j & 1]);
+        return true;
+      };
+      for (int j = 0; j < nkt && ok; ++j) {
+        const int st = j & 1, n = j >> 1;
+        ok = mbar_wait(&s_free[st], (n & 1) ^ 1, abort, p.flags, p.wait_ns) &&
+             mbar_wait(&kv_full[st], n & 1, abort, p.flags, p.wait_ns);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t k0 = kv0 + st * (kKBytes + kVBytes);
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t da = smem_desc_sw128(q0 + a * kQAtom + kk * 32, 16, 1024);
+            const uint64_t db = smem_desc_sw128(k0 + a * kKAtom + kk * 32, 16, 1024);
+            mma_bf16(tmem + kTmemS + 64 * st, da, db, idesc_s, (a | kk) != 0);
+          }
+        mma_commit(&s_full[st]);
+        issued = true;
+        if (j > 0) ok = pv(j - 1);
+      }
+      if (ok && nkt > 0) ok = pv(nkt - 1);
+      if (issued) {
+        mma_commit(&mma_done);
+        volatile int no_abort = 0;
+        mbar_wait(&mma_done, 0, &no_abort, p.flags, p.wait_ns > kDrainNs ? p.wait_ns : kDrainNs);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax warps 2..5 (one query row each)
+    const int wq = warp & 3;
+    const int m = 32 * wq + lane;
+    const int s = s0 + m;
+    const bool row_ok = s < p.S;
+    const int pos = p.pos_base + s;
+    const uint32_t t_lane = (uint32_t)(32 * wq) << 16;
+    // rotary part of the query row into Q atom 3 (128-byte swizzled like TMA would)
+    {
+      uint32_t pk[32];
+      if (row_ok) {
+        const __nv_bfloat16* qr = p.q + (((size_t)b * p.S + s) * kH + h) * kDq + kDn;
+#pragma unroll
+        for (int j = 0; j < kDr / 2; j += 2) {
+          float r0[2], r1[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const double ang = (double)pos * p.theta[j + u];
+            const double kq = rint(ang * 0.15915494309189535);
+            const float red = (float)fma(-kq, 6.283185307179586, ang);
+            float sn, cs;
+            sincosf(red, &sn, &cs);
+            const float x0 = __bfloat162float(qr[2 * (j + u)]), x1 = __bfloat162float(qr[2 * (j + u) + 1]);
+            r0[u] = x0 * cs - x1 * sn;   // -> y[j + u]
+            r1[u] = x1 * cs + x0 * sn;   // -> y[32 + j + u]
+          }
+          pk[j / 2] = pack2(r0[0], r0[1]);
+          pk[16 + j / 2] = pack2(r1[0], r1[1]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pk[i] = 0u;
+      }
+      unsigned char* row = sQ + 3 * kQAtom + m * 128;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc)
+        *reinterpret_cast<uint4*>(row + ((cc ^ (m & 7)) << 4)) = make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+      fence_proxy_async_smem();
+      mbar_arrive(&q_rope);
+    }
+    const float c = p.c;
+    float m_run = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkt && ok; ++j) {
+      const int st = j & 1;
+      ok = mbar_wait(&s_full[st], (j >> 1) & 1, abort, p.flags, p.wait_ns);
+      ok = __all_sync(0xffffffffu, ok);  // the warp leaves together (warp-wide tcgen05 ops follow)
+      if (!ok) break;
+      tc_fence_after();
+      float v[64];
+      tmem_ld64(tmem + t_lane + kTmemS + 64 * st, v);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&s_free[st]);
+      const int t0 = j * kKT;
+      const int nvalid = row_ok ? min(kKT, pos - t0 + 1) : 0;  // keys t0..t0+nvalid-1 are visible
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 64; ++i)
+        if (i < nvalid) mx = fmaxf(mx, v[i]);
+      float alpha = 1.f;
+      const float cand = mx * c;
+      if (cand > m_run + kTau) {
+        alpha = exp2f(m_run - cand);
+        m_run = cand;
+      }
+      uint32_t pk[32];
+      float psum = 0.f;
+#pragma unroll
+      for (int i = 0; i < 64; i += 2) {
+        const float e0 = i < nvalid ? exp2f(fmaf(v[i], c, -m_run)) : 0.f;
+        const float e1 = i + 1 < nvalid ? exp2f(fmaf(v[i + 1], c, -m_run)) : 0.f;
+        pk[i / 2] = pack2(e0, e1);
+        const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&pk[i / 2]));
+        psum += f.x + f.y;
+      }
+      l = l * alpha + psum;
+      unsigned char* prow = sP + st * kPBytes + m * 128;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc)
+        *reinterpret_cast<uint4*>(prow + ((cc ^ (m & 7)) << 4)) = make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+      // O rows of this warp rescaled (tcgen05.ld/st are warp-wide) once O += P(j-1)V(j-1) retired
+      if (__any_sync(0xffffffffu, alpha != 1.f && j > 0)) {
+        ok = mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort, p.flags, p.wait_ns);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int cb = 0; cb < kDv; cb += 64) {
+          float w[64];
+          tmem_ld64(tmem + t_lane + kTmemO + cb, w);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 64; ++i) w[i] *= alpha;
+          tmem_st64(tmem + t_lane + kTmemO + cb, w);
+        }
+        tmem_wait_st();
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&p_full[st]);
+    }
+    if (ok && nkt > 0) ok = mbar_wait(&o_done[(nkt - 1) & 1], ((nkt - 1) >> 1) & 1, abort, p.flags, p.wait_ns);
+    if (__all_sync(0xffffffffu, ok) && nkt > 0) {
+      tc_fence_after();
+      float* orow = p.out + (((size_t)b * p.S + s) * kH + h) * kDv;
+      const float il = 1.f / l;
+#pragma unroll 1
+      for (int cb = 0; cb < kDv; cb += 64) {
+        float w[64];
+        tmem_ld64(tmem + t_lane + kTmemO + cb, w);
+        tmem_wait_ld();
+        if (row_ok) {
+#pragma unroll
+          for (int i = 0; i < 64; i += 4)
+            *reinterpret_cast<float4*>(orow + cb + i) = make_float4(w[i] * il, w[i + 1] * il, w[i + 2] * il, w[i + 3] * il);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+std::atomic<unsigned long long> g_flash_attr{0};
+
+}  // namespace
+
+bool tc_prefill_geometry_ok(const Geometry& g) {
+  return g.H == kH && g.Dn == kDn && g.Dr == kDr && g.Dv == kDv && g.Dl >= 64 && g.Dl % 64 == 0 && g.Dl <= 4096;
+}
+
+cudaError_t launch_prefill_tc(const PrefillArgs& a, unsigned int* flags, long long wait_ns, cudaStream_t st) {
+  const Geometry& g = a.g;
+  const int Tk = a.pos_base + a.S;
+  // 1. KV[t, h*448 + j] = sum_l Lc[t, l] kv_b[h*448 + j, l]
+  GemmArgs ga{};
+  ga.a_base = a.Lc;
+  ga.a_ld_z = g.Dl;
+  ga.a_ld_m = g.Dl;
+  ga.b_base = a.kv_b;
+  ga.b_rows = (long long)kH * kDkv;
+  ga.b_cols = g.Dl;
+  ga.b_ld = g.Dl;
+  ga.b_mn_major = 0;
+  ga.b_row0 = 0;
+  ga.b_rows_per_z = 0;
+  ga.b_col0 = 0;
+  ga.c_base = a.kv;
+  ga.c_ld_m = (long long)kH * kDkv;
+  ga.c_ld_z = 0;
+  ga.out_kind = kGemmOutBf16;
+  ga.M = a.B * Tk;
+  ga.N = kH * kDkv;
+  ga.K = g.Dl;
+  ga.Z = 1;
+  ga.flags = flags;
+  ga.wait_ns = wait_ns;
+  cudaError_t e = launch_gemm_tc(ga, false, st);
+  if (e != cudaSuccess) return e;
+  // 2. causal flash attention over the rebuilt keys / values
+  FlashParams fp{};
+  const uint64_t qdims[3] = {(uint64_t)kDq, (uint64_t)kH, (uint64_t)a.B * a.S};
+  const uint64_t qstr[2] = {(uint64_t)kDq * 2, (uint64_t)kH * kDq * 2};
+  const uint32_t qbox[3] = {64, 1, (uint32_t)kQT};
+  if (!make_tmap_3d_bf16(&fp.mQ, a.q, qdims, qstr, qbox) ||
+      !make_tmap_2d_bf16(&fp.mKV, a.kv, (uint64_t)a.B * Tk, (uint64_t)kH * kDkv, (uint64_t)kH * kDkv, kKT, 64) ||
+      !make_tmap_2d_bf16(&fp.mR, a.Rc, (uint64_t)a.B * Tk, kDr, kDr, kKT, 64))
+    return cudaErrorInvalidValue;
+  fp.q = static_cast<const __nv_bfloat16*>(a.q);
+  fp.out = a.out;
+  fp.B = a.B;
+  fp.S = a.S;
+  fp.Tk = Tk;
+  fp.pos_base = a.pos_base;
+  fp.c = g.scale * kLog2e;
+  for (int j = 0; j < kDr / 2; ++j) fp.theta[j] = std::pow(g.rope_base, -2.0 * j / kDr);
+  fp.flags = flags;
+  fp.wait_ns = wait_ns;
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(g_flash_attr.load() & bit)) {
+    e = cudaFuncSetAttribute(flash_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrefillSmem);
+    if (e != cudaSuccess) return e;
+    g_flash_attr.fetch_or(bit);
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((a.S + kQT - 1) / kQT, kH, a.B);
+  cfg.blockDim = dim3(kPThreads);
+  cfg.dynamicSmemBytes = kPrefillSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, flash_kernel, fp);
+}
+
+}  // namespace mla

@@ -216,6 +216,20 @@ def test_prefill_naive(cuda_lib, dtype, dims, S, pos_base):
     assert max_rel_err(to_np(out[0]), ref) < TOL[dtype]
 
 
+def test_prefill_glm_full_size_sampled(cuda_lib):
+    """The chunked-prefill workload at full size (S=2048 new tokens at pos_base=8192,
+    Tk=10240): every output computed on the GPU, sampled (query, head) pairs checked."""
+    x = workload_inputs("glm_prefill_s2048", DEV)
+    out = to_np(cuda_lib.prefill_naive(x["q"], x["Lc"], x["Rc"], x["kv_b"], GLM, x["pos_base"]))
+    assert cuda_lib.device_status() == 0
+    assert np.all(np.isfinite(out))
+    queries, heads = [0, 1, 127, 128, 1000, 2047], [0, 17, 63]
+    ref = oracle.prefill_nonabsorbed(to_np(x["q"][0]), to_np(x["Lc"][0]), to_np(x["Rc"][0]), to_np(x["kv_b"]),
+                                     GLM.qk_nope, GLM.softmax_scale, x["pos_base"], queries=queries, heads=heads)
+    got = out[0][np.ix_(queries, heads)]
+    assert max_rel_err(got, ref[np.ix_(queries, heads)]) < TOL["bf16"]
+
+
 def test_prefill_equals_decode_on_gpu(cuda_lib):
     """Absorbed decode and non-absorbed prefill of the same block agree ([MLA-KV] §2.3)."""
     S, pos_base = 6, 500
