@@ -12,23 +12,29 @@ namespace mla {
 namespace {
 
 // ---------------------------------------------------------------------------
-// Index scores.  CTA = (token tile of kTile keys, s, b).  The key tile is
-// staged in shared memory with coalesced loads; each thread then owns one key
-// and half of the index heads.
+// Index scores.  CTA = (128 keys, s, b), 256 threads.  The key tile (fp32,
+// rows padded to 132 floats) and the query block sit in shared memory.  Warp
+// w owns index heads 4w..4w+3 (broadcast reads); lane l owns keys l, l+32,
+// l+64, l+96 (consecutive lanes hit consecutive rows: no bank conflicts), so
+// every float4 of keys and of queries feeds 64 FMAs.  The eight head groups
+// meet in shared memory and are summed in a fixed order.
+// General head counts / widths fall back to a plain one-key-per-thread loop.
 // ---------------------------------------------------------------------------
 constexpr int kIdxThreads = 256;
 constexpr int kTile = 128;
+constexpr int kKPitch = 132;  // floats per staged key row
 
+template <bool kFast>
 __global__ void __launch_bounds__(kIdxThreads) index_scores_kernel(IndexArgs a) {
   const int tile = blockIdx.x, s = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int hd = a.hd, nh = a.n_ih;
-  const int ld = hd + 1;  // padded row: thread i reads bank (i + d) % 32
-  extern __shared__ float sm[];
-  float* qs = sm;                     // [nh][hd]
-  float* ws = qs + nh * hd;           // [nh]
-  float* ks = ws + nh;                // [kTile][hd + 1]
-  float* part = ks + kTile * ld;      // [2][kTile]
+  extern __shared__ __align__(16) float sm[];
+  float* qs = sm;                       // [nh][hd]
+  float* ws = qs + nh * hd;             // [nh] (padded to 4)
+  float* ks = ws + ((nh + 3) & ~3);     // [kTile][kKPitch]  (fast path) or [kTile][hd + 1]
+  const int ld = kFast ? kKPitch : hd + 1;
+  float* part = ks + kTile * ld;        // [8][kTile]
 
   const int Tb = a.T[b];
   const int t0 = tile * kTile;
@@ -49,27 +55,87 @@ __global__ void __launch_bounds__(kIdxThreads) index_scores_kernel(IndexArgs a) 
   for (int i = tid; i < nh * hd; i += kIdxThreads) qs[i] = qsrc[i];
   for (int i = tid; i < nh; i += kIdxThreads) ws[i] = a.w[((size_t)b * a.S + s) * nh + i];
   const float* Ic = a.Ic + (size_t)b * a.T_cap * hd;
-  // Stage keys t0 .. t0+kTile-1 that are <= pos (others are zero; never read past pos).
-  for (int e = tid; e < kTile * hd; e += kIdxThreads) {
-    int i = e / hd, d = e - i * hd;
-    int t = t0 + i;
-    ks[i * ld + d] = (t <= pos) ? Ic[(size_t)t * hd + d] : 0.f;
+  const int nvalid = min(kTile, pos + 1 - t0);  // keys t0 .. t0+nvalid-1 are <= pos
+  if (kFast) {
+    // 128 rows x 32 float4; every load is issued before the first store
+    float4 v[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int e = tid + u * kIdxThreads, i = e >> 5, c4 = e & 31;
+      v[u] = i < nvalid ? __ldg(reinterpret_cast<const float4*>(Ic + (size_t)(t0 + i) * 128) + c4)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int e = tid + u * kIdxThreads, i = e >> 5, c4 = e & 31;
+      *reinterpret_cast<float4*>(ks + i * kKPitch + 4 * c4) = v[u];
+    }
+  } else {
+    for (int e = tid; e < kTile * hd; e += kIdxThreads) {
+      const int i = e / hd, d = e - i * hd;
+      ks[i * ld + d] = i < nvalid ? Ic[(size_t)(t0 + i) * hd + d] : 0.f;
+    }
   }
   __syncthreads();
-  const int i = tid % kTile, grp = tid / kTile;  // two head groups
-  float acc = 0.f;
-  for (int h = grp; h < nh; h += 2) {
-    const float* qh = qs + h * hd;
-    const float* kr = ks + i * ld;
-    float dot = 0.f;
-    for (int d = 0; d < hd; ++d) dot = fmaf(qh[d], kr[d], dot);
-    acc = fmaf(ws[h], fmaxf(dot, 0.f), acc);
-  }
-  part[grp * kTile + i] = acc;
-  __syncthreads();
-  if (tid < kTile) {
-    int t = t0 + tid;
-    if (t < a.T_cap) srow[t] = (t <= pos) ? part[tid] + part[kTile + tid] : -INFINITY;
+  if (kFast) {
+    // 32 index heads x 128 dims: warp w -> heads 4w..4w+3, lane -> keys lane + 32i
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    const float* q0 = qs + (4 * warp) * 128;
+    const float* k0 = ks + lane * kKPitch;
+#pragma unroll 4
+    for (int d = 0; d < 128; d += 4) {
+      float4 kv[4], qv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) kv[i] = *reinterpret_cast<const float4*>(k0 + 32 * i * kKPitch + d);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) qv[j] = *reinterpret_cast<const float4*>(q0 + j * 128 + d);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float x = acc[i][j];
+          x = fmaf(qv[j].x, kv[i].x, x);
+          x = fmaf(qv[j].y, kv[i].y, x);
+          x = fmaf(qv[j].z, kv[i].z, x);
+          x = fmaf(qv[j].w, kv[i].w, x);
+          acc[i][j] = x;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float sc = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sc = fmaf(ws[4 * warp + j], fmaxf(acc[i][j], 0.f), sc);
+      part[warp * kTile + lane + 32 * i] = sc;
+    }
+    __syncthreads();
+    if (tid < kTile) {
+      float sc = 0.f;
+#pragma unroll
+      for (int w8 = 0; w8 < 8; ++w8) sc += part[w8 * kTile + tid];
+      const int t = t0 + tid;
+      if (t < a.T_cap) srow[t] = (t <= pos) ? sc : -INFINITY;
+    }
+  } else {
+    const int i = tid % kTile, grp = tid / kTile;  // two head groups
+    float acc = 0.f;
+    for (int h = grp; h < nh; h += 2) {
+      const float* qh = qs + h * hd;
+      const float* kr = ks + i * ld;
+      float dot = 0.f;
+      for (int d = 0; d < hd; ++d) dot = fmaf(qh[d], kr[d], dot);
+      acc = fmaf(ws[h], fmaxf(dot, 0.f), acc);
+    }
+    part[grp * kTile + i] = acc;
+    __syncthreads();
+    if (tid < kTile) {
+      const int t = t0 + tid;
+      if (t < a.T_cap) srow[t] = (t <= pos) ? part[tid] + part[kTile + tid] : -INFINITY;
+    }
   }
 }
 
@@ -108,16 +174,59 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* red, int* total)
   return before;
 }
 
+constexpr int kCand = 16384;  // candidate keys of the threshold bin kept in shared memory
+
+// Finds, among the keys k with (k & mask) == prefix, the digit d (of the
+// `nbins` digits at `shift`) holding the remaining-th largest key.  hist[]
+// holds the digit histogram.  Returns the new prefix; *remaining becomes the
+// rank inside that digit.  Called by all threads; uses red[] for the scan.
+__device__ __forceinline__ uint32_t pick_digit(const int* hist, int nbins, int shift, uint32_t prefix,
+                                               int* remaining, int* red, uint32_t* sh_prefix, int* sh_rem) {
+  // suffix counts from the top bin down: thread i owns bins nbins-1-2i and nbins-2-2i
+  const int tid = threadIdx.x;
+  const int per = nbins / kTopkThreads;  // 1 or 2
+  int c = 0;
+  for (int u = 0; u < per; ++u) c += hist[nbins - 1 - (tid * per + u)];
+  int tot;
+  const int before = block_exclusive_scan(c, red, &tot);  // keys in higher bins than my group
+  const int need = *remaining;
+  if (before < need && before + c >= need) {
+    int cum = before;
+    for (int u = 0; u < per; ++u) {
+      const int bin = nbins - 1 - (tid * per + u);
+      if (cum + hist[bin] >= need) {
+        *sh_prefix = prefix | ((uint32_t)bin << shift);
+        *sh_rem = need - cum;
+        break;
+      }
+      cum += hist[bin];
+    }
+  }
+  __syncthreads();
+  *remaining = *sh_rem;
+  const uint32_t np = *sh_prefix;
+  __syncthreads();
+  return np;
+}
+
+// Top-k.  One CTA per (b, s).  (1) histogram of the top 11 bits of the
+// ordered keys (one pass over the scores); (2) the keys of the bin holding
+// the k-th largest go to shared memory; (3) radix select of their low 21 bits
+// there (11 + 10 bits) gives the exact k-th largest key K and how many keys
+// equal to K are kept; (4) an index-ordered compaction writes the kept keys in
+// ascending order, equal keys from the lowest index up.  A threshold bin with
+// more than kCand keys falls back to 8-bit radix passes over global memory.
 __global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(TopkArgs a) {
   const int row = blockIdx.x;
   const int b = row / a.S, s = row - b * a.S;
   const int tid = threadIdx.x;
   const int k = a.topk;
   int32_t* sel = a.sel + (size_t)row * k;
-  __shared__ int hist[256];
+  __shared__ int hist[2048];
   __shared__ int red[32];
   __shared__ uint32_t sh_prefix;
-  __shared__ int sh_remaining;
+  __shared__ int sh_rem, sh_cnt;
+  extern __shared__ uint32_t cand[];  // [kCand]
 
   const int Tb = a.T[b];
   if (Tb < a.S || Tb > a.T_cap) {
@@ -135,53 +244,86 @@ __global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(TopkArgs a) {
     return;
   }
   const float* sc = a.scores + (size_t)row * a.T_cap;
-  uint32_t prefix = 0, mask = 0;
   int remaining = k;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
-    __syncthreads();
-    for (int t = tid; t < n; t += kTopkThreads) {
-      uint32_t key = ordered_key(sc[t]);
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
+  uint32_t prefix;
+  // (1) top 11 bits
+  for (int i = tid; i < 2048; i += kTopkThreads) hist[i] = 0;
+  if (tid == 0) sh_cnt = 0;
+  __syncthreads();
+  for (int t = tid; t < n; t += kTopkThreads) atomicAdd(&hist[ordered_key(sc[t]) >> 21], 1);
+  __syncthreads();
+  prefix = pick_digit(hist, 2048, 21, 0u, &remaining, red, &sh_prefix, &sh_rem);
+  // (2) candidates of that bin
+  for (int t = tid; t < n; t += kTopkThreads) {
+    const uint32_t key = ordered_key(sc[t]);
+    if ((key >> 21) == (prefix >> 21)) {
+      const int at = atomicAdd(&sh_cnt, 1);
+      if (at < kCand) cand[at] = key;
     }
+  }
+  __syncthreads();
+  const int ncand = sh_cnt;
+  if (ncand <= kCand) {
+    // (3) bits 20..10, then 9..0, on the candidates
+    for (int i = tid; i < 2048; i += kTopkThreads) hist[i] = 0;
     __syncthreads();
-    if (tid == 0) {
-      int cum = 0, d = 255;
-      for (; d > 0; --d) {
-        if (cum + hist[d] >= remaining) break;
-        cum += hist[d];
+    for (int i = tid; i < ncand; i += kTopkThreads) atomicAdd(&hist[(cand[i] >> 10) & 2047u], 1);
+    __syncthreads();
+    prefix = pick_digit(hist, 2048, 10, prefix, &remaining, red, &sh_prefix, &sh_rem);
+    for (int i = tid; i < 1024; i += kTopkThreads) hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < ncand; i += kTopkThreads)
+      if ((cand[i] >> 10) == (prefix >> 10)) atomicAdd(&hist[cand[i] & 1023u], 1);
+    __syncthreads();
+    prefix = pick_digit(hist, 1024, 0, prefix, &remaining, red, &sh_prefix, &sh_rem);
+  } else {
+    // fallback: 8-bit digits 20..13, 12..5, 4..0 over global memory
+    uint32_t mask = 0xFFE00000u;
+    const int shifts[3] = {13, 5, 0}, widths[3] = {8, 8, 5};
+    for (int pass = 0; pass < 3; ++pass) {
+      const int sh = shifts[pass], nb = 1 << widths[pass];
+      for (int i = tid; i < 2048; i += kTopkThreads) hist[i] = 0;
+      __syncthreads();
+      for (int t = tid; t < n; t += kTopkThreads) {
+        const uint32_t key = ordered_key(sc[t]);
+        if ((key & mask) == prefix) atomicAdd(&hist[(key >> sh) & (uint32_t)(nb - 1)], 1);
       }
-      sh_prefix = prefix | ((uint32_t)d << shift);
-      sh_remaining = remaining - cum;
+      __syncthreads();
+      if (tid == 0) {  // small histograms: serial scan from the top
+        int cum = 0, d = nb - 1;
+        for (; d > 0; --d) {
+          if (cum + hist[d] >= remaining) break;
+          cum += hist[d];
+        }
+        sh_prefix = prefix | ((uint32_t)d << sh);
+        sh_rem = remaining - cum;
+      }
+      __syncthreads();
+      prefix = sh_prefix;
+      remaining = sh_rem;
+      mask |= (uint32_t)(nb - 1) << sh;
+      __syncthreads();
     }
-    __syncthreads();
-    prefix = sh_prefix;
-    remaining = sh_remaining;
-    mask |= 255u << shift;
-    __syncthreads();
   }
   // prefix = key of the k-th largest score; `remaining` keys equal to it are kept.
+  // (4) ordered compaction over contiguous segments
   const int seg = (n + kTopkThreads - 1) / kTopkThreads;
   const int ta = min(n, tid * seg), tb = min(n, ta + seg);
-  int n_eq = 0;
-  for (int t = ta; t < tb; ++t) n_eq += (ordered_key(sc[t]) == prefix);
+  int n_eq = 0, n_gt = 0;
+  for (int t = ta; t < tb; ++t) {
+    const uint32_t key = ordered_key(sc[t]);
+    n_eq += key == prefix;
+    n_gt += key > prefix;
+  }
   int tot;
   const int eq_before = block_exclusive_scan(n_eq, red, &tot);
-  int n_sel = 0;
-  {
-    int eq_rank = eq_before;
-    for (int t = ta; t < tb; ++t) {
-      uint32_t key = ordered_key(sc[t]);
-      if (key > prefix) ++n_sel;
-      else if (key == prefix) n_sel += (eq_rank++ < remaining);
-    }
-  }
-  const int out_before = block_exclusive_scan(n_sel, red, &tot);
+  const int n_take_eq = max(0, min(n_eq, remaining - eq_before));
+  const int out_before = block_exclusive_scan(n_gt + n_take_eq, red, &tot);
   {
     int eq_rank = eq_before, o = out_before;
     for (int t = ta; t < tb; ++t) {
-      uint32_t key = ordered_key(sc[t]);
-      bool take = (key > prefix) || (key == prefix && eq_rank++ < remaining);
+      const uint32_t key = ordered_key(sc[t]);
+      const bool take = (key > prefix) || (key == prefix && eq_rank++ < remaining);
       if (take) sel[o++] = t;
     }
   }
@@ -192,19 +334,24 @@ __global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(TopkArgs a) {
 }  // namespace
 
 cudaError_t launch_index_scores(const IndexArgs& a, cudaStream_t st) {
-  size_t smem = sizeof(float) * ((size_t)a.n_ih * a.hd + a.n_ih + (size_t)kTile * (a.hd + 1) + 2 * kTile);
+  const bool fast = a.n_ih == 32 && a.hd == 128;
+  const int ld = fast ? kKPitch : a.hd + 1;
+  size_t smem = sizeof(float) * ((size_t)a.n_ih * a.hd + ((a.n_ih + 3) & ~3) + (size_t)kTile * ld + 8 * kTile);
+  auto kern = fast ? index_scores_kernel<true> : index_scores_kernel<false>;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(index_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
   dim3 grid((a.T_cap + kTile - 1) / kTile, a.S, a.B);
-  index_scores_kernel<<<grid, kIdxThreads, smem, st>>>(a);
+  kern<<<grid, kIdxThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_topk_select(const TopkArgs& a, cudaStream_t st) {
-  topk_select_kernel<<<a.B * a.S, kTopkThreads, 0, st>>>(a);
+  const int smem = kCand * 4;
+  cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  topk_select_kernel<<<a.B * a.S, kTopkThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 

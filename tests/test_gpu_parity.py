@@ -144,6 +144,23 @@ def test_topk_ties_and_negative_zero(cuda_lib):
     assert np.array_equal(sel.cpu().numpy(), rsel) and np.array_equal(nsel.cpu().numpy(), rn)
 
 
+@pytest.mark.parametrize("lo,hi,T", [(1.0, 1.25, [40000, 39000]), (1.0, 1.25, [9000]), (-3.0, 5.0, [65536])])
+def test_topk_crowded_and_spread_scores(cuda_lib, lo, hi, T):
+    """Scores in [1, 1.25) share their top 11 key bits: more than 16384 of them
+    overflow the in-smem candidate list (fallback passes); fewer stay in smem."""
+    r = np.random.default_rng(9)
+    T_cap = max(T)
+    k = 2048
+    sc = r.uniform(lo, hi, (len(T), 1, T_cap)).astype(np.float32)
+    sc[0, 0, 100:140] = sc[0, 0, 7]  # exact ties across the threshold region
+    g = torch.from_numpy(sc).to(DEV)
+    Tt = torch.tensor(T, dtype=torch.int32, device=DEV)
+    sel, nsel = cuda_lib.topk_select(g, Tt, k)
+    rsel, rn = oracle.topk_select(sc.astype(np.float64), T, 1, k)
+    assert np.array_equal(nsel.cpu().numpy(), rn)
+    assert np.array_equal(sel.cpu().numpy(), rsel)
+
+
 def test_dsa_glm_t65536_pipeline(cuda_lib):
     """B=4, T=65536: indexer and top-2048 bit-exact, sparse decode within 2e-2 on every output."""
     x = workload_inputs("glm_dsa_t65536", DEV)
