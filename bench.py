@@ -1,17 +1,22 @@
 """Benchmark of the MLA latent-KV hot path on GB300 (one JSON line on rank 0).
 
-Default workload: GLM-5.2-shaped single-sequence absorbed decode, B=1, S=1,
+Headline workload: GLM-5.2-shaped single-sequence absorbed decode, B=1, S=1,
 T=4096 (bf16 cache, fp32 accumulate).  One step = one mla_decode_absorbed
 call (query RoPE, absorb through W_UK, scores over Lc/Rc, softmax, latent
 context, W_UV lift).  L2 is flushed (256 MiB write) before every timed step,
-outside the timed interval, because the step's inputs fit in L2.
+outside the timed interval, because the step's inputs fit in L2.  The timed
+steps replay a CUDA graph of the API call; a second, instrumented replay
+records CUDA events between the library's kernels (mla_set_kernel_events) to
+attribute time per kernel, and the roofline object describes the dominant
+kernel.
 
-Other workloads (--workload): glm_decode_t<T>, glm_batched_b32_s1,
-glm_batched_b32_s6, glm_dsa_t65536 (indexer + top-2048 + sparse decode),
-glm_prefill_s2048 (non-absorbed prefill).
+The default run also measures the other workloads of the hot path ("rows"):
+batched decode B=32 with S=1 and S=6, DSA (indexer + top-2048 + sparse
+decode) at B=4, T=65536, and the non-absorbed prefill S=2048 at pos_base=8192,
+plus the T sweep 4k..64k of the headline metric.
 
-Multi-GPU (torchrun): replicas only -- every rank runs the same workload on
-its own GPU, no collective on the data path; value = all ranks' tokens / the
+Multi-GPU (torchrun): replicas -- every rank runs the same workload on its own
+GPU with no collective on the data path; value = all ranks' tokens / the
 slowest rank's time (weak scaling).
 
 --impl reference times the fp64 CPU oracle on the host cores on a bounded
@@ -35,23 +40,23 @@ METRIC = "MLA decode tokens/s and latent-cache HBM GB/s (% roofline) at T=4k–6
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
+ROW_WORKLOADS = ("glm_batched_b32_s1", "glm_batched_b32_s6", "glm_dsa_t65536", "glm_prefill_s2048")
 
 
 def peaks():
     try:
         with open(PEAKS_FILE) as f:
-            p = json.load(f)
-        return p, "measured"
+            return json.load(f), "measured"
     except OSError:
         return FALLBACK, "fallback"
 
 
 # ------------------------------------------------------------------ workloads
 def build_workload(name, device):
-    """Inputs + a closure running one step + the step's algorithmic accounting."""
+    """Inputs, the step as a list of API calls, and per-kernel algorithmic work."""
     import torch
     import mla_latent_kv_06_gb300 as mla
-    from workload import GLM, WORKLOADS, mla_inputs, workload_inputs, SEED_BASE
+    from workload import GLM, mla_inputs, workload_inputs, SEED_BASE
 
     if name.startswith("glm_decode_t"):
         T = int(name[len("glm_decode_t"):])
@@ -62,8 +67,7 @@ def build_workload(name, device):
             x.update(mla_inputs(GLM, 1, 1, [T], T, "bf16", SEED_BASE + 1, device))
         kind = "decode"
     elif name.startswith("glm_batched_b32_s"):
-        S = int(name[len("glm_batched_b32_s"):])
-        x = workload_inputs("glm_batched_b32", device, S=S)
+        x = workload_inputs("glm_batched_b32", device, S=int(name[len("glm_batched_b32_s"):]))
         kind = "decode"
     elif name == "glm_dsa_t65536":
         x = workload_inputs(name, device)
@@ -74,81 +78,76 @@ def build_workload(name, device):
     else:
         raise SystemExit(f"unknown workload {name}")
 
-    dims = x["dims"]
+    d = x["dims"]
     B, S = x["B"], x["S"]
+    R = B * S
     T_list = x["T_list"]
-    tokens = B * S
-    w_bytes = 2 * dims.H * (dims.qk_nope + dims.v_head) * dims.kv_lora
-    row = 2 * (dims.kv_lora + dims.qk_rope)
-    q_bytes = 2 * B * S * dims.H * dims.qk_head
-    out_bytes = 4 * B * S * dims.H * dims.v_head
-    acct = {"tokens": tokens}
-    out = torch.empty(B, S, dims.H, dims.v_head, dtype=torch.float32, device=device)
+    row = 2 * (d.kv_lora + d.qk_rope)                      # latent-cache bytes per key
+    w_uk = 2 * d.H * d.qk_nope * d.kv_lora
+    w_uv = 2 * d.H * d.v_head * d.kv_lora
+    q_bytes = 2 * R * d.H * d.qk_head
+    out_bytes = 4 * R * d.H * d.v_head
+    qcat = 2 * R * d.H * (d.kv_lora + d.qk_rope)
+    out = torch.empty(B, S, d.H, d.v_head, dtype=torch.float32, device=device)
+    info = {"tokens": R, "B": B, "S": S, "T_list": T_list}
 
     if kind == "decode":
-        need = mla.decode_workspace_size(dims, mla.MLA_BF16, B, S, x["T_cap"])
+        need = mla.decode_workspace_size(d, mla.MLA_BF16, B, S, x["T_cap"])
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
-
-        def step():
-            mla.decode_absorbed(x["q"], x["Lc"], x["Rc"], x["T"], x["kv_b"], dims, out=out, workspace=ws)
-
-        cache = row * sum(T_list)
-        acct.update(cache_bytes=cache, alg_bytes=cache + w_bytes + q_bytes + out_bytes + 4 * B,
-                    flops=2 * dims.H * sum(sum(T - S + s + 1 for s in range(S)) * (dims.kv_lora * 2 + dims.qk_rope)
-                                           for T in T_list)
-                    + 2 * dims.H * B * S * (dims.qk_nope + dims.v_head) * dims.kv_lora,
-                    bound="hbm", kernels_per_step=mla_kernels_per_call("decode", dims, B, S))
+        calls = [lambda: mla.decode_absorbed(x["q"], x["Lc"], x["Rc"], x["T"], x["kv_b"], d, out=out, workspace=ws)]
+        cache = row * sum(T_list)  # every cached key read once per sequence
+        info.update(cache_bytes=cache, alg_bytes=cache + w_uk + w_uv + q_bytes + out_bytes)
+        clat = 2 * R * d.H * d.kv_lora
+        work = {"absorb": ("hbm", w_uk + q_bytes), "absorb_gemm": ("hbm", w_uk + q_bytes + qcat),
+                "plan_rope": ("hbm", q_bytes), "attention": ("hbm", cache + qcat),
+                "combine": ("hbm", w_uv + out_bytes), "merge": ("hbm", clat),
+                "up_gemm": ("hbm", w_uv + clat + out_bytes)}
         e2e = dict(inputs=[x["q"], x["T"]], run=lambda q, T: mla.decode_absorbed(
-            q, x["Lc"], x["Rc"], T, x["kv_b"], dims, out=out, workspace=ws), out=out)
+            q, x["Lc"], x["Rc"], T, x["kv_b"], d, out=out, workspace=ws), out=out)
     elif kind == "dsa":
         k = x["topk"]
-        sc = torch.empty(B, S, x["T_cap"], dtype=torch.float32, device=device)
+        T_cap = x["T_cap"]
+        sc = torch.empty(B, S, T_cap, dtype=torch.float32, device=device)
         sel = torch.empty(B, S, k, dtype=torch.int32, device=device)
         nsel = torch.empty(B, S, dtype=torch.int32, device=device)
-        need = mla.lib().mla_sparse_decode_workspace_size(
-            mla.ctypes.byref(mla.make_dims(dims)), mla.MLA_BF16, B, S, k)
+        need = mla.lib().mla_sparse_decode_workspace_size(mla.ctypes.byref(mla.make_dims(d)), mla.MLA_BF16, B, S, k)
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
-
-        def step():
-            mla.index_scores(x["q_idx"], x["w"], x["Ic"], x["T"], out=sc)
-            mla.topk_select(sc, x["T"], k, sel=sel, nsel=nsel)
-            mla.sparse_decode(x["q"], x["Lc"], x["Rc"], x["T"], x["kv_b"], sel, nsel, dims, out=out,
-                              workspace=ws)
-
-        ic_bytes = 4 * x["Ic"].shape[2] * sum(T_list)
-        gathered = row * B * S * k
-        acct.update(cache_bytes=gathered, alg_bytes=ic_bytes + 2 * 4 * B * S * x["T_cap"] + gathered + w_bytes
-                    + q_bytes + out_bytes, flops=0, bound="hbm",
-                    kernels_per_step=2 + mla_kernels_per_call("sparse", dims, B, S))
-        e2e = dict(inputs=[x["q"], x["q_idx"], x["w"], x["T"]], run=None, out=out)
+        calls = [lambda: mla.index_scores(x["q_idx"], x["w"], x["Ic"], x["T"], out=sc),
+                 lambda: mla.topk_select(sc, x["T"], k, sel=sel, nsel=nsel),
+                 lambda: mla.sparse_decode(x["q"], x["Lc"], x["Rc"], x["T"], x["kv_b"], sel, nsel, d, out=out,
+                                           workspace=ws)]
+        ic = 4 * x["Ic"].shape[2] * sum(T_list)
+        scores = 4 * R * T_cap
+        gathered = row * R * k
+        clat = 2 * R * d.H * d.kv_lora
+        info.update(cache_bytes=gathered, alg_bytes=ic + 2 * scores + gathered + w_uk + w_uv + q_bytes + out_bytes)
+        work = {"index_scores": ("hbm", ic + scores), "topk_select": ("hbm", scores + 4 * R * k),
+                "gather": ("hbm", 2 * gathered), "absorb": ("hbm", w_uk + q_bytes),
+                "attention": ("hbm", gathered + qcat), "combine": ("hbm", w_uv + out_bytes),
+                "absorb_gemm": ("hbm", w_uk + q_bytes + qcat), "plan_rope": ("hbm", q_bytes),
+                "merge": ("hbm", clat), "up_gemm": ("hbm", w_uv + clat + out_bytes)}
+        e2e = None
     else:
         pos_base = x["pos_base"]
-        need = mla.lib().mla_prefill_naive_workspace_size(
-            mla.ctypes.byref(mla.make_dims(dims)), mla.MLA_BF16, B, S, pos_base)
+        need = mla.lib().mla_prefill_naive_workspace_size(mla.ctypes.byref(mla.make_dims(d)), mla.MLA_BF16, B, S,
+                                                           pos_base)
         ws = torch.empty(need, dtype=torch.uint8, device=device)
-
-        def step():
-            mla.prefill_naive(x["q"], x["Lc"], x["Rc"], x["kv_b"], dims, pos_base, out=out, workspace=ws)
-
+        calls = [lambda: mla.prefill_naive(x["q"], x["Lc"], x["Rc"], x["kv_b"], d, pos_base, out=out, workspace=ws)]
         Tk = pos_base + S
         pairs = sum(pos_base + s + 1 for s in range(S))
-        acct.update(cache_bytes=row * Tk, alg_bytes=row * Tk + w_bytes + q_bytes + out_bytes,
-                    flops=2 * Tk * dims.kv_lora * dims.H * (dims.qk_nope + dims.v_head)
-                    + 2 * dims.H * pairs * (dims.qk_head + dims.v_head),
-                    bound="tensor", kernels_per_step=2)
-        e2e = dict(inputs=[x["q"]], run=None, out=out)
-    return x, step, acct, e2e
-
-
-def mla_kernels_per_call(kind, dims, B, S):
-    """Kernels one API call launches (queried from the library)."""
-    import mla_latent_kv_06_gb300 as mla
-    return mla.kernels_per_call(kind, dims, B, S)
+        gemm_flops = 2 * B * Tk * d.kv_lora * d.H * (d.qk_nope + d.v_head)
+        attn_flops = 2 * B * d.H * pairs * (d.qk_head + d.v_head)
+        info.update(cache_bytes=row * Tk, alg_bytes=row * Tk + w_uk + w_uv + q_bytes + out_bytes,
+                    flops=gemm_flops + attn_flops)
+        work = {"kv_gemm": ("tensor", gemm_flops), "flash_attention": ("tensor", attn_flops)}
+        e2e = dict(inputs=[x["q"]], run=lambda q: mla.prefill_naive(q, x["Lc"], x["Rc"], x["kv_b"], d, pos_base,
+                                                                     out=out, workspace=ws), out=out)
+    return x, calls, info, work, e2e
 
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi clocks/throttle sampling during the timed region."""
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -201,17 +200,19 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ timing
-def graph_of(step, stream):
-    """Capture one step into a CUDA graph (the library's launches, PDL edges included)."""
+def capture(calls, stream):
+    """A CUDA graph of the step's API calls (the library's launches, PDL edges included)."""
     import torch
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
-        step()
+        for c in calls:
+            c()
     torch.cuda.synchronize()
-    return g.replay
+    return g
 
 
 def time_steps(step, K, W, flush, stream):
+    """Device time (ms) of K steps, each after an L2 flush that is not timed."""
     import torch
     for _ in range(W):
         flush.zero_()
@@ -228,6 +229,35 @@ def time_steps(step, K, W, flush, stream):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
+def kernel_times(calls, K, flush, stream):
+    """Per-kernel device time (us) from events the library records around its launches."""
+    import torch
+    import mla_latent_kv_06_gb300 as mla
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in calls]
+    for ev in evs:  # create the CUDA events before the capture
+        for e in ev:
+            e.record(stream)
+    torch.cuda.synchronize()
+    names = []
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for c, ev in zip(calls, evs):
+            mla.set_kernel_events(ev)
+            c()
+            names.append(mla.last_launch_names())
+    mla.set_kernel_events(None)
+    torch.cuda.synchronize()
+    acc = {}
+    for _ in range(K):
+        flush.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for nm, ev in zip(names, evs):
+            for i, n in enumerate(nm):
+                acc.setdefault(n, []).append(ev[i].elapsed_time(ev[i + 1]) * 1e3)
+    return {n: statistics.mean(v) for n, v in acc.items()}
+
+
 def time_e2e(e2e, K, W, flush, stream):
     """Public-API call with host buffers: pinned H2D of the step inputs, the call, D2H of out."""
     import torch
@@ -238,13 +268,47 @@ def time_e2e(e2e, K, W, flush, stream):
     d2h = host_out.numel() * host_out.element_size()
 
     def one():
-        for d, h in zip(dev_in, host_in):
-            d.copy_(h, non_blocking=True)
+        for dd, h in zip(dev_in, host_in):
+            dd.copy_(h, non_blocking=True)
         e2e["run"](*dev_in)
         host_out.copy_(e2e["out"], non_blocking=True)
 
-    ms = time_steps(one, K, W, flush, stream)
-    return ms, h2d, d2h
+    return time_steps(one, K, W, flush, stream), h2d, d2h
+
+
+def roofline(work, ktimes, pk, pk_kind):
+    """Roofline of the kernel with the largest share of the step."""
+    dom = max(ktimes, key=ktimes.get)
+    bound, amount = work.get(dom, ("hbm", 0))
+    t = ktimes[dom] * 1e-6
+    if bound == "tensor":
+        achieved, peak, unit = amount / t / 1e12, pk["bf16_tflops_sustained"], "TFLOP/s"
+    else:
+        achieved, peak, unit = amount / t / 1e9, pk["hbm_gbs"], "GB/s"
+    total = sum(ktimes.values())
+    return {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "peak_source": pk_kind, "algorithmic_per_launch": amount,
+            "kernel_us": ktimes[dom], "traffic": None,
+            "kernels": {n: {"us": round(v, 2), "share": round(v / total, 3)} for n, v in ktimes.items()}}
+
+
+def measure(name, dev, stream, flush, K, W, pk, pk_kind, want_e2e):
+    import torch
+    import mla_latent_kv_06_gb300 as mla
+    x, calls, info, work, e2e = build_workload(name, dev)
+    for c in calls:
+        c()
+    torch.cuda.synchronize()
+    assert mla.device_status() == 0, "device flags raised while warming up"
+    g = capture(calls, stream)
+    ms = time_steps(g.replay, K, W, flush, stream)
+    kt = kernel_times(calls, max(3, min(K, 20)), flush, stream)
+    res = {"ms": ms, "info": info, "ktimes": kt, "roof": roofline(work, kt, pk, pk_kind)}
+    if want_e2e and e2e is not None:
+        res["e2e"] = time_e2e(e2e, K, W, flush, stream)
+    del x, calls, g
+    torch.cuda.empty_cache()
+    return res
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -252,34 +316,8 @@ def oracle_sample(name, budget_s=12.0):
     """Time the fp64 oracle on the host cores on a bounded sample of the workload."""
     import numpy as np
     import oracle
-    from workload import WORKLOADS, GLM, mla_inputs, workload_inputs, SEED_BASE
-
-    x = build_workload_cpu(name)
-    q, Lc, Rc, kvb = (x[k] for k in ("q", "Lc", "Rc", "kv_b"))
-    T_list, S = x["T_list"], x["S"]
-    B = len(T_list)
-    rows = [(b, s) for b in range(B) for s in range(S)]
-    done, t0 = 0, time.perf_counter()
-    while True:
-        b, s = rows[done % len(rows)]
-        pos = T_list[b] - S + s
-        if x["kind"] == "prefill":
-            oracle.prefill_nonabsorbed(q[0], Lc[0], Rc[0], kvb, GLM.qk_nope, GLM.softmax_scale,
-                                       x["pos_base"], queries=[done % S])
-        else:
-            oracle.attend_absorbed(q[b, s], Lc[b, :pos + 1], Rc[b, :pos + 1], kvb, GLM.qk_nope, pos,
-                                   GLM.softmax_scale)
-        done += 1
-        el = time.perf_counter() - t0
-        if el > budget_s or done >= 4 * len(rows):
-            break
-    return done / el, done, el
-
-
-def build_workload_cpu(name):
-    """fp64 numpy copies of a workload's MLA inputs (CPU generator)."""
-    import numpy as np
     from workload import GLM, mla_inputs, workload_inputs, SEED_BASE
+
     if name.startswith("glm_decode_t") and name != "glm_decode_t4096":
         T = int(name[len("glm_decode_t"):])
         x = dict(T_list=[T], S=1)
@@ -289,17 +327,31 @@ def build_workload_cpu(name):
     else:
         x = workload_inputs(name, "cpu")
     f = lambda t: t.float().numpy().astype(np.float64)
-    out = {k: f(x[k]) for k in ("q", "Lc", "Rc", "kv_b")}
-    out.update(T_list=x["T_list"], S=x["S"], kind="prefill" if name == "glm_prefill_s2048" else "decode",
-               pos_base=x.get("pos_base", 0))
-    return out
+    q, Lc, Rc, kvb = (f(x[k]) for k in ("q", "Lc", "Rc", "kv_b"))
+    T_list, S = x["T_list"], x["S"]
+    rows = [(b, s) for b in range(len(T_list)) for s in range(S)]
+    done, t0 = 0, time.perf_counter()
+    while True:
+        b, s = rows[done % len(rows)]
+        pos = T_list[b] - S + s
+        if name == "glm_prefill_s2048":
+            oracle.prefill_nonabsorbed(q[0], Lc[0], Rc[0], kvb, GLM.qk_nope, GLM.softmax_scale, x["pos_base"],
+                                       queries=[done % S])
+        else:
+            oracle.attend_absorbed(q[b, s], Lc[b, :pos + 1], Rc[b, :pos + 1], kvb, GLM.qk_nope, pos,
+                                   GLM.softmax_scale)
+        done += 1
+        el = time.perf_counter() - t0
+        if el > budget_s:
+            break
+    return done / el, done, el
 
 
 def host_threads():
     try:
         from threadpoolctl import threadpool_info
         import numpy  # noqa: F401  (loads BLAS)
-        n = [d.get("num_threads") for d in threadpool_info() if d.get("user_api") == "blas"]
+        n = [dd.get("num_threads") for dd in threadpool_info() if dd.get("user_api") == "blas"]
         if n:
             return int(n[0])
     except Exception:
@@ -316,8 +368,8 @@ def main():
     ap.add_argument("--impl", choices=["mla", "reference"], default="mla")
     ap.add_argument("--workload", default="glm_decode_t4096")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-rows", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--no-graph", action="store_true", help="time plain API calls instead of graph replays")
     args = ap.parse_args()
     W = max(args.warmup, 3)
     K = args.steps
@@ -329,7 +381,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        tok_s, n, el = oracle_sample(args.workload, budget_s=max(5.0, 2.0 * K))
+        tok_s, n, el = oracle_sample(args.workload, budget_s=min(60.0, max(5.0, 2.0 * K)))
         cores = host_threads()
         line = {"impl": "reference", "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": args.gpus,
                 "steps": K, "warmup": W, "ms_per_step": 1e3 / tok_s, "higher_is_better": True,
@@ -349,104 +401,84 @@ def main():
     dev = torch.device(f"cuda:{local}")
     import mla_latent_kv_06_gb300 as mla
     mla.load()
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-
-    x, step, acct, e2e = build_workload(args.workload, dev)
-    for _ in range(2):
-        step()
-    torch.cuda.synchronize()
-    assert mla.device_status() == 0
-    # Timed steps replay a CUDA graph of the step so that host-side launch
-    # cost (ctypes marshalling, tensor-map encoding) stays out of device time;
-    # the e2e figure below goes through the plain API call instead.
-    cap = torch.cuda.Stream(device=dev)
-    cap.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(cap):
-        replay = graph_of(step, cap) if not args.no_graph else step
-    timed_step = replay
-
-    clocks = ClockSampler(local)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    t_wall = time.perf_counter()
-    ms = time_steps(timed_step, K, W, flush, stream)
-    t_wall = time.perf_counter() - t_wall
-    clk = clocks.stop()
-    total_ms = sum(ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-        dist.barrier()
-    ms_per_step = total_ms / K
-    value = world * acct["tokens"] * K / (total_ms / 1e3)
-
     pk, pk_kind = peaks()
-    line = None
-    if rank == 0:
+
+    with torch.cuda.stream(stream):
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        clocks = ClockSampler(local)
+        clocks.start()
+        t_wall = time.perf_counter()
+        res = measure(args.workload, dev, stream, flush, K, W, pk, pk_kind, want_e2e=True)
+        t_wall = time.perf_counter() - t_wall
+        clk = clocks.stop()
+        total_ms = sum(res["ms"])
+        if world > 1:
+            t = torch.tensor([total_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            total_ms = float(t.item())
+            dist.barrier()
+        info = res["info"]
+        ms_per_step = total_ms / K
+        value = world * info["tokens"] * K / (total_ms / 1e3)
         step_s = ms_per_step / 1e3
-        if acct["bound"] == "hbm":
-            achieved = acct["alg_bytes"] / step_s / 1e9
-            peak = pk["hbm_gbs"]
-            unit = "GB/s"
-        else:
-            achieved = acct["flops"] / step_s / 1e12
-            peak = pk["bf16_tflops_sustained"]
-            unit = "TFLOP/s"
-        roof = {"bound": acct["bound"], "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "peak_source": pk_kind,
-                "kernel": "whole step" if acct["kernels_per_step"] > 1 else "the step's one kernel",
-                "alg_bytes_per_launch": acct["alg_bytes"], "traffic": None}
-        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
-                "warmup": W, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": args.workload, "B": x["B"], "S": x["S"],
-                           "T": x["T_list"] if len(x["T_list"]) <= 4 else f"sum {sum(x['T_list'])}",
-                           "heads": 64, "kv_lora": 512, "qk_rope": 64, "qk_nope": 192, "v_head": 256,
-                           "parallelism": f"replicas x{world}",
-                           "l2": "256 MiB flush write before every timed step (outside the timed interval)",
-                           "launch": "plain API calls" if args.no_graph else "CUDA graph replay of one API call"},
-                "latent_cache_gbs": acct["cache_bytes"] / step_s / 1e9,
-                "hbm_gbs_algorithmic": acct["alg_bytes"] / step_s / 1e9,
-                "hbm_frac_of_8tbs": acct["alg_bytes"] / step_s / 8e12,
-                "roofline": roof, "clocks": clk,
-                "gpu_launches": acct["kernels_per_step"] * K,
-                "step_ms_min": min(ms), "step_ms_median": statistics.median(ms),
-                "wall_s_timed_region": t_wall}
-    # end-to-end through the public API with host buffers
-    if e2e.get("run") is not None:
-        ems, h2d, d2h = time_e2e(e2e, K, W, flush, stream)
         if rank == 0:
-            ev = acct["tokens"] * K / (sum(ems) / 1e3) * world
-            line["e2e"] = {"value": ev, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                           "d2h_bytes_per_step": d2h, "ms_per_step": sum(ems) / K}
-    elif rank == 0:
-        line["e2e"] = None
-    # T sweep of the metric (4k..64k) for the decode headline
-    if rank == 0 and args.workload == "glm_decode_t4096" and not args.no_sweep:
-        sweep = {}
-        del x, step
-        for T in (4096, 8192, 16384, 32768, 65536):
-            xs, st_, ac, _ = build_workload(f"glm_decode_t{T}", dev)
-            st_()
-            with torch.cuda.stream(cap):
-                rp = graph_of(st_, cap) if not args.no_graph else st_
-            m = time_steps(rp, 20, 3, flush, stream)
-            t = statistics.median(m) / 1e3
-            sweep[str(T)] = {"tokens_s": 1 / t, "us": t * 1e6, "latent_cache_gbs": ac["cache_bytes"] / t / 1e9,
-                             "hbm_gbs_algorithmic": ac["alg_bytes"] / t / 1e9,
-                             "frac_of_measured_hbm": ac["alg_bytes"] / t / 1e9 / pk["hbm_gbs"]}
-            del xs, st_
-        line["t_sweep"] = sweep
-    if rank == 0 and not args.no_cpu:
-        tok_s, n, el = oracle_sample(args.workload)
-        line["cpu_baseline"] = {"value": tok_s, "unit": "tokens/s", "cores": host_threads(), "kind": "oracle",
-                                "sample": f"{n} query tokens x 64 heads of {args.workload} in {el:.1f} s"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+            T_list = info["T_list"]
+            line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+                    "warmup": W, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                    "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, GLM-5.2-shaped)",
+                    "config": {"workload": args.workload, "B": info["B"], "S": info["S"],
+                               "T": T_list if len(T_list) <= 4 else f"sum {sum(T_list)}",
+                               "heads": 64, "kv_lora": 512, "qk_rope": 64, "qk_nope": 192, "v_head": 256,
+                               "parallelism": f"replicas x{world}",
+                               "l2": "256 MiB flush write before every timed step (outside the timed interval)",
+                               "launch": "CUDA graph replay of one API call"},
+                    "latent_cache_gbs": info["cache_bytes"] / step_s / 1e9,
+                    "hbm_gbs_algorithmic": info["alg_bytes"] / step_s / 1e9,
+                    "step_frac_of_measured_hbm": info["alg_bytes"] / step_s / 1e9 / pk["hbm_gbs"],
+                    "step_frac_of_8tbs": info["alg_bytes"] / step_s / 8e12,
+                    "roofline": res["roof"], "clocks": clk,
+                    "gpu_launches": len(res["ktimes"]) * K,
+                    "step_ms_min": min(res["ms"]), "step_ms_median": statistics.median(res["ms"]),
+                    "wall_s_timed_region": t_wall}
+            if "e2e" in res:
+                ems, h2d, d2h = res["e2e"]
+                line["e2e"] = {"value": info["tokens"] * K / (sum(ems) / 1e3) * world, "unit": "tokens/s",
+                               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": sum(ems) / K}
+            else:
+                line["e2e"] = None
+            if args.workload == "glm_decode_t4096" and not args.no_sweep:
+                sweep = {}
+                for T in (4096, 8192, 16384, 32768, 65536):
+                    r = measure(f"glm_decode_t{T}", dev, stream, flush, 20, 3, pk, pk_kind, want_e2e=False)
+                    t = statistics.median(r["ms"]) / 1e3
+                    sweep[str(T)] = {"tokens_s": 1 / t, "us": t * 1e6,
+                                     "latent_cache_gbs": r["info"]["cache_bytes"] / t / 1e9,
+                                     "hbm_gbs_algorithmic": r["info"]["alg_bytes"] / t / 1e9,
+                                     "frac_of_measured_hbm": r["info"]["alg_bytes"] / t / 1e9 / pk["hbm_gbs"],
+                                     "dominant": r["roof"]["kernel"]}
+                line["t_sweep"] = sweep
+            if args.workload == "glm_decode_t4096" and not args.no_rows:
+                rows = {}
+                for wl in ROW_WORKLOADS:
+                    r = measure(wl, dev, stream, flush, 10, 3, pk, pk_kind, want_e2e=False)
+                    t = statistics.median(r["ms"]) / 1e3
+                    rows[wl] = {"us_per_step": t * 1e6, "tokens_s": r["info"]["tokens"] / t,
+                                "hbm_gbs_algorithmic": r["info"]["alg_bytes"] / t / 1e9,
+                                "roofline": {k: r["roof"][k] for k in ("kernel", "bound", "achieved", "unit", "frac",
+                                                                       "kernels")}}
+                    if "flops" in r["info"]:
+                        rows[wl]["tflops"] = r["info"]["flops"] / t / 1e12
+                line["rows"] = rows
+            if not args.no_cpu:
+                tok_s, n, el = oracle_sample(args.workload)
+                line["cpu_baseline"] = {"value": tok_s, "unit": "tokens/s", "cores": host_threads(),
+                                        "kind": "oracle",
+                                        "sample": f"{n} query tokens x 64 heads of {args.workload} in {el:.1f} s"}
+            print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()

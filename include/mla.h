@@ -78,6 +78,18 @@ int mla_abi_version(void);
  * MLA_ERR_CUDA. */
 int mla_device_status(void* stream, int* flags);
 
+/* Optional per-kernel timing.  While set on the calling thread, every later
+ * mla_* / dsa_* call records events[i] on its stream just before launching
+ * its i-th kernel and, after its last kernel, one more event (so a call with n
+ * kernels uses events[0..n]; it records no more than `count`).  `events` are
+ * caller-owned cudaEvent_t handles; the array must stay valid while set.
+ * Pass NULL, 0 to switch it off.  Returns MLA_OK. */
+int mla_set_kernel_events(void* const* events, int count);
+
+/* Comma-separated names of the kernels launched by the last call on this
+ * thread, in launch order (for example "absorb,attention,combine"). */
+const char* mla_last_launch_names(void);
+
 /* Limit of every bounded wait inside the kernels, in nanoseconds of
  * %globaltimer (default 2e9).  Host-side setting, read at each launch. */
 void mla_set_wait_limit_ns(long long ns);

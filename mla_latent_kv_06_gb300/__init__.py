@@ -22,6 +22,7 @@ MLA_DEV_BAD_LENGTH, MLA_DEV_BAD_INDEX, MLA_DEV_TIMEOUT = 1, 2, 4
 # Every symbol declared in include/mla.h.
 EXPORTS = (
     "mla_last_error", "mla_abi_version", "mla_device_status", "mla_set_wait_limit_ns",
+    "mla_set_kernel_events", "mla_last_launch_names",
     "mla_decode_absorbed_workspace_size", "mla_decode_absorbed", "mla_decode_launch_count",
     "mla_sparse_decode_workspace_size", "mla_sparse_decode",
     "mla_prefill_naive_workspace_size", "mla_prefill_naive", "mla_prefill_naive_noalloc",
@@ -55,6 +56,8 @@ def _declare(lib: ctypes.CDLL) -> None:
         "mla_abi_version": (_I, []),
         "mla_device_status": (_I, [_P, ctypes.POINTER(_I)]),
         "mla_set_wait_limit_ns": (None, [ctypes.c_longlong]),
+        "mla_set_kernel_events": (_I, [ctypes.POINTER(ctypes.c_void_p), _I]),
+        "mla_last_launch_names": (ctypes.c_char_p, []),
         "mla_decode_absorbed_workspace_size": (_SZ, [_DP, _I, _I, _I, _I]),
         "mla_decode_launch_count": (_I, [_DP, _I, _I, _I, _I]),
         "mla_decode_absorbed": (_I, [_DP, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _P, _SZ, _P]),
@@ -154,6 +157,29 @@ def device_status(stream=None) -> int:
 
 def set_wait_limit_ns(ns: int) -> None:
     lib().mla_set_wait_limit_ns(int(ns))
+
+
+_event_array = None
+
+
+def set_kernel_events(events) -> None:
+    """Record these torch.cuda.Event objects around the kernels of every later
+    call on this thread (see mla_set_kernel_events); None switches it off."""
+    global _event_array
+    if not events:
+        _event_array = None
+        lib().mla_set_kernel_events(None, 0)
+        return
+    for e in events:
+        if not e.cuda_event:
+            e.record()  # torch creates the CUDA event lazily
+    _event_array = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    lib().mla_set_kernel_events(_event_array, len(events))
+
+
+def last_launch_names():
+    """Kernels launched by the last call on this thread, in order."""
+    return [n for n in lib().mla_last_launch_names().decode().split(",") if n]
 
 
 # ------------------------------------------------------------------ ops

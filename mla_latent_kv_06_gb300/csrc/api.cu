@@ -17,6 +17,10 @@
 namespace {
 
 thread_local std::string g_err;
+thread_local void* const* g_events = nullptr;
+thread_local int g_event_count = 0;
+thread_local int g_event_next = 0;
+thread_local std::string g_launch_names;
 std::atomic<long long> g_wait_limit_ns{2000000000LL};
 
 // Flags raised by kernels on this device (see mla_device_flag).
@@ -89,6 +93,42 @@ bool tc_decode_ok(const mla::Geometry& g, int dtype, const void* q, const void* 
 
 void mla::set_last_error(const char* msg) { g_err = msg ? msg : ""; }
 
+namespace {
+// Inside a stream capture a plain record only orders the graph; the external
+// flag makes the graph record a timestamp on every replay.
+void record_event(void* ev, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(st, &cs);
+  if (cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev), st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(static_cast<cudaEvent_t>(ev), st);
+}
+}  // namespace
+
+void mla::call_begin() {
+  g_event_next = 0;
+  g_launch_names.clear();
+}
+
+void mla::kernel_mark(cudaStream_t st, const char* name) {
+  if (g_events && g_event_next < g_event_count) record_event(g_events[g_event_next++], st);
+  if (!g_launch_names.empty()) g_launch_names += ",";
+  g_launch_names += name;
+}
+
+void mla::call_end(cudaStream_t st) {
+  if (g_events && g_event_next < g_event_count) record_event(g_events[g_event_next++], st);
+}
+
+MLA_EXPORT int mla_set_kernel_events(void* const* events, int count) {
+  g_events = count > 0 ? events : nullptr;
+  g_event_count = count > 0 ? count : 0;
+  return MLA_OK;
+}
+
+MLA_EXPORT const char* mla_last_launch_names(void) { return g_launch_names.c_str(); }
+
 MLA_EXPORT const char* mla_last_error(void) { return g_err.c_str(); }
 
 MLA_EXPORT int mla_abi_version(void) { return 1; }
@@ -144,6 +184,7 @@ MLA_EXPORT int mla_decode_absorbed(const mla_dims* d, int dtype, int B, int S, c
   if (!a.flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
+  mla::call_begin();
   if (tc_decode_ok(g, dtype, q, Lc, Rc, kv_b)) {
     size_t need = mla::tc_decode_workspace_bytes(g, B, S, T_cap, 0);
     if (need && (!workspace || workspace_bytes < need))
@@ -152,8 +193,10 @@ MLA_EXPORT int mla_decode_absorbed(const mla_dims* d, int dtype, int B, int S, c
       return fail(MLA_ERR_INVALID, "workspace must be 256-byte aligned");
     e = mla::launch_decode_tc(a, workspace, workspace_bytes, st);
   } else {
+    mla::kernel_mark(st, "decode_simt");
     e = mla::launch_decode_simt(a, dtype, /*sparse=*/false, st);
   }
+  mla::call_end(st);
   if (e != cudaSuccess) return cuda_fail(e, "mla_decode_absorbed launch");
   return MLA_OK;
 }
@@ -205,6 +248,7 @@ MLA_EXPORT int mla_sparse_decode(const mla_dims* d, int dtype, int B, int S, con
   if (!a.flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
+  mla::call_begin();
   if (tc_decode_ok(g, dtype, q, Lc, Rc, kv_b)) {
     size_t need = mla::tc_decode_workspace_bytes(g, B, S, topk, topk);
     if (need && (!workspace || workspace_bytes < need))
@@ -213,8 +257,10 @@ MLA_EXPORT int mla_sparse_decode(const mla_dims* d, int dtype, int B, int S, con
       return fail(MLA_ERR_INVALID, "workspace must be 256-byte aligned");
     e = mla::launch_sparse_decode_tc(a, workspace, workspace_bytes, st);
   } else {
+    mla::kernel_mark(st, "sparse_decode_simt");
     e = mla::launch_decode_simt(a, dtype, /*sparse=*/true, st);
   }
+  mla::call_end(st);
   if (e != cudaSuccess) return cuda_fail(e, "mla_sparse_decode launch");
   return MLA_OK;
 }
@@ -253,14 +299,17 @@ MLA_EXPORT int mla_prefill_naive(const mla_dims* d, int dtype, int B, int S, int
   a.out = out;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
+  mla::call_begin();
   if (dtype == MLA_BF16 && mla::tc_prefill_geometry_ok(g) && aligned16(q) && aligned16(Lc) && aligned16(Rc) &&
       aligned16(kv_b) && aligned16(workspace)) {
     unsigned int* flags = flags_ptr();
     if (!flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
     e = mla::launch_prefill_tc(a, flags, g_wait_limit_ns.load(), st);
   } else {
+    mla::kernel_mark(st, "prefill_simt");
     e = mla::launch_prefill_simt(a, dtype, st);
   }
+  mla::call_end(st);
   if (e != cudaSuccess) return cuda_fail(e, "mla_prefill_naive launch");
   return MLA_OK;
 }
@@ -278,7 +327,11 @@ MLA_EXPORT int dsa_index_scores(int B, int S, int n_ih, int index_hd, const floa
     return fail(MLA_ERR_UNSUPPORTED, "n_ih*index_hd too large for one CTA (%zu bytes)", smem);
   mla::IndexArgs a{B, S, n_ih, index_hd, T_cap, q_idx, w, Ic, T, scores, flags_ptr()};
   if (!a.flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
-  cudaError_t e = mla::launch_index_scores(a, static_cast<cudaStream_t>(stream));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  mla::call_begin();
+  mla::kernel_mark(st, "index_scores");
+  cudaError_t e = mla::launch_index_scores(a, st);
+  mla::call_end(st);
   if (e != cudaSuccess) return cuda_fail(e, "dsa_index_scores launch");
   return MLA_OK;
 }
@@ -301,7 +354,11 @@ MLA_EXPORT int dsa_topk_select(int B, int S, const float* scores, int T_cap, con
   if (!scores || !T || !sel || !nsel) return fail(MLA_ERR_INVALID, "null tensor pointer");
   mla::TopkArgs a{B, S, T_cap, topk, scores, T, sel, nsel, flags_ptr()};
   if (!a.flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
-  cudaError_t e = mla::launch_topk_select(a, static_cast<cudaStream_t>(stream));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  mla::call_begin();
+  mla::kernel_mark(st, "topk_select");
+  cudaError_t e = mla::launch_topk_select(a, st);
+  mla::call_end(st);
   if (e != cudaSuccess) return cuda_fail(e, "dsa_topk_select launch");
   return MLA_OK;
 }

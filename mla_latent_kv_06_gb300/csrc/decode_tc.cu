@@ -605,6 +605,11 @@ struct AbsorbParams {
   int32_t* bad;         // [NR]
   int B, S, T_cap, Dn, Dv, topk, sparse;
   int do_qabs;            // 0: plan and rotary part only (qabs comes from the GEMM kernel)
+  // L2 prefetch (small batches): the latent cache rows [0, T[b]) of every
+  // sequence and the W_UV rows this CTA's combine counterpart will read
+  const __nv_bfloat16* Lc;
+  const __nv_bfloat16* Rc;
+  int prefetch;
   double theta[kDr / 2];  // RoPE frequencies rope_base^(-2j/qk_rope), from the host
   unsigned int* flags;
 };
@@ -633,6 +638,24 @@ __global__ void __launch_bounds__(kAbsThreads) absorb_kernel(const AbsorbParams 
   grid_dep_launch();
   extern __shared__ __align__(16) unsigned char sm[];
   const int cb = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  if (p.prefetch && tid == 0) {
+    // Everything the later kernels of this call read streams from HBM now,
+    // while this kernel works on W_UK: W_UV rows (64 per CTA) and 1/nblk of
+    // every sequence's cache rows.
+    const int nblk = gridDim.x * gridDim.y, me = h * gridDim.x + cb;
+    const __nv_bfloat16* wuv = p.kv_b + ((size_t)h * (p.Dn + p.Dv) + p.Dn + (size_t)cb * (p.Dv / gridDim.x)) * kDl;
+    l2_prefetch(wuv, (uint32_t)(p.Dv / gridDim.x) * kDl * 2);
+    for (int b = 0; b < p.B; ++b) {
+      const int Tb = min(max(p.T[b], 0), p.T_cap);
+      const size_t lb = (size_t)Tb * kDl * 2, rb = (size_t)Tb * kDr * 2;
+      const size_t l0 = (lb * me / nblk) & ~(size_t)15, l1 = (lb * (me + 1) / nblk) & ~(size_t)15;
+      const size_t r0 = (rb * me / nblk) & ~(size_t)15, r1 = (rb * (me + 1) / nblk) & ~(size_t)15;
+      const unsigned char* lbase = reinterpret_cast<const unsigned char*>(p.Lc + (size_t)b * p.T_cap * kDl);
+      const unsigned char* rbase = reinterpret_cast<const unsigned char*>(p.Rc + (size_t)b * p.T_cap * kDr);
+      if (l1 > l0) l2_prefetch(lbase + l0, (uint32_t)(l1 - l0));
+      if (r1 > r0) l2_prefetch(rbase + r0, (uint32_t)(r1 - r0));
+    }
+  }
   const int Dn = p.Dn, Dq = Dn + kDr;
   const int R = p.B * p.S;
   __nv_bfloat16* Ws = reinterpret_cast<__nv_bfloat16*>(sm);                      // [Dn][128]
@@ -705,6 +728,24 @@ __global__ void __launch_bounds__(kAbsThreads) absorb_kernel(const AbsorbParams 
   }
   __syncthreads();
 
+  if (!p.do_qabs) {  // rotary part only, every (row, pair) in parallel
+    for (int e = tid; e < R * (kDr / 2); e += kAbsThreads) {
+      const int r = e / (kDr / 2), j = e % (kDr / 2), b = r / p.S, s = r % p.S;
+      const int Tb = p.T[b];
+      const int pos = (Tb < p.S || Tb > p.T_cap) ? 0 : Tb - p.S + s;
+      const double ang = (double)pos * p.theta[j];
+      const double k = rint(ang * 0.15915494309189535);
+      const float red = (float)fma(-k, 6.283185307179586, ang);
+      float sn, cs;
+      sincosf(red, &sn, &cs);
+      const __nv_bfloat16* qr = p.q + ((size_t)r * kH + h) * Dq + Dn;
+      const float x0 = __bfloat162float(qr[2 * j]), x1 = __bfloat162float(qr[2 * j + 1]);
+      __nv_bfloat16* dst = p.qcat + ((size_t)r * kH + h) * kDc + kDl;
+      dst[j] = __float2bfloat16_rn(x0 * cs - x1 * sn);
+      dst[kDr / 2 + j] = __float2bfloat16_rn(x1 * cs + x0 * sn);
+    }
+    return;
+  }
   // Thread (col, half) sums i over one half of qk_nope; the halves meet in smem.
   const int col = tid % kAbsCols, half = tid / kAbsCols;
   const int i0 = half * (Dn / 2), i1 = i0 + Dn / 2;
@@ -1190,6 +1231,7 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
     gp.topk = a.topk;
     gp.Kpad = pl.Kpad;
     gp.flags = a.flags;
+    kernel_mark(st, "gather");
     gather_kernel<<<dim3(pl.Kpad / 32, pl.R), 256, 0, st>>>(gp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -1213,12 +1255,17 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   ap.sparse = sparse ? 1 : 0;
   const bool big = pl.R > kSmallRows;
   ap.do_qabs = big ? 0 : 1;
+  ap.Lc = static_cast<const __nv_bfloat16*>(a.Lc);
+  ap.Rc = static_cast<const __nv_bfloat16*>(a.Rc);
+  // L2 prefetch on the small-batch path while the cache stays well inside L2
+  ap.prefetch = (!big && !sparse && (long long)B * a.T_cap * (kDl + kDr) * 2 <= (48ll << 20)) ? 1 : 0;
   for (int j = 0; j < kDr / 2; ++j) ap.theta[j] = std::pow(g.rope_base, -2.0 * j / kDr);
   ap.flags = a.flags;
   const size_t abs_smem = (size_t)g.Dn * kAbsCols * 2 + (size_t)kAbsRows * g.Dn * 4 +
                           (size_t)2 * kAbsRows * kAbsCols * 4;
   e = set_smem_once(absorb_kernel, 200 * 1024, &g_abs_attr);
   if (e != cudaSuccess) return e;
+  kernel_mark(st, big ? "plan_rope" : "absorb");
   e = launch_pdl(absorb_kernel, dim3(big ? 1 : kDl / kAbsCols, kH), dim3(kAbsThreads), abs_smem, st, ap);
   if (e != cudaSuccess) return e;
   if (big) {  // qabs for many rows: per-head GEMM [R x qk_nope] x W_UK[h] on the tensor cores
@@ -1244,6 +1291,7 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
     ga.Z = kH;
     ga.flags = a.flags;
     ga.wait_ns = a.wait_limit_ns;
+    kernel_mark(st, "absorb_gemm");
     e = launch_gemm_tc(ga, true, st);
     if (e != cudaSuccess) return e;
   }
@@ -1281,6 +1329,7 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   e = set_smem_once(kern, (int)kAttnDynSmem, &g_attn_attr[sparse ? 1 : 0]);
   if (e != cudaSuccess) return e;
   const int nblk = sparse ? pl.G : pl.G * S;
+  kernel_mark(st, "attention");
   e = launch_pdl(kern, dim3(nblk), dim3(kAttnThreads), kAttnDynSmem, st, tp);
   if (e != cudaSuccess) return e;
 
@@ -1298,6 +1347,7 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
     mp.S = S;
     mp.G = pl.G;
     mp.sparse = sparse ? 1 : 0;
+    kernel_mark(st, "merge");
     e = launch_pdl(merge_kernel, dim3((pl.R * kH + 7) / 8), dim3(256), 0, st, mp);
     if (e != cudaSuccess) return e;
     GemmArgs gu{};
@@ -1323,6 +1373,7 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
     gu.Z = kH;
     gu.flags = a.flags;
     gu.wait_ns = a.wait_limit_ns;
+    kernel_mark(st, "up_gemm");
     return launch_gemm_tc(gu, true, st);
   }
   CombineParams cp{};
@@ -1344,6 +1395,7 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
                           (size_t)kCmbRows * kMaxPieces * 12;
   e = set_smem_once(combine_kernel, (int)cmb_smem, &g_cmb_attr);
   if (e != cudaSuccess) return e;
+  kernel_mark(st, "combine");
   return launch_pdl(combine_kernel, dim3(g.Dv / kCmbJ, kH), dim3(kCmbThreads), cmb_smem, st, cp);
 }
 

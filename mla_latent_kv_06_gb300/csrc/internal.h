@@ -72,4 +72,11 @@ cudaError_t launch_topk_select(const TopkArgs& a, cudaStream_t st);
 // Sets the thread-local message returned by mla_last_error().
 void set_last_error(const char* msg);
 
+// Per-call launch bookkeeping behind mla_set_kernel_events / mla_last_launch_names:
+// call_begin() at the start of each API call, kernel_mark() right before each
+// kernel launch, call_end() after the last one.
+void call_begin();
+void kernel_mark(cudaStream_t st, const char* name);
+void call_end(cudaStream_t st);
+
 }  // namespace mla

@@ -352,6 +352,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, unsigned int* flags, long lo
   ga.Z = 1;
   ga.flags = flags;
   ga.wait_ns = wait_ns;
+  kernel_mark(st, "kv_gemm");
   cudaError_t e = launch_gemm_tc(ga, false, st);
   if (e != cudaSuccess) return e;
   // 2. causal flash attention over the rebuilt keys / values
@@ -392,6 +393,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, unsigned int* flags, long lo
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  kernel_mark(st, "flash_attention");
   return cudaLaunchKernelEx(&cfg, flash_kernel, fp);
 }
 
