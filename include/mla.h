@@ -113,7 +113,7 @@ void mla_set_wait_limit_ns(long long ns);
  *   kv_b [H, qk_nope+v_head, kv_lora]
  *   out  [B, S, H, v_head] float
  * The tensor-core path takes BF16 with H == 64, kv_lora == 512, qk_rope == 64,
- * qk_nope % 64 == 0 (<= 256), v_head % 64 == 0 and 16-byte aligned pointers;
+ * qk_nope % 64 == 0 (<= 256), v_head % 128 == 0 and 16-byte aligned pointers;
  * every other valid request runs on the CUDA-core path.
  * ------------------------------------------------------------------------- */
 size_t mla_decode_absorbed_workspace_size(const mla_dims* d, int dtype, int B, int S, int T_cap);

@@ -16,9 +16,9 @@
 //                  S^T[128 keys x 64 heads]  = [Lc|Rc] tile (smem, K-major) x qcat^T
 //                  O^T[512 latent x 64 heads] += Lc^T (smem, MN-major) x P^T (smem, MN-major)
 //                Warp 0 streams the tile's nine 64-column atoms with TMA,
-//                warp 1 issues the MMAs,
-//                warps 2-5 run the online softmax (one key per thread) and
-//                write the per-split (m, l, O) partials.
+//                warp 1 issues the MMAs, warps 2-9 run the online softmax
+//                (one key row and 32 heads per thread) and write the
+//                per-split (m, l, O) partials.
 //  3. combine  : log-sum-exp merge of the splits, then out = W_UV clat / l.
 // The sparse variant first gathers each query's selected [Lc | Rc] rows into
 // a contiguous staging buffer (row-major, 576 values per key, zero past nsel),
@@ -40,18 +40,19 @@ constexpr int kH = 64, kDl = 512, kDr = 64, kDc = 576;  // kDc = kv_lora + qk_ro
 constexpr int kTile = 128;
 constexpr int kSlots = 9;                      // 8 latent atoms + 1 rope atom per key tile
 constexpr uint32_t kSlotBytes = 16384;         // 128 keys x 64 bf16
-constexpr uint32_t kQAtomBytes = 8192;         // 64 heads x 64 bf16
+constexpr uint32_t kQAtomBytes = 8192;         // 64 rows x 64 bf16
 constexpr uint32_t kQBytes = 9 * kQAtomBytes;  // 73728
 constexpr uint32_t kKVBytes = 9 * kSlotBytes;  // 147456
 constexpr uint32_t kAttnDynSmem = kQBytes + kKVBytes + 1024;
-constexpr int kAttnThreads = 192;
+constexpr int kSoftWarps = 8;
+constexpr int kSoftThreads = 32 * kSoftWarps;
+constexpr int kAttnThreads = 64 + kSoftThreads;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;    // S^T: 64 columns
-constexpr uint32_t kTmemO = 128;  // O^T: 4 M-tiles x 64 columns
+constexpr uint32_t kTmemO = 128;  // O^T: 4 M-blocks x 64 columns
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kTau = 8.f;  // lazy rescale threshold (log2 units)
-constexpr int kPlanMax = 1024;
-constexpr int kPrefetchTiles = 2;  // key tiles pulled into L2 ahead of the tile loads  // tile-list rows whose plan the attention CTA builds itself
+constexpr float kTau = 8.f;       // lazy rescale threshold (log2 units)
+constexpr int kPlanMax = 1024;    // tile-list rows whose plan the attention CTA builds itself
 // Waits that drain in-flight copies / MMAs before a CTA exits use at least
 // this limit, whatever the caller's wait limit.
 constexpr long long kDrainNs = 1000000000LL;
@@ -65,8 +66,9 @@ struct AttnParams {
   const int32_t* nsel;
   const int32_t* tile_start;  // [NR + 1]
   int B, S, T_cap, G, topk;
-  int kv_rows;  // rows of the key source per tile-list row: T_cap (dense) or Kpad (sparse)
-  float c;  // softmax scale * log2(e)
+  int kv_rows;    // rows of the key source per tile-list row: T_cap (dense) or Kpad (sparse)
+  int read_once;  // every key tile is loaded by exactly one CTA: mark its lines evict-first in L2
+  float c;        // softmax scale * log2(e)
   float* o_part;
   float* ml_part;
   unsigned int* flags;
@@ -177,8 +179,67 @@ __device__ __forceinline__ int first_row(const int32_t* ts, int NR, long long c0
   return lo;
 }
 
+// Reduce 32 per-lane values over the 32 lanes of a warp; afterwards lane L
+// holds the result for entry L in v[0].
+template <bool kMax>
+__device__ __forceinline__ void transpose_reduce32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int step = 0; step < 5; ++step) {
+    const int o = 16 >> step;
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float send = upper ? v[i] : v[i + o];
+      const float keep = upper ? v[i + o] : v[i];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, o);
+      v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+}
+
+// Walks the key tiles of one attention CTA in processing order: the pieces
+// (tile-list rows) of chunk g, and within a piece its tiles lo..hi-1.
+template <bool kSparse>
+struct TileCursor {
+  int row, lo, hi, k;
+  bool live;
+  __device__ __forceinline__ void start(const AttnParams& p, const int32_t* ts, int NR, long long N, int g, int s,
+                                        int row0) {
+    row = row0;
+    live = next_piece<kSparse>(p, ts, NR, N, g, s, &row, &lo, &hi);
+    k = lo;
+  }
+  __device__ __forceinline__ void next(const AttnParams& p, const int32_t* ts, int NR, long long N, int g, int s) {
+    if (++k < hi) return;
+    ++row;
+    live = next_piece<kSparse>(p, ts, NR, N, g, s, &row, &lo, &hi);
+    k = lo;
+  }
+  __device__ __forceinline__ bool first() const { return k == lo; }
+  __device__ __forceinline__ bool last() const { return k == hi - 1; }
+};
+
+// Keys of tile k of tile-list row `row` that the query attends to (>= 1 for a
+// tile inside a piece).
+template <bool kSparse>
+__device__ __forceinline__ int tile_keys(const AttnParams& p, int row, int s, int k) {
+  const int nk = kSparse ? p.nsel[row] : p.T[row] - p.S + s + 1;
+  const int n = nk - k * kTile;
+  return n < kTile ? n : kTile;
+}
+
 // ===========================================================================
 // Attention kernel
+//
+// Per key tile the tensor pipe runs two products,
+//   S^T[128 keys x 64 rows]   = [Lc | Rc] tile x qcat^T              (K = 576)
+//   O^T[512 x 64 rows]       += Lc tile^T x P^T                      (K = keys)
+// with the softmax warps turning S^T into P^T in between.  The tile is read
+// from memory once: shared memory holds the query block and the nine atoms of
+// one tile (eight latent, one rope-key atom that P^T reuses once the score
+// product is done).  The value product releases the latent atoms pairwise, so
+// the next tile's loads start while it still runs, and the next score product
+// accumulates atom by atom as they land.
 // ===========================================================================
 template <bool kSparse>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
@@ -189,7 +250,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   unsigned char* sKV = smem + kQBytes;
 
   __shared__ uint64_t full_bar[kSlots], empty_bar[kSlots];
-  __shared__ uint64_t q_full, q_empty, s_full, s_free, p_full, o_done, o_free, mma_done;
+  __shared__ uint64_t q_full, q_empty, s_full, s_free, p_full, o_done, mma_done;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ __align__(16) float red_max[4][kH];
@@ -212,10 +273,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     mbar_init(&q_full, 1);
     mbar_init(&q_empty, 1);
     mbar_init(&s_full, 1);
-    mbar_init(&s_free, 128);
-    mbar_init(&p_full, 128);
+    mbar_init(&s_free, kSoftThreads);
+    mbar_init(&p_full, kSoftThreads);
     mbar_init(&o_done, 1);
-    mbar_init(&o_free, 128);
     mbar_init(&mma_done, 1);
     abort_flag = 0;
     fence_mbar_init();
@@ -276,307 +336,312 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    int it = 0, pc = 0, row = row0, lo, hi;
-    bool ok = true;
-    int last_it[kSlots];
-    for (int a = 0; a < kSlots; ++a) last_it[a] = -1;
-    int last_q = -1;
-    bool waited = !local_plan;
-    // L2 prefetch cursor, kPrefetchTiles key tiles ahead of the tile loads:
-    // HBM keeps streaming while a tile's score product, softmax and value
-    // product run, and the tile loads then hit L2.
-    int pf_row = row0, pf_lo = 0, pf_hi = 0, pf_k = 0;
-    bool pf_live = true;
-    auto prefetch_next = [&]() {
-      if (!pf_live) return;
-      if (pf_k >= pf_hi) {
-        if (pf_hi > 0) ++pf_row;
-        if (!next_piece<kSparse>(p, ts, NR, N, g, s, &pf_row, &pf_lo, &pf_hi)) {
-          pf_live = false;
-          return;
-        }
-        pf_k = pf_lo;
-      }
-      const int y = (kSparse ? pf_row : pf_row) * p.kv_rows + pf_k * kTile;
-      for (int a = 0; a < 8; ++a) tma_prefetch_l2_2d(&p.mL, 64 * a, y);
-      tma_prefetch_l2_2d(&p.mR, 0, y);
-      ++pf_k;
-    };
-    if (lane == 0)
-      for (int i = 0; i <= kPrefetchTiles; ++i) prefetch_next();
-    while (ok && next_piece<kSparse>(p, ts, NR, N, g, s, &row, &lo, &hi)) {
-      const int qrow = kSparse ? row : row * S + s;
-      const int b = kSparse ? row / S : row;
-      const int kvrow = kSparse ? row : b;
-      for (int k = lo; ok && k < hi; ++k, ++it) {
-        const uint32_t par = (it & 1) ^ 1;
-        if (lane == 0 && it > 0) prefetch_next();
-        if (lane == 0) {
-          const int y = kvrow * p.kv_rows + k * kTile;
-          for (int a = 0; a < kSlots && ok; ++a) {
-            ok = mbar_wait(&empty_bar[a], par, abort, p.flags, p.wait_ns);
-            if (!ok) break;
-            mbar_arrive_expect_tx(&full_bar[a], kSlotBytes);
-            if (a < 8) tma_load_2d(sKV + a * kSlotBytes, &p.mL, 64 * a, y, &full_bar[a]);
-            else tma_load_2d(sKV + a * kSlotBytes, &p.mR, 0, y, &full_bar[a]);
-            last_it[a] = it;
-          }
-          if (ok && k == lo) {  // the piece's query block, once its first key tile is on its way
-            if (!waited) {
-              grid_dep_wait();  // qcat comes from the absorb kernel
-              waited = true;
-            }
-            ok = mbar_wait(&q_empty, (pc & 1) ^ 1, abort, p.flags, p.wait_ns);
-            if (ok) {
-              mbar_arrive_expect_tx(&q_full, kQBytes);
-              for (int a = 0; a < kSlots; ++a) tma_load_2d(sQ + a * kQAtomBytes, &p.mQ, 64 * a, qrow * kH, &q_full);
-              last_q = pc;
-            }
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-      }
-      ++pc;
-      ++row;
-    }
-    // Never leave with copies in flight: wait for the last load of each slot.
     if (lane == 0) {
+      const uint64_t pol_once = l2_policy_evict_first();
+      TileCursor<kSparse> c;
+      c.start(p, ts, NR, N, g, s, row0);
+      int it = 0, pc = -1, last_it[kSlots], last_q = -1;
+      for (int a = 0; a < kSlots; ++a) last_it[a] = -1;
+      bool ok = true, dep_waited = !local_plan;
+      while (ok && c.live) {
+        const bool first = c.first();
+        if (first) ++pc;
+        const int y = c.row * p.kv_rows + c.k * kTile;  // tile-list row = block of key-source rows
+        const uint32_t par = (it & 1) ^ 1;
+        for (int a = 0; a < kSlots && ok; ++a) {
+          ok = mbar_wait(&empty_bar[a], par, abort, p.flags, p.wait_ns);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&full_bar[a], kSlotBytes);
+          const CUtensorMap* map = a < 8 ? &p.mL : &p.mR;
+          const int x = a < 8 ? 64 * a : 0;
+          if (p.read_once) tma_load_2d_hint(sKV + a * kSlotBytes, map, x, y, &full_bar[a], pol_once);
+          else tma_load_2d(sKV + a * kSlotBytes, map, x, y, &full_bar[a]);
+          last_it[a] = it;
+        }
+        if (ok && first) {  // the piece's query block, once its first key tile is on its way
+          if (!dep_waited) {
+            grid_dep_wait();  // qcat comes from the absorb kernel
+            dep_waited = true;
+          }
+          ok = mbar_wait(&q_empty, (pc & 1) ^ 1, abort, p.flags, p.wait_ns);
+          if (ok) {
+            mbar_arrive_expect_tx(&q_full, kQBytes);
+            const int qrow = kSparse ? c.row : c.row * S + s;
+            for (int a = 0; a < kSlots; ++a) tma_load_2d(sQ + a * kQAtomBytes, &p.mQ, 64 * a, qrow * kH, &q_full);
+            last_q = pc;
+          }
+        }
+        ++it;
+        c.next(p, ts, NR, N, g, s);
+      }
+      // Never leave with copies in flight: wait for the last load of each slot.
       volatile int no_abort = 0;
       const long long drain_ns = p.wait_ns > kDrainNs ? p.wait_ns : kDrainNs;
       for (int a = 0; a < kSlots; ++a)
         if (last_it[a] >= 0) mbar_wait(&full_bar[a], last_it[a] & 1, &no_abort, p.flags, drain_ns);
       if (last_q >= 0) mbar_wait(&q_full, last_q & 1, &no_abort, p.flags, drain_ns);
     }
+    __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc1 = idesc_bf16_f32(128, 64, 0, 0);
-      const uint32_t idesc2 = idesc_bf16_f32(128, 64, 1, 1);
-      const uint32_t kv0 = smem_u32(sKV), q0 = smem_u32(sQ);
-      int it = 0, pc = 0, row = row0, lo, hi;
-      bool ok = true, issued = false;
-      while (ok && next_piece<kSparse>(p, ts, NR, N, g, s, &row, &lo, &hi)) {
-        ok = mbar_wait(&q_full, pc & 1, abort, p.flags, p.wait_ns);
-        if (ok && pc > 0) ok = mbar_wait(&o_free, (pc - 1) & 1, abort, p.flags, p.wait_ns);
-        for (int k = lo; ok && k < hi; ++k, ++it) {
-          ok = mbar_wait(&s_free, (it & 1) ^ 1, abort, p.flags, p.wait_ns);
-          if (!ok) break;
-          tc_fence_after();
-          for (int a = 0; a < kSlots && ok; ++a) {
-            ok = mbar_wait(&full_bar[a], it & 1, abort, p.flags, p.wait_ns);
-            if (!ok) break;
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t da = smem_desc_sw128(kv0 + a * kSlotBytes + kk * 32, 16, 1024);
-              const uint64_t db = smem_desc_sw128(q0 + a * kQAtomBytes + kk * 32, 16, 1024);
-              mma_bf16(tmem + kTmemS, da, db, idesc1, (a | kk) != 0);
-            }
-            issued = true;
-          }
-          if (!ok) break;
-          mma_commit(&s_full);
-          if (k == hi - 1) mma_commit(&q_empty);
-          ok = mbar_wait(&p_full, it & 1, abort, p.flags, p.wait_ns);
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t da = smem_desc_sw128(kv0 + (2 * m) * kSlotBytes + kk * 2048, kSlotBytes, 1024);
-              const uint64_t db = smem_desc_sw128(kv0 + 8 * kSlotBytes + kk * 2048, kSlotBytes, 1024);
-              mma_bf16(tmem + kTmemO + 64 * m, da, db, idesc2, (kk > 0 || k > lo) ? 1u : 0u);
-            }
-            mma_commit(&empty_bar[2 * m]);
-            mma_commit(&empty_bar[2 * m + 1]);
-          }
-          mma_commit(&empty_bar[8]);
-          mma_commit(&o_done);
-        }
+    // ------------------------------------------------------------ MMA issuer (whole warp waits, lane 0 issues)
+    const uint32_t idS = idesc_bf16_f32(128, 64, 0, 0);
+    const uint32_t idO = idesc_bf16_f32(128, 64, 1, 1);
+    const uint32_t kv0 = smem_u32(sKV), q0 = smem_u32(sQ);
+    TileCursor<kSparse> c;
+    c.start(p, ts, NR, N, g, s, row0);
+    int it = 0, pc = -1;
+    bool ok = true, issued = false;
+    auto wait = [&](uint64_t* bar, uint32_t par) -> bool {
+      const bool r = mbar_wait(bar, par, abort, p.flags, p.wait_ns);
+      return __all_sync(0xffffffffu, r);
+    };
+    while (ok && c.live) {
+      const bool first = c.first();
+      if (first) {
         ++pc;
-        ++row;
+        ok = wait(&q_full, pc & 1);
       }
-      if (issued) {  // all MMAs retired before TMEM is released
-        mma_commit(&mma_done);
-        volatile int no_abort = 0;
-        mbar_wait(&mma_done, 0, &no_abort, p.flags, p.wait_ns > kDrainNs ? p.wait_ns : kDrainNs);
+      ok = ok && wait(&s_free, (it & 1) ^ 1);
+      if (!ok) break;
+      tc_fence_after();
+      for (int a = 0; a < kSlots && ok; ++a) {
+        ok = wait(&full_bar[a], it & 1);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t da = smem_desc_sw128(kv0 + a * kSlotBytes + kk * 32, 16, 1024);
+            const uint64_t db = smem_desc_sw128(q0 + a * kQAtomBytes + kk * 32, 16, 1024);
+            mma_bf16(tmem + kTmemS, da, db, idS, (a | kk) != 0 ? 1u : 0u);
+          }
+        }
+        __syncwarp();
+        issued = true;
       }
+      if (!ok) break;
+      if (lane == 0) {
+        mma_commit(&s_full);
+        if (c.last()) mma_commit(&q_empty);
+      }
+      __syncwarp();
+      ok = wait(&p_full, it & 1);
+      if (!ok) break;
+      tc_fence_after();
+      if (lane == 0) {
+        const int ksteps = (tile_keys<kSparse>(p, c.row, s, c.k) + 15) >> 4;
+        for (int m = 0; m < 4; ++m) {
+          for (int kk = 0; kk < ksteps; ++kk) {
+            const uint64_t da = smem_desc_sw128(kv0 + (2 * m) * kSlotBytes + kk * 2048, kSlotBytes, 1024);
+            const uint64_t db = smem_desc_sw128(kv0 + 8 * kSlotBytes + kk * 2048, kSlotBytes, 1024);
+            mma_bf16(tmem + kTmemO + 64 * m, da, db, idO, (kk > 0 || !first) ? 1u : 0u);
+          }
+          mma_commit(&empty_bar[2 * m]);
+          mma_commit(&empty_bar[2 * m + 1]);
+        }
+        mma_commit(&empty_bar[8]);
+        mma_commit(&o_done);
+      }
+      __syncwarp();
+      ++it;
+      c.next(p, ts, NR, N, g, s);
+    }
+    if (issued) {  // all MMAs retired before TMEM is released
+      if (lane == 0) mma_commit(&mma_done);
+      __syncwarp();
+      volatile int no_abort = 0;
+      mbar_wait(&mma_done, 0, &no_abort, p.flags, p.wait_ns > kDrainNs ? p.wait_ns : kDrainNs);
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax warps 2..5
-    const int tr = threadIdx.x - 64;                 // 0..127
-    const int wq = warp & 3;                         // TMEM lane quadrant of this warp
-    const int trow = 32 * wq + lane;                 // key row of the tile / latent row of O^T
-    const int widx = warp - 2;
-    const uint32_t t_lane = (uint32_t)(32 * wq) << 16;
+    // ------------------------------------------------------------ softmax warps 2..9
+    const int tsm = threadIdx.x - 64;         // 0..255
+    const int qd = warp & 3;                  // TMEM lane quadrant of this warp
+    const int half = (warp - 2) >> 2;         // which 32 of the 64 query rows (heads) this warp covers
+    const int col0 = 32 * half;
+    const int trow = 32 * qd + lane;          // key row of the tile / latent row of an O^T block
+    const uint32_t t_lane = (uint32_t)(32 * qd) << 16;
     const float c = p.c;
-    int it = 0, pc = 0, row = row0, lo, hi;
-    bool ok = true;
-    while (ok && next_piece<kSparse>(p, ts, NR, N, g, s, &row, &lo, &hi)) {
-      const int b = kSparse ? row / S : row;
-      const int qs = kSparse ? row % S : s;
-      const int pos = p.T[b] - S + qs;
-      const int nkeys = kSparse ? p.nsel[row] : pos + 1;
-      const int32_t* srow = kSparse ? p.sel + (size_t)row * p.topk : nullptr;
-      float lp[kH];
+    TileCursor<kSparse> cur;
+    cur.start(p, ts, NR, N, g, s, row0);
+    int it = 0, slot = 0, pos = 0, nkeys = 0;
+    const int32_t* srow = nullptr;
+    bool ok = true, bad_idx = false;
+    float lp[32];
 #pragma unroll
-      for (int h = 0; h < kH; ++h) lp[h] = 0.f;
-      bool bad_idx = false;
-      for (int k = lo; ok && k < hi; ++k, ++it) {
-        const bool first = (k == lo);
-        // A failed wait is decided jointly by the 128 softmax threads (bar.red
-        // below), so that no thread is left waiting at a barrier the others quit.
-        bool fail = !mbar_wait(&s_full, it & 1, abort, p.flags, p.wait_ns);
-        if (bar_red_or(1, 128, fail)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        float v[kH];
-        tmem_ld64(tmem + t_lane + kTmemS, v);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&s_free);
-        const int j = k * kTile + trow;
-        bool valid = j < nkeys;
-        if (kSparse && valid) {
-          const int idx = srow[j];
-          if (idx < 0 || idx > pos) {
-            valid = false;
-            bad_idx = true;
-          }
-        }
-        if (!valid) {
-#pragma unroll
-          for (int h = 0; h < kH; ++h) v[h] = -INFINITY;
-        }
-        float mx[kH];
-#pragma unroll
-        for (int h = 0; h < kH; ++h) mx[h] = v[h];
-        transpose_reduce64<true>(mx, lane);
-        *reinterpret_cast<float2*>(&red_max[widx][2 * lane]) = make_float2(mx[0], mx[1]);
-        named_barrier(1, 128);
-        bool need = false;
-        if (tr < kH) {
-          const float tmax = fmaxf(fmaxf(red_max[0][tr], red_max[1][tr]), fmaxf(red_max[2][tr], red_max[3][tr]));
-          const float cand = tmax * c;
-          const float mo = first ? -INFINITY : m_sh[tr];
-          float mn = mo, al = 1.f;
-          if (cand > mo + kTau) {
-            mn = cand;
-            al = exp2f(mo - mn);
-          }
-          m_sh[tr] = mn;
-          alpha_sh[tr] = al;
-          need = !first && al != 1.f;
-        }
-        const bool rescale = bar_red_or(2, 128, need);
-        // probabilities, row sums, P^T row into the rope slot (free after the score MMAs)
-        uint32_t pk[kH / 2];
-#pragma unroll
-        for (int h2 = 0; h2 < kH; h2 += 4) {
-          const float4 mu = *reinterpret_cast<const float4*>(&m_sh[h2]);
-          const float e0 = exp2f(fmaf(v[h2 + 0], c, -mu.x));
-          const float e1 = exp2f(fmaf(v[h2 + 1], c, -mu.y));
-          const float e2 = exp2f(fmaf(v[h2 + 2], c, -mu.z));
-          const float e3 = exp2f(fmaf(v[h2 + 3], c, -mu.w));
-          pk[h2 / 2] = pack_bf16(e0, e1);
-          pk[h2 / 2 + 1] = pack_bf16(e2, e3);
-        }
-        if (rescale || first) {
-#pragma unroll
-          for (int h2 = 0; h2 < kH; h2 += 4) {
-            const float4 al = *reinterpret_cast<const float4*>(&alpha_sh[h2]);
-            lp[h2 + 0] *= al.x;
-            lp[h2 + 1] *= al.y;
-            lp[h2 + 2] *= al.z;
-            lp[h2 + 3] *= al.w;
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < kH / 2; ++i) {
-          __nv_bfloat162 t = *reinterpret_cast<__nv_bfloat162*>(&pk[i]);
-          const float2 f = __bfloat1622float2(t);
-          lp[2 * i] += f.x;
-          lp[2 * i + 1] += f.y;
-        }
-        unsigned char* prow = sKV + 8 * kSlotBytes + trow * 128;
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          uint4 val = make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-          *reinterpret_cast<uint4*>(prow + ((cc ^ (trow & 7)) << 4)) = val;
-        }
-        if (!valid) {  // masked key: its latent row must be finite for the value product
-#pragma unroll
-          for (int a = 0; a < 8; ++a) {
-            unsigned char* lr = sKV + a * kSlotBytes + trow * 128;
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc) *reinterpret_cast<uint4*>(lr + 16 * cc) = make_uint4(0, 0, 0, 0);
-          }
-        }
-        if (rescale) {  // O^T columns scaled by alpha once the previous value product retired
-          fail = !mbar_wait(&o_done, (it - 1) & 1, abort, p.flags, p.wait_ns);
-          if (bar_red_or(2, 128, fail)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll 1
-          for (int m = 0; m < 4; ++m) {
-            float w[kH];
-            tmem_ld64(tmem + t_lane + kTmemO + 64 * m, w);
-            tmem_wait_ld();
-#pragma unroll
-            for (int h2 = 0; h2 < kH; h2 += 4) {
-              const float4 al = *reinterpret_cast<const float4*>(&alpha_sh[h2]);
-              w[h2] *= al.x;
-              w[h2 + 1] *= al.y;
-              w[h2 + 2] *= al.z;
-              w[h2 + 3] *= al.w;
-            }
-            tmem_st64(tmem + t_lane + kTmemO + 64 * m, w);
-          }
-          tmem_wait_st();
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(&p_full);
-      }
-      if (!ok) break;
-      // ---- end of piece: write the split's partials
-      const int slot = kSparse ? g + row : (g + row) * S + s;
-      const bool fail_end = !mbar_wait(&o_done, (it - 1) & 1, abort, p.flags, p.wait_ns);
-      if (bar_red_or(1, 128, fail_end)) {
-        ok = false;
-        break;
-      }
+    for (int i = 0; i < 32; ++i) lp[i] = 0.f;
+
+    // Partials of a finished piece once its last value product (tile j) retired.
+    auto epilogue = [&](int j) -> bool {
+      const bool fail = !mbar_wait(&o_done, j & 1, abort, p.flags, p.wait_ns);
+      if (bar_red_or(1, kSoftThreads, fail)) return false;
       tc_fence_after();
       float* op = p.o_part + (size_t)slot * kH * kDl;
 #pragma unroll 1
       for (int m = 0; m < 4; ++m) {
-        float w[kH];
-        tmem_ld64(tmem + t_lane + kTmemO + 64 * m, w);
+        float w[32];
+        tmem_ld32(tmem + t_lane + kTmemO + 64 * m + col0, w);
         tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < kH; ++h) op[(size_t)h * kDl + 128 * m + trow] = w[h];
+        for (int i = 0; i < 32; ++i) op[(size_t)(col0 + i) * kDl + 128 * m + trow] = w[i];
       }
       tc_fence_before();
-      mbar_arrive(&o_free);
-      transpose_reduce64<false>(lp, lane);
-      *reinterpret_cast<float2*>(&red_sum[widx][2 * lane]) = make_float2(lp[0], lp[1]);
-      const bool bad = bar_red_or(1, 128, bad_idx);
-      if (tr < kH) {
-        const float l = red_sum[0][tr] + red_sum[1][tr] + red_sum[2][tr] + red_sum[3][tr];
-        float* ml = p.ml_part + ((size_t)slot * kH + tr) * 2;
-        ml[0] = m_sh[tr];
+      transpose_reduce32<false>(lp, lane);
+      red_sum[qd][col0 + lane] = lp[0];
+      const bool bad = bar_red_or(1, kSoftThreads, bad_idx);
+      if (tsm < kH) {
+        const float l = red_sum[0][tsm] + red_sum[1][tsm] + red_sum[2][tsm] + red_sum[3][tsm];
+        float* ml = p.ml_part + ((size_t)slot * kH + tsm) * 2;
+        ml[0] = m_sh[tsm];
         ml[1] = bad ? __int_as_float(0x7fc00000) : l;
       }
-      if (bad && tr == 0) raise_flag(p.flags, MLA_DEV_BAD_INDEX);
-      ++pc;
-      ++row;
+      if (bad && tsm == 0) raise_flag(p.flags, MLA_DEV_BAD_INDEX);
+      return true;
+    };
+
+    while (ok && cur.live) {
+      const bool first = cur.first();
+      if (first) {
+        if (it > 0 && !epilogue(it - 1)) {
+          ok = false;
+          break;
+        }
+        const int b = kSparse ? cur.row / S : cur.row;
+        const int qs = kSparse ? cur.row % S : s;
+        pos = p.T[b] - S + qs;
+        nkeys = kSparse ? p.nsel[cur.row] : pos + 1;
+        srow = kSparse ? p.sel + (size_t)cur.row * p.topk : nullptr;
+        slot = kSparse ? g + cur.row : (g + cur.row) * S + s;
+        bad_idx = false;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) lp[i] = 0.f;
+      }
+      // A failed wait is decided jointly by the softmax threads (bar.red), so
+      // that no thread is left waiting at a barrier the others quit.
+      bool fail = !mbar_wait(&s_full, it & 1, abort, p.flags, p.wait_ns);
+      if (bar_red_or(1, kSoftThreads, fail)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float v[32];
+      tmem_ld32(tmem + t_lane + kTmemS + col0, v);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&s_free);
+      const int j = cur.k * kTile + trow;
+      bool valid = j < nkeys;
+      if (kSparse && valid) {
+        const int idx = srow[j];
+        if (idx < 0 || idx > pos) {
+          valid = false;
+          bad_idx = true;
+        }
+      }
+      if (!valid) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = -INFINITY;
+      }
+      float mx[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) mx[i] = v[i];
+      transpose_reduce32<true>(mx, lane);
+      red_max[qd][col0 + lane] = mx[0];
+      named_barrier(1, kSoftThreads);
+      bool need = false;
+      if (tsm < kH) {
+        const float tmax = fmaxf(fmaxf(red_max[0][tsm], red_max[1][tsm]), fmaxf(red_max[2][tsm], red_max[3][tsm]));
+        const float cand = tmax * c;
+        const float mo = first ? -INFINITY : m_sh[tsm];
+        float mn = mo, al = 1.f;
+        if (cand > mo + kTau) {
+          mn = cand;
+          al = exp2f(mo - mn);
+        }
+        m_sh[tsm] = mn;
+        alpha_sh[tsm] = al;
+        need = !first && al != 1.f;
+      }
+      const bool rescale = bar_red_or(2, kSoftThreads, need);
+      // probabilities (bf16, the value-product operand) and their row sums
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        const float4 mu = *reinterpret_cast<const float4*>(&m_sh[col0 + i]);
+        pk[i / 2] = pack_bf16(exp2f(fmaf(v[i + 0], c, -mu.x)), exp2f(fmaf(v[i + 1], c, -mu.y)));
+        pk[i / 2 + 1] = pack_bf16(exp2f(fmaf(v[i + 2], c, -mu.z)), exp2f(fmaf(v[i + 3], c, -mu.w)));
+      }
+      if (rescale) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float4 al = *reinterpret_cast<const float4*>(&alpha_sh[col0 + i]);
+          lp[i + 0] *= al.x;
+          lp[i + 1] *= al.y;
+          lp[i + 2] *= al.z;
+          lp[i + 3] *= al.w;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        __nv_bfloat162 t = *reinterpret_cast<__nv_bfloat162*>(&pk[i]);
+        const float2 f = __bfloat1622float2(t);
+        lp[2 * i] += f.x;
+        lp[2 * i + 1] += f.y;
+      }
+      // P^T row into the rope atom's slot (its score product is done): a
+      // 128-byte row per key, 16-byte chunks XOR-swizzled by row
+      unsigned char* prow = sKV + 8 * kSlotBytes + trow * 128;
+      const int cbase = col0 >> 3;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const uint4 val = make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+        *reinterpret_cast<uint4*>(prow + (((cbase + cc) ^ (trow & 7)) << 4)) = val;
+      }
+      // Masked key rows inside the value product's last 16-key step: their
+      // probability is 0, but the latent row must be finite too.
+      const int z1 = (cur.k * kTile + kTile <= nkeys) ? kTile : (((nkeys - cur.k * kTile) + 15) & ~15);
+      if (!valid && trow < z1) {
+#pragma unroll
+        for (int a = 4 * half; a < 4 * half + 4; ++a) {
+          unsigned char* lr = sKV + a * kSlotBytes + trow * 128;
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) *reinterpret_cast<uint4*>(lr + 16 * cc) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      if (!first) {
+        // O^T is stable once the previous value product retired
+        fail = !mbar_wait(&o_done, (it - 1) & 1, abort, p.flags, p.wait_ns);
+        if (bar_red_or(2, kSoftThreads, fail)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (rescale) {
+#pragma unroll 1
+          for (int m = 0; m < 4; ++m) {
+            float w[32];
+            tmem_ld32(tmem + t_lane + kTmemO + 64 * m + col0, w);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              const float4 al = *reinterpret_cast<const float4*>(&alpha_sh[col0 + i]);
+              w[i] *= al.x;
+              w[i + 1] *= al.y;
+              w[i + 2] *= al.z;
+              w[i + 3] *= al.w;
+            }
+            tmem_st32(tmem + t_lane + kTmemO + 64 * m + col0, w);
+          }
+          tmem_wait_st();
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&p_full);
+      ++it;
+      cur.next(p, ts, NR, N, g, s);
     }
+    if (ok && it > 0) epilogue(it - 1);
   }
   tc_fence_before();
   __syncthreads();
@@ -592,8 +657,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
 // validates the lengths / selections and writes the tile plan.
 // ===========================================================================
 constexpr int kAbsThreads = 256;
-constexpr int kAbsCols = 128;
-constexpr int kAbsRows = 16;
+constexpr int kAbsCols = 128;     // W_UK columns per CTA
+constexpr int kAbsRows = 8;       // query rows of the GEMV path (larger batches use the GEMM)
+constexpr int kAbsGroups = kAbsThreads / (kAbsCols / 8);  // 16 row groups of 8-column threads
 
 struct AbsorbParams {
   const __nv_bfloat16* q;     // [R, 64, Dn+64]
@@ -614,23 +680,54 @@ struct AbsorbParams {
   unsigned int* flags;
 };
 
-// Partial dot products of NR query rows with one W_UK column over i in [i0, i1).
-template <int NR>
-__device__ __forceinline__ void absorb_rows(const __nv_bfloat16* Ws, const float* qn, int Dn, int col, int i0,
-                                            int i1, float* part, int half) {
-  float acc[NR];
-#pragma unroll
-  for (int u = 0; u < NR; ++u) acc[u] = 0.f;
-  for (int i = i0; i < i1; ++i) {
-    const float wv = __bfloat162float(Ws[i * kAbsCols + col]);
-#pragma unroll
-    for (int u = 0; u < NR; ++u) acc[u] = fmaf(qn[u * Dn + i], wv, acc[u]);
-  }
-#pragma unroll
-  for (int u = 0; u < NR; ++u) part[(half * kAbsRows + u) * kAbsCols + col] = acc[u];
+// Rotary part of query row r of head h, rotated to the row's own position.
+__device__ __forceinline__ void rope_row(const AbsorbParams& p, int r, int h, int j) {
+  const int Dq = p.Dn + kDr;
+  const int b = r / p.S, s = r % p.S;
+  const int Tb = p.T[b];
+  const int pos = (Tb < p.S || Tb > p.T_cap) ? 0 : Tb - p.S + s;
+  // angle in double, reduced to [-pi, pi] before the float sincos
+  const double ang = (double)pos * p.theta[j];
+  const double k = rint(ang * 0.15915494309189535);
+  const float red = (float)fma(-k, 6.283185307179586, ang);
+  float sn, cs;
+  sincosf(red, &sn, &cs);
+  const __nv_bfloat16* qr = p.q + ((size_t)r * kH + h) * Dq + p.Dn;
+  const float x0 = __bfloat162float(qr[2 * j]), x1 = __bfloat162float(qr[2 * j + 1]);
+  __nv_bfloat16* dst = p.qcat + ((size_t)r * kH + h) * kDc + kDl;
+  dst[j] = __float2bfloat16_rn(x0 * cs - x1 * sn);
+  dst[kDr / 2 + j] = __float2bfloat16_rn(x1 * cs + x0 * sn);
 }
 
-__global__ void __launch_bounds__(kAbsThreads) absorb_kernel(const AbsorbParams p) {
+// Partial products of every query row with the thread's W_UK registers
+// (rows grp + 16u, columns c8*8 .. c8*8+7), one row at a time.
+template <int NV>
+__device__ __forceinline__ void absorb_regs(const uint4 (&wv)[NV], const float* qn, int Dn, int grp, int nr,
+                                            float* part, int c8) {
+  for (int r = 0; r < nr; ++r) {
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+#pragma unroll
+    for (int u = 0; u < NV; ++u) {
+      const float qv = qn[r * Dn + grp + kAbsGroups * u];
+      const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&wv[u]);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float2 f = __bfloat1622float2(w2[t]);
+        acc[2 * t] = fmaf(qv, f.x, acc[2 * t]);
+        acc[2 * t + 1] = fmaf(qv, f.y, acc[2 * t + 1]);
+      }
+    }
+    float4* d = reinterpret_cast<float4*>(part + ((size_t)grp * kAbsRows + r) * kAbsCols + c8 * 8);
+    d[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    d[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+}
+
+// NV = qk_nope / 16: W_UK registers (16-byte vectors) per thread.
+template <int NV>
+__global__ void __launch_bounds__(kAbsThreads, 2) absorb_kernel(const AbsorbParams p) {
   // Under programmatic serialization this kernel may start before the
   // previous kernel of the stream retires (for example the combine of an
   // earlier call that still reads the workspace): wait before touching memory.
@@ -638,51 +735,11 @@ __global__ void __launch_bounds__(kAbsThreads) absorb_kernel(const AbsorbParams 
   grid_dep_launch();
   extern __shared__ __align__(16) unsigned char sm[];
   const int cb = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
-  if (p.prefetch && tid == 0) {
-    // Everything the later kernels of this call read streams from HBM now,
-    // while this kernel works on W_UK: W_UV rows (64 per CTA) and 1/nblk of
-    // every sequence's cache rows.
-    const int nblk = gridDim.x * gridDim.y, me = h * gridDim.x + cb;
-    const __nv_bfloat16* wuv = p.kv_b + ((size_t)h * (p.Dn + p.Dv) + p.Dn + (size_t)cb * (p.Dv / gridDim.x)) * kDl;
-    l2_prefetch(wuv, (uint32_t)(p.Dv / gridDim.x) * kDl * 2);
-    for (int b = 0; b < p.B; ++b) {
-      const int Tb = min(max(p.T[b], 0), p.T_cap);
-      const size_t lb = (size_t)Tb * kDl * 2, rb = (size_t)Tb * kDr * 2;
-      const size_t l0 = (lb * me / nblk) & ~(size_t)15, l1 = (lb * (me + 1) / nblk) & ~(size_t)15;
-      const size_t r0 = (rb * me / nblk) & ~(size_t)15, r1 = (rb * (me + 1) / nblk) & ~(size_t)15;
-      const unsigned char* lbase = reinterpret_cast<const unsigned char*>(p.Lc + (size_t)b * p.T_cap * kDl);
-      const unsigned char* rbase = reinterpret_cast<const unsigned char*>(p.Rc + (size_t)b * p.T_cap * kDr);
-      if (l1 > l0) l2_prefetch(lbase + l0, (uint32_t)(l1 - l0));
-      if (r1 > r0) l2_prefetch(rbase + r0, (uint32_t)(r1 - r0));
-    }
-  }
   const int Dn = p.Dn, Dq = Dn + kDr;
   const int R = p.B * p.S;
-  __nv_bfloat16* Ws = reinterpret_cast<__nv_bfloat16*>(sm);                      // [Dn][128]
-  float* qn = reinterpret_cast<float*>(sm + (size_t)Dn * kAbsCols * 2);           // [kAbsRows][Dn]
 
-  // W_UK[h][:, cb*128 : cb*128+128] -> smem: every 16-byte load is issued
-  // before the first store so that the whole tile is in flight at once.
-  const __nv_bfloat16* W = p.kv_b + (size_t)h * (Dn + p.Dv) * kDl + cb * kAbsCols;
-  const int nvec = p.do_qabs ? Dn * kAbsCols / 8 : 0;
-  constexpr int kMaxVec = 256 * kAbsCols / 8 / kAbsThreads;  // qk_nope <= 256
-  uint4 wv[kMaxVec];
-#pragma unroll
-  for (int u = 0; u < kMaxVec; ++u) {
-    const int e = tid + u * kAbsThreads;
-    if (e < nvec) {
-      const int i = e / (kAbsCols / 8), c8 = e % (kAbsCols / 8);
-      wv[u] = __ldg(reinterpret_cast<const uint4*>(W + (size_t)i * kDl + c8 * 8));
-    }
-  }
-#pragma unroll
-  for (int u = 0; u < kMaxVec; ++u) {
-    const int e = tid + u * kAbsThreads;
-    if (e < nvec) {
-      const int i = e / (kAbsCols / 8), c8 = e % (kAbsCols / 8);
-      *reinterpret_cast<uint4*>(Ws + i * kAbsCols + c8 * 8) = wv[u];
-    }
-  }
+  float* qn = reinterpret_cast<float*>(sm);      // [kAbsRows][Dn]
+  float* part = qn + kAbsRows * Dn;               // [kAbsGroups][kAbsRows][kAbsCols]
 
   if (cb == 0 && h == 0) {  // tile plan: tile_start[row] (exclusive prefix), bad[row]
     const int NR = p.sparse ? R : p.B;
@@ -726,79 +783,66 @@ __global__ void __launch_bounds__(kAbsThreads) absorb_kernel(const AbsorbParams 
     }
     if (tid == 0) p.tile_start[0] = 0;
   }
-  __syncthreads();
 
-  if (!p.do_qabs) {  // rotary part only, every (row, pair) in parallel
-    for (int e = tid; e < R * (kDr / 2); e += kAbsThreads) {
-      const int r = e / (kDr / 2), j = e % (kDr / 2), b = r / p.S, s = r % p.S;
-      const int Tb = p.T[b];
-      const int pos = (Tb < p.S || Tb > p.T_cap) ? 0 : Tb - p.S + s;
-      const double ang = (double)pos * p.theta[j];
-      const double k = rint(ang * 0.15915494309189535);
-      const float red = (float)fma(-k, 6.283185307179586, ang);
-      float sn, cs;
-      sincosf(red, &sn, &cs);
-      const __nv_bfloat16* qr = p.q + ((size_t)r * kH + h) * Dq + Dn;
-      const float x0 = __bfloat162float(qr[2 * j]), x1 = __bfloat162float(qr[2 * j + 1]);
-      __nv_bfloat16* dst = p.qcat + ((size_t)r * kH + h) * kDc + kDl;
-      dst[j] = __float2bfloat16_rn(x0 * cs - x1 * sn);
-      dst[kDr / 2 + j] = __float2bfloat16_rn(x1 * cs + x0 * sn);
+  // W_UK[h][:, cb*128 : cb*128+128] straight into registers: thread (grp, c8)
+  // holds rows grp, grp+16, ... of columns c8*8 .. c8*8+7.  All loads are in
+  // flight before anything else touches memory.
+  const int c8 = tid % (kAbsCols / 8), grp = tid / (kAbsCols / 8);
+  uint4 wv[NV];
+  if (p.do_qabs) {
+    const __nv_bfloat16* W = p.kv_b + (size_t)h * (Dn + p.Dv) * kDl + cb * kAbsCols + c8 * 8;
+#pragma unroll
+    for (int u = 0; u < NV; ++u) wv[u] = __ldg(reinterpret_cast<const uint4*>(W + (size_t)(grp + kAbsGroups * u) * kDl));
+  }
+  if (p.prefetch && tid == 0) {
+    // Everything the later kernels of this call read streams from HBM now,
+    // behind W_UK: W_UV rows (64 per CTA) and 1/nblk of every sequence's
+    // cache rows.
+    const int nblk = gridDim.x * gridDim.y, me = h * gridDim.x + cb;
+    const __nv_bfloat16* wuv = p.kv_b + ((size_t)h * (p.Dn + p.Dv) + p.Dn + (size_t)cb * (p.Dv / gridDim.x)) * kDl;
+    l2_prefetch(wuv, (uint32_t)(p.Dv / gridDim.x) * kDl * 2);
+    for (int b = 0; b < p.B; ++b) {
+      const int Tb = min(max(p.T[b], 0), p.T_cap);
+      const size_t lb = (size_t)Tb * kDl * 2, rb = (size_t)Tb * kDr * 2;
+      const size_t l0 = (lb * me / nblk) & ~(size_t)15, l1 = (lb * (me + 1) / nblk) & ~(size_t)15;
+      const size_t r0 = (rb * me / nblk) & ~(size_t)15, r1 = (rb * (me + 1) / nblk) & ~(size_t)15;
+      const unsigned char* lbase = reinterpret_cast<const unsigned char*>(p.Lc + (size_t)b * p.T_cap * kDl);
+      const unsigned char* rbase = reinterpret_cast<const unsigned char*>(p.Rc + (size_t)b * p.T_cap * kDr);
+      if (l1 > l0) l2_prefetch(lbase + l0, (uint32_t)(l1 - l0));
+      if (r1 > r0) l2_prefetch(rbase + r0, (uint32_t)(r1 - r0));
     }
+  }
+  if (!p.do_qabs) {  // rotary part only, every (row, pair) in parallel
+    for (int e = tid; e < R * (kDr / 2); e += kAbsThreads) rope_row(p, e / (kDr / 2), h, e % (kDr / 2));
     return;
   }
-  // Thread (col, half) sums i over one half of qk_nope; the halves meet in smem.
-  const int col = tid % kAbsCols, half = tid / kAbsCols;
-  const int i0 = half * (Dn / 2), i1 = i0 + Dn / 2;
-  float* part = qn + kAbsRows * Dn;  // [2][kAbsRows][kAbsCols]
-  for (int r0 = 0; r0 < R; r0 += kAbsRows) {
-    const int nr = min(kAbsRows, R - r0);
-    for (int e = tid; e < nr * Dn; e += kAbsThreads) {
-      const int rr = e / Dn, i = e % Dn;
-      qn[rr * Dn + i] = __bfloat162float(p.q[((size_t)(r0 + rr) * kH + h) * Dq + i]);
-    }
-    __syncthreads();
-    if (!p.do_qabs) {
-    } else if (nr == 1) absorb_rows<1>(Ws, qn, Dn, col, i0, i1, part, half);
-    else if (nr <= 4) absorb_rows<4>(Ws, qn, Dn, col, i0, i1, part, half);
-    else if (nr <= 8) absorb_rows<8>(Ws, qn, Dn, col, i0, i1, part, half);
-    else absorb_rows<kAbsRows>(Ws, qn, Dn, col, i0, i1, part, half);
-    __syncthreads();
-    for (int e = tid; e < (p.do_qabs ? nr * kAbsCols : 0); e += kAbsThreads) {
-      const int u = e / kAbsCols, c = e % kAbsCols;
-      const float v = part[u * kAbsCols + c] + part[(kAbsRows + u) * kAbsCols + c];
-      p.qcat[((size_t)(r0 + u) * kH + h) * kDc + cb * kAbsCols + c] = __float2bfloat16_rn(v);
-    }
-    if (cb == 0) {  // rotary part of the query, rotated to the row's own position
-      for (int e = tid; e < nr * (kDr / 2); e += kAbsThreads) {
-        const int rr = e / (kDr / 2), j = e % (kDr / 2);
-        const int r = r0 + rr, b = r / p.S, s = r % p.S;
-        const int Tb = p.T[b];
-        const int pos = (Tb < p.S || Tb > p.T_cap) ? 0 : Tb - p.S + s;
-        // angle in double, reduced to [-pi, pi] before the float sincos
-        const double ang = (double)pos * p.theta[j];
-        const double k = rint(ang * 0.15915494309189535);
-        const float red = (float)fma(-k, 6.283185307179586, ang);
-        float sn, cs;
-        sincosf(red, &sn, &cs);
-        const __nv_bfloat16* qr = p.q + ((size_t)r * kH + h) * Dq + Dn;
-        const float x0 = __bfloat162float(qr[2 * j]), x1 = __bfloat162float(qr[2 * j + 1]);
-        __nv_bfloat16* dst = p.qcat + ((size_t)r * kH + h) * kDc + kDl;
-        dst[j] = __float2bfloat16_rn(x0 * cs - x1 * sn);
-        dst[kDr / 2 + j] = __float2bfloat16_rn(x1 * cs + x0 * sn);
-      }
-    }
-    __syncthreads();
+  // R <= kAbsRows here (larger batches take the GEMM path)
+  for (int e = tid; e < R * Dn; e += kAbsThreads) {
+    const int rr = e / Dn, i = e % Dn;
+    qn[rr * Dn + i] = __bfloat162float(p.q[((size_t)rr * kH + h) * Dq + i]);
   }
+  __syncthreads();
+  absorb_regs<NV>(wv, qn, Dn, grp, R, part, c8);
+  __syncthreads();
+  for (int e = tid; e < R * kAbsCols; e += kAbsThreads) {
+    const int r = e / kAbsCols, col = e % kAbsCols;
+    float v = 0.f;
+#pragma unroll
+    for (int k = 0; k < kAbsGroups; ++k) v += part[((size_t)k * kAbsRows + r) * kAbsCols + col];
+    p.qcat[((size_t)r * kH + h) * kDc + cb * kAbsCols + col] = __float2bfloat16_rn(v);
+  }
+  if (cb == 0)
+    for (int e = tid; e < R * (kDr / 2); e += kAbsThreads) rope_row(p, e / (kDr / 2), h, e % (kDr / 2));
 }
 
 // ===========================================================================
 // Combine kernel: merge the splits of every (row, head) and lift with W_UV.
-// CTA = (64 output columns j, head h).  W_UV[h][j0:j0+64][:] is one
-// contiguous 64 KiB block, fetched with a single bulk async copy that runs
+// CTA = (128 output columns j, head h).  W_UV[h][j0:j0+128][:] is one
+// contiguous 128 KiB block, fetched with a single bulk async copy that runs
 // while the kernel waits for the attention grid.
 // ===========================================================================
 constexpr int kCmbThreads = 256;
-constexpr int kCmbJ = 64;
+constexpr int kCmbJ = 128;
 constexpr int kCmbRows = 8;
 constexpr int kCPitch = kDl + 4;   // floats per clat row in smem
 constexpr int kMaxPieces = 256;    // splits per row (<= CTAs of the attention grid)
@@ -832,6 +876,7 @@ __global__ void __launch_bounds__(kCmbThreads) combine_kernel(const CombineParam
   int* pslot = pcnt + kCmbRows;                                            // [kCmbRows][kMaxPieces]
   float* pm = reinterpret_cast<float*>(pslot + kCmbRows * kMaxPieces);     // split weights
   float* pw = pm + kCmbRows * kMaxPieces;                                  // split row sums
+  float4* red = reinterpret_cast<float4*>(pw + kCmbRows * kMaxPieces);     // [8 warps][128] partial clat
   __shared__ uint64_t wbar;
   const int jb = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
@@ -900,32 +945,44 @@ __global__ void __launch_bounds__(kCmbThreads) combine_kernel(const CombineParam
       if (lane == 0) pcnt[warp] = cnt;
     }
     __syncthreads();
-    // (b) clat[w][l] = sum_i weight_i * O_i[h][l]: all threads, two latents each
+    // (b) clat[w][l] = sum_i weight_i * O_i[h][l]: warp k takes splits k, k+8, ...
+    //     (all of their loads in flight together), lane covers latents
+    //     4*lane + 128*q; the eight warp sums meet in shared memory.
     for (int w = 0; w < nr; ++w) {
       const int cnt = pcnt[w];
-      float2 acc = make_float2(0.f, 0.f);
-      int i = 0;
-      for (; i + 4 <= cnt; i += 4) {
-        float2 o[4];
+      float4 acc[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          o[u] = *reinterpret_cast<const float2*>(p.o_part + ((size_t)pslot[w * kMaxPieces + i + u] * kH + h) * kDl +
-                                                  2 * tid);
+      for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (int i = warp; i < cnt; i += kCmbThreads / 32) {
+        const float wg = pm[w * kMaxPieces + i];
+        const float4* src =
+            reinterpret_cast<const float4*>(p.o_part + ((size_t)pslot[w * kMaxPieces + i] * kH + h) * kDl);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float wg = pm[w * kMaxPieces + i + u];
-          acc.x = fmaf(wg, o[u].x, acc.x);
-          acc.y = fmaf(wg, o[u].y, acc.y);
+        for (int q = 0; q < 4; ++q) {
+          const float4 o = src[lane + 32 * q];
+          acc[q].x = fmaf(wg, o.x, acc[q].x);
+          acc[q].y = fmaf(wg, o.y, acc[q].y);
+          acc[q].z = fmaf(wg, o.z, acc[q].z);
+          acc[q].w = fmaf(wg, o.w, acc[q].w);
         }
       }
-      for (; i < cnt; ++i) {
-        const float2 o =
-            *reinterpret_cast<const float2*>(p.o_part + ((size_t)pslot[w * kMaxPieces + i] * kH + h) * kDl + 2 * tid);
-        const float wg = pm[w * kMaxPieces + i];
-        acc.x = fmaf(wg, o.x, acc.x);
-        acc.y = fmaf(wg, o.y, acc.y);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) red[warp * 128 + lane + 32 * q] = acc[q];
+      __syncthreads();
+      if (tid < 128) {
+        float4 t = red[tid];
+#pragma unroll
+        for (int k = 1; k < kCmbThreads / 32; ++k) {
+          const float4 u = red[k * 128 + tid];
+          t.x += u.x;
+          t.y += u.y;
+          t.z += u.z;
+          t.w += u.w;
+        }
+        *reinterpret_cast<float4*>(clat + w * kCPitch + 4 * tid) = t;
       }
-      *reinterpret_cast<float2*>(clat + w * kCPitch + 2 * tid) = acc;
+      __syncthreads();
     }
     if (!w_ready) {
       volatile int no_abort = 0;
@@ -933,40 +990,62 @@ __global__ void __launch_bounds__(kCmbThreads) combine_kernel(const CombineParam
       w_ready = true;
     }
     __syncthreads();
-    // (c) out[r][h][j0 + j] = W_UV[j] . clat[r] (lanes split the latent axis)
+    // (c) out[r][h][j0 + j] = W_UV[j] . clat[r]: warp k owns kCmbJ/8 outputs, eight at a time;
+    //     lanes split the latent axis (16 values each), and the eight partial
+    //     sums are reduced together by a transposing butterfly.
 #pragma unroll 1
-    for (int jj = 0; jj < kCmbJ / 8; ++jj) {
-      const int j = warp * (kCmbJ / 8) + jj;
-      const __nv_bfloat16* wr = Ws + (size_t)j * kDl;
-      const uint4 wlo = *reinterpret_cast<const uint4*>(wr + 8 * lane);
-      const uint4 whi = *reinterpret_cast<const uint4*>(wr + 256 + 8 * lane);
-      float wf[16];
-      {
-        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&wlo);
-        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&whi);
+    for (int jb8 = 0; jb8 < kCmbJ / 64; ++jb8) {
+      const int jw = warp * (kCmbJ / 8) + 8 * jb8;
+      uint4 wlo[8], whi[8];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 fa = __bfloat1622float2(a2[q]);
-          const float2 fb = __bfloat1622float2(b2[q]);
-          wf[2 * q] = fa.x;
-          wf[2 * q + 1] = fa.y;
-          wf[8 + 2 * q] = fb.x;
-          wf[8 + 2 * q + 1] = fb.y;
-        }
+      for (int jj = 0; jj < 8; ++jj) {
+        const __nv_bfloat16* wr = Ws + (size_t)(jw + jj) * kDl;
+        wlo[jj] = *reinterpret_cast<const uint4*>(wr + 8 * lane);
+        whi[jj] = *reinterpret_cast<const uint4*>(wr + 256 + 8 * lane);
       }
       for (int w = 0; w < nr; ++w) {
         const float* cr = clat + w * kCPitch;
-        const float4 c0 = *reinterpret_cast<const float4*>(cr + 8 * lane);
-        const float4 c1 = *reinterpret_cast<const float4*>(cr + 8 * lane + 4);
-        const float4 c2 = *reinterpret_cast<const float4*>(cr + 256 + 8 * lane);
-        const float4 c3 = *reinterpret_cast<const float4*>(cr + 256 + 8 * lane + 4);
-        float d = wf[0] * c0.x;
-        d = fmaf(wf[1], c0.y, d); d = fmaf(wf[2], c0.z, d); d = fmaf(wf[3], c0.w, d);
-        d = fmaf(wf[4], c1.x, d); d = fmaf(wf[5], c1.y, d); d = fmaf(wf[6], c1.z, d); d = fmaf(wf[7], c1.w, d);
-        d = fmaf(wf[8], c2.x, d); d = fmaf(wf[9], c2.y, d); d = fmaf(wf[10], c2.z, d); d = fmaf(wf[11], c2.w, d);
-        d = fmaf(wf[12], c3.x, d); d = fmaf(wf[13], c3.y, d); d = fmaf(wf[14], c3.z, d); d = fmaf(wf[15], c3.w, d);
-        d = warp_sum(d);
-        if (lane == 0) p.out[((size_t)(r0 + w) * kH + h) * p.Dv + j0 + j] = d * inv_l[w];
+        float cv[16];
+        *reinterpret_cast<float4*>(&cv[0]) = *reinterpret_cast<const float4*>(cr + 8 * lane);
+        *reinterpret_cast<float4*>(&cv[4]) = *reinterpret_cast<const float4*>(cr + 8 * lane + 4);
+        *reinterpret_cast<float4*>(&cv[8]) = *reinterpret_cast<const float4*>(cr + 256 + 8 * lane);
+        *reinterpret_cast<float4*>(&cv[12]) = *reinterpret_cast<const float4*>(cr + 256 + 8 * lane + 4);
+        float d[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&wlo[jj]);
+          const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&whi[jj]);
+          float acc = 0.f;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const float2 fa = __bfloat1622float2(a2[t]);
+            const float2 fb = __bfloat1622float2(b2[t]);
+            acc = fmaf(fa.x, cv[2 * t], acc);
+            acc = fmaf(fa.y, cv[2 * t + 1], acc);
+            acc = fmaf(fb.x, cv[8 + 2 * t], acc);
+            acc = fmaf(fb.y, cv[8 + 2 * t + 1], acc);
+          }
+          d[jj] = acc;
+        }
+        // butterfly: after offsets 16, 8, 4 lane L holds output jw + ((L >> 2) & 7)'s
+        // partial over lanes {L ^ 3 mask}; offsets 2 and 1 finish the sum.
+#pragma unroll
+        for (int step = 0; step < 3; ++step) {
+          const int o = 16 >> step, hh = 4 >> step;
+          const bool upper = (lane & o) != 0;
+#pragma unroll
+          for (int i = 0; i < hh; ++i) {
+            const float send = upper ? d[i] : d[i + hh];
+            const float keep = upper ? d[i + hh] : d[i];
+            d[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+          }
+        }
+        d[0] += __shfl_xor_sync(0xffffffffu, d[0], 2);
+        d[0] += __shfl_xor_sync(0xffffffffu, d[0], 1);
+        if ((lane & 3) == 0) {
+          const int jj = 4 * ((lane >> 4) & 1) + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1);
+          p.out[((size_t)(r0 + w) * kH + h) * p.Dv + j0 + jw + jj] = d[0] * inv_l[w];
+        }
       }
     }
     __syncthreads();
@@ -1140,7 +1219,7 @@ cudaError_t set_smem_once(Kern kern, int bytes, std::atomic<unsigned long long>*
   return e;
 }
 
-std::atomic<unsigned long long> g_abs_attr{0}, g_attn_attr[2] = {{0}, {0}}, g_cmb_attr{0};
+std::atomic<unsigned long long> g_abs_attr[4] = {{0}, {0}, {0}, {0}}, g_attn_attr[2] = {{0}, {0}}, g_cmb_attr{0};
 
 Plan make_plan(int B, int S, int T_cap, int sparse_topk) {
   Plan pl{};
@@ -1261,12 +1340,14 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   ap.prefetch = (!big && !sparse && (long long)B * a.T_cap * (kDl + kDr) * 2 <= (48ll << 20)) ? 1 : 0;
   for (int j = 0; j < kDr / 2; ++j) ap.theta[j] = std::pow(g.rope_base, -2.0 * j / kDr);
   ap.flags = a.flags;
-  const size_t abs_smem = (size_t)g.Dn * kAbsCols * 2 + (size_t)kAbsRows * g.Dn * 4 +
-                          (size_t)2 * kAbsRows * kAbsCols * 4;
-  e = set_smem_once(absorb_kernel, 200 * 1024, &g_abs_attr);
+  const size_t abs_smem = (size_t)kAbsRows * g.Dn * 4 + (size_t)kAbsGroups * kAbsRows * kAbsCols * 4;
+  auto akern = absorb_kernel<4>;
+  if (!big) akern = g.Dn == 64 ? absorb_kernel<4> : g.Dn == 128 ? absorb_kernel<8> : g.Dn == 192 ? absorb_kernel<12>
+                                                                                               : absorb_kernel<16>;
+  e = set_smem_once(akern, (int)abs_smem, &g_abs_attr[big ? 0 : g.Dn / 64 - 1]);
   if (e != cudaSuccess) return e;
   kernel_mark(st, big ? "plan_rope" : "absorb");
-  e = launch_pdl(absorb_kernel, dim3(big ? 1 : kDl / kAbsCols, kH), dim3(kAbsThreads), abs_smem, st, ap);
+  e = launch_pdl(akern, dim3(big ? 1 : kDl / kAbsCols, kH), dim3(kAbsThreads), abs_smem, st, ap);
   if (e != cudaSuccess) return e;
   if (big) {  // qabs for many rows: per-head GEMM [R x qk_nope] x W_UK[h] on the tensor cores
     GemmArgs ga{};
@@ -1320,6 +1401,7 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   tp.T_cap = a.T_cap;
   tp.G = pl.G;
   tp.topk = a.topk;
+  tp.read_once = (sparse || S == 1) ? 1 : 0;
   tp.c = g.scale * kLog2e;
   tp.o_part = o_part;
   tp.ml_part = ml_part;
@@ -1392,7 +1474,7 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   cp.sparse = sparse ? 1 : 0;
   cp.flags = a.flags;
   const size_t cmb_smem = (size_t)kCmbWBytes + (size_t)kCmbRows * kCPitch * 4 + kCmbRows * 8 +
-                          (size_t)kCmbRows * kMaxPieces * 12;
+                          (size_t)kCmbRows * kMaxPieces * 12 + (size_t)(kCmbThreads / 32) * 128 * 16;
   e = set_smem_once(combine_kernel, (int)cmb_smem, &g_cmb_attr);
   if (e != cudaSuccess) return e;
   kernel_mark(st, "combine");
