@@ -41,6 +41,16 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 ROW_WORKLOADS = ("glm_batched_b32_s1", "glm_batched_b32_s6", "glm_dsa_t65536", "glm_prefill_s2048")
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a
+# workload's dominant kernel, from one ncu capture of that kernel on this
+# workload; an entry is dropped as soon as its kernel changes.
+NCU_TRAFFIC = {
+    ("glm_decode_t4096", "attention"): 4874240,
+    ("glm_batched_b32_s1", "attention"): 583135232,
+    ("glm_dsa_t65536", "index_scores"): 138084864,
+    ("glm_dsa_t65536", "topk_select"): 1097984,
+    ("glm_prefill_s2048", "flash_attention"): 795490304,
+}
 
 
 def peaks():
@@ -276,7 +286,7 @@ def time_e2e(e2e, K, W, flush, stream):
     return time_steps(one, K, W, flush, stream), h2d, d2h
 
 
-def roofline(work, ktimes, pk, pk_kind):
+def roofline(name, work, ktimes, pk, pk_kind):
     """Roofline of the kernel with the largest share of the step."""
     dom = max(ktimes, key=ktimes.get)
     bound, amount = work.get(dom, ("hbm", 0))
@@ -288,7 +298,7 @@ def roofline(work, ktimes, pk, pk_kind):
     total = sum(ktimes.values())
     return {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
             "frac": achieved / peak, "peak_source": pk_kind, "algorithmic_per_launch": amount,
-            "kernel_us": ktimes[dom], "traffic": None,
+            "kernel_us": ktimes[dom], "traffic": NCU_TRAFFIC.get((name, dom)),
             "kernels": {n: {"us": round(v, 2), "share": round(v / total, 3)} for n, v in ktimes.items()}}
 
 
@@ -303,7 +313,7 @@ def measure(name, dev, stream, flush, K, W, pk, pk_kind, want_e2e):
     g = capture(calls, stream)
     ms = time_steps(g.replay, K, W, flush, stream)
     kt = kernel_times(calls, max(3, min(K, 20)), flush, stream)
-    res = {"ms": ms, "info": info, "ktimes": kt, "roof": roofline(work, kt, pk, pk_kind)}
+    res = {"ms": ms, "info": info, "ktimes": kt, "roof": roofline(name, work, kt, pk, pk_kind)}
     if want_e2e and e2e is not None:
         res["e2e"] = time_e2e(e2e, K, W, flush, stream)
     del x, calls, g
@@ -469,6 +479,7 @@ def main():
                     rows[wl] = {"us_per_step": t * 1e6, "tokens_s": r["info"]["tokens"] / t,
                                 "hbm_gbs_algorithmic": r["info"]["alg_bytes"] / t / 1e9,
                                 "roofline": {k: r["roof"][k] for k in ("kernel", "bound", "achieved", "unit", "frac",
+                                                                       "traffic", "algorithmic_per_launch",
                                                                        "kernels")}}
                     if "flops" in r["info"]:
                         rows[wl]["tflops"] = r["info"]["flops"] / t / 1e12
