@@ -397,6 +397,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     };
     while (ok && c.live) {
       const bool first = c.first();
+      // keys of this tile, read now so that the load overlaps the waits below
+      const int ksteps = (tile_keys<kSparse>(p, c.row, s, c.k) + 15) >> 4;
       if (first) {
         ++pc;
         ok = wait(&q_full, pc & 1);
@@ -429,7 +431,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       if (!ok) break;
       tc_fence_after();
       if (lane == 0) {
-        const int ksteps = (tile_keys<kSparse>(p, c.row, s, c.k) + 15) >> 4;
         for (int m = 0; m < 4; ++m) {
           for (int kk = 0; kk < ksteps; ++kk) {
             const uint64_t da = smem_desc_sw128(kv0 + (2 * m) * kSlotBytes + kk * 2048, kSlotBytes, 1024);

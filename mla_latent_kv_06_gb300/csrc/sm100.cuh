@@ -122,6 +122,11 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x
 }
 
 // Pull a contiguous global range (16-byte aligned, size a multiple of 16) into L2.
+// One 128-byte line into L2 through the load/store unit (never blocks the issuing thread).
+__device__ __forceinline__ void l2_prefetch_line(const void* gaddr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(gaddr));
+}
+
 __device__ __forceinline__ void l2_prefetch(const void* gaddr, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gaddr), "r"(bytes) : "memory");
 }
