@@ -331,6 +331,166 @@ __global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(TopkArgs a) {
   if (tid == 0) a.nsel[row] = tot;
 }
 
+
+// ---------------------------------------------------------------------------
+// Cluster top-k.  A cluster of kTkC CTAs (1024 threads each) handles one
+// (b, s) row: thread t of cluster rank r holds the ordered keys of scores
+// [(r*1024 + t)*per, +per) in registers, so the scores are read once.  Three
+// radix passes (digits 31..21, 20..10, 9..0) each build a shared-memory
+// histogram per CTA; every CTA then sums the kTkC histograms through
+// distributed shared memory and picks the same digit.  The result is the key
+// K of the k-th largest score and the number of keys equal to K to keep; an
+// index-ordered compaction (CTA totals exchanged the same way) writes the
+// kept indices in ascending order, equal keys from the lowest index up.
+// ---------------------------------------------------------------------------
+constexpr int kTkC = 8;          // CTAs per row (portable cluster size)
+constexpr int kTkMaxPer = 16;    // keys per thread held in registers
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Read an int from the shared memory of CTA `rank` of this cluster, at the
+// address that `p` has in this CTA.
+__device__ __forceinline__ int ld_cluster_int(const int* p, uint32_t rank) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  int v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(ra) : "memory");
+  return v;
+}
+
+// Adds 1 to hist[bin] for every lane with active != 0, one atomic per
+// distinct bin in the warp (the integer-valued scores crowd a few bins).
+__device__ __forceinline__ void warp_hist_add(int* hist, uint32_t bin, bool active) {
+  const unsigned am = __ballot_sync(0xffffffffu, active);
+  if (!active) return;
+  const unsigned peers = __match_any_sync(am, bin);
+  const int leader = __ffs(peers) - 1;
+  if ((int)(threadIdx.x & 31) == leader) atomicAdd(&hist[bin], __popc(peers));
+}
+
+// Global histogram of one pass: the kTkC per-CTA histograms summed into
+// tot[] (bins split over the threads).  Bracketed by cluster barriers: local
+// histograms complete before, tot[] ready after.
+__device__ __forceinline__ void cluster_hist_sum(const int* local, int* tot, int nbins) {
+  cluster_sync_all();
+  for (int i = threadIdx.x; i < nbins; i += kTopkThreads) {
+    int v = 0;
+#pragma unroll
+    for (int c = 0; c < kTkC; ++c) v += ld_cluster_int(local + i, (uint32_t)c);
+    tot[i] = v;
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kTopkThreads) topk_cluster_kernel(TopkArgs a, int per) {
+  const uint32_t rank = cluster_rank();
+  const int row = blockIdx.x / kTkC;
+  const int b = row / a.S, s = row - b * a.S;
+  const int tid = threadIdx.x;
+  const int k = a.topk;
+  int32_t* sel = a.sel + (size_t)row * k;
+  __shared__ int hist[3][2048];  // this CTA's histogram of each pass (read by the cluster)
+  __shared__ int tot[2048];      // the pass's cluster-wide histogram
+  __shared__ int red[32];
+  __shared__ uint32_t sh_prefix;
+  __shared__ int sh_rem;
+  __shared__ int cta_cnt[2];     // this CTA's keys > K and keys == K (read by the cluster)
+
+  const int Tb = a.T[b];
+  // Rows that need no selection: every CTA of the cluster takes the same branch.
+  if (Tb < a.S || Tb > a.T_cap) {
+    if (rank == 0) {
+      if (tid == 0) {
+        raise_flag(a.flags, MLA_DEV_BAD_LENGTH);
+        a.nsel[row] = 0;
+      }
+      for (int j = tid; j < k; j += kTopkThreads) sel[j] = -1;
+    }
+    return;
+  }
+  const int n = Tb - a.S + s + 1;
+  if (n <= k) {  // keep all keys 0..pos
+    if (rank == 0) {
+      for (int j = tid; j < k; j += kTopkThreads) sel[j] = (j < n) ? j : -1;
+      if (tid == 0) a.nsel[row] = n;
+    }
+    return;
+  }
+  const float* sc = a.scores + (size_t)row * a.T_cap;
+  const int base = ((int)rank * kTopkThreads + tid) * per;
+  uint32_t key[kTkMaxPer];
+#pragma unroll
+  for (int i = 0; i < kTkMaxPer; ++i) key[i] = (i < per && base + i < n) ? ordered_key(sc[base + i]) : 0u;
+  for (int i = tid; i < 3 * 2048; i += kTopkThreads) (&hist[0][0])[i] = 0;
+  __syncthreads();
+
+  // pass 1: bits 31..21
+#pragma unroll
+  for (int i = 0; i < kTkMaxPer; ++i)
+    if (i < per) warp_hist_add(hist[0], key[i] >> 21, base + i < n);
+  cluster_hist_sum(hist[0], tot, 2048);
+  int remaining = k;
+  uint32_t prefix = pick_digit(tot, 2048, 21, 0u, &remaining, red, &sh_prefix, &sh_rem);
+  // pass 2: bits 20..10 of the keys in the chosen bin
+#pragma unroll
+  for (int i = 0; i < kTkMaxPer; ++i)
+    if (i < per) warp_hist_add(hist[1], (key[i] >> 10) & 2047u, base + i < n && (key[i] >> 21) == (prefix >> 21));
+  cluster_hist_sum(hist[1], tot, 2048);
+  prefix = pick_digit(tot, 2048, 10, prefix, &remaining, red, &sh_prefix, &sh_rem);
+  // pass 3: bits 9..0
+#pragma unroll
+  for (int i = 0; i < kTkMaxPer; ++i)
+    if (i < per) warp_hist_add(hist[2], key[i] & 1023u, base + i < n && (key[i] >> 10) == (prefix >> 10));
+  cluster_hist_sum(hist[2], tot, 1024);
+  prefix = pick_digit(tot, 1024, 0, prefix, &remaining, red, &sh_prefix, &sh_rem);
+  // prefix = key K of the k-th largest score; `remaining` keys equal to K are kept.
+
+  int n_gt = 0, n_eq = 0;
+#pragma unroll
+  for (int i = 0; i < kTkMaxPer; ++i)
+    if (i < per && base + i < n) {
+      n_gt += key[i] > prefix;
+      n_eq += key[i] == prefix;
+    }
+  int cta_eq, cta_gt;
+  const int eq_before_cta = block_exclusive_scan(n_eq, red, &cta_eq);
+  const int gt_before_cta = block_exclusive_scan(n_gt, red, &cta_gt);
+  if (tid == 0) {
+    cta_cnt[0] = cta_gt;
+    cta_cnt[1] = cta_eq;
+  }
+  cluster_sync_all();
+  // keys kept by the lower-ranked CTAs
+  int eq_lower = 0, out_lower = 0;
+  for (uint32_t c = 0; c < rank; ++c) {
+    const int g_c = ld_cluster_int(&cta_cnt[0], c), e_c = ld_cluster_int(&cta_cnt[1], c);
+    out_lower += g_c + max(0, min(e_c, remaining - eq_lower));
+    eq_lower += e_c;
+  }
+  const int eq_before = eq_lower + eq_before_cta;
+  // equal keys kept before this thread's segment, inside this CTA
+  const int take_before_cta = max(0, min(eq_before_cta, remaining - eq_lower));
+  int o = out_lower + gt_before_cta + take_before_cta;
+  int eq_rank = eq_before;
+#pragma unroll
+  for (int i = 0; i < kTkMaxPer; ++i)
+    if (i < per && base + i < n) {
+      const bool take = (key[i] > prefix) || (key[i] == prefix && eq_rank++ < remaining);
+      if (take) sel[o++] = base + i;
+    }
+  if (rank == 0 && tid == 0) a.nsel[row] = k;
+  cluster_sync_all();  // no CTA leaves while another may still read its shared memory
+}
+
 }  // namespace
 
 cudaError_t launch_index_scores(const IndexArgs& a, cudaStream_t st) {
@@ -348,6 +508,25 @@ cudaError_t launch_index_scores(const IndexArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_topk_select(const TopkArgs& a, cudaStream_t st) {
+  // Rows up to kTkC * 1024 * kTkMaxPer keys: one cluster per row, keys in registers.
+  const long long per = ((long long)a.T_cap + kTkC * kTopkThreads - 1) / (kTkC * kTopkThreads);
+  if (per <= kTkMaxPer) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(a.B * a.S * kTkC);
+    cfg.blockDim = dim3(kTopkThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kTkC;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, a, (int)(per < 1 ? 1 : per));
+    if (e == cudaSuccess) return cudaSuccess;
+    (void)cudaGetLastError();  // clusters unavailable: single-CTA kernel below
+  }
   const int smem = kCand * 4;
   cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;

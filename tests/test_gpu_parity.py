@@ -144,10 +144,13 @@ def test_topk_ties_and_negative_zero(cuda_lib):
     assert np.array_equal(sel.cpu().numpy(), rsel) and np.array_equal(nsel.cpu().numpy(), rn)
 
 
-@pytest.mark.parametrize("lo,hi,T", [(1.0, 1.25, [40000, 39000]), (1.0, 1.25, [9000]), (-3.0, 5.0, [65536])])
+@pytest.mark.parametrize("lo,hi,T", [(1.0, 1.25, [40000, 39000]), (1.0, 1.25, [9000]), (-3.0, 5.0, [65536]),
+                                     (1.0, 1.25, [140000, 2500]), (-3.0, 5.0, [140000])])
 def test_topk_crowded_and_spread_scores(cuda_lib, lo, hi, T):
-    """Scores in [1, 1.25) share their top 11 key bits: more than 16384 of them
-    overflow the in-smem candidate list (fallback passes); fewer stay in smem."""
+    """Scores in [1, 1.25) share their top 11 key bits (crowded radix bins).
+    Rows up to 131072 keys run the cluster kernel; the 140000-key cases run
+    the single-CTA kernel, whose crowded case overflows its in-smem candidate
+    list and takes the fallback passes."""
     r = np.random.default_rng(9)
     T_cap = max(T)
     k = 2048
