@@ -325,7 +325,7 @@ MLA_EXPORT int dsa_index_scores(int B, int S, int n_ih, int index_hd, const floa
   size_t smem = sizeof(float) * ((size_t)n_ih * index_hd + n_ih + 128 * (size_t)(index_hd + 1) + 256);
   if (smem > 220 * 1024)
     return fail(MLA_ERR_UNSUPPORTED, "n_ih*index_hd too large for one CTA (%zu bytes)", smem);
-  mla::IndexArgs a{B, S, n_ih, index_hd, T_cap, q_idx, w, Ic, T, scores, flags_ptr()};
+  mla::IndexArgs a{B, S, n_ih, index_hd, T_cap, q_idx, w, Ic, T, scores, flags_ptr(), g_wait_limit_ns.load()};
   if (!a.flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   mla::call_begin();

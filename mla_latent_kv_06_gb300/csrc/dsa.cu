@@ -494,6 +494,9 @@ __global__ void __launch_bounds__(kTopkThreads) topk_cluster_kernel(TopkArgs a, 
 }  // namespace
 
 cudaError_t launch_index_scores(const IndexArgs& a, cudaStream_t st) {
+  // 32 heads x 128: the tensor-core kernel (index_tc.cu); other shapes stay on the CUDA cores
+  const cudaError_t tc = launch_index_scores_tc(a, st);
+  if (tc != cudaErrorNotSupported) return tc;
   const bool fast = a.n_ih == 32 && a.hd == 128;
   const int ld = fast ? kKPitch : a.hd + 1;
   size_t smem = sizeof(float) * ((size_t)a.n_ih * a.hd + ((a.n_ih + 3) & ~3) + (size_t)kTile * ld + 8 * kTile);

@@ -54,9 +54,13 @@ struct IndexArgs {
   const int32_t* T;
   float* scores;
   unsigned int* flags;
+  long long wait_ns;  // bound of every wait inside a kernel
 };
 
 cudaError_t launch_index_scores(const IndexArgs& a, cudaStream_t st);
+// Tensor-core indexer (32 index heads x 128, fp32 through three tf32 products);
+// returns cudaErrorNotSupported when the request does not fit it.
+cudaError_t launch_index_scores_tc(const IndexArgs& a, cudaStream_t st);
 
 struct TopkArgs {
   int B, S, T_cap, topk;

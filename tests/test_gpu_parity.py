@@ -131,6 +131,27 @@ def test_index_and_topk_bit_exact(cuda_lib, T, S, nh, hd, k):
     assert np.array_equal(sel.cpu().numpy(), rsel)
 
 
+@pytest.mark.parametrize("T,S,nh,hd", [([3000, 517, 129], 2, 32, 128), ([70000], 1, 32, 128), ([1000, 300], 1, 4, 32)])
+def test_index_scores_general_floats(cuda_lib, T, S, nh, hd):
+    """Non-integer fp32 indexer inputs: scores within 1e-5 (normwise) of the fp64
+    definition, -inf exactly past each query's position.  32 heads x 128 run
+    on the tensor cores (three tf32 products), other shapes on the CUDA cores."""
+    r = np.random.default_rng(11)
+    B, T_cap = len(T), max(T) + 45
+    q = r.standard_normal((B, S, nh, hd)).astype(np.float32)
+    w = r.standard_normal((B, S, nh)).astype(np.float32)
+    Ic = r.standard_normal((B, T_cap, hd)).astype(np.float32)
+    for b, t in enumerate(T):
+        Ic[b, t:] = np.nan
+    Tt = torch.tensor(T, dtype=torch.int32, device=DEV)
+    sc = to_np(cuda_lib.index_scores(*(torch.from_numpy(x).to(DEV) for x in (q, w, Ic)), Tt))
+    ref = oracle.index_scores(q.astype(np.float64), w.astype(np.float64), Ic.astype(np.float64), T)
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isneginf(sc), np.isneginf(ref)) and np.all(np.isfinite(sc[fin]))
+    assert max_rel_err(sc[fin], ref[fin]) < 1e-5
+    assert cuda_lib.device_status() == 0
+
+
 def test_topk_ties_and_negative_zero(cuda_lib):
     """Many equal scores, +0.0 and -0.0 mixed: the lower index wins."""
     r = np.random.default_rng(3)
