@@ -734,7 +734,7 @@ __global__ void __launch_bounds__(kAbsThreads, 2) absorb_kernel(const AbsorbPara
   // earlier call that still reads the workspace): wait before touching memory.
   grid_dep_wait();
   grid_dep_launch();
-  extern __shared__ __align__(16) unsigned char sm[];
+  extern __shared__ __align__(128) unsigned char sm[];
   const int cb = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   const int Dn = p.Dn, Dq = Dn + kDr;
   const int R = p.B * p.S;
