@@ -47,8 +47,8 @@ ROW_WORKLOADS = ("glm_batched_b32_s1", "glm_batched_b32_s6", "glm_dsa_t65536", "
 NCU_TRAFFIC = {
     ("glm_decode_t4096", "attention"): 4874240,
     ("glm_batched_b32_s1", "attention"): 583135232,
-    ("glm_dsa_t65536", "index_scores"): 138084864,
-    ("glm_dsa_t65536", "topk_select"): 1097984,
+    ("glm_dsa_t65536", "index_scores"): 138440192,
+    ("glm_dsa_t65536", "topk_select"): 1111552,
     ("glm_prefill_s2048", "flash_attention"): 795490304,
 }
 
