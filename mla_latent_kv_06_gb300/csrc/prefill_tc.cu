@@ -8,12 +8,14 @@
 //      k_rot = Rc[t] shared by all heads, softmax, and a value sum.
 //
 // Step 2 is a flash-attention forward on tcgen05.  CTA = (128 queries, head,
-// sequence).  Query rows live in the 128 TMEM lanes, so every softmax thread
-// owns one query row and its max / sum / rescale stay in registers.  Per
+// sequence).  Query rows live in the 128 TMEM lanes; two softmax threads share
+// a row (32 keys of each tile and 128 value columns each), so max, sum and
+// rescale stay in registers but for one shared-memory exchange.  Per
 // 64-key tile j:
 //   S(j)  = Q K(j)^T       M=128, N=64,  K=256  (Q and K K-major)
 //   O    += P(j-1) V(j-1)  M=128, N=256, K=64   (P K-major, V MN-major)
-// with K/V double-buffered in shared memory (TMA), S and P double-buffered.
+// with K and V double-buffered in shared memory (TMA; K released by the score
+// product, V by the value product), S and P double-buffered.
 #include <atomic>
 #include <cmath>
 
@@ -42,7 +44,8 @@ constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffKV = kQBytes;                        // 2 stages of K | V
 constexpr uint32_t kOffP = kOffKV + 2 * (kKBytes + kVBytes);
 constexpr uint32_t kPrefillSmem = kOffP + 2 * kPBytes + 1024;
-constexpr int kPThreads = 192;
+constexpr int kSoftThreads = 256;  // eight softmax warps
+constexpr int kPThreads = 64 + kSoftThreads;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;    // two S buffers of 64 columns
 constexpr uint32_t kTmemO = 128;  // O: 256 columns
@@ -65,6 +68,16 @@ struct FlashParams {
 
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+__device__ __forceinline__ bool bar_red_or(int id, int n, bool x) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)x), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
 __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_constant__ FlashParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -74,9 +87,14 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
   unsigned char* sP = smem + kOffP;
   // o_done[j & 1] completes its (j >> 1)-th phase when O += P(j) V(j) retires;
   // the product for tile j + 2 needs P(j + 2), so parity waits never alias.
-  __shared__ uint64_t q_full, q_rope, kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full[2], o_done[2], mma_done;
+  __shared__ uint64_t q_full, q_rope, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2], p_full[2],
+      o_done[2], mma_done;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
+  // [half][row]: the halves' maxima, after the loop their row sums.  A thread
+  // rewrites its entry only after the bar.red that ends each tile, which its
+  // partner reaches after reading it.
+  __shared__ float red_row[2][kQT];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int s0 = qt * kQT;
@@ -85,13 +103,15 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
 
   if (threadIdx.x == 0) {
     mbar_init(&q_full, 1);
-    mbar_init(&q_rope, 128);
+    mbar_init(&q_rope, kSoftThreads);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 128);
-      mbar_init(&p_full[i], 128);
+      mbar_init(&s_free[i], kSoftThreads);
+      mbar_init(&p_full[i], kSoftThreads);
       mbar_init(&o_done[i], 1);
     }
     mbar_init(&mma_done, 1);
@@ -118,25 +138,42 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
       bool ok = true;
       mbar_arrive_expect_tx(&q_full, 3 * kQAtom);
       for (int a = 0; a < 3; ++a) tma_load_3d(sQ + a * kQAtom, &p.mQ, 64 * a, h, b * p.S + s0, &q_full);
-      int last = -1;
-      for (int j = 0; j < nkt && ok; ++j) {
+      // K of tile j is released by its score product, V by its value product:
+      // the key half of the stream runs one tile ahead of the value half.
+      int last_k = -1, last_v = -1;
+      auto load_k = [&](int j) -> bool {
         const int st = j & 1;
-        ok = mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1, abort, p.flags, p.wait_ns);
-        if (!ok) break;
+        if (!mbar_wait(&k_empty[st], ((j >> 1) & 1) ^ 1, abort, p.flags, p.wait_ns)) return false;
         unsigned char* sK = sKV + st * (kKBytes + kVBytes);
-        unsigned char* sV = sK + kKBytes;
         const int y = b * p.Tk + j * kKT;
-        mbar_arrive_expect_tx(&kv_full[st], kKBytes + kVBytes);
-        for (int a = 0; a < 3; ++a) tma_load_2d(sK + a * kKAtom, &p.mKV, h * kDkv + 64 * a, y, &kv_full[st]);
-        tma_load_2d(sK + 3 * kKAtom, &p.mR, 0, y, &kv_full[st]);
-        for (int a = 0; a < 4; ++a) tma_load_2d(sV + a * kKAtom, &p.mKV, h * kDkv + kDn + 64 * a, y, &kv_full[st]);
-        last = j;
+        mbar_arrive_expect_tx(&k_full[st], kKBytes);
+        for (int a = 0; a < 3; ++a) tma_load_2d(sK + a * kKAtom, &p.mKV, h * kDkv + 64 * a, y, &k_full[st]);
+        tma_load_2d(sK + 3 * kKAtom, &p.mR, 0, y, &k_full[st]);
+        last_k = j;
+        return true;
+      };
+      auto load_v = [&](int j) -> bool {
+        const int st = j & 1;
+        if (!mbar_wait(&v_empty[st], ((j >> 1) & 1) ^ 1, abort, p.flags, p.wait_ns)) return false;
+        unsigned char* sV = sKV + st * (kKBytes + kVBytes) + kKBytes;
+        const int y = b * p.Tk + j * kKT;
+        mbar_arrive_expect_tx(&v_full[st], kVBytes);
+        for (int a = 0; a < 4; ++a) tma_load_2d(sV + a * kKAtom, &p.mKV, h * kDkv + kDn + 64 * a, y, &v_full[st]);
+        last_v = j;
+        return true;
+      };
+      if (nkt > 0) ok = load_k(0);
+      for (int j = 0; j < nkt && ok; ++j) {
+        if (j + 1 < nkt) ok = load_k(j + 1);
+        if (ok) ok = load_v(j);
       }
       volatile int no_abort = 0;
       const long long dn = p.wait_ns > kDrainNs ? p.wait_ns : kDrainNs;
       mbar_wait(&q_full, 0, &no_abort, p.flags, dn);
-      for (int j = last - 1; j <= last; ++j)
-        if (j >= 0) mbar_wait(&kv_full[j & 1], (j >> 1) & 1, &no_abort, p.flags, dn);
+      for (int j = last_k - 1; j <= last_k; ++j)
+        if (j >= 0) mbar_wait(&k_full[j & 1], (j >> 1) & 1, &no_abort, p.flags, dn);
+      for (int j = last_v - 1; j <= last_v; ++j)
+        if (j >= 0) mbar_wait(&v_full[j & 1], (j >> 1) & 1, &no_abort, p.flags, dn);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -149,6 +186,7 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
       bool issued = false;
       auto pv = [&](int j) -> bool {  // O += P(j) V(j)
         if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1, abort, p.flags, p.wait_ns)) return false;
+        if (!mbar_wait(&v_full[j & 1], (j >> 1) & 1, abort, p.flags, p.wait_ns)) return false;
         tc_fence_after();
         const uint32_t v0 = kv0 + (j & 1) * (kKBytes + kVBytes) + kKBytes;
         const uint32_t pp = p0 + (j & 1) * kPBytes;
@@ -158,14 +196,14 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
           const uint64_t db = smem_desc_sw128(v0 + kk * 2048, kKAtom, 1024);
           mma_bf16(tmem + kTmemO, da, db, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&kv_empty[j & 1]);
+        mma_commit(&v_empty[j & 1]);
         mma_commit(&o_done[j & 1]);
         return true;
       };
       for (int j = 0; j < nkt && ok; ++j) {
         const int st = j & 1, n = j >> 1;
         ok = mbar_wait(&s_free[st], (n & 1) ^ 1, abort, p.flags, p.wait_ns) &&
-             mbar_wait(&kv_full[st], n & 1, abort, p.flags, p.wait_ns);
+             mbar_wait(&k_full[st], n & 1, abort, p.flags, p.wait_ns);
         if (!ok) break;
         tc_fence_after();
         const uint32_t k0 = kv0 + st * (kKBytes + kVBytes);
@@ -178,6 +216,7 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
             mma_bf16(tmem + kTmemS + 64 * st, da, db, idesc_s, (a | kk) != 0);
           }
         mma_commit(&s_full[st]);
+        mma_commit(&k_empty[st]);
         issued = true;
         if (j > 0) ok = pv(j - 1);
       }
@@ -190,43 +229,52 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax warps 2..5 (one query row each)
+    // ------------------------------------------------------------ softmax warps 2..9
+    // Thread (row m, half) owns keys 32*half .. 32*half+31 of each tile of
+    // query row m and value columns 128*half .. 128*half+127; the two halves of
+    // a row exchange their maxima through shared memory.
     const int wq = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int m = 32 * wq + lane;
     const int s = s0 + m;
     const bool row_ok = s < p.S;
     const int pos = p.pos_base + s;
     const uint32_t t_lane = (uint32_t)(32 * wq) << 16;
-    // rotary part of the query row into Q atom 3 (128-byte swizzled like TMA would)
+    // rotary part of the query row into Q atom 3 (128-byte swizzled like TMA
+    // would): this half writes y[16*half ..] and y[32 + 16*half ..]
     {
-      uint32_t pk[32];
+      uint32_t lo[8], hi[8];
       if (row_ok) {
         const __nv_bfloat16* qr = p.q + (((size_t)b * p.S + s) * kH + h) * kDq + kDn;
 #pragma unroll
-        for (int j = 0; j < kDr / 2; j += 2) {
+        for (int u = 0; u < 16; u += 2) {
           float r0[2], r1[2];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const double ang = (double)pos * p.theta[j + u];
+          for (int v2 = 0; v2 < 2; ++v2) {
+            const int jj = 16 * half + u + v2;
+            const double ang = (double)pos * p.theta[jj];
             const double kq = rint(ang * 0.15915494309189535);
             const float red = (float)fma(-kq, 6.283185307179586, ang);
             float sn, cs;
             sincosf(red, &sn, &cs);
-            const float x0 = __bfloat162float(qr[2 * (j + u)]), x1 = __bfloat162float(qr[2 * (j + u) + 1]);
-            r0[u] = x0 * cs - x1 * sn;   // -> y[j + u]
-            r1[u] = x1 * cs + x0 * sn;   // -> y[32 + j + u]
+            const float x0 = __bfloat162float(qr[2 * jj]), x1 = __bfloat162float(qr[2 * jj + 1]);
+            r0[v2] = x0 * cs - x1 * sn;   // -> y[jj]
+            r1[v2] = x1 * cs + x0 * sn;   // -> y[32 + jj]
           }
-          pk[j / 2] = pack2(r0[0], r0[1]);
-          pk[16 + j / 2] = pack2(r1[0], r1[1]);
+          lo[u / 2] = pack2(r0[0], r0[1]);
+          hi[u / 2] = pack2(r1[0], r1[1]);
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) pk[i] = 0u;
+        for (int i = 0; i < 8; ++i) lo[i] = hi[i] = 0u;
       }
       unsigned char* row = sQ + 3 * kQAtom + m * 128;
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc)
-        *reinterpret_cast<uint4*>(row + ((cc ^ (m & 7)) << 4)) = make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c_lo = 2 * half + cc, c_hi = 4 + 2 * half + cc;
+        *reinterpret_cast<uint4*>(row + ((c_lo ^ (m & 7)) << 4)) = make_uint4(lo[4 * cc], lo[4 * cc + 1], lo[4 * cc + 2], lo[4 * cc + 3]);
+        *reinterpret_cast<uint4*>(row + ((c_hi ^ (m & 7)) << 4)) = make_uint4(hi[4 * cc], hi[4 * cc + 1], hi[4 * cc + 2], hi[4 * cc + 3]);
+      }
       fence_proxy_async_smem();
       mbar_arrive(&q_rope);
     }
@@ -235,31 +283,38 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
     bool ok = true;
     for (int j = 0; j < nkt && ok; ++j) {
       const int st = j & 1;
-      ok = mbar_wait(&s_full[st], (j >> 1) & 1, abort, p.flags, p.wait_ns);
-      ok = __all_sync(0xffffffffu, ok);  // the warp leaves together (warp-wide tcgen05 ops follow)
-      if (!ok) break;
+      // failed waits are decided jointly by the 256 softmax threads (bar.red),
+      // so that none is left at a barrier the others quit
+      bool fail = !mbar_wait(&s_full[st], (j >> 1) & 1, abort, p.flags, p.wait_ns);
+      if (bar_red_or(2, kSoftThreads, fail)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
-      float v[64];
-      tmem_ld64(tmem + t_lane + kTmemS + 64 * st, v);
+      float v[32];
+      tmem_ld32(tmem + t_lane + kTmemS + 64 * st + 32 * half, v);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&s_free[st]);
-      const int t0 = j * kKT;
-      const int nvalid = row_ok ? min(kKT, pos - t0 + 1) : 0;  // keys t0..t0+nvalid-1 are visible
+      const int t0 = j * kKT + 32 * half;
+      const int nvalid = row_ok ? max(0, min(32, pos - t0 + 1)) : 0;  // keys t0..t0+nvalid-1 are visible
       float mx = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 64; ++i)
+      for (int i = 0; i < 32; ++i)
         if (i < nvalid) mx = fmaxf(mx, v[i]);
+      red_row[half][m] = mx;
+      named_barrier(1, kSoftThreads);
+      mx = fmaxf(red_row[0][m], red_row[1][m]);
       float alpha = 1.f;
       const float cand = mx * c;
       if (cand > m_run + kTau) {
         alpha = exp2f(m_run - cand);
         m_run = cand;
       }
-      uint32_t pk[32];
+      uint32_t pk[16];
       float psum = 0.f;
 #pragma unroll
-      for (int i = 0; i < 64; i += 2) {
+      for (int i = 0; i < 32; i += 2) {
         const float e0 = i < nvalid ? exp2f(fmaf(v[i], c, -m_run)) : 0.f;
         const float e1 = i + 1 < nvalid ? exp2f(fmaf(v[i + 1], c, -m_run)) : 0.f;
         pk[i / 2] = pack2(e0, e1);
@@ -269,36 +324,46 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
       l = l * alpha + psum;
       unsigned char* prow = sP + st * kPBytes + m * 128;
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc)
-        *reinterpret_cast<uint4*>(prow + ((cc ^ (m & 7)) << 4)) = make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-      // O rows of this warp rescaled (tcgen05.ld/st are warp-wide) once O += P(j-1)V(j-1) retired
+      for (int cc = 0; cc < 4; ++cc)
+        *reinterpret_cast<uint4*>(prow + (((4 * half + cc) ^ (m & 7)) << 4)) =
+            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+      // this thread's O columns rescaled (tcgen05.ld/st are warp-wide) once O += P(j-1)V(j-1) retired
+      fail = false;
       if (__any_sync(0xffffffffu, alpha != 1.f && j > 0)) {
-        ok = mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort, p.flags, p.wait_ns);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after();
+        fail = !__all_sync(0xffffffffu,
+                           mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort, p.flags, p.wait_ns));
+        if (!fail) {
+          tc_fence_after();
 #pragma unroll 1
-        for (int cb = 0; cb < kDv; cb += 64) {
-          float w[64];
-          tmem_ld64(tmem + t_lane + kTmemO + cb, w);
-          tmem_wait_ld();
+          for (int cb = 128 * half; cb < 128 * half + 128; cb += 64) {
+            float w[64];
+            tmem_ld64(tmem + t_lane + kTmemO + cb, w);
+            tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 64; ++i) w[i] *= alpha;
-          tmem_st64(tmem + t_lane + kTmemO + cb, w);
+            for (int i = 0; i < 64; ++i) w[i] *= alpha;
+            tmem_st64(tmem + t_lane + kTmemO + cb, w);
+          }
+          tmem_wait_st();
         }
-        tmem_wait_st();
+      }
+      if (bar_red_or(2, kSoftThreads, fail)) {
+        ok = false;
+        break;
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&p_full[st]);
     }
-    if (ok && nkt > 0) ok = mbar_wait(&o_done[(nkt - 1) & 1], ((nkt - 1) >> 1) & 1, abort, p.flags, p.wait_ns);
-    if (__all_sync(0xffffffffu, ok) && nkt > 0) {
+    // row sums: the two halves of a row
+    red_row[half][m] = l;
+    bool fail = !ok;
+    if (!fail && nkt > 0) fail = !mbar_wait(&o_done[(nkt - 1) & 1], ((nkt - 1) >> 1) & 1, abort, p.flags, p.wait_ns);
+    if (!bar_red_or(2, kSoftThreads, fail) && nkt > 0) {
       tc_fence_after();
       float* orow = p.out + (((size_t)b * p.S + s) * kH + h) * kDv;
-      const float il = 1.f / l;
+      const float il = 1.f / (red_row[0][m] + red_row[1][m]);
 #pragma unroll 1
-      for (int cb = 0; cb < kDv; cb += 64) {
+      for (int cb = 128 * half; cb < 128 * half + 128; cb += 64) {
         float w[64];
         tmem_ld64(tmem + t_lane + kTmemO + cb, w);
         tmem_wait_ld();
