@@ -45,11 +45,11 @@ ROW_WORKLOADS = ("glm_batched_b32_s1", "glm_batched_b32_s6", "glm_dsa_t65536", "
 # workload's dominant kernel, from one ncu capture of that kernel on this
 # workload; an entry is dropped as soon as its kernel changes.
 NCU_TRAFFIC = {
-    ("glm_decode_t4096", "attention"): 4874240,
-    ("glm_batched_b32_s1", "attention"): 583135232,
+    ("glm_decode_t4096", "attention"): 4873984,
+    ("glm_batched_b32_s1", "attention"): 583138304,
     ("glm_dsa_t65536", "index_scores"): 138440192,
     ("glm_dsa_t65536", "topk_select"): 1111552,
-    ("glm_prefill_s2048", "flash_attention"): 795490304,
+    ("glm_prefill_s2048", "flash_attention"): 794383360,
 }
 
 
