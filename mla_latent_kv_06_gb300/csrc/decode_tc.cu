@@ -114,11 +114,19 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&t);
 }
 
+// a / d for a >= 0, d > 0: a 32-bit division whenever a fits in 32 bits
+// (always, for tile counts below 2^23), the 64-bit one otherwise.
+__device__ __forceinline__ long long div_nonneg(long long a, long long d) {
+  if (((unsigned long long)a >> 32) == 0 && ((unsigned long long)d >> 32) == 0)
+    return (long long)((unsigned)a / (unsigned)d);
+  return a / d;
+}
+
 // Chunk g of the flattened tile list covers tiles [N*g/G, N*(g+1)/G).
-__device__ __forceinline__ long long chunk_begin(long long N, int g, int G) { return (N * g) / G; }
+__device__ __forceinline__ long long chunk_begin(long long N, int g, int G) { return div_nonneg(N * g, G); }
 
 __device__ __forceinline__ int chunk_of(long long x, long long N, int G) {
-  int g = (int)((x * G) / N);
+  int g = (int)div_nonneg(x * G, N);
   if (g > G - 1) g = G - 1;
   while (g + 1 < G && chunk_begin(N, g + 1, G) <= x) ++g;
   while (g > 0 && chunk_begin(N, g, G) > x) --g;
@@ -853,11 +861,10 @@ struct CombineParams {
   const __nv_bfloat16* kv_b;
   const float* o_part;
   const float* ml_part;
-  const int32_t* tile_start;
   const int32_t* T;
-  const int32_t* bad;
-  float* out;  // [R, 64, Dv]
-  int B, S, G, Dn, Dv, sparse;
+  const int32_t* nsel;
+  float* out;  // [R, 64, Dv], R <= kCmbRows
+  int B, S, G, Dn, Dv, sparse, T_cap, topk;
   unsigned int* flags;
 };
 
@@ -892,58 +899,81 @@ __global__ void __launch_bounds__(kCmbThreads) combine_kernel(const CombineParam
     bulk_copy_g2s(sm, p.kv_b + ((size_t)h * (p.Dn + p.Dv) + p.Dn + j0) * kDl, kCmbWBytes, &wbar);
   }
   grid_dep_launch();
-  grid_dep_wait();  // partials come from the attention kernel
+  // The call's rows (R <= kCmbRows) and their tile plan come from the kernel
+  // inputs alone -- the same tile counts as the absorb kernel's plan -- so
+  // the list of each row's splits is ready before the attention grid ends.
   const int R = p.B * p.S;
   const int NR = p.sparse ? R : p.B;
-  const long long N = p.tile_start[NR];
-  bool w_ready = false;
-  for (int r0 = 0; r0 < R; r0 += kCmbRows) {
-    const int nr = min(kCmbRows, R - r0);
-    // (a) warp w lists the splits of row r0 + w with their normalised weights
-    if (warp < nr) {
-      const int r = r0 + warp, b = r / p.S, s = r % p.S;
-      const int row = p.sparse ? r : b;
-      int cnt = 0;
-      if (!p.bad[row] && N > 0) {
-        const long long a = p.tile_start[row], e = p.tile_start[row + 1];
-        const int glo = chunk_of(a, N, p.G), ghi = chunk_of(e - 1, N, p.G);
-        float M = -INFINITY;
-        for (int g0 = glo; g0 <= ghi; g0 += 32) {
-          const int gg = g0 + lane;
-          int lo = 0, hi = 0;
-          if (gg <= ghi) {
-            if (p.sparse) piece_range<true>(p.tile_start, p.T, p.S, s, row, gg, p.G, N, &lo, &hi);
-            else piece_range<false>(p.tile_start, p.T, p.S, s, row, gg, p.G, N, &lo, &hi);
-          }
-          const bool has = lo < hi;
-          const int slot = p.sparse ? gg + row : (gg + row) * p.S + s;
-          float2 ml = make_float2(-INFINITY, 0.f);
-          if (has) ml = *reinterpret_cast<const float2*>(p.ml_part + ((size_t)slot * kH + h) * 2);
-          const unsigned m = __ballot_sync(0xffffffffu, has);
-          const int at = cnt + __popc(m & ((1u << lane) - 1));
-          if (has) {
-            pslot[warp * kMaxPieces + at] = slot;
-            pm[warp * kMaxPieces + at] = ml.x;
-            pw[warp * kMaxPieces + at] = ml.y;
-          }
-          cnt += __popc(m);
-          M = fmaxf(M, ml.x);
+  __shared__ int cts[kCmbRows + 1], cbad[kCmbRows];
+  if (tid < NR) {
+    const int b = p.sparse ? tid / p.S : tid;
+    const int Tb = p.T[b];
+    int bad = (Tb < p.S || Tb > p.T_cap) ? 1 : 0, nk = Tb;
+    if (!bad && p.sparse) {
+      nk = p.nsel[tid];
+      bad = (nk < 1 || nk > p.topk) ? 1 : 0;
+    }
+    cbad[tid] = bad;
+    cts[tid + 1] = bad ? 0 : (nk + kTile - 1) / kTile;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    cts[0] = 0;
+    for (int r = 0; r < NR; ++r) cts[r + 1] += cts[r];
+  }
+  __syncthreads();
+  const long long N = cts[NR];
+  const int nr = R;
+  const int r0 = 0;
+  // (a) warp w lists the splits of row w ...
+  if (warp < nr) {
+    const int r = warp, b = r / p.S, s = r % p.S;
+    const int row = p.sparse ? r : b;
+    int cnt = 0;
+    if (!cbad[row] && N > 0) {
+      const long long a = cts[row], e = cts[row + 1];
+      const int glo = chunk_of(a, N, p.G), ghi = chunk_of(e - 1, N, p.G);
+      for (int g0 = glo; g0 <= ghi; g0 += 32) {
+        const int gg = g0 + lane;
+        int lo = 0, hi = 0;
+        if (gg <= ghi) {
+          if (p.sparse) piece_range<true>(cts, p.T, p.S, s, row, gg, p.G, N, &lo, &hi);
+          else piece_range<false>(cts, p.T, p.S, s, row, gg, p.G, N, &lo, &hi);
         }
-        M = warp_max(M);
-        __syncwarp();  // entries were listed by other lanes
-        float L = 0.f;
-        for (int i = lane; i < cnt; i += 32) {
-          const float wg = exp2f(pm[warp * kMaxPieces + i] - M);
-          pm[warp * kMaxPieces + i] = wg;
-          L = fmaf(wg, pw[warp * kMaxPieces + i], L);
-        }
-        L = warp_sum(L);
-        for (int i = lane; i < cnt; i += 32) pm[warp * kMaxPieces + i] /= L;
-        if (lane == 0) inv_l[warp] = 1.f;
-      } else if (lane == 0) {
-        inv_l[warp] = __int_as_float(0x7fc00000);
+        const bool has = lo < hi;
+        const unsigned m = __ballot_sync(0xffffffffu, has);
+        if (has) pslot[warp * kMaxPieces + cnt + __popc(m & ((1u << lane) - 1))] = p.sparse ? gg + row : (gg + row) * p.S + s;
+        cnt += __popc(m);
       }
-      if (lane == 0) pcnt[warp] = cnt;
+    }
+    if (lane == 0) {
+      pcnt[warp] = cnt;
+      inv_l[warp] = (cbad[row] || N <= 0) ? __int_as_float(0x7fc00000) : 1.f;
+    }
+  }
+  grid_dep_wait();  // partials come from the attention kernel
+  bool w_ready = false;
+  {
+    // ... then, with the partials complete, their normalised weights
+    if (warp < nr) {
+      __syncwarp();  // entries were listed by other lanes
+      const int cnt = pcnt[warp];
+      float M = -INFINITY;
+      for (int i = lane; i < cnt; i += 32) {
+        const float2 ml = *reinterpret_cast<const float2*>(p.ml_part + ((size_t)pslot[warp * kMaxPieces + i] * kH + h) * 2);
+        pm[warp * kMaxPieces + i] = ml.x;
+        pw[warp * kMaxPieces + i] = ml.y;
+        M = fmaxf(M, ml.x);
+      }
+      M = warp_max(M);
+      float L = 0.f;
+      for (int i = lane; i < cnt; i += 32) {
+        const float wg = exp2f(pm[warp * kMaxPieces + i] - M);
+        pm[warp * kMaxPieces + i] = wg;
+        L = fmaf(wg, pw[warp * kMaxPieces + i], L);
+      }
+      L = warp_sum(L);
+      for (int i = lane; i < cnt; i += 32) pm[warp * kMaxPieces + i] /= L;
     }
     __syncthreads();
     // (b) clat[w][l] = sum_i weight_i * O_i[h][l]: warp k takes splits k, k+8, ...
@@ -1463,9 +1493,10 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   cp.kv_b = static_cast<const __nv_bfloat16*>(a.kv_b);
   cp.o_part = o_part;
   cp.ml_part = ml_part;
-  cp.tile_start = ts;
   cp.T = a.T;
-  cp.bad = bad;
+  cp.nsel = a.nsel;
+  cp.T_cap = a.T_cap;
+  cp.topk = a.topk;
   cp.out = a.out;
   cp.B = B;
   cp.S = S;
