@@ -805,11 +805,9 @@ __global__ void __launch_bounds__(kAbsThreads, 2) absorb_kernel(const AbsorbPara
   }
   if (p.prefetch && tid == 0) {
     // Everything the later kernels of this call read streams from HBM now,
-    // behind W_UK: W_UV rows (64 per CTA) and 1/nblk of every sequence's
-    // cache rows.
+    // behind W_UK, in the order it is needed: 1/nblk of every sequence's
+    // cache rows (the attention kernel), then W_UV rows (the combine).
     const int nblk = gridDim.x * gridDim.y, me = h * gridDim.x + cb;
-    const __nv_bfloat16* wuv = p.kv_b + ((size_t)h * (p.Dn + p.Dv) + p.Dn + (size_t)cb * (p.Dv / gridDim.x)) * kDl;
-    l2_prefetch(wuv, (uint32_t)(p.Dv / gridDim.x) * kDl * 2);
     for (int b = 0; b < p.B; ++b) {
       const int Tb = min(max(p.T[b], 0), p.T_cap);
       const size_t lb = (size_t)Tb * kDl * 2, rb = (size_t)Tb * kDr * 2;
@@ -820,6 +818,8 @@ __global__ void __launch_bounds__(kAbsThreads, 2) absorb_kernel(const AbsorbPara
       if (l1 > l0) l2_prefetch(lbase + l0, (uint32_t)(l1 - l0));
       if (r1 > r0) l2_prefetch(rbase + r0, (uint32_t)(r1 - r0));
     }
+    const __nv_bfloat16* wuv = p.kv_b + ((size_t)h * (p.Dn + p.Dv) + p.Dn + (size_t)cb * (p.Dv / gridDim.x)) * kDl;
+    l2_prefetch(wuv, (uint32_t)(p.Dv / gridDim.x) * kDl * 2);
   }
   if (!p.do_qabs) {  // rotary part only, every (row, pair) in parallel
     for (int e = tid; e < R * (kDr / 2); e += kAbsThreads) rope_row(p, e / (kDr / 2), h, e % (kDr / 2));
