@@ -35,8 +35,17 @@ Parity status of each function (what pins it, see tests/test_oracle_pins.py):
                           comparator; keep-all; -0.0 == +0.0 tie case.
 * sparse_decode         - keep-all equals dense; a subset equals dense attention
                           over the gathered rows.
+* rms_norm, layer_norm  - constant-vector closed forms, unit mean/variance of the
+                          normalised values, hand-worked examples.
+* cache_append,         - composed of the pinned norms and rope_interleave; rows
+  index_key_append        land at pos = T[b] - S + s.
 """
 from .mla import (  # noqa: F401
+    rms_norm,
+    layer_norm,
+    new_token_positions,
+    cache_append,
+    index_key_append,
     rope_interleave,
     split_kv_b,
     attend_dense,

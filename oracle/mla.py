@@ -260,3 +260,58 @@ def sparse_decode(q, Lc, Rc, T, kv_b, sel, nsel, qk_nope, scale, rope_base=10000
             out[b, s] = attend_absorbed(q[b, s], np.asarray(Lc)[b, idx], np.asarray(Rc)[b, idx],
                                         kv_b, qk_nope, pos, scale, rope_base)
     return out
+
+
+# ---------------------------------------------------------------------------
+# Cache append ([MLA-KV] §2.1, KV path: the kv_a output comp[kv_lora + qk_rope]
+# of each new token -> the first kv_lora values through RMSNorm(kv_a_ln) into
+# Lc[pos], the last qk_rope values through the RoPE shared by all heads into
+# Rc[pos]; [MLA-KV] §2.2: the indexer key through LayerNorm (eps 1e-6) and
+# RoPE into Ic[pos]).
+# ---------------------------------------------------------------------------
+def rms_norm(x, w, eps: float):
+    """x / sqrt(mean(x^2) + eps) * w over the last axis.  The pages print no
+    eps for kv_a_ln: the caller passes it."""
+    x = _f64(x)
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * _f64(w)
+
+
+def layer_norm(x, w, b, eps: float = 1e-6):
+    """(x - mean) / sqrt(var + eps) * w + b over the last axis (biased variance).
+    Reading: the indexer's "layernorm" has a weight and a bias (b may be None)."""
+    x = _f64(x)
+    mu = np.mean(x, axis=-1, keepdims=True)
+    var = np.mean((x - mu) ** 2, axis=-1, keepdims=True)
+    y = (x - mu) / np.sqrt(var + eps) * _f64(w)
+    return y if b is None else y + _f64(b)
+
+
+def new_token_positions(T, S: int):
+    """[B, S] cache rows of the S new tokens of each sequence: T[b] - S + s."""
+    T = np.asarray(T, dtype=np.int64)
+    return T[:, None] - S + np.arange(S)[None, :]
+
+
+def cache_append(comp, kv_a_ln, eps: float, T, kv_lora: int, base: float = 10000.0):
+    """comp [B,S,kv_lora+qk_rope] -> (Lc rows [B,S,kv_lora], Rc rows [B,S,qk_rope],
+    positions [B,S]) for the new tokens at pos = T[b] - S + s."""
+    comp = _f64(comp)
+    S = comp.shape[1]
+    pos = new_token_positions(T, S)
+    lc = rms_norm(comp[..., :kv_lora], kv_a_ln, eps)
+    rc = rope_interleave(comp[..., kv_lora:], pos, base)
+    return lc, rc, pos
+
+
+def index_key_append(k_idx, ln_w, ln_b, eps: float, T, rope_dim: int, base: float = 10000.0):
+    """k_idx [B,S,index_hd] -> (Ic rows [B,S,index_hd], positions [B,S]): LayerNorm,
+    then the interleaved RoPE on the last rope_dim values (reading: the page
+    names LayerNorm and RoPE but not which values rotate; the same tail
+    rotation as the attention key is taken)."""
+    k = layer_norm(k_idx, ln_w, ln_b, eps)
+    S = k.shape[1]
+    pos = new_token_positions(T, S)
+    if rope_dim > 0:
+        k = k.copy()
+        k[..., k.shape[-1] - rope_dim:] = rope_interleave(k[..., k.shape[-1] - rope_dim:], pos, base)
+    return k, pos

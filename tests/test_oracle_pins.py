@@ -383,3 +383,52 @@ def test_oracle_is_independent_of_the_cuda_path():
             src = open(os.path.join(here, fn)).read()
             assert "mla_latent_kv_06_gb300" not in src
             assert "ctypes" not in src and "import torch" not in src
+
+
+# --------------------------------------------------------------- cache append ([MLA-KV] §2.1, §2.2)
+def test_rms_norm_hand_values_and_invariances():
+    """x = (1,-1,1,-1) has mean square 1, so RMSNorm (eps 0) returns x * w exactly;
+    a zero vector stays zero; the result does not depend on the scale of x."""
+    w = np.array([2.0, 3.0, 4.0, 5.0])
+    assert np.array_equal(oracle.rms_norm(np.array([1.0, -1.0, 1.0, -1.0]), w, 0.0), [2.0, -3.0, 4.0, -5.0])
+    assert np.array_equal(oracle.rms_norm(np.zeros(4), w, 1e-6), np.zeros(4))
+    r = np.random.default_rng(1).standard_normal((3, 16))
+    assert np.allclose(oracle.rms_norm(7.5 * r, np.ones(16), 0.0), oracle.rms_norm(r, np.ones(16), 0.0), atol=1e-13)
+    y = oracle.rms_norm(r, np.ones(16), 0.0)
+    assert np.allclose(np.mean(y * y, axis=-1), 1.0, atol=1e-13)
+
+
+def test_layer_norm_hand_values_and_moments():
+    """(1,2,3): mean 2, variance 2/3, so the normalised values are (-1,0,1)*sqrt(3/2);
+    weight 1 and bias 5 shift them by 5.  Normalised rows have mean 0 and variance 1."""
+    y = oracle.layer_norm(np.array([1.0, 2.0, 3.0]), np.ones(3), np.full(3, 5.0), 0.0)
+    assert np.allclose(y, [5.0 - 1.224744871391589, 5.0, 5.0 + 1.224744871391589], atol=1e-14)
+    r = np.random.default_rng(2).standard_normal((4, 128)) * 3.0 + 1.5
+    z = oracle.layer_norm(r, np.ones(128), None, 0.0)
+    assert np.allclose(z.mean(axis=-1), 0.0, atol=1e-13) and np.allclose(z.var(axis=-1), 1.0, atol=1e-12)
+
+
+def test_cache_append_rows_and_positions():
+    """New tokens land at pos = T[b] - S + s; at pos 0 the rope part is only
+    de-interleaved (pairs (x0,x1),(x2,x3) -> x0,x2 | x1,x3)."""
+    assert np.array_equal(oracle.new_token_positions([10, 7], 2), [[8, 9], [5, 6]])
+    comp = np.arange(1, 13, dtype=np.float64).reshape(1, 1, 12)  # kv_lora 8, qk_rope 4
+    lc, rc, pos = oracle.cache_append(comp, np.ones(8), 0.0, [1], 8)
+    assert pos.tolist() == [[0]]
+    assert np.array_equal(rc[0, 0], [9.0, 11.0, 10.0, 12.0])
+    x = comp[0, 0, :8]
+    assert np.allclose(lc[0, 0], x / np.sqrt(np.mean(x * x)), atol=1e-14)
+
+
+def test_index_key_append_layout():
+    """rope_dim 0 is LayerNorm alone; with a rotated tail the leading values are untouched
+    and the tail keeps its norm pairwise (a rotation)."""
+    r = np.random.default_rng(4).standard_normal((2, 3, 16))
+    w, b = np.random.default_rng(5).standard_normal(16), np.random.default_rng(6).standard_normal(16)
+    plain, _ = oracle.index_key_append(r, w, b, 1e-6, [40, 3], 0)
+    assert np.allclose(plain, oracle.layer_norm(r, w, b, 1e-6))
+    rot, pos = oracle.index_key_append(r, w, b, 1e-6, [40, 3], 8)
+    assert np.array_equal(rot[..., :8], plain[..., :8])
+    a0, a1 = plain[..., 8::2], plain[..., 9::2]
+    assert np.allclose(rot[..., 8:12] ** 2 + rot[..., 12:16] ** 2, a0 ** 2 + a1 ** 2, atol=1e-12)
+    assert pos.tolist() == [[37, 38, 39], [0, 1, 2]]
