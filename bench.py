@@ -12,8 +12,9 @@ kernel.
 
 The default run also measures the other workloads of the hot path ("rows"):
 batched decode B=32 with S=1 and S=6, DSA (indexer + top-2048 + sparse
-decode) at B=4, T=65536, and the non-absorbed prefill S=2048 at pos_base=8192,
-plus the T sweep 4k..64k of the headline metric.
+decode) at B=4, T=65536, the non-absorbed prefill S=2048 at pos_base=8192 and
+the cache writers (latent + indexer key rows of 32 x 6 new tokens), plus the
+T sweep 4k..64k of the headline metric.
 
 Multi-GPU (torchrun): replicas -- every rank runs the same workload on its own
 GPU with no collective on the data path; value = all ranks' tokens / the
@@ -40,7 +41,9 @@ METRIC = "MLA decode tokens/s and latent-cache HBM GB/s (% roofline) at T=4k–6
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
-ROW_WORKLOADS = ("glm_batched_b32_s1", "glm_batched_b32_s6", "glm_dsa_t65536", "glm_prefill_s2048")
+ROW_WORKLOADS = ("glm_batched_b32_s1", "glm_batched_b32_s6", "glm_dsa_t65536", "glm_prefill_s2048",
+                 "glm_append_b32_s6")
+APPEND_RMS_EPS = 1e-6
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a
 # workload's dominant kernel, from one ncu capture of that kernel on this
 # workload; an entry is dropped as soon as its kernel changes.
@@ -85,6 +88,9 @@ def build_workload(name, device):
     elif name == "glm_prefill_s2048":
         x = workload_inputs(name, device)
         kind = "prefill"
+    elif name == "glm_append_b32_s6":
+        x = workload_inputs("glm_batched_b32", device, S=6)
+        kind = "append"
     else:
         raise SystemExit(f"unknown workload {name}")
 
@@ -136,6 +142,18 @@ def build_workload(name, device):
                 "attention": ("hbm", gathered + qcat), "combine": ("hbm", w_uv + out_bytes),
                 "absorb_gemm": ("hbm", w_uk + q_bytes + qcat), "plan_rope": ("hbm", q_bytes),
                 "merge": ("hbm", clat), "up_gemm": ("hbm", w_uv + clat + out_bytes)}
+        e2e = None
+    elif kind == "append":
+        from workload import append_inputs
+        hd, rope_dim = 128, d.qk_rope
+        a = append_inputs(d, B, S, "bf16", SEED_BASE + 5, device, index_hd=hd)
+        Ic = torch.zeros(B, x["T_cap"], hd, dtype=torch.float32, device=device)
+        calls = [lambda: mla.cache_append(a["comp"], a["kv_a_ln"], x["T"], x["Lc"], x["Rc"], d, APPEND_RMS_EPS),
+                 lambda: mla.index_key_append(a["k_idx"], a["ln_w"], a["ln_b"], x["T"], Ic, rope_dim)]
+        kv_rows = 2 * 2 * R * (d.kv_lora + d.qk_rope) + 2 * d.kv_lora  # comp read, Lc/Rc rows written, kv_a_ln
+        ic_rows = 2 * 4 * R * hd + 2 * 4 * hd                          # k_idx read, Ic rows written, ln_w/ln_b
+        info.update(cache_bytes=R * (row + 4 * hd), alg_bytes=kv_rows + ic_rows)
+        work = {"cache_append": ("hbm", kv_rows), "index_key_append": ("hbm", ic_rows)}
         e2e = None
     else:
         pos_base = x["pos_base"]

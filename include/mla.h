@@ -220,6 +220,42 @@ int dsa_topk_select(int B, int S, const float* scores, int T_cap, const int32_t*
                     int32_t* sel, int32_t* nsel, void* workspace, size_t workspace_bytes,
                     void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Cache append ([MLA-KV] §2.1, KV path: the kv_a output comp of each new
+ * token -> the first kv_lora values through RMSNorm(kv_a_ln) into Lc, the
+ * last qk_rope values through the RoPE shared by all heads into Rc)
+ *
+ * The S new tokens of sequence b sit at pos = T[b] - S + s (T counts them):
+ *   Lc[b,pos,:] = comp[b,s,0:kv_lora] / sqrt(mean(comp^2) + rms_eps) * kv_a_ln
+ *   Rc[b,pos,:] = RoPE(comp[b,s,kv_lora:kv_lora+qk_rope], pos)  (pairs (x[2j],x[2j+1])
+ *                 -> y[j], y[qk_rope/2+j], angle pos * rope_base^(-2j/qk_rope))
+ *   comp    [B, S, kv_lora + qk_rope]   dtype
+ *   kv_a_ln [kv_lora]                   dtype
+ *   Lc      [B, T_cap, kv_lora]         dtype: only the rows pos are written
+ *   Rc      [B, T_cap, qk_rope]         dtype: likewise
+ * Arithmetic in fp32 (the angle reduced in double), rounded once to dtype.
+ * Sequences with T[b] outside [S, T_cap] are left untouched and raise
+ * MLA_DEV_BAD_LENGTH.  Uses d->kv_lora, d->qk_rope and d->rope_base only;
+ * qk_rope above 256 returns MLA_ERR_UNSUPPORTED.
+ * ------------------------------------------------------------------------- */
+int mla_cache_append(const mla_dims* d, int dtype, int B, int S, const void* comp, const void* kv_a_ln,
+                     float rms_eps, int T_cap, const int32_t* T, void* Lc, void* Rc, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Indexer key append ([MLA-KV] §2.2: the indexer key of each new token goes
+ * through layernorm (eps 1e-6) and RoPE into Ic; Ic is fp32, [FDSA] §二)
+ *
+ *   Ic[b,pos,:] = (k - mean) / sqrt(var + ln_eps) * ln_w + ln_b, k = k_idx[b,s,:],
+ *                 then its last rope_dim values rotated as in mla_cache_append
+ *   k_idx [B, S, index_hd] float, ln_w [index_hd] float, ln_b [index_hd] float or NULL
+ *   Ic    [B, T_cap, index_hd] float: only the rows pos = T[b] - S + s are written
+ * rope_dim: even, 0 .. index_hd (0: no rotation), at most 256 (else
+ * MLA_ERR_UNSUPPORTED); rope_base <= 0 means 10000.  Bad lengths as above.
+ * ------------------------------------------------------------------------- */
+int dsa_index_key_append(int B, int S, int index_hd, int rope_dim, const float* k_idx, const float* ln_w,
+                         const float* ln_b, float ln_eps, float rope_base, int T_cap, const int32_t* T,
+                         float* Ic, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -27,6 +27,7 @@ EXPORTS = (
     "mla_sparse_decode_workspace_size", "mla_sparse_decode",
     "mla_prefill_naive_workspace_size", "mla_prefill_naive", "mla_prefill_naive_noalloc",
     "dsa_index_scores", "dsa_topk_select_workspace_size", "dsa_topk_select",
+    "mla_cache_append", "dsa_index_key_append",
 )
 
 
@@ -70,6 +71,9 @@ def _declare(lib: ctypes.CDLL) -> None:
         "dsa_index_scores": (_I, [_I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P]),
         "dsa_topk_select_workspace_size": (_SZ, [_I, _I, _I, _I]),
         "dsa_topk_select": (_I, [_I, _I, _P, _I, _P, _I, _P, _P, _P, _SZ, _P]),
+        "mla_cache_append": (_I, [_DP, _I, _I, _I, _P, _P, ctypes.c_float, _I, _P, _P, _P, _P]),
+        "dsa_index_key_append": (_I, [_I, _I, _I, _I, _P, _P, _P, ctypes.c_float, ctypes.c_float, _I, _P,
+                                      _P, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -271,3 +275,30 @@ def topk_select(scores, T, topk: int, S: Optional[int] = None, sel=None, nsel=No
     _check(lib().dsa_topk_select(B, S, _ptr(scores), T_cap, _ptr(T), topk, _ptr(sel), _ptr(nsel),
                                  _ptr(workspace), wsb, _stream(stream)))
     return sel, nsel
+
+
+def cache_append(comp, kv_a_ln, T, Lc, Rc, dims, rms_eps: float, stream=None):
+    """Writes the S new tokens of each sequence into Lc/Rc in place at rows
+    T[b]-S+s: comp [B,S,kv_lora+qk_rope] (the kv_a output), kv_a_ln [kv_lora]."""
+    B, S = comp.shape[0], comp.shape[1]
+    T_cap = Lc.shape[1]
+    code = _dtype_code(comp)
+    for t in (kv_a_ln, Lc, Rc):
+        if t.dtype != comp.dtype:
+            raise TypeError("comp, kv_a_ln, Lc and Rc must share one dtype")
+    d = make_dims(dims)
+    _check(lib().mla_cache_append(ctypes.byref(d), code, B, S, _ptr(comp), _ptr(kv_a_ln), float(rms_eps),
+                                  T_cap, _ptr(T), _ptr(Lc), _ptr(Rc), _stream(stream)))
+    return Lc, Rc
+
+
+def index_key_append(k_idx, ln_w, ln_b, T, Ic, rope_dim: int, ln_eps: float = 1e-6,
+                     rope_base: float = 10000.0, stream=None):
+    """Writes the indexer keys of the S new tokens (k_idx [B,S,index_hd] fp32)
+    into Ic [B,T_cap,index_hd] in place: LayerNorm, then RoPE on the last rope_dim."""
+    B, S, hd = k_idx.shape
+    T_cap = Ic.shape[1]
+    _check(lib().dsa_index_key_append(B, S, hd, int(rope_dim), _ptr(k_idx), _ptr(ln_w), _ptr(ln_b),
+                                      float(ln_eps), float(rope_base), T_cap, _ptr(T), _ptr(Ic),
+                                      _stream(stream)))
+    return Ic

@@ -362,3 +362,54 @@ MLA_EXPORT int dsa_topk_select(int B, int S, const float* scores, int T_cap, con
   if (e != cudaSuccess) return cuda_fail(e, "dsa_topk_select launch");
   return MLA_OK;
 }
+
+// ---------------------------------------------------------------- cache append
+MLA_EXPORT int mla_cache_append(const mla_dims* d, int dtype, int B, int S, const void* comp,
+                                const void* kv_a_ln, float rms_eps, int T_cap, const int32_t* T, void* Lc,
+                                void* Rc, void* stream) {
+  mla::Geometry g;
+  int rc = check_common(d, dtype, B, S, &g);
+  if (rc != MLA_OK) return rc;
+  if (T_cap < S) return fail(MLA_ERR_INVALID, "T_cap=%d < S=%d", T_cap, S);
+  if (!(rms_eps >= 0.f)) return fail(MLA_ERR_INVALID, "rms_eps must be >= 0");
+  if (!comp || !kv_a_ln || !T || !Lc || (g.Dr > 0 && !Rc)) return fail(MLA_ERR_INVALID, "null tensor pointer");
+  if (g.Dr > 2 * mla::kMaxRopePairs) return fail(MLA_ERR_UNSUPPORTED, "qk_rope=%d above %d", g.Dr, 2 * mla::kMaxRopePairs);
+  if (g.Dl > mla::kMaxAppendWidth)
+    return fail(MLA_ERR_UNSUPPORTED, "kv_lora=%d above %d", g.Dl, mla::kMaxAppendWidth);
+  mla::AppendArgs a{B, S, T_cap, g.Dl, g.Dr, comp, kv_a_ln, rms_eps, T, Lc, Rc, flags_ptr(), {}};
+  for (int j = 0; j < g.Dr / 2; ++j) a.theta[j] = std::pow(g.rope_base, -2.0 * j / g.Dr);
+  if (!a.flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  mla::call_begin();
+  mla::kernel_mark(st, "cache_append");
+  cudaError_t e = mla::launch_cache_append(a, dtype, st);
+  mla::call_end(st);
+  if (e != cudaSuccess) return cuda_fail(e, "mla_cache_append launch");
+  return MLA_OK;
+}
+
+MLA_EXPORT int dsa_index_key_append(int B, int S, int index_hd, int rope_dim, const float* k_idx,
+                                    const float* ln_w, const float* ln_b, float ln_eps, float rope_base,
+                                    int T_cap, const int32_t* T, float* Ic, void* stream) {
+  if (B < 1 || S < 1 || index_hd < 1 || T_cap < S)
+    return fail(MLA_ERR_INVALID, "bad sizes B=%d S=%d index_hd=%d T_cap=%d", B, S, index_hd, T_cap);
+  if (rope_dim < 0 || rope_dim > index_hd || rope_dim % 2 != 0)
+    return fail(MLA_ERR_INVALID, "rope_dim=%d must be even and within [0, index_hd=%d]", rope_dim, index_hd);
+  if (index_hd > mla::kMaxAppendWidth)
+    return fail(MLA_ERR_UNSUPPORTED, "index_hd=%d above %d", index_hd, mla::kMaxAppendWidth);
+  if (!(ln_eps >= 0.f)) return fail(MLA_ERR_INVALID, "ln_eps must be >= 0");
+  if (!k_idx || !ln_w || !T || !Ic) return fail(MLA_ERR_INVALID, "null tensor pointer");
+  if (rope_dim > 2 * mla::kMaxRopePairs)
+    return fail(MLA_ERR_UNSUPPORTED, "rope_dim=%d above %d", rope_dim, 2 * mla::kMaxRopePairs);
+  mla::KeyAppendArgs a{B, S, T_cap, index_hd, rope_dim, k_idx, ln_w, ln_b, ln_eps, T, Ic, flags_ptr(), {}};
+  const double base = rope_base > 0.f ? (double)rope_base : 10000.0;
+  for (int j = 0; j < rope_dim / 2; ++j) a.theta[j] = std::pow(base, -2.0 * j / rope_dim);
+  if (!a.flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  mla::call_begin();
+  mla::kernel_mark(st, "index_key_append");
+  cudaError_t e = mla::launch_index_key_append(a, st);
+  mla::call_end(st);
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_index_key_append launch");
+  return MLA_OK;
+}

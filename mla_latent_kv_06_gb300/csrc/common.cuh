@@ -40,6 +40,40 @@ __device__ __forceinline__ void rope_cos_sin(int pos, int j, int d, double base,
   *s = (float)sn;
 }
 
+// cos/sin of the rotary angle pos * theta, theta = base^(-2j/d) given in
+// double: the product is formed and reduced to [-pi, pi] in double, so only
+// the reduced angle is rounded to float before the float sincos.
+__device__ __forceinline__ void rope_cs_theta(int pos, double theta, float* c, float* s) {
+  const double ang = (double)pos * theta;
+  const double k = rint(ang * 0.15915494309189535);
+  const float red = (float)fma(-k, 6.283185307179586, ang);
+  sincosf(red, s, c);
+}
+
+// Programmatic dependent launch: wait for the preceding kernel's results /
+// let the next kernel in the stream start its prologue.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch with programmatic stream serialisation allowed (pdl == false: a plain launch).
+template <typename Kern, typename Arg>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st, const Arg& arg,
+                       bool pdl = true) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, arg);
+}
+
 // %globaltimer in nanoseconds.
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;

@@ -75,11 +75,6 @@ struct AttnParams {
   long long wait_ns;
 };
 
-__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void grid_dep_launch() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 __device__ __forceinline__ bool bar_red_or(int id, int n, bool x) {
   uint32_t r;
   asm volatile(
@@ -1294,21 +1289,6 @@ Plan make_plan(int B, int S, int T_cap, int sparse_topk) {
   off = align256(off + (pl.R > kSmallRows ? (size_t)pl.R * kH * 4 : 0));
   pl.total = off;
   return pl;
-}
-
-template <typename Kern, typename Arg>
-cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st, const Arg& arg) {
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, arg);
 }
 
 cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {

@@ -42,9 +42,6 @@ struct GemmParams {
   long long wait_ns;
 };
 
-__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-
 template <int BN, bool kBMN>
 __global__ void __launch_bounds__(kGThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
   using Cfg = GemmCfg<BN>;

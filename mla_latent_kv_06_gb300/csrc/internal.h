@@ -73,6 +73,38 @@ struct TopkArgs {
 
 cudaError_t launch_topk_select(const TopkArgs& a, cudaStream_t st);
 
+// RoPE frequencies base^(-2j/d) travel in the launch parameters: rope widths up to 2 * kMaxRopePairs.
+constexpr int kMaxRopePairs = 128;
+// The append kernels hold a row in registers: at most kMaxAppendPer values per thread of 128.
+constexpr int kMaxAppendPer = 32;
+constexpr int kMaxAppendWidth = 128 * kMaxAppendPer;
+
+struct AppendArgs {
+  int B, S, T_cap, kv_lora, qk_rope;
+  const void* comp;     // [B, S, kv_lora + qk_rope]
+  const void* kv_a_ln;  // [kv_lora]
+  float eps;
+  const int32_t* T;
+  void* Lc;  // [B, T_cap, kv_lora]
+  void* Rc;  // [B, T_cap, qk_rope]
+  unsigned int* flags;
+  double theta[kMaxRopePairs];
+};
+cudaError_t launch_cache_append(const AppendArgs& a, int dtype, cudaStream_t st);
+
+struct KeyAppendArgs {
+  int B, S, T_cap, hd, rope_dim;
+  const float* k;     // [B, S, hd]
+  const float* ln_w;  // [hd]
+  const float* ln_b;  // [hd] or null
+  float eps;
+  const int32_t* T;
+  float* Ic;  // [B, T_cap, hd]
+  unsigned int* flags;
+  double theta[kMaxRopePairs];
+};
+cudaError_t launch_index_key_append(const KeyAppendArgs& a, cudaStream_t st);
+
 // Sets the thread-local message returned by mla_last_error().
 void set_last_error(const char* msg);
 

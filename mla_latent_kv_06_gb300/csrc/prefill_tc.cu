@@ -66,8 +66,6 @@ struct FlashParams {
   long long wait_ns;
 };
 
-__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 __device__ __forceinline__ bool bar_red_or(int id, int n, bool x) {
   uint32_t r;
   asm volatile(

@@ -64,6 +64,19 @@ def test_host_rejects_bad_arguments_without_a_gpu(lib):
     assert lib.dsa_index_scores(0, 1, 32, 128, None, None, None, 16, None, None, None) == mla.MLA_ERR_INVALID
     assert lib.mla_prefill_naive(ctypes.byref(d), 1, 1, 4, -1, None, None, None, None, None, None, 0,
                                  None) == mla.MLA_ERR_INVALID
+    # cache writers: null tensors, S > T_cap, negative eps, odd / too wide rotary part
+    p = ctypes.c_void_p(16)
+    assert lib.mla_cache_append(ctypes.byref(d), 1, 1, 1, None, p, 1e-6, 8, p, p, p, None) == mla.MLA_ERR_INVALID
+    assert lib.mla_cache_append(ctypes.byref(d), 1, 1, 9, p, p, 1e-6, 8, p, p, p, None) == mla.MLA_ERR_INVALID
+    assert lib.mla_cache_append(ctypes.byref(d), 1, 1, 1, p, p, -1.0, 8, p, p, p, None) == mla.MLA_ERR_INVALID
+    wide = mla.MlaDims(64, 192, 258, 512, 256, 0.0, 0.0)
+    assert lib.mla_cache_append(ctypes.byref(wide), 1, 1, 1, p, p, 1e-6, 8, p, p, p,
+                                None) == mla.MLA_ERR_UNSUPPORTED
+    assert lib.dsa_index_key_append(1, 1, 128, 63, p, p, None, 1e-6, 1e4, 8, p, p, None) == mla.MLA_ERR_INVALID
+    assert lib.dsa_index_key_append(1, 1, 128, 130, p, p, None, 1e-6, 1e4, 8, p, p, None) == mla.MLA_ERR_INVALID
+    assert lib.dsa_index_key_append(1, 1, 600, 300, p, p, None, 1e-6, 1e4, 8, p, p,
+                                    None) == mla.MLA_ERR_UNSUPPORTED
+    assert lib.dsa_index_key_append(1, 1, 128, 64, None, p, None, 1e-6, 1e4, 8, p, p, None) == mla.MLA_ERR_INVALID
 
 
 def test_workspace_sizes_are_host_only(lib):

@@ -142,6 +142,26 @@ def dsa_inputs(B: int, S: int, T: Sequence[int], T_cap: int, n_ih: int, index_hd
     return dict(q_idx=q_idx, w=w, Ic=Ic)
 
 
+def append_inputs(dims: Dims, B: int, S: int, dtype: str, seed: int, device="cpu",
+                  index_hd: int = 0) -> Dict[str, torch.Tensor]:
+    """Inputs of the cache writers for S new tokens per sequence.
+
+    ``comp [B,S,kv_lora+qk_rope]`` (the kv_a projection of each new token) and
+    ``kv_a_ln [kv_lora]`` (gain around 1) in ``dtype``; with ``index_hd > 0``
+    also the fp32 indexer keys ``k_idx [B,S,index_hd]`` (mean 0.3, so the
+    LayerNorm centring matters) with ``ln_w`` and ``ln_b [index_hd]``."""
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    g = _gen(seed + 0x2000, device)
+    comp = _normal((B, S, dims.kv_lora + dims.qk_rope), 1.0, g, device, tdt)
+    kv_a_ln = (1.0 + _normal((dims.kv_lora,), 0.1, g, device, torch.float32)).to(tdt)
+    out = dict(comp=comp, kv_a_ln=kv_a_ln)
+    if index_hd > 0:
+        out["k_idx"] = 0.3 + _normal((B, S, index_hd), 1.0, g, device, torch.float32)
+        out["ln_w"] = 1.0 + _normal((index_hd,), 0.1, g, device, torch.float32)
+        out["ln_b"] = _normal((index_hd,), 0.1, g, device, torch.float32)
+    return out
+
+
 def workload_inputs(name: str, device="cpu", S: Optional[int] = None) -> Dict[str, object]:
     """All inputs of a named workload (see ``WORKLOADS``)."""
     wl = WORKLOADS[name]
