@@ -39,8 +39,12 @@ Parity status of each function (what pins it, see tests/test_oracle_pins.py):
                           normalised values, hand-worked examples.
 * cache_append,         - composed of the pinned norms and rope_interleave; rows
   index_key_append        land at pos = T[b] - S + s.
+* page_row, unpage      - hand-worked block table; identity table equals the
+                          contiguous layout.
 """
 from .mla import (  # noqa: F401
+    page_row,
+    unpage,
     rms_norm,
     layer_norm,
     new_token_positions,

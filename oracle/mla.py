@@ -315,3 +315,25 @@ def index_key_append(k_idx, ln_w, ln_b, eps: float, T, rope_dim: int, base: floa
         k = k.copy()
         k[..., k.shape[-1] - rope_dim:] = rope_interleave(k[..., k.shape[-1] - rope_dim:], pos, base)
     return k, pos
+
+
+# --------------------------------------------------------------- paged cache layout
+def page_row(block_table, b: int, t: int, page_size: int) -> int:
+    """Pool row of token t of sequence b: the page that the block table names
+    for t // page_size, row t % page_size inside it.  The pages fix no storage
+    layout beyond one row per token ([MLA-KV] §1); this is the paged layout's
+    own definition."""
+    return int(block_table[b][t // page_size]) * page_size + t % page_size
+
+
+def unpage(pool, block_table, T):
+    """[num_pages, page_size, D] pool -> contiguous [B, max(T), D] cache whose
+    rows 0..T[b]-1 of sequence b are read through page_row; the rest are NaN."""
+    pool = _f64(pool)
+    page_size, D = pool.shape[1], pool.shape[2]
+    rows = pool.reshape(-1, D)
+    out = np.full((len(T), max(T), D), np.nan)
+    for b, n in enumerate(T):
+        for t in range(n):
+            out[b, t] = rows[page_row(block_table, b, t, page_size)]
+    return out

@@ -432,3 +432,26 @@ def test_index_key_append_layout():
     a0, a1 = plain[..., 8::2], plain[..., 9::2]
     assert np.allclose(rot[..., 8:12] ** 2 + rot[..., 12:16] ** 2, a0 ** 2 + a1 ** 2, atol=1e-12)
     assert pos.tolist() == [[37, 38, 39], [0, 1, 2]]
+
+
+# --------------------------------------------------------------- paged layout
+def test_page_row_hand_example():
+    """Pages of 2 rows; sequence 0 uses pages 2 then 0, sequence 1 uses page 1:
+    token rows worked out by hand from the block table."""
+    table = [[2, 0], [1, -1]]
+    assert [oracle.page_row(table, 0, t, 2) for t in range(4)] == [4, 5, 0, 1]
+    assert [oracle.page_row(table, 1, t, 2) for t in range(2)] == [2, 3]
+    pool = np.arange(3 * 2 * 1, dtype=np.float64).reshape(3, 2, 1)  # row r holds the value r
+    out = oracle.unpage(pool, table, [3, 2])
+    assert out[0, :3, 0].tolist() == [4.0, 5.0, 0.0] and out[1, :2, 0].tolist() == [2.0, 3.0]
+    assert np.isnan(out[1, 2, 0])
+
+
+def test_identity_block_table_is_the_contiguous_layout():
+    """With page b*max_pages + i at table[b, i], the pool read as [B, T_cap, D] is
+    the contiguous cache itself."""
+    r = np.random.default_rng(7).standard_normal((2, 8, 3))  # B=2, T_cap=8, D=3
+    pool = r.reshape(8, 2, 3)                                 # 8 pages of 2 rows
+    table = [[0, 1, 2, 3], [4, 5, 6, 7]]
+    assert np.array_equal(oracle.unpage(pool, table, [8, 5])[0], r[0])
+    assert np.array_equal(oracle.unpage(pool, table, [8, 5])[1, :5], r[1, :5])
