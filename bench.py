@@ -13,8 +13,9 @@ kernel.
 The default run also measures the other workloads of the hot path ("rows"):
 batched decode B=32 with S=1 and S=6, DSA (indexer + top-2048 + sparse
 decode) at B=4, T=65536, the non-absorbed prefill S=2048 at pos_base=8192 and
-the cache writers (latent + indexer key rows of 32 x 6 new tokens), plus the
-T sweep 4k..64k of the headline metric.
+the cache writers (latent + indexer key rows of 32 x 6 new tokens) and the
+batched decode over a shuffled 128-row page pool, plus the T sweep 4k..64k of
+the headline metric.
 
 Multi-GPU (torchrun): replicas -- every rank runs the same workload on its own
 GPU with no collective on the data path; value = all ranks' tokens / the
@@ -42,7 +43,7 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 ROW_WORKLOADS = ("glm_batched_b32_s1", "glm_batched_b32_s6", "glm_dsa_t65536", "glm_prefill_s2048",
-                 "glm_append_b32_s6")
+                 "glm_append_b32_s6", "glm_paged_b32_s1")
 APPEND_RMS_EPS = 1e-6
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a
 # workload's dominant kernel, from one ncu capture of that kernel on this
@@ -91,6 +92,14 @@ def build_workload(name, device):
     elif name == "glm_append_b32_s6":
         x = workload_inputs("glm_batched_b32", device, S=6)
         kind = "append"
+    elif name == "glm_paged_b32_s1":
+        from workload import paged_layout, to_pages
+        x = workload_inputs("glm_batched_b32", device, S=1)
+        table, num_pages = paged_layout(x["T_list"], 128, SEED_BASE + 6)
+        x["table"] = table.to(device)
+        x["Lc"] = to_pages(x["Lc"], table, x["T_list"], 128, num_pages)
+        x["Rc"] = to_pages(x["Rc"], table, x["T_list"], 128, num_pages)
+        kind = "decode"
     else:
         raise SystemExit(f"unknown workload {name}")
 
@@ -107,10 +116,17 @@ def build_workload(name, device):
     out = torch.empty(B, S, d.H, d.v_head, dtype=torch.float32, device=device)
     info = {"tokens": R, "B": B, "S": S, "T_list": T_list}
 
-    if kind == "decode":
+    if kind == "decode" and "table" in x:  # shuffled 128-row pages of one pool
+        need = mla.lib().mla_decode_paged_workspace_size(mla.ctypes.byref(mla.make_dims(d)), mla.MLA_BF16, B, S,
+                                                         x["table"].shape[1], 128)
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+        calls = [lambda: mla.decode_paged(x["q"], x["Lc"], x["Rc"], x["table"], x["T"], x["kv_b"], d, out=out,
+                                          workspace=ws)]
+    elif kind == "decode":
         need = mla.decode_workspace_size(d, mla.MLA_BF16, B, S, x["T_cap"])
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
         calls = [lambda: mla.decode_absorbed(x["q"], x["Lc"], x["Rc"], x["T"], x["kv_b"], d, out=out, workspace=ws)]
+    if kind == "decode":
         cache = row * sum(T_list)  # every cached key read once per sequence
         info.update(cache_bytes=cache, alg_bytes=cache + w_uk + w_uv + q_bytes + out_bytes)
         clat = 2 * R * d.H * d.kv_lora
@@ -118,7 +134,7 @@ def build_workload(name, device):
                 "plan_rope": ("hbm", q_bytes), "attention": ("hbm", cache + qcat),
                 "combine": ("hbm", w_uv + out_bytes), "merge": ("hbm", clat),
                 "up_gemm": ("hbm", w_uv + clat + out_bytes)}
-        e2e = dict(inputs=[x["q"], x["T"]], run=lambda q, T: mla.decode_absorbed(
+        e2e = None if "table" in x else dict(inputs=[x["q"], x["T"]], run=lambda q, T: mla.decode_absorbed(
             q, x["Lc"], x["Rc"], T, x["kv_b"], d, out=out, workspace=ws), out=out)
     elif kind == "dsa":
         k = x["topk"]

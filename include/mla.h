@@ -143,6 +143,39 @@ int mla_sparse_decode(const mla_dims* d, int dtype, int B, int S,
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Paged cache layout (the same operations on a shared page pool)
+ *
+ * The pages fix no storage layout beyond one 576-value row per token
+ * ([MLA-KV] §1); this layout lets sequences grow without a per-sequence
+ * T_cap reservation.  Token t of sequence b lives at row
+ *   block_table[b, t / page_size] * page_size + t % page_size
+ * of the pools
+ *   Lc_pages [num_pages, page_size, kv_lora]   dtype
+ *   Rc_pages [num_pages, page_size, qk_rope]   dtype
+ *   block_table [B, max_pages] int32: page indices in [0, num_pages); only the
+ *               entries below ceil(T[b] / page_size) are read
+ * The capacity of a sequence is max_pages * page_size (it plays the role of
+ * T_cap: S <= T[b] <= max_pages * page_size).  A page index outside
+ * [0, num_pages) is never dereferenced: the kernels raise MLA_DEV_BAD_INDEX
+ * and that sequence's outputs are undefined.  Pools and per-sequence
+ * capacities of 2^31 rows or more return MLA_ERR_UNSUPPORTED.  With bf16 and
+ * the GLM-5.2 geometry the tensor-core kernels run when page_size is a
+ * multiple of 128 (one key tile never spans two pages); other page sizes run
+ * the CUDA-core kernels.  Workspace: mla_decode_paged_workspace_size and
+ * mla_sparse_decode_workspace_size.
+ * ------------------------------------------------------------------------- */
+size_t mla_decode_paged_workspace_size(const mla_dims* d, int dtype, int B, int S, int max_pages, int page_size);
+int mla_decode_paged(const mla_dims* d, int dtype, int B, int S, const void* q,
+                     const void* Lc_pages, const void* Rc_pages, int num_pages, int page_size,
+                     const int32_t* block_table, int max_pages, const int32_t* T, const void* kv_b,
+                     float* out, void* workspace, size_t workspace_bytes, void* stream);
+int mla_sparse_decode_paged(const mla_dims* d, int dtype, int B, int S, const void* q,
+                            const void* Lc_pages, const void* Rc_pages, int num_pages, int page_size,
+                            const int32_t* block_table, int max_pages, const int32_t* T, const void* kv_b,
+                            const int32_t* sel, const int32_t* nsel, int topk, float* out,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Non-absorbed prefill ([MLA-KV] §2.3, non-absorbed path)
  *
  * Step 1: one kv_b product rebuilds, for every key t < Tk = pos_base + S,
@@ -240,6 +273,10 @@ int dsa_topk_select(int B, int S, const float* scores, int T_cap, const int32_t*
  * ------------------------------------------------------------------------- */
 int mla_cache_append(const mla_dims* d, int dtype, int B, int S, const void* comp, const void* kv_a_ln,
                      float rms_eps, int T_cap, const int32_t* T, void* Lc, void* Rc, void* stream);
+/* The same rows written into the paged pools (layout as for mla_decode_paged). */
+int mla_cache_append_paged(const mla_dims* d, int dtype, int B, int S, const void* comp, const void* kv_a_ln,
+                           float rms_eps, void* Lc_pages, void* Rc_pages, int num_pages, int page_size,
+                           const int32_t* block_table, int max_pages, const int32_t* T, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Indexer key append ([MLA-KV] §2.2: the indexer key of each new token goes

@@ -28,6 +28,7 @@ EXPORTS = (
     "mla_prefill_naive_workspace_size", "mla_prefill_naive", "mla_prefill_naive_noalloc",
     "dsa_index_scores", "dsa_topk_select_workspace_size", "dsa_topk_select",
     "mla_cache_append", "dsa_index_key_append",
+    "mla_decode_paged_workspace_size", "mla_decode_paged", "mla_sparse_decode_paged", "mla_cache_append_paged",
 )
 
 
@@ -74,6 +75,11 @@ def _declare(lib: ctypes.CDLL) -> None:
         "mla_cache_append": (_I, [_DP, _I, _I, _I, _P, _P, ctypes.c_float, _I, _P, _P, _P, _P]),
         "dsa_index_key_append": (_I, [_I, _I, _I, _I, _P, _P, _P, ctypes.c_float, ctypes.c_float, _I, _P,
                                       _P, _P]),
+        "mla_decode_paged_workspace_size": (_SZ, [_DP, _I, _I, _I, _I, _I]),
+        "mla_decode_paged": (_I, [_DP, _I, _I, _I, _P, _P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _SZ, _P]),
+        "mla_sparse_decode_paged": (_I, [_DP, _I, _I, _I, _P, _P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _I, _P,
+                                         _P, _SZ, _P]),
+        "mla_cache_append_paged": (_I, [_DP, _I, _I, _I, _P, _P, ctypes.c_float, _P, _P, _I, _I, _P, _I, _P, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -302,3 +308,59 @@ def index_key_append(k_idx, ln_w, ln_b, T, Ic, rope_dim: int, ln_eps: float = 1e
                                       float(ln_eps), float(rope_base), T_cap, _ptr(T), _ptr(Ic),
                                       _stream(stream)))
     return Ic
+
+
+# ------------------------------------------------------------------ paged cache
+def decode_paged(q, Lc_pages, Rc_pages, block_table, T, kv_b, dims, out=None, workspace=None, stream=None):
+    """Absorbed decode over a page pool: Lc_pages [num_pages, page_size, kv_lora],
+    Rc_pages [num_pages, page_size, qk_rope], block_table [B, max_pages] int32."""
+    torch = _torch()
+    B, S, H = q.shape[0], q.shape[1], q.shape[2]
+    num_pages, page_size = Lc_pages.shape[0], Lc_pages.shape[1]
+    max_pages = block_table.shape[1]
+    code = _dtype_code(q)
+    if out is None:
+        out = torch.empty(B, S, H, dims.v_head, dtype=torch.float32, device=q.device)
+    d = make_dims(dims)
+    need = lib().mla_decode_paged_workspace_size(ctypes.byref(d), code, B, S, max_pages, page_size)
+    workspace, wsb = _workspace(need, q.device, workspace)
+    _check(lib().mla_decode_paged(ctypes.byref(d), code, B, S, _ptr(q), _ptr(Lc_pages), _ptr(Rc_pages), num_pages,
+                                  page_size, _ptr(block_table), max_pages, _ptr(T), _ptr(kv_b), _ptr(out),
+                                  _ptr(workspace), wsb, _stream(stream)))
+    return out
+
+
+def sparse_decode_paged(q, Lc_pages, Rc_pages, block_table, T, kv_b, sel, nsel, dims, out=None, workspace=None,
+                        stream=None):
+    """Absorbed decode over the selected keys of a paged cache (sel holds token indices)."""
+    torch = _torch()
+    B, S, H = q.shape[0], q.shape[1], q.shape[2]
+    num_pages, page_size = Lc_pages.shape[0], Lc_pages.shape[1]
+    max_pages = block_table.shape[1]
+    topk = sel.shape[2]
+    code = _dtype_code(q)
+    if out is None:
+        out = torch.empty(B, S, H, dims.v_head, dtype=torch.float32, device=q.device)
+    d = make_dims(dims)
+    need = lib().mla_sparse_decode_workspace_size(ctypes.byref(d), code, B, S, topk)
+    workspace, wsb = _workspace(need, q.device, workspace)
+    _check(lib().mla_sparse_decode_paged(ctypes.byref(d), code, B, S, _ptr(q), _ptr(Lc_pages), _ptr(Rc_pages),
+                                         num_pages, page_size, _ptr(block_table), max_pages, _ptr(T), _ptr(kv_b),
+                                         _ptr(sel), _ptr(nsel), topk, _ptr(out), _ptr(workspace), wsb,
+                                         _stream(stream)))
+    return out
+
+
+def cache_append_paged(comp, kv_a_ln, block_table, T, Lc_pages, Rc_pages, dims, rms_eps: float, stream=None):
+    """mla_cache_append into the page pools (in place)."""
+    B, S = comp.shape[0], comp.shape[1]
+    num_pages, page_size = Lc_pages.shape[0], Lc_pages.shape[1]
+    code = _dtype_code(comp)
+    for t in (kv_a_ln, Lc_pages, Rc_pages):
+        if t.dtype != comp.dtype:
+            raise TypeError("comp, kv_a_ln and the pools must share one dtype")
+    d = make_dims(dims)
+    _check(lib().mla_cache_append_paged(ctypes.byref(d), code, B, S, _ptr(comp), _ptr(kv_a_ln), float(rms_eps),
+                                        _ptr(Lc_pages), _ptr(Rc_pages), num_pages, page_size, _ptr(block_table),
+                                        block_table.shape[1], _ptr(T), _stream(stream)))
+    return Lc_pages, Rc_pages

@@ -159,6 +159,52 @@ MLA_EXPORT size_t mla_decode_absorbed_workspace_size(const mla_dims* d, int dtyp
   return 0;
 }
 
+namespace {
+// Enqueues one absorbed decode (dense or over selected keys) on either path.
+int run_decode(mla::DecodeArgs& a, int dtype, bool sparse, void* workspace, size_t workspace_bytes,
+               void* stream, const char* what) {
+  if (!a.pages.table && (long long)a.B * a.T_cap >= (1ll << 31))
+    return fail(MLA_ERR_UNSUPPORTED, "B*T_cap of 2^31 rows or more");
+  a.flags = flags_ptr();
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  if (!a.flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool pages_ok = !a.pages.table || a.pages.page_size % 128 == 0;
+  cudaError_t e;
+  mla::call_begin();
+  if (pages_ok && tc_decode_ok(a.g, dtype, a.q, a.Lc, a.Rc, a.kv_b)) {
+    size_t need = mla::tc_decode_workspace_bytes(a.g, a.B, a.S, sparse ? a.topk : a.T_cap, sparse ? a.topk : 0);
+    if (need && (!workspace || workspace_bytes < need))
+      return fail(MLA_ERR_INVALID, "workspace of %zu bytes < %zu required", workspace_bytes, need);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+      return fail(MLA_ERR_INVALID, "workspace must be 256-byte aligned");
+    e = sparse ? mla::launch_sparse_decode_tc(a, workspace, workspace_bytes, st)
+               : mla::launch_decode_tc(a, workspace, workspace_bytes, st);
+  } else {
+    mla::kernel_mark(st, sparse ? "sparse_decode_simt" : "decode_simt");
+    e = mla::launch_decode_simt(a, dtype, sparse, st);
+  }
+  mla::call_end(st);
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  return MLA_OK;
+}
+
+// Page-pool arguments of the paged entry points.
+int check_pages(int S, int num_pages, int page_size, const int32_t* block_table, int max_pages,
+                mla::PageTable* pt) {
+  if (!block_table) return fail(MLA_ERR_INVALID, "null block table");
+  if (num_pages < 1 || page_size < 1 || max_pages < 1)
+    return fail(MLA_ERR_INVALID, "num_pages=%d, page_size=%d and max_pages=%d must be >= 1", num_pages, page_size,
+                max_pages);
+  const long long cap = (long long)max_pages * page_size, pool = (long long)num_pages * page_size;
+  if (cap >= (1ll << 31) || pool >= (1ll << 31))
+    return fail(MLA_ERR_UNSUPPORTED, "page pool or per-sequence capacity of 2^31 rows or more");
+  if (cap < S) return fail(MLA_ERR_INVALID, "max_pages*page_size=%lld < S=%d", cap, S);
+  *pt = mla::PageTable{block_table, max_pages, page_size, num_pages};
+  return MLA_OK;
+}
+}  // namespace
+
 MLA_EXPORT int mla_decode_absorbed(const mla_dims* d, int dtype, int B, int S, const void* q,
                                    const void* Lc, const void* Rc, int T_cap, const int32_t* T,
                                    const void* kv_b, float* out, void* workspace,
@@ -179,26 +225,42 @@ MLA_EXPORT int mla_decode_absorbed(const mla_dims* d, int dtype, int B, int S, c
   a.T = T;
   a.kv_b = kv_b;
   a.out = out;
-  a.flags = flags_ptr();
-  a.wait_limit_ns = g_wait_limit_ns.load();
-  if (!a.flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  mla::call_begin();
-  if (tc_decode_ok(g, dtype, q, Lc, Rc, kv_b)) {
-    size_t need = mla::tc_decode_workspace_bytes(g, B, S, T_cap, 0);
-    if (need && (!workspace || workspace_bytes < need))
-      return fail(MLA_ERR_INVALID, "workspace of %zu bytes < %zu required", workspace_bytes, need);
-    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
-      return fail(MLA_ERR_INVALID, "workspace must be 256-byte aligned");
-    e = mla::launch_decode_tc(a, workspace, workspace_bytes, st);
-  } else {
-    mla::kernel_mark(st, "decode_simt");
-    e = mla::launch_decode_simt(a, dtype, /*sparse=*/false, st);
-  }
-  mla::call_end(st);
-  if (e != cudaSuccess) return cuda_fail(e, "mla_decode_absorbed launch");
-  return MLA_OK;
+  return run_decode(a, dtype, false, workspace, workspace_bytes, stream, "mla_decode_absorbed launch");
+}
+
+MLA_EXPORT size_t mla_decode_paged_workspace_size(const mla_dims* d, int dtype, int B, int S, int max_pages,
+                                                  int page_size) {
+  mla::Geometry g;
+  if (!resolve(d, &g) || B < 1 || S < 1 || max_pages < 1 || page_size < 1) return 0;
+  const long long cap = (long long)max_pages * page_size;
+  if (cap < S || cap >= (1ll << 31)) return 0;
+  if (dtype == MLA_BF16 && mla::tc_decode_geometry_ok(g) && page_size % 128 == 0)
+    return round256(mla::tc_decode_workspace_bytes(g, B, S, (int)cap, /*sparse_topk=*/0));
+  return 0;
+}
+
+MLA_EXPORT int mla_decode_paged(const mla_dims* d, int dtype, int B, int S, const void* q, const void* Lc_pages,
+                                const void* Rc_pages, int num_pages, int page_size, const int32_t* block_table,
+                                int max_pages, const int32_t* T, const void* kv_b, float* out, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  mla::Geometry g;
+  int rc = check_common(d, dtype, B, S, &g);
+  if (rc) return rc;
+  mla::DecodeArgs a{};
+  rc = check_pages(S, num_pages, page_size, block_table, max_pages, &a.pages);
+  if (rc) return rc;
+  if (!q || !Lc_pages || !Rc_pages || !T || !kv_b || !out) return fail(MLA_ERR_INVALID, "null tensor pointer");
+  a.g = g;
+  a.B = B;
+  a.S = S;
+  a.T_cap = max_pages * page_size;
+  a.q = q;
+  a.Lc = Lc_pages;
+  a.Rc = Rc_pages;
+  a.T = T;
+  a.kv_b = kv_b;
+  a.out = out;
+  return run_decode(a, dtype, false, workspace, workspace_bytes, stream, "mla_decode_paged launch");
 }
 
 MLA_EXPORT int mla_decode_launch_count(const mla_dims* d, int dtype, int B, int S, int sparse) {
@@ -243,26 +305,37 @@ MLA_EXPORT int mla_sparse_decode(const mla_dims* d, int dtype, int B, int S, con
   a.sel = sel;
   a.nsel = nsel;
   a.topk = topk;
-  a.flags = flags_ptr();
-  a.wait_limit_ns = g_wait_limit_ns.load();
-  if (!a.flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  mla::call_begin();
-  if (tc_decode_ok(g, dtype, q, Lc, Rc, kv_b)) {
-    size_t need = mla::tc_decode_workspace_bytes(g, B, S, topk, topk);
-    if (need && (!workspace || workspace_bytes < need))
-      return fail(MLA_ERR_INVALID, "workspace of %zu bytes < %zu required", workspace_bytes, need);
-    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
-      return fail(MLA_ERR_INVALID, "workspace must be 256-byte aligned");
-    e = mla::launch_sparse_decode_tc(a, workspace, workspace_bytes, st);
-  } else {
-    mla::kernel_mark(st, "sparse_decode_simt");
-    e = mla::launch_decode_simt(a, dtype, /*sparse=*/true, st);
-  }
-  mla::call_end(st);
-  if (e != cudaSuccess) return cuda_fail(e, "mla_sparse_decode launch");
-  return MLA_OK;
+  return run_decode(a, dtype, true, workspace, workspace_bytes, stream, "mla_sparse_decode launch");
+}
+
+MLA_EXPORT int mla_sparse_decode_paged(const mla_dims* d, int dtype, int B, int S, const void* q,
+                                       const void* Lc_pages, const void* Rc_pages, int num_pages, int page_size,
+                                       const int32_t* block_table, int max_pages, const int32_t* T,
+                                       const void* kv_b, const int32_t* sel, const int32_t* nsel, int topk,
+                                       float* out, void* workspace, size_t workspace_bytes, void* stream) {
+  mla::Geometry g;
+  int rc = check_common(d, dtype, B, S, &g);
+  if (rc) return rc;
+  mla::DecodeArgs a{};
+  rc = check_pages(S, num_pages, page_size, block_table, max_pages, &a.pages);
+  if (rc) return rc;
+  if (topk < 1) return fail(MLA_ERR_INVALID, "topk=%d must be >= 1", topk);
+  if (!q || !Lc_pages || !Rc_pages || !T || !kv_b || !out || !sel || !nsel)
+    return fail(MLA_ERR_INVALID, "null tensor pointer");
+  a.g = g;
+  a.B = B;
+  a.S = S;
+  a.T_cap = max_pages * page_size;
+  a.q = q;
+  a.Lc = Lc_pages;
+  a.Rc = Rc_pages;
+  a.T = T;
+  a.kv_b = kv_b;
+  a.out = out;
+  a.sel = sel;
+  a.nsel = nsel;
+  a.topk = topk;
+  return run_decode(a, dtype, true, workspace, workspace_bytes, stream, "mla_sparse_decode_paged launch");
 }
 
 // ---------------------------------------------------------------- prefill
@@ -364,9 +437,10 @@ MLA_EXPORT int dsa_topk_select(int B, int S, const float* scores, int T_cap, con
 }
 
 // ---------------------------------------------------------------- cache append
-MLA_EXPORT int mla_cache_append(const mla_dims* d, int dtype, int B, int S, const void* comp,
-                                const void* kv_a_ln, float rms_eps, int T_cap, const int32_t* T, void* Lc,
-                                void* Rc, void* stream) {
+namespace {
+int run_cache_append(const mla_dims* d, int dtype, int B, int S, const void* comp, const void* kv_a_ln,
+                     float rms_eps, int T_cap, const int32_t* T, void* Lc, void* Rc, const mla::PageTable& pages,
+                     void* stream, const char* what) {
   mla::Geometry g;
   int rc = check_common(d, dtype, B, S, &g);
   if (rc != MLA_OK) return rc;
@@ -376,7 +450,9 @@ MLA_EXPORT int mla_cache_append(const mla_dims* d, int dtype, int B, int S, cons
   if (g.Dr > 2 * mla::kMaxRopePairs) return fail(MLA_ERR_UNSUPPORTED, "qk_rope=%d above %d", g.Dr, 2 * mla::kMaxRopePairs);
   if (g.Dl > mla::kMaxAppendWidth)
     return fail(MLA_ERR_UNSUPPORTED, "kv_lora=%d above %d", g.Dl, mla::kMaxAppendWidth);
-  mla::AppendArgs a{B, S, T_cap, g.Dl, g.Dr, comp, kv_a_ln, rms_eps, T, Lc, Rc, flags_ptr(), {}};
+  if (!pages.table && (long long)B * T_cap >= (1ll << 31))
+    return fail(MLA_ERR_UNSUPPORTED, "B*T_cap of 2^31 rows or more");
+  mla::AppendArgs a{B, S, T_cap, g.Dl, g.Dr, comp, kv_a_ln, rms_eps, T, Lc, Rc, flags_ptr(), pages, {}};
   for (int j = 0; j < g.Dr / 2; ++j) a.theta[j] = std::pow(g.rope_base, -2.0 * j / g.Dr);
   if (!a.flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -384,8 +460,27 @@ MLA_EXPORT int mla_cache_append(const mla_dims* d, int dtype, int B, int S, cons
   mla::kernel_mark(st, "cache_append");
   cudaError_t e = mla::launch_cache_append(a, dtype, st);
   mla::call_end(st);
-  if (e != cudaSuccess) return cuda_fail(e, "mla_cache_append launch");
+  if (e != cudaSuccess) return cuda_fail(e, what);
   return MLA_OK;
+}
+}  // namespace
+
+MLA_EXPORT int mla_cache_append(const mla_dims* d, int dtype, int B, int S, const void* comp,
+                                const void* kv_a_ln, float rms_eps, int T_cap, const int32_t* T, void* Lc,
+                                void* Rc, void* stream) {
+  return run_cache_append(d, dtype, B, S, comp, kv_a_ln, rms_eps, T_cap, T, Lc, Rc, mla::PageTable{}, stream,
+                          "mla_cache_append launch");
+}
+
+MLA_EXPORT int mla_cache_append_paged(const mla_dims* d, int dtype, int B, int S, const void* comp,
+                                      const void* kv_a_ln, float rms_eps, void* Lc_pages, void* Rc_pages,
+                                      int num_pages, int page_size, const int32_t* block_table, int max_pages,
+                                      const int32_t* T, void* stream) {
+  mla::PageTable pt{};
+  int rc = check_pages(S, num_pages, page_size, block_table, max_pages, &pt);
+  if (rc) return rc;
+  return run_cache_append(d, dtype, B, S, comp, kv_a_ln, rms_eps, max_pages * page_size, T, Lc_pages, Rc_pages, pt,
+                          stream, "mla_cache_append_paged launch");
 }
 
 MLA_EXPORT int dsa_index_key_append(int B, int S, int index_hd, int rope_dim, const float* k_idx,

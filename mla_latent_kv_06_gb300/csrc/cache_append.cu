@@ -83,14 +83,20 @@ __global__ void __launch_bounds__(kAppThreads) cache_append_kernel(AppendArgs a)
   const float inv = rsqrtf(block_sum(ss, red) / (float)a.kv_lora + a.eps);
   const int pos = new_row(Tb, s, a.S, a.T_cap, a.flags);
   if (pos < 0) return;
-  Tv* lc = static_cast<Tv*>(a.Lc) + ((size_t)b * a.T_cap + pos) * a.kv_lora;
+  bool bad_page = false;
+  const long long row = cache_row(a.pages, b, a.T_cap, pos, &bad_page);
+  if (bad_page) {
+    if (tid == 0) raise_flag(a.flags, MLA_DEV_BAD_INDEX);
+    return;
+  }
+  Tv* lc = static_cast<Tv*>(a.Lc) + (size_t)row * a.kv_lora;
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
     const int i = tid + k * kAppThreads;
     if (i < a.kv_lora) store(lc + i, xv[k] * inv * wv[k]);
   }
   if (tid < half) {
-    Tv* rc = static_cast<Tv*>(a.Rc) + ((size_t)b * a.T_cap + pos) * a.qk_rope;
+    Tv* rc = static_cast<Tv*>(a.Rc) + (size_t)row * a.qk_rope;
     float y0, y1;
     rope_pair(pos, a.theta[tid], r0, r1, &y0, &y1);
     store(rc + tid, y0);

@@ -33,7 +33,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeArgs a) {
   float* qabs = qr + g.Dr;        // [Dl]
   float* clat = qabs + g.Dl;      // [Dl]
   float* sc = clat + g.Dl;        // [kChunk] scores, then probabilities
-  int* tok = reinterpret_cast<int*>(sc + kChunk);  // [kChunk] key index of each slot
+  int* tok = reinterpret_cast<int*>(sc + kChunk);  // [kChunk] cache row of each slot, -1 if masked
 
   const int Tb = a.T[b];
   const bool bad_len = (Tb < a.S || Tb > a.T_cap);
@@ -52,8 +52,8 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeArgs a) {
   const int32_t* sel = kSparse ? a.sel + ((size_t)b * a.S + s) * a.topk : nullptr;
 
   const Tin* q = static_cast<const Tin*>(a.q) + (((size_t)b * a.S + s) * g.H + h) * Dq;
-  const Tin* Lc = static_cast<const Tin*>(a.Lc) + (size_t)b * a.T_cap * g.Dl;
-  const Tin* Rc = static_cast<const Tin*>(a.Rc) + (size_t)b * a.T_cap * g.Dr;
+  const Tin* Lc = static_cast<const Tin*>(a.Lc);  // rows: cache_row() of (b, t)
+  const Tin* Rc = static_cast<const Tin*>(a.Rc);
   const Tin* Wuk = static_cast<const Tin*>(a.kv_b) + (size_t)h * Dkv * g.Dl;
   const Tin* Wuv = Wuk + (size_t)g.Dn * g.Dl;
 
@@ -83,17 +83,23 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeArgs a) {
     for (int j = warp; j < cn; j += kWarps) {
       int t = kSparse ? sel[c0 + j] : c0 + j;
       bool ok = (t >= 0 && t <= pos);
+      long long row = 0;
+      if (ok) {
+        bool bad_page = false;
+        row = cache_row(a.pages, b, a.T_cap, t, &bad_page);
+        ok = !bad_page;
+      }
       float dot = 0.f;
       if (ok) {
-        const Tin* lrow = Lc + (size_t)t * g.Dl;
-        const Tin* rrow = Rc + (size_t)t * g.Dr;
+        const Tin* lrow = Lc + (size_t)row * g.Dl;
+        const Tin* rrow = Rc + (size_t)row * g.Dr;
         for (int l = lane; l < g.Dl; l += 32) dot = fmaf(qabs[l], to_f32(lrow[l]), dot);
         for (int r = lane; r < g.Dr; r += 32) dot = fmaf(qr[r], to_f32(rrow[r]), dot);
         dot = warp_sum(dot);
       }
       if (lane == 0) {
         sc[j] = ok ? dot * g.scale : -INFINITY;
-        tok[j] = ok ? t : -1;
+        tok[j] = ok ? (int)row : -1;  // pool row (< 2^31, checked on the host)
       }
     }
     __syncthreads();

@@ -73,6 +73,7 @@ struct AttnParams {
   float* ml_part;
   unsigned int* flags;
   long long wait_ns;
+  PageTable pages;  // dense path: key tiles come from pages (page_size a multiple of kTile)
 };
 
 __device__ __forceinline__ bool bar_red_or(int id, int n, bool x) {
@@ -349,7 +350,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       while (ok && c.live) {
         const bool first = c.first();
         if (first) ++pc;
-        const int y = c.row * p.kv_rows + c.k * kTile;  // tile-list row = block of key-source rows
+        int y = c.row * p.kv_rows + c.k * kTile;  // tile-list row = block of key-source rows
+        if (!kSparse && p.pages.table) {  // the tile's 128 rows lie in one page
+          bool bad_page = false;
+          y = (int)cache_row(p.pages, c.row, p.T_cap, c.k * kTile, &bad_page);
+          if (bad_page) raise_flag(p.flags, MLA_DEV_BAD_INDEX);
+        }
         const uint32_t par = (it & 1) ^ 1;
         for (int a = 0; a < kSlots && ok; ++a) {
           ok = mbar_wait(&empty_bar[a], par, abort, p.flags, p.wait_ns);
@@ -682,6 +688,7 @@ struct AbsorbParams {
   int prefetch;
   double theta[kDr / 2];  // RoPE frequencies rope_base^(-2j/qk_rope), from the host
   unsigned int* flags;
+  PageTable pages;
 };
 
 // Rotary part of query row r of head h, rotated to the row's own position.
@@ -803,7 +810,22 @@ __global__ void __launch_bounds__(kAbsThreads, 2) absorb_kernel(const AbsorbPara
     // behind W_UK, in the order it is needed: 1/nblk of every sequence's
     // cache rows (the attention kernel), then W_UV rows (the combine).
     const int nblk = gridDim.x * gridDim.y, me = h * gridDim.x + cb;
-    for (int b = 0; b < p.B; ++b) {
+    // Paged caches: units of 16 KB, nine per key tile (eight 16-row blocks of
+    // latent rows, then the tile's rope rows), dealt round-robin to the CTAs.
+    for (int b = 0, base = 0; p.pages.table && b < p.B; ++b) {
+      const int Tb = min(max(p.T[b], 0), p.T_cap);
+      const int units = (Tb + kTile - 1) / kTile * 9;
+      for (int u = ((me - base) % nblk + nblk) % nblk; u < units; u += nblk) {
+        bool bad_page = false;
+        const long long row = cache_row(p.pages, b, p.T_cap, (u / 9) * kTile, &bad_page);
+        if (bad_page) continue;
+        const int part = u % 9;
+        if (part < 8) l2_prefetch(p.Lc + (size_t)(row + 16 * part) * kDl, 16 * kDl * 2);
+        else l2_prefetch(p.Rc + (size_t)row * kDr, kTile * kDr * 2);
+      }
+      base += units;
+    }
+    for (int b = 0; !p.pages.table && b < p.B; ++b) {
       const int Tb = min(max(p.T[b], 0), p.T_cap);
       const size_t lb = (size_t)Tb * kDl * 2, rb = (size_t)Tb * kDr * 2;
       const size_t l0 = (lb * me / nblk) & ~(size_t)15, l1 = (lb * (me + 1) / nblk) & ~(size_t)15;
@@ -1181,6 +1203,7 @@ struct GatherParams {
   __nv_bfloat16* stage;  // [R, Kpad, 576]
   int B, S, T_cap, topk, Kpad;
   unsigned int* flags;
+  PageTable pages;
 };
 
 __global__ void __launch_bounds__(256) gather_kernel(const GatherParams p) {
@@ -1200,9 +1223,19 @@ __global__ void __launch_bounds__(256) gather_kernel(const GatherParams p) {
         idx = -1;
       }
     }
+    long long row = 0;
+    if (idx >= 0) {
+      bool bad_page = false;
+      row = cache_row(p.pages, b, p.T_cap, idx, &bad_page);
+      if (bad_page) {
+        if (lane == 0) raise_flag(p.flags, MLA_DEV_BAD_INDEX);
+        idx = -1;
+        row = 0;
+      }
+    }
     uint4* dst = reinterpret_cast<uint4*>(p.stage + ((size_t)r * p.Kpad + j) * kDc);
-    const uint4* lsrc = reinterpret_cast<const uint4*>(p.Lc + ((size_t)b * p.T_cap + (idx < 0 ? 0 : idx)) * kDl);
-    const uint4* rsrc = reinterpret_cast<const uint4*>(p.Rc + ((size_t)b * p.T_cap + (idx < 0 ? 0 : idx)) * kDr);
+    const uint4* lsrc = reinterpret_cast<const uint4*>(p.Lc + (size_t)row * kDl);
+    const uint4* rsrc = reinterpret_cast<const uint4*>(p.Rc + (size_t)row * kDr);
     for (int c = lane; c < kDc / 8; c += 32) {
       uint4 v = make_uint4(0, 0, 0, 0);
       if (idx >= 0) v = c < kDl / 8 ? __ldg(lsrc + c) : __ldg(rsrc + (c - kDl / 8));
@@ -1295,7 +1328,10 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   const Geometry& g = a.g;
   const int B = a.B, S = a.S;
   const Plan pl = make_plan(B, S, a.T_cap, sparse ? a.topk : 0);
-  if ((long long)B * a.T_cap >= (1ll << 31)) return cudaErrorInvalidValue;
+  const bool paged = a.pages.table != nullptr;
+  const long long pool_rows = paged ? (long long)a.pages.num_pages * a.pages.page_size : (long long)B * a.T_cap;
+  if (pool_rows >= (1ll << 31) || (long long)B * a.T_cap >= (1ll << 31)) return cudaErrorInvalidValue;
+  if (paged && a.pages.page_size % kTile != 0) return cudaErrorInvalidValue;
   unsigned char* w = static_cast<unsigned char*>(ws);
   __nv_bfloat16* qcat = reinterpret_cast<__nv_bfloat16*>(w + pl.off_q);
   int32_t* ts = reinterpret_cast<int32_t*>(w + pl.off_ts);
@@ -1321,6 +1357,7 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
     gp.topk = a.topk;
     gp.Kpad = pl.Kpad;
     gp.flags = a.flags;
+    gp.pages = a.pages;
     kernel_mark(st, "gather");
     gather_kernel<<<dim3(pl.Kpad / 32, pl.R), 256, 0, st>>>(gp);
     e = cudaGetLastError();
@@ -1349,6 +1386,7 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   ap.Rc = static_cast<const __nv_bfloat16*>(a.Rc);
   // L2 prefetch on the small-batch path while the cache stays well inside L2
   ap.prefetch = (!big && !sparse && (long long)B * a.T_cap * (kDl + kDr) * 2 <= (48ll << 20)) ? 1 : 0;
+  ap.pages = sparse ? PageTable{} : a.pages;
   for (int j = 0; j < kDr / 2; ++j) ap.theta[j] = std::pow(g.rope_base, -2.0 * j / kDr);
   ap.flags = a.flags;
   const size_t abs_smem = (size_t)kAbsRows * g.Dn * 4 + (size_t)kAbsGroups * kAbsRows * kAbsCols * 4;
@@ -1392,7 +1430,7 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   AttnParams tp{};
   bool maps_ok = make_tmap_2d_bf16(&tp.mQ, qcat, (uint64_t)pl.R * kH, kDc, kDc, kH, 64);
   if (!sparse) {
-    const uint64_t rows = (uint64_t)B * a.T_cap;
+    const uint64_t rows = (uint64_t)pool_rows;
     maps_ok = maps_ok && make_tmap_2d_bf16(&tp.mL, a.Lc, rows, kDl, kDl, kTile, 64) &&
               make_tmap_2d_bf16(&tp.mR, a.Rc, rows, kDr, kDr, kTile, 64);
     tp.kv_rows = a.T_cap;
@@ -1418,6 +1456,7 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   tp.ml_part = ml_part;
   tp.flags = a.flags;
   tp.wait_ns = a.wait_limit_ns;
+  tp.pages = sparse ? PageTable{} : a.pages;
   auto kern = sparse ? attn_kernel<true> : attn_kernel<false>;
   e = set_smem_once(kern, (int)kAttnDynSmem, &g_attn_attr[sparse ? 1 : 0]);
   if (e != cudaSuccess) return e;

@@ -14,6 +14,26 @@ struct Geometry {
   double rope_base;       // resolved RoPE base
 };
 
+// Paged cache layout.  Token t of sequence b sits at row
+// table[b * max_pages + t / page_size] * page_size + t % page_size of the page
+// pool; table == nullptr means the contiguous layout (row b * T_cap + t).
+struct PageTable {
+  const int32_t* table;
+  int max_pages, page_size, num_pages;
+};
+
+// Pool row of token t of sequence b.  A page index outside [0, num_pages)
+// sets *bad and yields row 0, so that no access leaves the pool.
+__host__ __device__ __forceinline__ long long cache_row(const PageTable& pt, int b, int T_cap, int t, bool* bad) {
+  if (!pt.table) return (long long)b * T_cap + t;
+  const int pg = pt.table[(size_t)b * pt.max_pages + t / pt.page_size];
+  if (pg < 0 || pg >= pt.num_pages) {
+    *bad = true;
+    return 0;
+  }
+  return (long long)pg * pt.page_size + t % pt.page_size;
+}
+
 // Arguments common to the decode kernels (dense and sparse).
 struct DecodeArgs {
   Geometry g;
@@ -29,6 +49,7 @@ struct DecodeArgs {
   int topk;
   unsigned int* flags;
   long long wait_limit_ns;
+  PageTable pages;  // table == nullptr: contiguous [B, T_cap] caches
 };
 
 cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, bool sparse, cudaStream_t st);
@@ -85,9 +106,10 @@ struct AppendArgs {
   const void* kv_a_ln;  // [kv_lora]
   float eps;
   const int32_t* T;
-  void* Lc;  // [B, T_cap, kv_lora]
-  void* Rc;  // [B, T_cap, qk_rope]
+  void* Lc;  // [B, T_cap, kv_lora] or the page pool
+  void* Rc;  // [B, T_cap, qk_rope] or the page pool
   unsigned int* flags;
+  PageTable pages;
   double theta[kMaxRopePairs];
 };
 cudaError_t launch_cache_append(const AppendArgs& a, int dtype, cudaStream_t st);

@@ -77,6 +77,21 @@ def test_host_rejects_bad_arguments_without_a_gpu(lib):
     assert lib.dsa_index_key_append(1, 1, 600, 300, p, p, None, 1e-6, 1e4, 8, p, p,
                                     None) == mla.MLA_ERR_UNSUPPORTED
     assert lib.dsa_index_key_append(1, 1, 128, 64, None, p, None, 1e-6, 1e4, 8, p, p, None) == mla.MLA_ERR_INVALID
+    # paged entries: null block table, zero page size, capacity below S, pool of 2^31 rows
+    assert lib.mla_decode_paged(ctypes.byref(d), 1, 1, 1, p, p, p, 4, 128, None, 2, p, p, p, None, 0,
+                                None) == mla.MLA_ERR_INVALID
+    assert lib.mla_decode_paged(ctypes.byref(d), 1, 1, 1, p, p, p, 4, 0, p, 2, p, p, p, None, 0,
+                                None) == mla.MLA_ERR_INVALID
+    assert lib.mla_decode_paged(ctypes.byref(d), 1, 1, 9, p, p, p, 4, 2, p, 2, p, p, p, None, 0,
+                                None) == mla.MLA_ERR_INVALID
+    assert lib.mla_decode_paged(ctypes.byref(d), 1, 1, 1, p, p, p, 1 << 24, 1 << 8, p, 2, p, p, p, None, 0,
+                                None) == mla.MLA_ERR_UNSUPPORTED
+    assert lib.mla_sparse_decode_paged(ctypes.byref(d), 1, 1, 1, p, p, p, 4, 128, p, 2, p, p, p, p, 0, p, None, 0,
+                                       None) == mla.MLA_ERR_INVALID
+    assert lib.mla_cache_append_paged(ctypes.byref(d), 1, 1, 1, p, p, 1e-6, p, p, 4, 128, None, 2, p,
+                                      None) == mla.MLA_ERR_INVALID
+    assert lib.mla_decode_paged_workspace_size(ctypes.byref(d), 1, 1, 1, 2, 64) == 0  # not a multiple of 128
+    assert lib.mla_decode_paged_workspace_size(ctypes.byref(d), 1, 1, 1, 2, 128) > 0
 
 
 def test_workspace_sizes_are_host_only(lib):

@@ -162,6 +162,40 @@ def append_inputs(dims: Dims, B: int, S: int, dtype: str, seed: int, device="cpu
     return out
 
 
+def paged_layout(T: Sequence[int], page_size: int, seed: int, spare_pages: int = 3):
+    """A shuffled page assignment for sequences of lengths T: returns
+    ``(block_table [B, max_pages] int32, num_pages)``.  Sequence b owns
+    ceil(T[b] / page_size) pages, drawn from a seeded permutation of the pool
+    (which has ``spare_pages`` unused pages); table entries past a sequence's
+    last page are -1."""
+    need = [(t + page_size - 1) // page_size for t in T]
+    max_pages = max(need)
+    num_pages = sum(need) + spare_pages
+    g = _gen(seed + 0x3000, "cpu")
+    perm = torch.randperm(num_pages, generator=g).tolist()
+    table = torch.full((len(T), max_pages), -1, dtype=torch.int32)
+    k = 0
+    for b, n in enumerate(need):
+        table[b, :n] = torch.tensor(perm[k:k + n], dtype=torch.int32)
+        k += n
+    return table, num_pages
+
+
+def to_pages(cache, block_table, T: Sequence[int], page_size: int, num_pages: int, fill=float("nan")):
+    """Copies rows 0..T[b]-1 of a contiguous cache [B, T_cap, D] into a pool
+    [num_pages, page_size, D] at the rows the block table names; every other
+    pool row holds ``fill``."""
+    D = cache.shape[2]
+    pool = torch.full((num_pages * page_size, D), fill, dtype=cache.dtype, device=cache.device)
+    tbl = block_table.tolist()
+    for b, n in enumerate(T):
+        for i in range((n + page_size - 1) // page_size):
+            lo, hi = i * page_size, min(n, (i + 1) * page_size)
+            r0 = tbl[b][i] * page_size
+            pool[r0:r0 + hi - lo] = cache[b, lo:hi]
+    return pool.view(num_pages, page_size, D)
+
+
 def workload_inputs(name: str, device="cpu", S: Optional[int] = None) -> Dict[str, object]:
     """All inputs of a named workload (see ``WORKLOADS``)."""
     wl = WORKLOADS[name]
