@@ -43,7 +43,7 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 ROW_WORKLOADS = ("glm_batched_b32_s1", "glm_batched_b32_s6", "glm_dsa_t65536", "glm_prefill_s2048",
-                 "glm_append_b32_s6", "glm_paged_b32_s1")
+                 "glm_append_b32_s6", "glm_paged_b32_s1", "glm_dsa_t65536_l4")
 APPEND_RMS_EPS = 1e-6
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a
 # workload's dominant kernel, from one ncu capture of that kernel on this
@@ -83,8 +83,14 @@ def build_workload(name, device):
     elif name.startswith("glm_batched_b32_s"):
         x = workload_inputs("glm_batched_b32", device, S=int(name[len("glm_batched_b32_s"):]))
         kind = "decode"
-    elif name == "glm_dsa_t65536":
-        x = workload_inputs(name, device)
+    elif name in ("glm_dsa_t65536", "glm_dsa_t65536_l4"):
+        x = workload_inputs("glm_dsa_t65536", device)
+        x["layers"] = [x]
+        if name.endswith("_l4"):  # three more layers reuse the first layer's selection
+            for layer in range(1, 4):
+                y = mla_inputs(x["dims"], x["B"], x["S"], x["T_list"], x["T_cap"], "bf16", SEED_BASE + 10 + layer,
+                               device)
+                x["layers"].append(y)
         kind = "dsa"
     elif name == "glm_prefill_s2048":
         x = workload_inputs(name, device)
@@ -144,15 +150,20 @@ def build_workload(name, device):
         nsel = torch.empty(B, S, dtype=torch.int32, device=device)
         need = mla.lib().mla_sparse_decode_workspace_size(mla.ctypes.byref(mla.make_dims(d)), mla.MLA_BF16, B, S, k)
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+        L = len(x["layers"])
+        outs = [out] + [torch.empty_like(out) for _ in range(L - 1)]
         calls = [lambda: mla.index_scores(x["q_idx"], x["w"], x["Ic"], x["T"], out=sc),
-                 lambda: mla.topk_select(sc, x["T"], k, sel=sel, nsel=nsel),
-                 lambda: mla.sparse_decode(x["q"], x["Lc"], x["Rc"], x["T"], x["kv_b"], sel, nsel, d, out=out,
-                                           workspace=ws)]
+                 lambda: mla.topk_select(sc, x["T"], k, sel=sel, nsel=nsel)]
+        for y, o in zip(x["layers"], outs):
+            calls.append(lambda y=y, o=o: mla.sparse_decode(y["q"], y["Lc"], y["Rc"], x["T"], y["kv_b"], sel, nsel, d,
+                                                            out=o, workspace=ws))
+        info["tokens"] = R * L  # one query token per layer
         ic = 4 * x["Ic"].shape[2] * sum(T_list)
         scores = 4 * R * T_cap
         gathered = row * R * k
         clat = 2 * R * d.H * d.kv_lora
-        info.update(cache_bytes=gathered, alg_bytes=ic + 2 * scores + gathered + w_uk + w_uv + q_bytes + out_bytes)
+        info.update(cache_bytes=gathered * L,
+                    alg_bytes=ic + 2 * scores + L * (gathered + w_uk + w_uv + q_bytes + out_bytes))
         work = {"index_scores": ("hbm", ic + scores), "topk_select": ("hbm", scores + 4 * R * k),
                 "gather": ("hbm", 2 * gathered), "absorb": ("hbm", w_uk + q_bytes),
                 "attention": ("hbm", gathered + qcat), "combine": ("hbm", w_uv + out_bytes),
@@ -299,7 +310,11 @@ def kernel_times(calls, K, flush, stream):
         for nm, ev in zip(names, evs):
             for i, n in enumerate(nm):
                 acc.setdefault(n, []).append(ev[i].elapsed_time(ev[i + 1]) * 1e3)
-    return {n: statistics.mean(v) for n, v in acc.items()}
+    counts = {}
+    for nm in names:
+        for n in nm:
+            counts[n] = counts.get(n, 0) + 1
+    return {n: statistics.mean(v) for n, v in acc.items()}, counts
 
 
 def time_e2e(e2e, K, W, flush, stream):
@@ -320,20 +335,23 @@ def time_e2e(e2e, K, W, flush, stream):
     return time_steps(one, K, W, flush, stream), h2d, d2h
 
 
-def roofline(name, work, ktimes, pk, pk_kind):
-    """Roofline of the kernel with the largest share of the step."""
-    dom = max(ktimes, key=ktimes.get)
+def roofline(name, work, ktimes, counts, pk, pk_kind):
+    """Roofline of the kernel with the largest share of the step (ktimes: mean
+    us per launch; counts: launches per step)."""
+    share_us = {n: v * counts.get(n, 1) for n, v in ktimes.items()}
+    dom = max(share_us, key=share_us.get)
     bound, amount = work.get(dom, ("hbm", 0))
     t = ktimes[dom] * 1e-6
     if bound == "tensor":
         achieved, peak, unit = amount / t / 1e12, pk["bf16_tflops_sustained"], "TFLOP/s"
     else:
         achieved, peak, unit = amount / t / 1e9, pk["hbm_gbs"], "GB/s"
-    total = sum(ktimes.values())
+    total = sum(share_us.values())
     return {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
             "frac": achieved / peak, "peak_source": pk_kind, "algorithmic_per_launch": amount,
             "kernel_us": ktimes[dom], "traffic": NCU_TRAFFIC.get((name, dom)),
-            "kernels": {n: {"us": round(v, 2), "share": round(v / total, 3)} for n, v in ktimes.items()}}
+            "kernels": {n: {"us": round(v, 2), "launches": counts.get(n, 1), "share": round(share_us[n] / total, 3)}
+                        for n, v in ktimes.items()}}
 
 
 def measure(name, dev, stream, flush, K, W, pk, pk_kind, want_e2e):
@@ -346,8 +364,9 @@ def measure(name, dev, stream, flush, K, W, pk, pk_kind, want_e2e):
     assert mla.device_status() == 0, "device flags raised while warming up"
     g = capture(calls, stream)
     ms = time_steps(g.replay, K, W, flush, stream)
-    kt = kernel_times(calls, max(3, min(K, 20)), flush, stream)
-    res = {"ms": ms, "info": info, "ktimes": kt, "roof": roofline(name, work, kt, pk, pk_kind)}
+    kt, counts = kernel_times(calls, max(3, min(K, 20)), flush, stream)
+    res = {"ms": ms, "info": info, "ktimes": kt, "counts": counts,
+           "roof": roofline(name, work, kt, counts, pk, pk_kind)}
     if want_e2e and e2e is not None:
         res["e2e"] = time_e2e(e2e, K, W, flush, stream)
     del x, calls, g
@@ -485,7 +504,7 @@ def main():
                     "step_frac_of_measured_hbm": info["alg_bytes"] / step_s / 1e9 / pk["hbm_gbs"],
                     "step_frac_of_8tbs": info["alg_bytes"] / step_s / 8e12,
                     "roofline": res["roof"], "clocks": clk,
-                    "gpu_launches": len(res["ktimes"]) * K,
+                    "gpu_launches": sum(res["counts"].values()) * K,
                     "step_ms_min": min(res["ms"]), "step_ms_median": statistics.median(res["ms"]),
                     "wall_s_timed_region": t_wall}
             if "e2e" in res:

@@ -205,6 +205,30 @@ def test_dsa_glm_t65536_pipeline(cuda_lib):
         assert max_rel_err(out[b, 0], ref) < TOL["bf16"], b
 
 
+def test_dsa_selection_shared_by_later_layers(cuda_lib):
+    """One indexer pass and top-2048 selection serve the attention of several
+    layers ([MLA-KV] §2.2: the shared layers reuse dsa_sel): each layer's
+    sparse decode, with its own query, cache and kv_b, equals the oracle over
+    the same selected keys."""
+    T, S, k = [9000, 20000], 1, 2048
+    d = dsa_inputs(2, S, T, max(T), 32, 128, 61, DEV)
+    Tt = torch.tensor(T, dtype=torch.int32, device=DEV)
+    sc = cuda_lib.index_scores(d["q_idx"], d["w"], d["Ic"], Tt)
+    sel, nsel = cuda_lib.topk_select(sc, Tt, k)
+    rsel, rn = oracle.topk_select(oracle.index_scores(to_np(d["q_idx"]), to_np(d["w"]), to_np(d["Ic"]), T), T, S, k)
+    assert np.array_equal(sel.cpu().numpy(), rsel) and np.array_equal(nsel.cpu().numpy(), rn)
+    for layer in range(3):
+        x = mla_inputs(GLM, 2, S, T, max(T), "bf16", 70 + layer, DEV)
+        out = to_np(cuda_lib.sparse_decode(x["q"], x["Lc"], x["Rc"], x["T"], x["kv_b"], sel, nsel, GLM))
+        assert cuda_lib.device_status() == 0
+        kvb = to_np(x["kv_b"])
+        for b in range(2):
+            idx = rsel[b, 0, :rn[b, 0]]
+            ref = oracle.attend_absorbed(to_np(x["q"][b, 0]), to_np(x["Lc"][b, idx]), to_np(x["Rc"][b, idx]),
+                                         kvb, GLM.qk_nope, T[b] - 1, GLM.softmax_scale)
+            assert max_rel_err(out[b, 0], ref) < TOL["bf16"], (layer, b)
+
+
 @pytest.mark.parametrize("dtype,dims", [("f32", TINY), ("bf16", GLM)])
 def test_sparse_decode_keep_all_and_subset(cuda_lib, dtype, dims):
     T = [50, 300]
