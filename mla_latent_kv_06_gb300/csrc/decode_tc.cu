@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   unsigned char* sKV = smem + kQBytes;
 
   __shared__ uint64_t full_bar[kSlots], empty_bar[kSlots];
-  __shared__ uint64_t q_full, q_empty, s_full, s_free, p_full, o_done, mma_done;
+  __shared__ uint64_t q_full, q_empty, s_full, s_free, p_full, o_done, mma_done, o_blk[4];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ __align__(16) float red_max[4][kH];
@@ -280,6 +280,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     mbar_init(&s_free, kSoftThreads);
     mbar_init(&p_full, kSoftThreads);
     mbar_init(&o_done, 1);
+    for (int m = 0; m < 4; ++m) mbar_init(&o_blk[m], 1);
     mbar_init(&mma_done, 1);
     abort_flag = 0;
     fence_mbar_init();
@@ -448,6 +449,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           }
           mma_commit(&empty_bar[2 * m]);
           mma_commit(&empty_bar[2 * m + 1]);
+          mma_commit(&o_blk[m]);  // the epilogue may read this block while the next ones run
         }
         mma_commit(&empty_bar[8]);
         mma_commit(&o_done);
@@ -481,14 +483,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
 #pragma unroll
     for (int i = 0; i < 32; ++i) lp[i] = 0.f;
 
-    // Partials of a finished piece once its last value product (tile j) retired.
+    // Partials of a finished piece: each 128-row block of O^T as soon as its
+    // part of the last value product (tile j) retired.
     auto epilogue = [&](int j) -> bool {
-      const bool fail = !mbar_wait(&o_done, j & 1, abort, p.flags, p.wait_ns);
-      if (bar_red_or(1, kSoftThreads, fail)) return false;
-      tc_fence_after();
       float* op = p.o_part + (size_t)slot * kH * kDl;
 #pragma unroll 1
       for (int m = 0; m < 4; ++m) {
+        const bool fail = !mbar_wait(&o_blk[m], j & 1, abort, p.flags, p.wait_ns);
+        if (bar_red_or(1, kSoftThreads, fail)) return false;
+        tc_fence_after();
         float w[32];
         tmem_ld32(tmem + t_lane + kTmemO + 64 * m + col0, w);
         tmem_wait_ld();
