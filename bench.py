@@ -52,8 +52,6 @@ NCU_TRAFFIC = {
     ("glm_decode_t4096", "attention"): 4890880,
     ("glm_batched_b32_s1", "attention"): 583203072,
     ("glm_append_b32_s6", "cache_append"): 233472,
-    ("glm_dsa_t65536", "index_scores"): 138440192,
-    ("glm_dsa_t65536", "topk_select"): 1111552,
     ("glm_prefill_s2048", "flash_attention"): 794383360,
 }
 
@@ -153,8 +151,10 @@ def build_workload(name, device):
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
         L = len(x["layers"])
         outs = [out] + [torch.empty_like(out) for _ in range(L - 1)]
-        calls = [lambda: mla.index_scores(x["q_idx"], x["w"], x["Ic"], x["T"], out=sc),
-                 lambda: mla.topk_select(sc, x["T"], k, sel=sel, nsel=nsel)]
+        sws = torch.empty(max(mla.lib().dsa_select_workspace_size(B, S, x["q_idx"].shape[2], x["q_idx"].shape[3],
+                                                                  T_cap, k), 1), dtype=torch.uint8, device=device)
+        calls = [lambda: mla.select(x["q_idx"], x["w"], x["Ic"], x["T"], k, scores=sc, sel=sel, nsel=nsel,
+                                    workspace=sws)]
         for y, o in zip(x["layers"], outs):
             calls.append(lambda y=y, o=o: mla.sparse_decode(y["q"], y["Lc"], y["Rc"], x["T"], y["kv_b"], sel, nsel, d,
                                                             out=o, workspace=ws))

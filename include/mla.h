@@ -143,6 +143,22 @@ int mla_sparse_decode(const mla_dims* d, int dtype, int B, int S,
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Fused DSA selection ([MLA-KV] §2.2: indexer scores, then the causal top-k)
+ *
+ * dsa_index_scores followed by dsa_topk_select in one call, with the same
+ * arguments and results (scores as written by dsa_index_scores; sel and nsel
+ * bit-identical to dsa_topk_select).  With 32 index heads of 128 values the
+ * indexer also writes, per CTA, the histogram of the top 11 bits of each
+ * candidate's ordered score key into the workspace, and the top-k takes its
+ * first radix pass from those histograms instead of recounting the scores.
+ *   workspace: dsa_select_workspace_size() bytes (0 for other shapes), 256-byte aligned
+ * ------------------------------------------------------------------------- */
+size_t dsa_select_workspace_size(int B, int S, int n_ih, int index_hd, int T_cap, int topk);
+int dsa_select(int B, int S, int n_ih, int index_hd, const float* q_idx, const float* w, const float* Ic,
+               int T_cap, const int32_t* T, int topk, float* scores, int32_t* sel, int32_t* nsel,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Paged cache layout (the same operations on a shared page pool)
  *
  * The pages fix no storage layout beyond one 576-value row per token

@@ -29,6 +29,7 @@ EXPORTS = (
     "dsa_index_scores", "dsa_topk_select_workspace_size", "dsa_topk_select",
     "mla_cache_append", "dsa_index_key_append",
     "mla_decode_paged_workspace_size", "mla_decode_paged", "mla_sparse_decode_paged", "mla_cache_append_paged",
+    "dsa_select_workspace_size", "dsa_select",
 )
 
 
@@ -80,6 +81,8 @@ def _declare(lib: ctypes.CDLL) -> None:
         "mla_sparse_decode_paged": (_I, [_DP, _I, _I, _I, _P, _P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _I, _P,
                                          _P, _SZ, _P]),
         "mla_cache_append_paged": (_I, [_DP, _I, _I, _I, _P, _P, ctypes.c_float, _P, _P, _I, _I, _P, _I, _P, _P]),
+        "dsa_select_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+        "dsa_select": (_I, [_I, _I, _I, _I, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _SZ, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -308,6 +311,25 @@ def index_key_append(k_idx, ln_w, ln_b, T, Ic, rope_dim: int, ln_eps: float = 1e
                                       float(ln_eps), float(rope_base), T_cap, _ptr(T), _ptr(Ic),
                                       _stream(stream)))
     return Ic
+
+
+def select(q_idx, w, Ic, T, topk: int, scores=None, sel=None, nsel=None, workspace=None, stream=None):
+    """Fused DSA selection: index scores then causal top-k -> (scores, sel, nsel)."""
+    torch = _torch()
+    B, S, n_ih, hd = q_idx.shape
+    T_cap = Ic.shape[1]
+    dev = q_idx.device
+    if scores is None:
+        scores = torch.empty(B, S, T_cap, dtype=torch.float32, device=dev)
+    if sel is None:
+        sel = torch.empty(B, S, topk, dtype=torch.int32, device=dev)
+    if nsel is None:
+        nsel = torch.empty(B, S, dtype=torch.int32, device=dev)
+    need = lib().dsa_select_workspace_size(B, S, n_ih, hd, T_cap, topk)
+    workspace, wsb = _workspace(need, dev, workspace)
+    _check(lib().dsa_select(B, S, n_ih, hd, _ptr(q_idx), _ptr(w), _ptr(Ic), T_cap, _ptr(T), topk, _ptr(scores),
+                            _ptr(sel), _ptr(nsel), _ptr(workspace), wsb, _stream(stream)))
+    return scores, sel, nsel
 
 
 # ------------------------------------------------------------------ paged cache

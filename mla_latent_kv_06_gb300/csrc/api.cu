@@ -398,7 +398,7 @@ MLA_EXPORT int dsa_index_scores(int B, int S, int n_ih, int index_hd, const floa
   size_t smem = sizeof(float) * ((size_t)n_ih * index_hd + n_ih + 128 * (size_t)(index_hd + 1) + 256);
   if (smem > 220 * 1024)
     return fail(MLA_ERR_UNSUPPORTED, "n_ih*index_hd too large for one CTA (%zu bytes)", smem);
-  mla::IndexArgs a{B, S, n_ih, index_hd, T_cap, q_idx, w, Ic, T, scores, flags_ptr(), g_wait_limit_ns.load()};
+  mla::IndexArgs a{B, S, n_ih, index_hd, T_cap, q_idx, w, Ic, T, scores, flags_ptr(), g_wait_limit_ns.load(), nullptr};
   if (!a.flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   mla::call_begin();
@@ -425,7 +425,7 @@ MLA_EXPORT int dsa_topk_select(int B, int S, const float* scores, int T_cap, con
   if (B < 1 || S < 1 || T_cap < S || topk < 1)
     return fail(MLA_ERR_INVALID, "bad sizes B=%d S=%d T_cap=%d topk=%d", B, S, T_cap, topk);
   if (!scores || !T || !sel || !nsel) return fail(MLA_ERR_INVALID, "null tensor pointer");
-  mla::TopkArgs a{B, S, T_cap, topk, scores, T, sel, nsel, flags_ptr()};
+  mla::TopkArgs a{B, S, T_cap, topk, scores, T, sel, nsel, flags_ptr(), nullptr, 0};
   if (!a.flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   mla::call_begin();
@@ -433,6 +433,58 @@ MLA_EXPORT int dsa_topk_select(int B, int S, const float* scores, int T_cap, con
   cudaError_t e = mla::launch_topk_select(a, st);
   mla::call_end(st);
   if (e != cudaSuccess) return cuda_fail(e, "dsa_topk_select launch");
+  return MLA_OK;
+}
+
+// ---------------------------------------------------------------- fused DSA selection
+namespace {
+size_t dsa_select_ws(int B, int S, int n_ih, int index_hd, int T_cap) {
+  const int parts = mla::index_tc_parts(B, S, n_ih, index_hd, T_cap);
+  return parts > 0 ? round256((size_t)B * S * parts * 2048 * sizeof(uint32_t)) : 0;
+}
+}  // namespace
+
+MLA_EXPORT size_t dsa_select_workspace_size(int B, int S, int n_ih, int index_hd, int T_cap, int topk) {
+  if (B < 1 || S < 1 || n_ih < 1 || index_hd < 1 || T_cap < S || topk < 1) return 0;
+  return dsa_select_ws(B, S, n_ih, index_hd, T_cap);
+}
+
+MLA_EXPORT int dsa_select(int B, int S, int n_ih, int index_hd, const float* q_idx, const float* w,
+                          const float* Ic, int T_cap, const int32_t* T, int topk, float* scores, int32_t* sel,
+                          int32_t* nsel, void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 1 || S < 1 || n_ih < 1 || index_hd < 1 || T_cap < S || topk < 1)
+    return fail(MLA_ERR_INVALID, "bad sizes B=%d S=%d n_ih=%d index_hd=%d T_cap=%d topk=%d", B, S, n_ih, index_hd,
+                T_cap, topk);
+  if (!q_idx || !w || !Ic || !T || !scores || !sel || !nsel) return fail(MLA_ERR_INVALID, "null tensor pointer");
+  size_t smem = sizeof(float) * ((size_t)n_ih * index_hd + n_ih + 128 * (size_t)(index_hd + 1) + 256);
+  if (smem > 220 * 1024)
+    return fail(MLA_ERR_UNSUPPORTED, "n_ih*index_hd too large for one CTA (%zu bytes)", smem);
+  const size_t need = dsa_select_ws(B, S, n_ih, index_hd, T_cap);
+  if (need && (!workspace || workspace_bytes < need))
+    return fail(MLA_ERR_INVALID, "workspace of %zu bytes < %zu required", workspace_bytes, need);
+  unsigned int* flags = flags_ptr();
+  if (!flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
+  uint32_t* hpart = need ? static_cast<uint32_t*>(workspace) : nullptr;
+  mla::IndexArgs ia{B, S, n_ih, index_hd, T_cap, q_idx, w, Ic, T, scores, flags, g_wait_limit_ns.load(), hpart};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  mla::call_begin();
+  mla::kernel_mark(st, "index_scores");
+  cudaError_t e = mla::launch_index_scores_tc(ia, st);
+  if (e == cudaErrorNotSupported) {  // other shapes: CUDA-core indexer, the top-k builds its own first pass
+    hpart = nullptr;
+    ia.hpart = nullptr;
+    e = mla::launch_index_scores(ia, st);
+  }
+  if (e != cudaSuccess) {
+    mla::call_end(st);
+    return cuda_fail(e, "dsa_select indexer launch");
+  }
+  const int parts = hpart ? mla::index_tc_parts(B, S, n_ih, index_hd, T_cap) : 0;
+  mla::TopkArgs ta{B, S, T_cap, topk, scores, T, sel, nsel, flags, hpart, parts};
+  mla::kernel_mark(st, "topk_select");
+  e = mla::launch_topk_select(ta, st);
+  mla::call_end(st);
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_select top-k launch");
   return MLA_OK;
 }
 

@@ -405,6 +405,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_cluster_kernel(TopkArgs a, 
   __shared__ int sh_rem;
   __shared__ int cta_cnt[2];     // this CTA's keys > K and keys == K (read by the cluster)
 
+  grid_dep_wait();  // scores (and histograms) come from the indexer
   const int Tb = a.T[b];
   // Rows that need no selection: every CTA of the cluster takes the same branch.
   if (Tb < a.S || Tb > a.T_cap) {
@@ -434,10 +435,24 @@ __global__ void __launch_bounds__(kTopkThreads) topk_cluster_kernel(TopkArgs a, 
   __syncthreads();
 
   // pass 1: bits 31..21
+  if (a.hpart) {
+    // The indexer's per-CTA histograms of this row: CTA `rank` sums bins
+    // 256*rank .. 256*rank+255 over them, the cluster gathers the slices.
+    const uint32_t* hp = a.hpart + (size_t)row * a.hparts * 2048 + 256 * rank;
+    for (int i = tid; i < 256; i += kTopkThreads) {
+      int v = 0;
+      for (int c = 0; c < a.hparts; ++c) v += (int)__ldg(hp + (size_t)c * 2048 + i);
+      hist[0][256 * rank + i] = v;
+    }
+    cluster_sync_all();
+    for (int i = tid; i < 2048; i += kTopkThreads) tot[i] = ld_cluster_int(&hist[0][i], (uint32_t)(i >> 8));
+    __syncthreads();
+  } else {
 #pragma unroll
-  for (int i = 0; i < kTkMaxPer; ++i)
-    if (i < per) warp_hist_add(hist[0], key[i] >> 21, base + i < n);
-  cluster_hist_sum(hist[0], tot, 2048);
+    for (int i = 0; i < kTkMaxPer; ++i)
+      if (i < per) warp_hist_add(hist[0], key[i] >> 21, base + i < n);
+    cluster_hist_sum(hist[0], tot, 2048);
+  }
   int remaining = k;
   uint32_t prefix = pick_digit(tot, 2048, 21, 0u, &remaining, red, &sh_prefix, &sh_rem);
   // pass 2: bits 20..10 of the keys in the chosen bin
@@ -519,13 +534,15 @@ cudaError_t launch_topk_select(const TopkArgs& a, cudaStream_t st) {
     cfg.blockDim = dim3(kTopkThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kTkC;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, a, (int)(per < 1 ? 1 : per));
     if (e == cudaSuccess) return cudaSuccess;
     (void)cudaGetLastError();  // clusters unavailable: single-CTA kernel below

@@ -46,6 +46,7 @@ struct IdxTcParams {
   const float* w;  // [B, S, 32]
   const int32_t* T;
   float* scores;   // [B, S, T_cap]
+  uint32_t* hpart; // [B*S, gridDim.x, 2048] or null
   int B, S, T_cap, ntiles, tpc;
   unsigned int* flags;
   long long wait_ns;
@@ -87,6 +88,11 @@ __global__ void __launch_bounds__(kIThreads, 1) index_tc_kernel(const __grid_con
   const int tb = blockIdx.x * p.tpc;
   const int te = min(p.ntiles, tb + p.tpc);
   float* srow = p.scores + ((size_t)b * p.S + s) * p.T_cap;
+  grid_dep_launch();  // the top-k of a fused selection may launch; it waits for this grid
+  // this CTA's slice of the first-pass histogram, filled by the epilogue
+  uint32_t* hp = p.hpart ? p.hpart + (((size_t)b * p.S + s) * gridDim.x + blockIdx.x) * 2048 : nullptr;
+  if (hp)
+    for (int i = threadIdx.x; i < 2048; i += kIThreads) hp[i] = 0u;
   const int Tb = p.T[b];
   if (Tb < p.S || Tb > p.T_cap) {  // whole CTA: NaN scores and the length flag
     if (threadIdx.x == 0 && blockIdx.x == 0 && s == 0) raise_flag(p.flags, MLA_DEV_BAD_LENGTH);
@@ -245,6 +251,15 @@ __global__ void __launch_bounds__(kIThreads, 1) index_tc_kernel(const __grid_con
       for (int h = 0; h < kIHeads; ++h) sc = fmaf(w_s[h], fmaxf(v[h], 0.f), sc);
       const int t = (tb + j) * kITile + 32 * qd + lane;
       if (t < p.T_cap) srow[t] = (t <= pos) ? sc : -INFINITY;
+      if (hp) {  // candidates only; one atomic per distinct bin of the warp
+        const bool cand = t <= pos;
+        const uint32_t bin = ordered_key(sc) >> 21;
+        const unsigned am = __ballot_sync(0xffffffffu, cand);
+        if (cand) {
+          const unsigned peers = __match_any_sync(am, bin);
+          if (lane == __ffs(peers) - 1) atomicAdd(&hp[bin], (uint32_t)__popc(peers));
+        }
+      }
       return true;
     };
     for (int i = 0; ok && i <= na; ++i) {
@@ -282,6 +297,27 @@ __global__ void __launch_bounds__(kIThreads, 1) index_tc_kernel(const __grid_con
 
 }  // namespace
 
+namespace {
+// Tiles per CTA: about two CTAs' worth of tiles per SM pass, at least 4 tiles per CTA to fill the ring.
+int tiles_per_cta(int B, int S, int T_cap) {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long ntiles = (T_cap + kITile - 1) / kITile;
+  const long long rows = (long long)B * S;
+  long long tpc = (rows * ntiles + sms - 1) / sms;
+  if (tpc < 4) tpc = 4;
+  if (tpc > ntiles) tpc = ntiles;
+  return (int)tpc;
+}
+}  // namespace
+
+int index_tc_parts(int B, int S, int n_ih, int hd, int T_cap) {
+  if (n_ih != kIHeads || hd != kIHd || B < 1 || S < 1 || T_cap < 1) return 0;
+  const int ntiles = (T_cap + kITile - 1) / kITile;
+  const int tpc = tiles_per_cta(B, S, T_cap);
+  return (ntiles + tpc - 1) / tpc;
+}
+
 cudaError_t launch_index_scores_tc(const IndexArgs& a, cudaStream_t st) {
   if (a.n_ih != kIHeads || a.hd != kIHd || (reinterpret_cast<uintptr_t>(a.Ic) & 15u) != 0)
     return cudaErrorNotSupported;
@@ -297,14 +333,10 @@ cudaError_t launch_index_scores_tc(const IndexArgs& a, cudaStream_t st) {
   p.ntiles = (a.T_cap + kITile - 1) / kITile;
   p.flags = a.flags;
   p.wait_ns = a.wait_ns;
-  // about two CTAs' worth of tiles per SM pass, at least 4 tiles per CTA to fill the ring
-  int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long long rows = (long long)a.B * a.S;
-  long long tpc = (rows * p.ntiles + sms - 1) / sms;
-  if (tpc < 4) tpc = 4;
-  if (tpc > p.ntiles) tpc = p.ntiles;
-  p.tpc = (int)tpc;
+  p.tpc = tiles_per_cta(a.B, a.S, a.T_cap);
+  p.hpart = a.hpart;
+  int dev = 0;
+  cudaGetDevice(&dev);
   static int attr_done = -1;
   if (attr_done != dev) {
     cudaError_t e = cudaFuncSetAttribute(index_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kIDynSmem);

@@ -76,12 +76,18 @@ struct IndexArgs {
   float* scores;
   unsigned int* flags;
   long long wait_ns;  // bound of every wait inside a kernel
+  // Optional [B*S, parts, 2048] histograms of the top 11 bits of the ordered
+  // score keys of the candidates t <= pos, one per indexer CTA of a row (the
+  // first radix pass of the top-k); only the tensor-core indexer writes them.
+  uint32_t* hpart;
 };
 
 cudaError_t launch_index_scores(const IndexArgs& a, cudaStream_t st);
 // Tensor-core indexer (32 index heads x 128, fp32 through three tf32 products);
 // returns cudaErrorNotSupported when the request does not fit it.
 cudaError_t launch_index_scores_tc(const IndexArgs& a, cudaStream_t st);
+// CTAs per (b, s) row of the tensor-core indexer, 0 when it does not take the shape.
+int index_tc_parts(int B, int S, int n_ih, int hd, int T_cap);
 
 struct TopkArgs {
   int B, S, T_cap, topk;
@@ -90,6 +96,8 @@ struct TopkArgs {
   int32_t* sel;
   int32_t* nsel;
   unsigned int* flags;
+  const uint32_t* hpart;  // optional first-pass histograms from the indexer (IndexArgs::hpart)
+  int hparts;
 };
 
 cudaError_t launch_topk_select(const TopkArgs& a, cudaStream_t st);

@@ -205,6 +205,43 @@ def test_dsa_glm_t65536_pipeline(cuda_lib):
         assert max_rel_err(out[b, 0], ref) < TOL["bf16"], b
 
 
+@pytest.mark.parametrize("T,S,nh,hd,k", [([65536, 9000, 2048, 2049], 1, 32, 128, 2048), ([3000, 517, 129], 2, 32, 128, 256),
+                                          ([300, 17, 1000], 2, 4, 32, 64), ([130000], 1, 32, 128, 2048)])
+def test_fused_select_bit_exact(cuda_lib, T, S, nh, hd, k):
+    """dsa_select (indexer histograms feed the top-k's first radix pass) gives the
+    oracle's scores and index sets bit for bit, and the same as the two calls."""
+    T_cap = max(T) + 3
+    d = dsa_inputs(len(T), S, T, T_cap, nh, hd, 200 + S + k, DEV)
+    Tt = torch.tensor(T, dtype=torch.int32, device=DEV)
+    sc, sel, nsel = cuda_lib.select(d["q_idx"], d["w"], d["Ic"], Tt, k)
+    assert cuda_lib.device_status() == 0
+    ref_sc = oracle.index_scores(to_np(d["q_idx"]), to_np(d["w"]), to_np(d["Ic"]), T)
+    got = to_np(sc)
+    for b, t in enumerate(T):  # rows past T_b are not defined by the indexer
+        assert np.array_equal(got[b, :, :t], ref_sc[b, :, :t])
+    rsel, rn = oracle.topk_select(ref_sc, T, S, k)
+    assert np.array_equal(sel.cpu().numpy(), rsel) and np.array_equal(nsel.cpu().numpy(), rn)
+    sel2, nsel2 = cuda_lib.topk_select(sc, Tt, k)
+    assert torch.equal(sel, sel2) and torch.equal(nsel, nsel2)
+
+
+def test_fused_select_crowded_scores(cuda_lib):
+    """Scores crowded into few first-pass bins (keys and queries in {0, 1}): the
+    histograms carry large counts and many ties at the threshold."""
+    T, S, k = [40000, 33000], 1, 2048
+    g = torch.Generator(device=DEV)
+    g.manual_seed(5)
+    q = torch.randint(0, 2, (2, S, 32, 128), generator=g, device=DEV, dtype=torch.int32).float()
+    w = torch.randint(0, 2, (2, S, 32), generator=g, device=DEV, dtype=torch.int32).float()
+    Ic = torch.randint(0, 2, (2, max(T), 128), generator=g, device=DEV, dtype=torch.int32).float()
+    Tt = torch.tensor(T, dtype=torch.int32, device=DEV)
+    sc, sel, nsel = cuda_lib.select(q, w, Ic, Tt, k)
+    assert cuda_lib.device_status() == 0
+    ref_sc = oracle.index_scores(to_np(q), to_np(w), to_np(Ic), T)
+    rsel, rn = oracle.topk_select(ref_sc, T, S, k)
+    assert np.array_equal(sel.cpu().numpy(), rsel) and np.array_equal(nsel.cpu().numpy(), rn)
+
+
 def test_dsa_selection_shared_by_later_layers(cuda_lib):
     """One indexer pass and top-2048 selection serve the attention of several
     layers ([MLA-KV] §2.2: the shared layers reuse dsa_sel): each layer's
