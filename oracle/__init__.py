@@ -41,8 +41,10 @@ Parity status of each function (what pins it, see tests/test_oracle_pins.py):
   index_key_append        land at pos = T[b] - S + s.
 * page_row, unpage      - hand-worked block table; identity table equals the
                           contiguous layout.
+* o_proj                - hand-worked 2x3 product; one-hot rows pick columns.
 """
 from .mla import (  # noqa: F401
+    o_proj,
     page_row,
     unpage,
     rms_norm,

@@ -337,3 +337,11 @@ def unpage(pool, block_table, T):
         for t in range(n):
             out[b, t] = rows[page_row(block_table, b, t, page_size)]
     return out
+
+
+# --------------------------------------------------------------- output projection
+def o_proj(x, w_o):
+    """y[r, n] = sum_k w_o[n, k] x[r, k]: the o output projection that ends both
+    attention paths ([MLA-KV] §2.3), x [R, in_dim] (a decode output flattened
+    per row), w_o [hidden, in_dim]."""
+    return _f64(x) @ _f64(w_o).T

@@ -455,3 +455,17 @@ def test_identity_block_table_is_the_contiguous_layout():
     table = [[0, 1, 2, 3], [4, 5, 6, 7]]
     assert np.array_equal(oracle.unpage(pool, table, [8, 5])[0], r[0])
     assert np.array_equal(oracle.unpage(pool, table, [8, 5])[1, :5], r[1, :5])
+
+
+# --------------------------------------------------------------- output projection
+def test_o_proj_hand_values_and_one_hot():
+    """y = x W^T worked by hand for a 2x3 weight; a one-hot row of x returns the
+    matching column of W."""
+    w = np.array([[1.0, 2.0, 3.0], [-1.0, 0.5, 4.0]])
+    x = np.array([[1.0, 1.0, 1.0], [2.0, 0.0, -1.0]])
+    assert np.array_equal(oracle.o_proj(x, w), [[6.0, 3.5], [-1.0, -6.0]])
+    r = np.random.default_rng(3).standard_normal((5, 7))
+    for k in range(7):
+        e = np.zeros((1, 7))
+        e[0, k] = 1.0
+        assert np.array_equal(oracle.o_proj(e, r)[0], r[:, k])
