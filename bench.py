@@ -43,7 +43,8 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 ROW_WORKLOADS = ("glm_batched_b32_s1", "glm_batched_b32_s6", "glm_dsa_t65536", "glm_prefill_s2048",
-                 "glm_append_b32_s6", "glm_paged_b32_s1", "glm_dsa_t65536_l4")
+                 "glm_append_b32_s6", "glm_paged_b32_s1", "glm_dsa_t65536_l4", "glm_decode_oproj_t4096")
+OPROJ_HIDDEN = 6144  # model width of the projection row: a size chosen here, the pages print none
 APPEND_RMS_EPS = 1e-6
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a
 # workload's dominant kernel, from one ncu capture of that kernel on this
@@ -97,6 +98,12 @@ def build_workload(name, device):
     elif name == "glm_append_b32_s6":
         x = workload_inputs("glm_batched_b32", device, S=6)
         kind = "append"
+    elif name == "glm_decode_oproj_t4096":
+        x = workload_inputs("glm_decode_t4096", device)
+        g = torch.Generator(device=device)
+        g.manual_seed(SEED_BASE + 7)
+        x["w_o"] = (torch.randn(OPROJ_HIDDEN, 64 * 256, generator=g, device=device) * 0.02).to(torch.bfloat16)
+        kind = "decode_oproj"
     elif name == "glm_paged_b32_s1":
         from workload import paged_layout, to_pages
         x = workload_inputs("glm_batched_b32", device, S=1)
@@ -170,6 +177,19 @@ def build_workload(name, device):
                 "attention": ("hbm", gathered + qcat), "combine": ("hbm", w_uv + out_bytes),
                 "absorb_gemm": ("hbm", w_uk + q_bytes + qcat), "plan_rope": ("hbm", q_bytes),
                 "merge": ("hbm", clat), "up_gemm": ("hbm", w_uv + clat + out_bytes)}
+        e2e = None
+    elif kind == "decode_oproj":
+        need = mla.lib().mla_decode_oproj_workspace_size(mla.ctypes.byref(mla.make_dims(d)), mla.MLA_BF16, B, S,
+                                                          x["T_cap"], OPROJ_HIDDEN)
+        ws = torch.empty(need, dtype=torch.uint8, device=device)
+        y = torch.empty(B, S, OPROJ_HIDDEN, dtype=torch.float32, device=device)
+        calls = [lambda: mla.decode_oproj(x["q"], x["Lc"], x["Rc"], x["T"], x["kv_b"], x["w_o"], d, y=y,
+                                          workspace=ws)]
+        cache = row * sum(T_list)
+        w_o = 2 * OPROJ_HIDDEN * d.H * d.v_head
+        info.update(cache_bytes=cache, alg_bytes=cache + w_uk + w_uv + w_o + q_bytes + out_bytes + 4 * R * OPROJ_HIDDEN)
+        work = {"absorb": ("hbm", w_uk + q_bytes), "attention": ("hbm", cache + qcat),
+                "combine": ("hbm", w_uv + out_bytes), "oproj_gemv": ("hbm", w_o + out_bytes + 4 * R * OPROJ_HIDDEN)}
         e2e = None
     elif kind == "append":
         from workload import append_inputs

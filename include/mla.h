@@ -143,6 +143,32 @@ int mla_sparse_decode(const mla_dims* d, int dtype, int B, int S,
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Output projection ([MLA-KV] §2.3: both attention paths end with the o
+ * output projection)
+ *
+ *   y[r, n] = sum_k w_o[n, k] * x[r, k]
+ *   w_o [hidden, in_dim]  dtype (bf16 or float), 16-byte aligned
+ *   x   [R, in_dim]       float, 16-byte aligned (a decode output [B, S, H, v_head] is R = B*S rows of
+ *                         in_dim = H*v_head)
+ *   y   [R, hidden]       float
+ * in_dim a multiple of 8.  Up to 8 rows: one streaming pass over w_o on the
+ * CUDA cores (fp32 arithmetic).  More rows with bf16 weights (in_dim and
+ * hidden multiples of 64): x is rounded to bf16 in the workspace and the
+ * product runs on the tensor cores; otherwise passes of 8 rows.
+ *   workspace: mla_o_proj_workspace_size() bytes (0 for the streaming path)
+ * mla_decode_oproj is mla_decode_absorbed followed by the projection of its
+ * output, which stays in the workspace; the projection launches as a
+ * programmatic dependent and starts reading w_o before the attention ends.
+ * ------------------------------------------------------------------------- */
+size_t mla_o_proj_workspace_size(int R, int in_dim, int hidden, int dtype);
+int mla_o_proj(int R, int in_dim, int hidden, int dtype, const void* w_o, const float* x, float* y,
+               void* workspace, size_t workspace_bytes, void* stream);
+size_t mla_decode_oproj_workspace_size(const mla_dims* d, int dtype, int B, int S, int T_cap, int hidden);
+int mla_decode_oproj(const mla_dims* d, int dtype, int B, int S, const void* q, const void* Lc, const void* Rc,
+                     int T_cap, const int32_t* T, const void* kv_b, const void* w_o, int hidden, float* y,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Fused DSA selection ([MLA-KV] §2.2: indexer scores, then the causal top-k)
  *
  * dsa_index_scores followed by dsa_topk_select in one call, with the same

@@ -30,6 +30,7 @@ EXPORTS = (
     "mla_cache_append", "dsa_index_key_append",
     "mla_decode_paged_workspace_size", "mla_decode_paged", "mla_sparse_decode_paged", "mla_cache_append_paged",
     "dsa_select_workspace_size", "dsa_select",
+    "mla_o_proj_workspace_size", "mla_o_proj", "mla_decode_oproj_workspace_size", "mla_decode_oproj",
 )
 
 
@@ -83,6 +84,10 @@ def _declare(lib: ctypes.CDLL) -> None:
         "mla_cache_append_paged": (_I, [_DP, _I, _I, _I, _P, _P, ctypes.c_float, _P, _P, _I, _I, _P, _I, _P, _P]),
         "dsa_select_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
         "dsa_select": (_I, [_I, _I, _I, _I, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _SZ, _P]),
+        "mla_o_proj_workspace_size": (_SZ, [_I, _I, _I, _I]),
+        "mla_o_proj": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
+        "mla_decode_oproj_workspace_size": (_SZ, [_DP, _I, _I, _I, _I, _I]),
+        "mla_decode_oproj": (_I, [_DP, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _SZ, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -311,6 +316,39 @@ def index_key_append(k_idx, ln_w, ln_b, T, Ic, rope_dim: int, ln_eps: float = 1e
                                       float(ln_eps), float(rope_base), T_cap, _ptr(T), _ptr(Ic),
                                       _stream(stream)))
     return Ic
+
+
+def o_proj(x, w_o, y=None, workspace=None, stream=None):
+    """y [R, hidden] = x [R, in_dim] (fp32) times w_o [hidden, in_dim]^T."""
+    torch = _torch()
+    x2 = x.reshape(-1, x.shape[-1]) if x.dim() == 2 else x.reshape(x.shape[0] * x.shape[1], -1)
+    R, in_dim = x2.shape
+    hidden = w_o.shape[0]
+    code = _dtype_code(w_o)
+    if y is None:
+        y = torch.empty(R, hidden, dtype=torch.float32, device=x.device)
+    need = lib().mla_o_proj_workspace_size(R, in_dim, hidden, code)
+    workspace, wsb = _workspace(need, x.device, workspace)
+    _check(lib().mla_o_proj(R, in_dim, hidden, code, _ptr(w_o), _ptr(x2), _ptr(y), _ptr(workspace), wsb,
+                            _stream(stream)))
+    return y
+
+
+def decode_oproj(q, Lc, Rc, T, kv_b, w_o, dims, y=None, workspace=None, stream=None):
+    """mla_decode_absorbed then the output projection: y [B, S, hidden]."""
+    torch = _torch()
+    B, S = q.shape[0], q.shape[1]
+    T_cap = Lc.shape[1]
+    hidden = w_o.shape[0]
+    code = _dtype_code(q)
+    if y is None:
+        y = torch.empty(B, S, hidden, dtype=torch.float32, device=q.device)
+    d = make_dims(dims)
+    need = lib().mla_decode_oproj_workspace_size(ctypes.byref(d), code, B, S, T_cap, hidden)
+    workspace, wsb = _workspace(need, q.device, workspace)
+    _check(lib().mla_decode_oproj(ctypes.byref(d), code, B, S, _ptr(q), _ptr(Lc), _ptr(Rc), T_cap, _ptr(T),
+                                  _ptr(kv_b), _ptr(w_o), hidden, _ptr(y), _ptr(workspace), wsb, _stream(stream)))
+    return y
 
 
 def select(q_idx, w, Ic, T, topk: int, scores=None, sel=None, nsel=None, workspace=None, stream=None):

@@ -162,7 +162,7 @@ MLA_EXPORT size_t mla_decode_absorbed_workspace_size(const mla_dims* d, int dtyp
 namespace {
 // Enqueues one absorbed decode (dense or over selected keys) on either path.
 int run_decode(mla::DecodeArgs& a, int dtype, bool sparse, void* workspace, size_t workspace_bytes,
-               void* stream, const char* what) {
+               void* stream, const char* what, bool own_call = true) {
   if (!a.pages.table && (long long)a.B * a.T_cap >= (1ll << 31))
     return fail(MLA_ERR_UNSUPPORTED, "B*T_cap of 2^31 rows or more");
   a.flags = flags_ptr();
@@ -171,7 +171,7 @@ int run_decode(mla::DecodeArgs& a, int dtype, bool sparse, void* workspace, size
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool pages_ok = !a.pages.table || a.pages.page_size % 128 == 0;
   cudaError_t e;
-  mla::call_begin();
+  if (own_call) mla::call_begin();
   if (pages_ok && tc_decode_ok(a.g, dtype, a.q, a.Lc, a.Rc, a.kv_b)) {
     size_t need = mla::tc_decode_workspace_bytes(a.g, a.B, a.S, sparse ? a.topk : a.T_cap, sparse ? a.topk : 0);
     if (need && (!workspace || workspace_bytes < need))
@@ -184,7 +184,7 @@ int run_decode(mla::DecodeArgs& a, int dtype, bool sparse, void* workspace, size
     mla::kernel_mark(st, sparse ? "sparse_decode_simt" : "decode_simt");
     e = mla::launch_decode_simt(a, dtype, sparse, st);
   }
-  mla::call_end(st);
+  if (own_call) mla::call_end(st);
   if (e != cudaSuccess) return cuda_fail(e, what);
   return MLA_OK;
 }
@@ -485,6 +485,107 @@ MLA_EXPORT int dsa_select(int B, int S, int n_ih, int index_hd, const float* q_i
   e = mla::launch_topk_select(ta, st);
   mla::call_end(st);
   if (e != cudaSuccess) return cuda_fail(e, "dsa_select top-k launch");
+  return MLA_OK;
+}
+
+// ---------------------------------------------------------------- output projection
+namespace {
+int check_oproj(int R, int in_dim, int hidden, int dtype, const void* w_o, const float* x, const float* y) {
+  if (R < 1 || in_dim < 8 || hidden < 1 || in_dim % 8 != 0)
+    return fail(MLA_ERR_INVALID, "bad sizes R=%d in_dim=%d hidden=%d (in_dim a multiple of 8)", R, in_dim, hidden);
+  if (dtype != MLA_F32 && dtype != MLA_BF16) return fail(MLA_ERR_INVALID, "unknown dtype %d", dtype);
+  if (!w_o || !x || !y) return fail(MLA_ERR_INVALID, "null tensor pointer");
+  if (!aligned16(w_o) || !aligned16(x)) return fail(MLA_ERR_INVALID, "w_o and x must be 16-byte aligned");
+  return MLA_OK;
+}
+}  // namespace
+
+MLA_EXPORT size_t mla_o_proj_workspace_size(int R, int in_dim, int hidden, int dtype) {
+  if (R < 1 || in_dim < 8 || hidden < 1) return 0;
+  return round256(mla::oproj_workspace_bytes(R, in_dim, hidden, dtype));
+}
+
+MLA_EXPORT int mla_o_proj(int R, int in_dim, int hidden, int dtype, const void* w_o, const float* x, float* y,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_oproj(R, in_dim, hidden, dtype, w_o, x, y);
+  if (rc) return rc;
+  const size_t need = mla::oproj_workspace_bytes(R, in_dim, hidden, dtype);
+  if (need && (!workspace || workspace_bytes < need))
+    return fail(MLA_ERR_INVALID, "workspace of %zu bytes < %zu required", workspace_bytes, need);
+  if (need && !aligned16(workspace)) return fail(MLA_ERR_INVALID, "workspace must be 256-byte aligned");
+  unsigned int* flags = flags_ptr();
+  if (!flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
+  mla::OprojArgs a{R, in_dim, hidden, dtype, w_o, x, y, workspace};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  mla::call_begin();
+  cudaError_t e = mla::launch_oproj(a, false, flags, g_wait_limit_ns.load(), st);
+  mla::call_end(st);
+  if (e != cudaSuccess) return cuda_fail(e, "mla_o_proj launch");
+  return MLA_OK;
+}
+
+namespace {
+// Decode workspace, then out [R, H, v_head] fp32, then the projection's scratch.
+struct OprojPlan {
+  size_t dec, out_off, op_off, total;
+};
+OprojPlan oproj_plan(const mla::Geometry& g, int dtype, int B, int S, int T_cap, int hidden) {
+  OprojPlan p{};
+  p.dec = (dtype == MLA_BF16 && mla::tc_decode_geometry_ok(g)) ? round256(mla::tc_decode_workspace_bytes(g, B, S, T_cap, 0))
+                                                               : 0;
+  p.out_off = p.dec;
+  p.op_off = p.out_off + round256((size_t)B * S * g.H * g.Dv * sizeof(float));
+  p.total = p.op_off + round256(mla::oproj_workspace_bytes(B * S, g.H * g.Dv, hidden, dtype));
+  return p;
+}
+}  // namespace
+
+MLA_EXPORT size_t mla_decode_oproj_workspace_size(const mla_dims* d, int dtype, int B, int S, int T_cap, int hidden) {
+  mla::Geometry g;
+  if (!resolve(d, &g) || B < 1 || S < 1 || T_cap < S || hidden < 1) return 0;
+  return oproj_plan(g, dtype, B, S, T_cap, hidden).total;
+}
+
+MLA_EXPORT int mla_decode_oproj(const mla_dims* d, int dtype, int B, int S, const void* q, const void* Lc,
+                                const void* Rc, int T_cap, const int32_t* T, const void* kv_b, const void* w_o,
+                                int hidden, float* y, void* workspace, size_t workspace_bytes, void* stream) {
+  mla::Geometry g;
+  int rc = check_common(d, dtype, B, S, &g);
+  if (rc) return rc;
+  if (T_cap < S) return fail(MLA_ERR_INVALID, "T_cap=%d < S=%d", T_cap, S);
+  if (!q || !Lc || !Rc || !T || !kv_b) return fail(MLA_ERR_INVALID, "null tensor pointer");
+  const int in_dim = g.H * g.Dv;
+  if (!workspace) return fail(MLA_ERR_INVALID, "null workspace (the attention output lives there)");
+  rc = check_oproj(B * S, in_dim, hidden, dtype, w_o, static_cast<const float*>(workspace), y);
+  if (rc) return rc;
+  const OprojPlan pl = oproj_plan(g, dtype, B, S, T_cap, hidden);
+  if (workspace_bytes < pl.total)
+    return fail(MLA_ERR_INVALID, "workspace of %zu bytes < %zu required", workspace_bytes, pl.total);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(MLA_ERR_INVALID, "workspace must be 256-byte aligned");
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  float* out = reinterpret_cast<float*>(ws + pl.out_off);
+  mla::DecodeArgs a{};
+  a.g = g;
+  a.B = B;
+  a.S = S;
+  a.T_cap = T_cap;
+  a.q = q;
+  a.Lc = Lc;
+  a.Rc = Rc;
+  a.T = T;
+  a.kv_b = kv_b;
+  a.out = out;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  mla::call_begin();
+  rc = run_decode(a, dtype, false, pl.dec ? ws : nullptr, pl.dec, stream, "mla_decode_oproj attention launch", false);
+  if (rc) {
+    mla::call_end(st);
+    return rc;
+  }
+  mla::OprojArgs o{B * S, in_dim, hidden, dtype, w_o, out, y, ws + pl.op_off};
+  cudaError_t e = mla::launch_oproj(o, true, a.flags, a.wait_limit_ns, st);
+  mla::call_end(st);
+  if (e != cudaSuccess) return cuda_fail(e, "mla_decode_oproj projection launch");
   return MLA_OK;
 }
 

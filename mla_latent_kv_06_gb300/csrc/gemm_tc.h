@@ -15,7 +15,8 @@ namespace mla {
 
 enum GemmOut {
   kGemmOutBf16 = 0,        // C (bf16)  = acc
-  kGemmOutF32Scaled = 1    // C (fp32)  = acc * scale[m * Z + z]
+  kGemmOutF32Scaled = 1,   // C (fp32)  = acc * scale[m * Z + z]
+  kGemmOutF32 = 2          // C (fp32)  = acc
 };
 
 struct GemmArgs {

@@ -102,6 +102,19 @@ struct TopkArgs {
 
 cudaError_t launch_topk_select(const TopkArgs& a, cudaStream_t st);
 
+// Output projection y[r, n] = sum_k W_O[n, k] x[r, k] (W_O [hidden, in_dim] in dtype, x and y fp32).
+struct OprojArgs {
+  int R, in_dim, hidden, dtype;
+  const void* w_o;
+  const float* x;
+  float* y;
+  void* x_bf16;  // [R, in_dim] scratch for the tensor-core path (R > 8, bf16 weights), else unused
+};
+// Rows per GEMV launch; more rows take the tensor-core GEMM (bf16 weights).
+constexpr int kOprojGemvRows = 8;
+size_t oproj_workspace_bytes(int R, int in_dim, int hidden, int dtype);
+cudaError_t launch_oproj(const OprojArgs& a, bool pdl, unsigned int* flags, long long wait_ns, cudaStream_t st);
+
 // RoPE frequencies base^(-2j/d) travel in the launch parameters: rope widths up to 2 * kMaxRopePairs.
 constexpr int kMaxRopePairs = 128;
 // The append kernels hold a row in registers: at most kMaxAppendPer values per thread of 128.
