@@ -142,8 +142,14 @@ def build_workload(name, device):
         cache = row * sum(T_list)  # every cached key read once per sequence
         info.update(cache_bytes=cache, alg_bytes=cache + w_uk + w_uv + q_bytes + out_bytes)
         clat = 2 * R * d.H * d.kv_lora
+        # S > 1: every key tile serves S query tokens, so the attention is bound by the tensor pipe
+        pairs = sum(S * t - S * (S - 1) // 2 for t in T_list)
+        attn_flops = 2 * d.H * (d.kv_lora + d.qk_rope + d.kv_lora) * pairs
+        if S > 1:
+            info["flops"] = attn_flops
         work = {"absorb": ("hbm", w_uk + q_bytes), "absorb_gemm": ("hbm", w_uk + q_bytes + qcat),
-                "plan_rope": ("hbm", q_bytes), "attention": ("hbm", cache + qcat),
+                "plan_rope": ("hbm", q_bytes),
+                "attention": ("tensor", attn_flops) if S > 1 else ("hbm", cache + qcat),
                 "combine": ("hbm", w_uv + out_bytes), "merge": ("hbm", clat),
                 "up_gemm": ("hbm", w_uv + clat + out_bytes)}
         e2e = None if "table" in x else dict(inputs=[x["q"], x["T"]], run=lambda q, T: mla.decode_absorbed(
