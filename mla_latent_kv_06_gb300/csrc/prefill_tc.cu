@@ -9,13 +9,16 @@
 //
 // Step 2 is a flash-attention forward on tcgen05.  CTA = (128 queries, head,
 // sequence).  Query rows live in the 128 TMEM lanes; two softmax threads share
-// a row (32 keys of each tile and 128 value columns each), so max, sum and
+// a row (64 keys of each tile and 128 value columns each), so max, sum and
 // rescale stay in registers but for one shared-memory exchange.  Per
-// 64-key tile j:
-//   S(j)  = Q K(j)^T       M=128, N=64,  K=256  (Q and K K-major)
-//   O    += P(j-1) V(j-1)  M=128, N=256, K=64   (P K-major, V MN-major)
-// with K and V double-buffered in shared memory (TMA; K released by the score
-// product, V by the value product), S and P double-buffered.
+// 128-key tile j:
+//   S(j)  = Q K(j)^T       M=128, N=128, K=256  (Q and K K-major)
+//   O    += P(j-1) V(j-1)  M=128, N=256, K=128  (P K-major, V MN-major)
+// A 128-key tile halves the score product's instructions and its re-reads of
+// the query block against 64-key tiles; shared memory then holds one K, one V
+// and one P buffer (K released by the score product, V by the value product,
+// P rewritten once the previous value product retired), S is double-buffered
+// in TMEM.
 #include <atomic>
 #include <cmath>
 
@@ -33,22 +36,22 @@ using namespace sm100;
 
 constexpr int kH = 64, kDn = 192, kDr = 64, kDq = 256, kDv = 256, kDkv = kDn + kDv;  // kDkv = 448
 constexpr int kQT = 128;                    // queries per CTA
-constexpr int kKT = 64;                     // keys per tile
-constexpr uint32_t kQAtom = kQT * 128;      // 16 KB: 128 rows x 64 bf16
-constexpr uint32_t kKAtom = kKT * 128;      // 8 KB:  64 rows x 64 bf16
-constexpr uint32_t kQBytes = 4 * kQAtom;    // 64 KB
-constexpr uint32_t kKBytes = 4 * kKAtom;    // 32 KB (192 k_nope + 64 k_rot dims)
-constexpr uint32_t kVBytes = 4 * kKAtom;    // 32 KB (256 value dims as 4 MN atoms)
-constexpr uint32_t kPBytes = kQT * 128;     // 16 KB: 128 queries x 64 keys bf16
+constexpr int kKT = 128;                    // keys per tile
+constexpr uint32_t kAtom = 128 * 128;       // 16 KB: 128 rows x 64 bf16 (one 128-byte swizzled atom)
+constexpr uint32_t kQBytes = 4 * kAtom;     // 64 KB: 256 query dims
+constexpr uint32_t kKBytes = 4 * kAtom;     // 64 KB: 192 k_nope + 64 k_rot dims of 128 keys
+constexpr uint32_t kVBytes = 4 * kAtom;     // 64 KB: 256 value dims of 128 keys (MN-major atoms)
+constexpr uint32_t kPBytes = 2 * kAtom;     // 32 KB: 128 queries x 128 keys bf16 (two K-major atoms)
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffKV = kQBytes;                        // 2 stages of K | V
-constexpr uint32_t kOffP = kOffKV + 2 * (kKBytes + kVBytes);
-constexpr uint32_t kPrefillSmem = kOffP + 2 * kPBytes + 1024;
+constexpr uint32_t kOffK = kQBytes;
+constexpr uint32_t kOffV = kOffK + kKBytes;
+constexpr uint32_t kOffP = kOffV + kVBytes;
+constexpr uint32_t kPrefillSmem = kOffP + kPBytes + 1024;
 constexpr int kSoftThreads = 256;  // eight softmax warps
 constexpr int kPThreads = 64 + kSoftThreads;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 0;    // two S buffers of 64 columns
-constexpr uint32_t kTmemO = 128;  // O: 256 columns
+constexpr uint32_t kTmemS = 0;    // two S buffers of 128 columns
+constexpr uint32_t kTmemO = 256;  // O: 256 columns
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kTau = 8.f;
 constexpr long long kDrainNs = 1000000000LL;
@@ -81,12 +84,15 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
   unsigned char* sQ = smem + kOffQ;
-  unsigned char* sKV = smem + kOffKV;
+  unsigned char* sK = smem + kOffK;
+  unsigned char* sV = smem + kOffV;
   unsigned char* sP = smem + kOffP;
-  // o_done[j & 1] completes its (j >> 1)-th phase when O += P(j) V(j) retires;
-  // the product for tile j + 2 needs P(j + 2), so parity waits never alias.
-  __shared__ uint64_t q_full, q_rope, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2], p_full[2],
-      o_done[2], mma_done;
+  // Single K, V and P buffers: a barrier completes once per tile (phase j for
+  // tile j); S is double-buffered (s_full/s_free[j & 1], phase j >> 1).  No
+  // wait can alias: the producer of phase j + 1 of any barrier depends on the
+  // waiter having passed phase j.
+  __shared__ uint64_t q_full, q_rope, k_full, k_empty, v_full, v_empty, s_full[2], s_free[2], p_full, o_done,
+      mma_done;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   // [half][row]: the halves' maxima, after the loop their row sums.  A thread
@@ -102,16 +108,16 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
   if (threadIdx.x == 0) {
     mbar_init(&q_full, 1);
     mbar_init(&q_rope, kSoftThreads);
+    mbar_init(&k_full, 1);
+    mbar_init(&k_empty, 1);
+    mbar_init(&v_full, 1);
+    mbar_init(&v_empty, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], 1);
-      mbar_init(&v_full[i], 1);
-      mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], kSoftThreads);
-      mbar_init(&p_full[i], kSoftThreads);
-      mbar_init(&o_done[i], 1);
     }
+    mbar_init(&p_full, kSoftThreads);
+    mbar_init(&o_done, 1);
     mbar_init(&mma_done, 1);
     abort_flag = 0;
     fence_mbar_init();
@@ -134,44 +140,38 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       bool ok = true;
-      mbar_arrive_expect_tx(&q_full, 3 * kQAtom);
-      for (int a = 0; a < 3; ++a) tma_load_3d(sQ + a * kQAtom, &p.mQ, 64 * a, h, b * p.S + s0, &q_full);
-      // K of tile j is released by its score product, V by its value product:
-      // the key half of the stream runs one tile ahead of the value half.
+      mbar_arrive_expect_tx(&q_full, 3 * kAtom);
+      for (int a = 0; a < 3; ++a) tma_load_3d(sQ + a * kAtom, &p.mQ, 64 * a, h, b * p.S + s0, &q_full);
+      // K(j) waits for the score product of tile j - 1, V(j) for the value
+      // product of tile j - 1: the key half of the stream runs one tile ahead.
       int last_k = -1, last_v = -1;
       auto load_k = [&](int j) -> bool {
-        const int st = j & 1;
-        if (!mbar_wait(&k_empty[st], ((j >> 1) & 1) ^ 1, abort, p.flags, p.wait_ns)) return false;
-        unsigned char* sK = sKV + st * (kKBytes + kVBytes);
+        if (j > 0 && !mbar_wait(&k_empty, (j - 1) & 1, abort, p.flags, p.wait_ns)) return false;
         const int y = b * p.Tk + j * kKT;
-        mbar_arrive_expect_tx(&k_full[st], kKBytes);
-        for (int a = 0; a < 3; ++a) tma_load_2d(sK + a * kKAtom, &p.mKV, h * kDkv + 64 * a, y, &k_full[st]);
-        tma_load_2d(sK + 3 * kKAtom, &p.mR, 0, y, &k_full[st]);
+        mbar_arrive_expect_tx(&k_full, kKBytes);
+        for (int a = 0; a < 3; ++a) tma_load_2d(sK + a * kAtom, &p.mKV, h * kDkv + 64 * a, y, &k_full);
+        tma_load_2d(sK + 3 * kAtom, &p.mR, 0, y, &k_full);
         last_k = j;
         return true;
       };
       auto load_v = [&](int j) -> bool {
-        const int st = j & 1;
-        if (!mbar_wait(&v_empty[st], ((j >> 1) & 1) ^ 1, abort, p.flags, p.wait_ns)) return false;
-        unsigned char* sV = sKV + st * (kKBytes + kVBytes) + kKBytes;
+        if (j > 0 && !mbar_wait(&v_empty, (j - 1) & 1, abort, p.flags, p.wait_ns)) return false;
         const int y = b * p.Tk + j * kKT;
-        mbar_arrive_expect_tx(&v_full[st], kVBytes);
-        for (int a = 0; a < 4; ++a) tma_load_2d(sV + a * kKAtom, &p.mKV, h * kDkv + kDn + 64 * a, y, &v_full[st]);
+        mbar_arrive_expect_tx(&v_full, kVBytes);
+        for (int a = 0; a < 4; ++a) tma_load_2d(sV + a * kAtom, &p.mKV, h * kDkv + kDn + 64 * a, y, &v_full);
         last_v = j;
         return true;
       };
       if (nkt > 0) ok = load_k(0);
       for (int j = 0; j < nkt && ok; ++j) {
-        if (j + 1 < nkt) ok = load_k(j + 1);
+        if (j + 1 < nkt) ok = load_k(j + 1);  // the score product S(j) retires before O(j - 1)
         if (ok) ok = load_v(j);
       }
       volatile int no_abort = 0;
       const long long dn = p.wait_ns > kDrainNs ? p.wait_ns : kDrainNs;
       mbar_wait(&q_full, 0, &no_abort, p.flags, dn);
-      for (int j = last_k - 1; j <= last_k; ++j)
-        if (j >= 0) mbar_wait(&k_full[j & 1], (j >> 1) & 1, &no_abort, p.flags, dn);
-      for (int j = last_v - 1; j <= last_v; ++j)
-        if (j >= 0) mbar_wait(&v_full[j & 1], (j >> 1) & 1, &no_abort, p.flags, dn);
+      if (last_k >= 0) mbar_wait(&k_full, last_k & 1, &no_abort, p.flags, dn);
+      if (last_v >= 0) mbar_wait(&v_full, last_v & 1, &no_abort, p.flags, dn);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -179,42 +179,39 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
     if (lane == 0) {
       const uint32_t idesc_s = idesc_bf16_f32(128, kKT, 0, 0);
       const uint32_t idesc_o = idesc_bf16_f32(128, kDv, 0, 1);
-      const uint32_t q0 = smem_u32(sQ), kv0 = smem_u32(sKV), p0 = smem_u32(sP);
+      const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), v0 = smem_u32(sV), p0 = smem_u32(sP);
       bool ok = mbar_wait(&q_full, 0, abort, p.flags, p.wait_ns) && mbar_wait(&q_rope, 0, abort, p.flags, p.wait_ns);
       bool issued = false;
       auto pv = [&](int j) -> bool {  // O += P(j) V(j)
-        if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1, abort, p.flags, p.wait_ns)) return false;
-        if (!mbar_wait(&v_full[j & 1], (j >> 1) & 1, abort, p.flags, p.wait_ns)) return false;
+        if (!mbar_wait(&p_full, j & 1, abort, p.flags, p.wait_ns)) return false;
+        if (!mbar_wait(&v_full, j & 1, abort, p.flags, p.wait_ns)) return false;
         tc_fence_after();
-        const uint32_t v0 = kv0 + (j & 1) * (kKBytes + kVBytes) + kKBytes;
-        const uint32_t pp = p0 + (j & 1) * kPBytes;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t da = smem_desc_sw128(pp + kk * 32, 16, 1024);
-          const uint64_t db = smem_desc_sw128(v0 + kk * 2048, kKAtom, 1024);
+        for (int kk = 0; kk < 8; ++kk) {  // 16 keys per step: P atom kk / 4, V rows 16 kk ..
+          const uint64_t da = smem_desc_sw128(p0 + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
+          const uint64_t db = smem_desc_sw128(v0 + kk * 2048, kAtom, 1024);
           mma_bf16(tmem + kTmemO, da, db, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&v_empty[j & 1]);
-        mma_commit(&o_done[j & 1]);
+        mma_commit(&v_empty);
+        mma_commit(&o_done);
         return true;
       };
       for (int j = 0; j < nkt && ok; ++j) {
         const int st = j & 1, n = j >> 1;
         ok = mbar_wait(&s_free[st], (n & 1) ^ 1, abort, p.flags, p.wait_ns) &&
-             mbar_wait(&k_full[st], n & 1, abort, p.flags, p.wait_ns);
+             mbar_wait(&k_full, j & 1, abort, p.flags, p.wait_ns);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t k0 = kv0 + st * (kKBytes + kVBytes);
 #pragma unroll
         for (int a = 0; a < 4; ++a)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t da = smem_desc_sw128(q0 + a * kQAtom + kk * 32, 16, 1024);
-            const uint64_t db = smem_desc_sw128(k0 + a * kKAtom + kk * 32, 16, 1024);
-            mma_bf16(tmem + kTmemS + 64 * st, da, db, idesc_s, (a | kk) != 0);
+            const uint64_t da = smem_desc_sw128(q0 + a * kAtom + kk * 32, 16, 1024);
+            const uint64_t db = smem_desc_sw128(k0 + a * kAtom + kk * 32, 16, 1024);
+            mma_bf16(tmem + kTmemS + kKT * st, da, db, idesc_s, (a | kk) != 0);
           }
         mma_commit(&s_full[st]);
-        mma_commit(&k_empty[st]);
+        mma_commit(&k_empty);
         issued = true;
         if (j > 0) ok = pv(j - 1);
       }
@@ -228,7 +225,7 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax warps 2..9
-    // Thread (row m, half) owns keys 32*half .. 32*half+31 of each tile of
+    // Thread (row m, half) owns keys 64*half .. 64*half+63 of each tile of
     // query row m and value columns 128*half .. 128*half+127; the two halves of
     // a row exchange their maxima through shared memory.
     const int wq = warp & 3;
@@ -266,7 +263,7 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
 #pragma unroll
         for (int i = 0; i < 8; ++i) lo[i] = hi[i] = 0u;
       }
-      unsigned char* row = sQ + 3 * kQAtom + m * 128;
+      unsigned char* row = sQ + 3 * kAtom + m * 128;
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int c_lo = 2 * half + cc, c_hi = 4 + 2 * half + cc;
@@ -289,16 +286,16 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
         break;
       }
       tc_fence_after();
-      float v[32];
-      tmem_ld32(tmem + t_lane + kTmemS + 64 * st + 32 * half, v);
+      float v[64];
+      tmem_ld64(tmem + t_lane + kTmemS + kKT * st + 64 * half, v);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&s_free[st]);
-      const int t0 = j * kKT + 32 * half;
-      const int nvalid = row_ok ? max(0, min(32, pos - t0 + 1)) : 0;  // keys t0..t0+nvalid-1 are visible
+      const int t0 = j * kKT + 64 * half;
+      const int nvalid = row_ok ? max(0, min(64, pos - t0 + 1)) : 0;  // keys t0..t0+nvalid-1 are visible
       float mx = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
+      for (int i = 0; i < 64; ++i)
         if (i < nvalid) mx = fmaxf(mx, v[i]);
       red_row[half][m] = mx;
       named_barrier(1, kSoftThreads);
@@ -309,10 +306,10 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
         alpha = exp2f(m_run - cand);
         m_run = cand;
       }
-      uint32_t pk[16];
+      uint32_t pk[32];
       float psum = 0.f;
 #pragma unroll
-      for (int i = 0; i < 32; i += 2) {
+      for (int i = 0; i < 64; i += 2) {
         const float e0 = i < nvalid ? exp2f(fmaf(v[i], c, -m_run)) : 0.f;
         const float e1 = i + 1 < nvalid ? exp2f(fmaf(v[i + 1], c, -m_run)) : 0.f;
         pk[i / 2] = pack2(e0, e1);
@@ -320,18 +317,13 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
         psum += f.x + f.y;
       }
       l = l * alpha + psum;
-      unsigned char* prow = sP + st * kPBytes + m * 128;
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
-        *reinterpret_cast<uint4*>(prow + (((4 * half + cc) ^ (m & 7)) << 4)) =
-            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-      // this thread's O columns rescaled (tcgen05.ld/st are warp-wide) once O += P(j-1)V(j-1) retired
+      // P(j) overwrites P(j - 1), and a rescale rewrites O: both wait until
+      // O += P(j - 1) V(j - 1) retired (tcgen05.ld/st are warp-wide).
       fail = false;
-      if (__any_sync(0xffffffffu, alpha != 1.f && j > 0)) {
-        fail = !__all_sync(0xffffffffu,
-                           mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort, p.flags, p.wait_ns));
-        if (!fail) {
-          tc_fence_after();
+      if (j > 0) fail = !__all_sync(0xffffffffu, mbar_wait(&o_done, (j - 1) & 1, abort, p.flags, p.wait_ns));
+      if (!fail) {
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f && j > 0)) {
 #pragma unroll 1
           for (int cb = 128 * half; cb < 128 * half + 128; cb += 64) {
             float w[64];
@@ -343,6 +335,12 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
           }
           tmem_wait_st();
         }
+        // this thread's 64 keys are one 128-byte row of P atom `half`
+        unsigned char* prow = sP + half * kAtom + m * 128;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          *reinterpret_cast<uint4*>(prow + ((cc ^ (m & 7)) << 4)) =
+              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
       }
       if (bar_red_or(2, kSoftThreads, fail)) {
         ok = false;
@@ -350,12 +348,12 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&p_full[st]);
+      mbar_arrive(&p_full);
     }
     // row sums: the two halves of a row
     red_row[half][m] = l;
     bool fail = !ok;
-    if (!fail && nkt > 0) fail = !mbar_wait(&o_done[(nkt - 1) & 1], ((nkt - 1) >> 1) & 1, abort, p.flags, p.wait_ns);
+    if (!fail && nkt > 0) fail = !mbar_wait(&o_done, (nkt - 1) & 1, abort, p.flags, p.wait_ns);
     if (!bar_red_or(2, kSoftThreads, fail) && nkt > 0) {
       tc_fence_after();
       float* orow = p.out + (((size_t)b * p.S + s) * kH + h) * kDv;
