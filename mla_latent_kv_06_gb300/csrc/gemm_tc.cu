@@ -1,9 +1,11 @@
 // gemm_tc.cu -- batched bf16 GEMM on tcgen05 tensor cores (see gemm_tc.h).
 //
-// One CTA computes a 128 x BN tile of C_z: warp 0 streams 64-wide K slabs of
-// A (3D TMA, 128-byte swizzle) and B through a ring of stages, warp 1 issues
-// tcgen05.mma (M=128, N=BN, K=16) into a TMEM accumulator, warps 2-5 (one
-// output row per thread) read the accumulator back and store C.
+// Persistent: one CTA per SM walks the 128 x BN tiles of C (n fastest).  Warp
+// 0 streams 64-wide K slabs of A (3D TMA, 128-byte swizzle) and B through a
+// ring of stages that runs on across tiles, warp 1 issues tcgen05.mma
+// (M=128, N=BN, K=16) into one of two TMEM accumulators, and warps 2-5 (one
+// output row per thread) read the other accumulator back and store C, so the
+// epilogue of a tile overlaps the products of the next.
 #include <atomic>
 
 #include "common.cuh"
@@ -42,32 +44,58 @@ struct GemmParams {
   long long wait_ns;
 };
 
+// OR of x over the 128 epilogue threads (named barrier 1).
+__device__ __forceinline__ bool epi_any(bool x) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)x)
+      : "memory");
+  return r != 0;
+}
+
 template <int BN, bool kBMN>
 __global__ void __launch_bounds__(kGThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
   using Cfg = GemmCfg<BN>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
-  __shared__ uint64_t full_bar[Cfg::kStages], empty_bar[Cfg::kStages], acc_full;
+  // The ring of K slabs runs on across the CTA's tiles; the accumulator is
+  // double-buffered in TMEM, so that the epilogue of one tile overlaps the
+  // products of the next.  acc_full/acc_empty[b] complete once per tile that
+  // uses buffer b.
+  __shared__ uint64_t full_bar[Cfg::kStages], empty_bar[Cfg::kStages], acc_full[2], acc_empty[2], mma_done;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * kGBM, z = blockIdx.z;
   const int nk = p.K / 64;
+  const int tn = (p.N + BN - 1) / BN, tm = (p.M + kGBM - 1) / kGBM;
+  const int ntiles = tn * tm * p.Z;
+  // tile t -> (z, m tile, n tile), n fastest
+  auto tile_of = [&](int t, int* n0, int* m0, int* z) {
+    *n0 = (t % tn) * BN;
+    *m0 = ((t / tn) % tm) * kGBM;
+    *z = t / (tn * tm);
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < Cfg::kStages; ++i) {
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], 1);
     }
-    mbar_init(&acc_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 128);
+    }
+    mbar_init(&mma_done, 1);
     abort_flag = 0;
     fence_mbar_init();
     prefetch_tensormap(&p.mA);
     prefetch_tensormap(&p.mB);
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_base, BN);
+    tmem_alloc(&tmem_base, 2 * BN);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -80,31 +108,35 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_kernel(const __grid_constan
 
   if (warp == 0) {
     if (lane == 0) {
-      int last = -1;
+      int g = 0, last = -1;  // slab counter over all tiles of this CTA
       bool ok = true;
-      const int brow = (int)(p.b_row0 + (long long)z * p.b_rows_per_z);
-      for (int kb = 0; kb < nk && ok; ++kb) {
-        const int st = kb % Cfg::kStages, u = kb / Cfg::kStages;
-        ok = mbar_wait(&empty_bar[st], (u & 1) ^ 1, abort, p.flags, p.wait_ns);
-        if (!ok) break;
-        unsigned char* sA = smem + st * Cfg::kStage;
-        unsigned char* sB = sA + Cfg::kA;
-        mbar_arrive_expect_tx(&full_bar[st], Cfg::kStage);
-        tma_load_3d(sA, &p.mA, kb * 64, z, m0, &full_bar[st]);
-        if (!kBMN) {
-          tma_load_2d(sB, &p.mB, (int)p.b_col0 + kb * 64, brow + n0, &full_bar[st]);
-        } else {
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        int n0, m0, z;
+        tile_of(t, &n0, &m0, &z);
+        const int brow = (int)(p.b_row0 + (long long)z * p.b_rows_per_z);
+        for (int kb = 0; kb < nk && ok; ++kb, ++g) {
+          const int st = g % Cfg::kStages, u = g / Cfg::kStages;
+          ok = mbar_wait(&empty_bar[st], (u & 1) ^ 1, abort, p.flags, p.wait_ns);
+          if (!ok) break;
+          unsigned char* sA = smem + st * Cfg::kStage;
+          unsigned char* sB = sA + Cfg::kA;
+          mbar_arrive_expect_tx(&full_bar[st], Cfg::kStage);
+          tma_load_3d(sA, &p.mA, kb * 64, z, m0, &full_bar[st]);
+          if (!kBMN) {
+            tma_load_2d(sB, &p.mB, (int)p.b_col0 + kb * 64, brow + n0, &full_bar[st]);
+          } else {
 #pragma unroll
-          for (int j = 0; j < BN / 64; ++j)
-            tma_load_2d(sB + j * 8192, &p.mB, (int)p.b_col0 + n0 + 64 * j, brow + kb * 64, &full_bar[st]);
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(sB + j * 8192, &p.mB, (int)p.b_col0 + n0 + 64 * j, brow + kb * 64, &full_bar[st]);
+          }
+          last = g;
         }
-        last = kb;
       }
       if (last >= 0) {  // never leave with copies in flight
         volatile int no_abort = 0;
         const long long dn = p.wait_ns > kGDrainNs ? p.wait_ns : kGDrainNs;
-        for (int kb = last - Cfg::kStages + 1; kb <= last; ++kb)
-          if (kb >= 0) mbar_wait(&full_bar[kb % Cfg::kStages], (kb / Cfg::kStages) & 1, &no_abort, p.flags, dn);
+        for (int q = last - Cfg::kStages + 1; q <= last; ++q)
+          if (q >= 0) mbar_wait(&full_bar[q % Cfg::kStages], (q / Cfg::kStages) & 1, &no_abort, p.flags, dn);
       }
     }
     __syncwarp();
@@ -112,42 +144,57 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_kernel(const __grid_constan
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(kGBM, BN, 0, kBMN ? 1 : 0);
       bool ok = true, issued = false;
-      for (int kb = 0; kb < nk && ok; ++kb) {
-        const int st = kb % Cfg::kStages, u = kb / Cfg::kStages;
-        ok = mbar_wait(&full_bar[st], u & 1, abort, p.flags, p.wait_ns);
+      int g = 0, i = 0;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++i) {
+        const int buf = i & 1;
+        ok = mbar_wait(&acc_empty[buf], ((i >> 1) & 1) ^ 1, abort, p.flags, p.wait_ns);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t a0 = smem_u32(smem + st * Cfg::kStage), b0 = a0 + Cfg::kA;
+        const uint32_t acc = tmem + BN * buf;
+        for (int kb = 0; kb < nk && ok; ++kb, ++g) {
+          const int st = g % Cfg::kStages, u = g / Cfg::kStages;
+          ok = mbar_wait(&full_bar[st], u & 1, abort, p.flags, p.wait_ns);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + st * Cfg::kStage), b0 = a0 + Cfg::kA;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t da = smem_desc_sw128(a0 + kk * 32, 16, 1024);
-          const uint64_t db = kBMN ? smem_desc_sw128(b0 + kk * 2048, 8192, 1024) : smem_desc_sw128(b0 + kk * 32, 16, 1024);
-          mma_bf16(tmem, da, db, idesc, (kb | kk) != 0);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t da = smem_desc_sw128(a0 + kk * 32, 16, 1024);
+            const uint64_t db = kBMN ? smem_desc_sw128(b0 + kk * 2048, 8192, 1024) : smem_desc_sw128(b0 + kk * 32, 16, 1024);
+            mma_bf16(acc, da, db, idesc, (kb | kk) != 0);
+          }
+          mma_commit(&empty_bar[st]);
+          issued = true;
         }
-        mma_commit(&empty_bar[st]);
-        issued = true;
+        if (ok) mma_commit(&acc_full[buf]);
       }
-      if (issued) mma_commit(&acc_full);
-      if (!ok && issued) {  // drain before TMEM is released
+      if (issued) {  // every product retired before TMEM is released
+        mma_commit(&mma_done);
         volatile int no_abort = 0;
-        mbar_wait(&acc_full, 0, &no_abort, p.flags, p.wait_ns > kGDrainNs ? p.wait_ns : kGDrainNs);
+        mbar_wait(&mma_done, 0, &no_abort, p.flags, p.wait_ns > kGDrainNs ? p.wait_ns : kGDrainNs);
       }
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
     const int wq = warp & 3;
-    const int m = m0 + 32 * wq + lane;
     const uint32_t t_lane = (uint32_t)(32 * wq) << 16;
-    const bool ok = mbar_wait(&acc_full, 0, abort, p.flags, p.wait_ns);
-    if (ok) {
+    int i = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+      const int buf = i & 1;
+      int n0, m0, z;
+      tile_of(t, &n0, &m0, &z);
+      const int m = m0 + 32 * wq + lane;
+      // a failed wait is decided jointly by the 128 epilogue threads
+      const bool fail = !mbar_wait(&acc_full[buf], (i >> 1) & 1, abort, p.flags, p.wait_ns);
+      if (epi_any(fail)) break;
       tc_fence_after();
       float scale = 1.f;
       if (p.out_kind == kGemmOutF32Scaled && m < p.M) scale = p.scale[(size_t)m * p.Z + z];
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 64) {
         float v[64];
-        tmem_ld64(tmem + t_lane + c0, v);
+        tmem_ld64(tmem + t_lane + BN * buf + c0, v);
         tmem_wait_ld();
         const int n = n0 + c0;
         if (m < p.M && n < p.N) {
@@ -170,13 +217,15 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_kernel(const __grid_constan
           }
         }
       }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[buf]);
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, BN);
+    tmem_dealloc(tmem, 2 * BN);
   }
 }
 
@@ -194,7 +243,10 @@ cudaError_t launch_one(const GemmParams& gp, bool pdl, cudaStream_t st) {
     done.fetch_or(bit);
   }
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3((gp.N + BN - 1) / BN, (gp.M + kGBM - 1) / kGBM, gp.Z);
+  const long long tiles = (long long)((gp.N + BN - 1) / BN) * ((gp.M + kGBM - 1) / kGBM) * gp.Z;
+  int sms = 148;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cfg.gridDim = dim3((unsigned)(tiles < sms ? tiles : sms));  // persistent: one CTA per SM walks the tiles
   cfg.blockDim = dim3(kGThreads);
   cfg.dynamicSmemBytes = Cfg::kSmem;
   cfg.stream = st;
