@@ -22,6 +22,8 @@
 #include <atomic>
 #include <cmath>
 
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "gemm_tc.h"
 #include "internal.h"
@@ -306,13 +308,18 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
         alpha = exp2f(m_run - cand);
         m_run = cand;
       }
+      // Probabilities two at a time through the half-precision exp2 (one
+      // MUFU operation per pair, the exponent unit being this loop's limit):
+      // the arguments are <= 0 and P is rounded to bf16 for the value
+      // product anyway; masked keys get -inf, whose exp2 is exactly 0.
       uint32_t pk[32];
       float psum = 0.f;
 #pragma unroll
       for (int i = 0; i < 64; i += 2) {
-        const float e0 = i < nvalid ? exp2f(fmaf(v[i], c, -m_run)) : 0.f;
-        const float e1 = i + 1 < nvalid ? exp2f(fmaf(v[i + 1], c, -m_run)) : 0.f;
-        pk[i / 2] = pack2(e0, e1);
+        const float x0 = i < nvalid ? fmaf(v[i], c, -m_run) : -INFINITY;
+        const float x1 = i + 1 < nvalid ? fmaf(v[i + 1], c, -m_run) : -INFINITY;
+        const float2 e = __half22float2(h2exp2(__floats2half2_rn(x0, x1)));
+        pk[i / 2] = pack2(e.x, e.y);
         const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&pk[i / 2]));
         psum += f.x + f.y;
       }
