@@ -403,6 +403,26 @@ def measure(name, dev, stream, flush, K, W, pk, pk_kind, want_e2e):
     return res
 
 
+# ------------------------------------------------------------------ ranks
+def slowest_rank_ms(total_ms, device):
+    """Max over the ranks of this job of a timed region (ms), each rank's
+    region bracketed by a barrier; the identity for a single process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return total_ms
+    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
+
+
+def job_throughput(tokens_per_step, steps, world, total_ms):
+    """Whole-job rate: every replica processes tokens_per_step per step (weak
+    scaling); the job's time is the slowest rank's."""
+    return world * tokens_per_step * steps / (total_ms / 1e3)
+
+
 # ------------------------------------------------------------------ CPU oracle
 def oracle_sample(name, budget_s=12.0):
     """Time the fp64 oracle on the host cores on a bounded sample of the workload."""
@@ -507,15 +527,10 @@ def main():
         res = measure(args.workload, dev, stream, flush, K, W, pk, pk_kind, want_e2e=True)
         t_wall = time.perf_counter() - t_wall
         clk = clocks.stop()
-        total_ms = sum(res["ms"])
-        if world > 1:
-            t = torch.tensor([total_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            total_ms = float(t.item())
-            dist.barrier()
+        total_ms = slowest_rank_ms(sum(res["ms"]), dev)
         info = res["info"]
         ms_per_step = total_ms / K
-        value = world * info["tokens"] * K / (total_ms / 1e3)
+        value = job_throughput(info["tokens"], K, world, total_ms)
         step_s = ms_per_step / 1e3
         if rank == 0:
             T_list = info["T_list"]
