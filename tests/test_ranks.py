@@ -29,7 +29,7 @@ def _rank(rank, world, port, out):
 
 @pytest.mark.parametrize("world", [2])
 def test_slowest_rank_and_job_rate(world):
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_rank, args=(world, _free_port(), out), nprocs=world, join=True)
     slow = 10.0 + 5.0 * (world - 1)
     for r in range(world):
