@@ -1209,40 +1209,58 @@ struct GatherParams {
   PageTable pages;
 };
 
+// Warp = 4 selected keys.  All index loads, then all row loads of the warp
+// are issued before the first store, so a warp waits for two memory round
+// trips instead of one per 16-byte chunk.
 __global__ void __launch_bounds__(256) gather_kernel(const GatherParams p) {
+  constexpr int kKeys = 4, kChunks = (kDc / 8 + 31) / 32;  // 72 chunks of 16 B per row: 3 per lane
   const int r = blockIdx.y, b = r / p.S, s = r % p.S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Tb = p.T[b];
   const int n = p.nsel[r];
   const bool row_ok = Tb >= p.S && Tb <= p.T_cap && n >= 1 && n <= p.topk;
   const int pos = Tb - p.S + s;
-  for (int kk = 0; kk < 4; ++kk) {
-    const int j = blockIdx.x * 32 + warp * 4 + kk;
-    int idx = -1;
-    if (row_ok && j < n) {
-      idx = p.sel[(size_t)r * p.topk + j];
-      if (idx < 0 || idx > pos) {
-        if (lane == 0) raise_flag(p.flags, MLA_DEV_BAD_INDEX);
-        idx = -1;
-      }
+  const int j0 = blockIdx.x * 32 + warp * kKeys;
+  int idx[kKeys];
+#pragma unroll
+  for (int kk = 0; kk < kKeys; ++kk) idx[kk] = (row_ok && j0 + kk < n) ? __ldg(p.sel + (size_t)r * p.topk + j0 + kk) : -1;
+  long long row[kKeys];
+#pragma unroll
+  for (int kk = 0; kk < kKeys; ++kk) {
+    row[kk] = 0;
+    if (row_ok && j0 + kk < n && (idx[kk] < 0 || idx[kk] > pos)) {
+      if (lane == 0) raise_flag(p.flags, MLA_DEV_BAD_INDEX);
+      idx[kk] = -1;
     }
-    long long row = 0;
-    if (idx >= 0) {
+    if (idx[kk] >= 0) {
       bool bad_page = false;
-      row = cache_row(p.pages, b, p.T_cap, idx, &bad_page);
+      row[kk] = cache_row(p.pages, b, p.T_cap, idx[kk], &bad_page);
       if (bad_page) {
         if (lane == 0) raise_flag(p.flags, MLA_DEV_BAD_INDEX);
-        idx = -1;
-        row = 0;
+        idx[kk] = -1;
+        row[kk] = 0;
       }
     }
-    uint4* dst = reinterpret_cast<uint4*>(p.stage + ((size_t)r * p.Kpad + j) * kDc);
-    const uint4* lsrc = reinterpret_cast<const uint4*>(p.Lc + (size_t)row * kDl);
-    const uint4* rsrc = reinterpret_cast<const uint4*>(p.Rc + (size_t)row * kDr);
-    for (int c = lane; c < kDc / 8; c += 32) {
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (idx >= 0) v = c < kDl / 8 ? __ldg(lsrc + c) : __ldg(rsrc + (c - kDl / 8));
-      dst[c] = v;
+  }
+  uint4 v[kKeys][kChunks];
+#pragma unroll
+  for (int kk = 0; kk < kKeys; ++kk) {
+    const uint4* lsrc = reinterpret_cast<const uint4*>(p.Lc + (size_t)row[kk] * kDl);
+    const uint4* rsrc = reinterpret_cast<const uint4*>(p.Rc + (size_t)row[kk] * kDr);
+#pragma unroll
+    for (int u = 0; u < kChunks; ++u) {
+      const int c = lane + 32 * u;
+      v[kk][u] = make_uint4(0, 0, 0, 0);
+      if (idx[kk] >= 0 && c < kDc / 8) v[kk][u] = c < kDl / 8 ? __ldg(lsrc + c) : __ldg(rsrc + (c - kDl / 8));
+    }
+  }
+#pragma unroll
+  for (int kk = 0; kk < kKeys; ++kk) {
+    uint4* dst = reinterpret_cast<uint4*>(p.stage + ((size_t)r * p.Kpad + j0 + kk) * kDc);
+#pragma unroll
+    for (int u = 0; u < kChunks; ++u) {
+      const int c = lane + 32 * u;
+      if (c < kDc / 8) dst[c] = v[kk][u];
     }
   }
 }
