@@ -996,42 +996,47 @@ __global__ void __launch_bounds__(kCmbThreads) combine_kernel(const CombineParam
       for (int i = lane; i < cnt; i += 32) pm[warp * kMaxPieces + i] /= L;
     }
     __syncthreads();
-    // (b) clat[w][l] = sum_i weight_i * O_i[h][l]: warp k takes splits k, k+8, ...
-    //     (all of their loads in flight together), lane covers latents
-    //     4*lane + 128*q; the eight warp sums meet in shared memory.
-    for (int w = 0; w < nr; ++w) {
-      const int cnt = pcnt[w];
-      float4 acc[4];
+    // (b) clat[w][l] = sum_i weight_i * O_i[h][l] for every row at once: the
+    //     8 warps are dealt to the rows (wpr each); warp k takes every wpr-th
+    //     split of its row (all of their loads in flight together), lane
+    //     covers latents 4*lane + 128*q; the warp sums meet in shared memory.
+    {
+      const int wpr = (kCmbThreads / 32) / nr;  // nr <= kCmbRows = 8
+      const int w = warp / wpr, sk = warp % wpr;
+      if (w < nr) {
+        const int cnt = pcnt[w];
+        float4 acc[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-      for (int i = warp; i < cnt; i += kCmbThreads / 32) {
-        const float wg = pm[w * kMaxPieces + i];
-        const float4* src =
-            reinterpret_cast<const float4*>(p.o_part + ((size_t)pslot[w * kMaxPieces + i] * kH + h) * kDl);
+        for (int i = sk; i < cnt; i += wpr) {
+          const float wg = pm[w * kMaxPieces + i];
+          const float4* src =
+              reinterpret_cast<const float4*>(p.o_part + ((size_t)pslot[w * kMaxPieces + i] * kH + h) * kDl);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 o = src[lane + 32 * q];
-          acc[q].x = fmaf(wg, o.x, acc[q].x);
-          acc[q].y = fmaf(wg, o.y, acc[q].y);
-          acc[q].z = fmaf(wg, o.z, acc[q].z);
-          acc[q].w = fmaf(wg, o.w, acc[q].w);
+          for (int q = 0; q < 4; ++q) {
+            const float4 o = src[lane + 32 * q];
+            acc[q].x = fmaf(wg, o.x, acc[q].x);
+            acc[q].y = fmaf(wg, o.y, acc[q].y);
+            acc[q].z = fmaf(wg, o.z, acc[q].z);
+            acc[q].w = fmaf(wg, o.w, acc[q].w);
+          }
         }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) red[warp * 128 + lane + 32 * q] = acc[q];
       }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) red[warp * 128 + lane + 32 * q] = acc[q];
       __syncthreads();
-      if (tid < 128) {
-        float4 t = red[tid];
-#pragma unroll
-        for (int k = 1; k < kCmbThreads / 32; ++k) {
-          const float4 u = red[k * 128 + tid];
+      for (int e = tid; e < nr * 128; e += kCmbThreads) {
+        const int rw = e >> 7, idx = e & 127;
+        float4 t = red[(rw * wpr) * 128 + idx];
+        for (int k = 1; k < wpr; ++k) {
+          const float4 u = red[(rw * wpr + k) * 128 + idx];
           t.x += u.x;
           t.y += u.y;
           t.z += u.z;
           t.w += u.w;
         }
-        *reinterpret_cast<float4*>(clat + w * kCPitch + 4 * tid) = t;
+        *reinterpret_cast<float4*>(clat + rw * kCPitch + 4 * idx) = t;
       }
       __syncthreads();
     }
