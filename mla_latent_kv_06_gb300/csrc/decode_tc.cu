@@ -68,6 +68,8 @@ struct AttnParams {
   int B, S, T_cap, G, topk;
   int kv_rows;    // rows of the key source per tile-list row: T_cap (dense) or Kpad (sparse)
   int read_once;  // every key tile is loaded by exactly one CTA: mark its lines evict-first in L2
+  int qsplit;     // CTAs per piece (1, 2 or 4): each repeats the score product and owns 4/qsplit
+                  // of the four 128-row blocks of O^T (the value product and its partial)
   float c;        // softmax scale * log2(e)
   float* o_part;
   float* ml_part;
@@ -266,8 +268,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.S;
-  const int g = kSparse ? (int)blockIdx.x : (int)blockIdx.x / S;
-  const int s = kSparse ? 0 : (int)blockIdx.x % S;
+  // blockIdx.x = piece row * qsplit + latent part; the part owns O^T blocks [mb0, mb1)
+  const int part = (int)blockIdx.x % p.qsplit, brow = (int)blockIdx.x / p.qsplit;
+  const int g = kSparse ? brow : brow / S;
+  const int s = kSparse ? 0 : brow % S;
+  const int mb0 = part * (4 / p.qsplit), mb1 = mb0 + 4 / p.qsplit;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kSlots; ++i) {
@@ -441,7 +446,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       if (!ok) break;
       tc_fence_after();
       if (lane == 0) {
-        for (int m = 0; m < 4; ++m) {
+        // latent atoms of the blocks another part owns: free once the score product retired
+        for (int m = 0; m < 4; ++m)
+          if (m < mb0 || m >= mb1) {
+            mma_commit(&empty_bar[2 * m]);
+            mma_commit(&empty_bar[2 * m + 1]);
+          }
+        for (int m = mb0; m < mb1; ++m) {
           for (int kk = 0; kk < ksteps; ++kk) {
             const uint64_t da = smem_desc_sw128(kv0 + (2 * m) * kSlotBytes + kk * 2048, kSlotBytes, 1024);
             const uint64_t db = smem_desc_sw128(kv0 + 8 * kSlotBytes + kk * 2048, kSlotBytes, 1024);
@@ -488,7 +499,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     auto epilogue = [&](int j) -> bool {
       float* op = p.o_part + (size_t)slot * kH * kDl;
 #pragma unroll 1
-      for (int m = 0; m < 4; ++m) {
+      for (int m = mb0; m < mb1; ++m) {
         const bool fail = !mbar_wait(&o_blk[m], j & 1, abort, p.flags, p.wait_ns);
         if (bar_red_or(1, kSoftThreads, fail)) return false;
         tc_fence_after();
@@ -502,13 +513,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       transpose_reduce32<false>(lp, lane);
       red_sum[qd][col0 + lane] = lp[0];
       const bool bad = bar_red_or(1, kSoftThreads, bad_idx);
-      if (tsm < kH) {
+      if (tsm < kH && part == 0) {  // every part holds the same m and l
         const float l = red_sum[0][tsm] + red_sum[1][tsm] + red_sum[2][tsm] + red_sum[3][tsm];
         float* ml = p.ml_part + ((size_t)slot * kH + tsm) * 2;
         ml[0] = m_sh[tsm];
         ml[1] = bad ? __int_as_float(0x7fc00000) : l;
       }
-      if (bad && tsm == 0) raise_flag(p.flags, MLA_DEV_BAD_INDEX);
+      if (bad && tsm == 0 && part == 0) raise_flag(p.flags, MLA_DEV_BAD_INDEX);
       return true;
     };
 
@@ -631,7 +642,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         tc_fence_after();
         if (rescale) {
 #pragma unroll 1
-          for (int m = 0; m < 4; ++m) {
+          for (int m = mb0; m < mb1; ++m) {
             float w[32];
             tmem_ld32(tmem + t_lane + kTmemO + 64 * m + col0, w);
             tmem_wait_ld();
@@ -1476,7 +1487,13 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   tp.T_cap = a.T_cap;
   tp.G = pl.G;
   tp.topk = a.topk;
-  tp.read_once = (sparse || S == 1) ? 1 : 0;
+  // Few pieces leave SMs idle: then 2 or 4 CTAs share a piece, each repeating
+  // the score product (the tile comes from L2 after the first) and taking its
+  // share of the value product and of the partial's stores.
+  const int pieces = sparse ? pl.G : pl.G * S;
+  const int sms = sm_count();
+  tp.qsplit = pieces * 4 <= sms ? 4 : pieces * 2 <= sms ? 2 : 1;
+  tp.read_once = ((sparse || S == 1) && tp.qsplit == 1) ? 1 : 0;
   tp.c = g.scale * kLog2e;
   tp.o_part = o_part;
   tp.ml_part = ml_part;
@@ -1486,7 +1503,7 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   auto kern = sparse ? attn_kernel<true> : attn_kernel<false>;
   e = set_smem_once(kern, (int)kAttnDynSmem, &g_attn_attr[sparse ? 1 : 0]);
   if (e != cudaSuccess) return e;
-  const int nblk = sparse ? pl.G : pl.G * S;
+  const int nblk = pieces * tp.qsplit;
   kernel_mark(st, "attention");
   e = launch_pdl(kern, dim3(nblk), dim3(kAttnThreads), kAttnDynSmem, st, tp);
   if (e != cudaSuccess) return e;
