@@ -42,8 +42,17 @@ Parity status of each function (what pins it, see tests/test_oracle_pins.py):
 * page_row, unpage      - hand-worked block table; identity table equals the
                           contiguous layout.
 * o_proj                - hand-worked 2x3 product; one-hot rows pick columns.
+* e4m3_decode,          - textbook values of the format (1.0, 448, 2^-9, 2^-6,
+  e4m3_encode             NaN codes); all 256 codes against torch's float8_e4m3fn;
+                          ties-to-even and saturation by hand; encode(decode(c)) = c.
+* dequant_latent,       - composed of the pinned e4m3 functions and cache_append;
+  cache_append_fp8        codes within half a quantum of the normalised row.
 """
 from .mla import (  # noqa: F401
+    e4m3_decode,
+    e4m3_encode,
+    dequant_latent,
+    cache_append_fp8,
     o_proj,
     page_row,
     unpage,

@@ -345,3 +345,50 @@ def o_proj(x, w_o):
     attention paths ([MLA-KV] §2.3), x [R, in_dim] (a decode output flattened
     per row), w_o [hidden, in_dim]."""
     return _f64(x) @ _f64(w_o).T
+
+
+# --------------------------------------------------------------- FP8 latent cache
+# The pages fix no cache quantisation (FP8 appears among the weight formats
+# only); this is the FP8 cache format's own definition.  The latent part of a
+# row is stored as kv_lora E4M3 codes with one dequantisation scale for the
+# whole cache, Lc[t] = lat_scale * e4m3(code[t]); the rotated key Rc stays
+# 16-bit.  E4M3 here is the OCP 8-bit format without infinities: 1 sign bit,
+# 4 exponent bits with bias 7, 3 mantissa bits; exponent field 0 holds the
+# subnormals M * 2^-9; S.1111.111 is NaN; the largest finite value is 448.
+def e4m3_decode(codes):
+    """uint8 codes -> float64 values (NaN for the two NaN codes)."""
+    c = np.asarray(codes, dtype=np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    E = (c >> 3) & 0xF
+    M = (c & 0x7).astype(np.float64)
+    mag = np.where(E == 0, M * 2.0 ** -9, (1.0 + M / 8.0) * 2.0 ** (E - 7.0))
+    mag = np.where((E == 15) & (M == 7), np.nan, mag)
+    return sign * mag
+
+
+def e4m3_encode(x):
+    """float -> uint8 code of the nearest E4M3 value, ties to the even code,
+    magnitudes past 448 saturated to 448, NaN to 0x7F.  The nearest value is
+    found among all 127 non-negative finite values, as the definition reads."""
+    x = _f64(x)
+    grid = e4m3_decode(np.arange(127))             # 0x00 .. 0x7E, increasing
+    a = np.minimum(np.abs(x), 448.0)
+    hi = np.clip(np.searchsorted(grid, a, side="left"), 0, 126)
+    lo = np.maximum(hi - 1, 0)
+    dlo, dhi = a - grid[lo], grid[hi] - a
+    pick = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(lo % 2 == 0, lo, hi)))
+    code = pick.astype(np.int64) | np.where(np.signbit(x), 0x80, 0)
+    return np.where(np.isnan(x), 0x7F, code).astype(np.uint8)
+
+
+def dequant_latent(codes, lat_scale: float):
+    """Latent rows of an FP8 cache: lat_scale * e4m3(code)."""
+    return float(lat_scale) * e4m3_decode(codes)
+
+
+def cache_append_fp8(comp, kv_a_ln, eps: float, T, kv_lora: int, lat_scale: float, base: float = 10000.0):
+    """cache_append into the FP8 format: the RMSNorm output divided by
+    lat_scale is rounded to E4M3 codes; Rc as in cache_append.
+    Returns (codes [B,S,kv_lora] uint8, rc [B,S,qk_rope], pos [B,S])."""
+    lc, rc, pos = cache_append(comp, kv_a_ln, eps, T, kv_lora, base)
+    return e4m3_encode(lc / float(lat_scale)), rc, pos

@@ -196,6 +196,33 @@ def _key_append_head_rope(k_idx, ln_w, ln_b, eps, T, rope_dim, base=10000.0):
     return k, pos
 
 
+def _e4m3_decode(bias=7, subnormal_as_normal=False):
+    def decode(codes):
+        c = np.asarray(codes, dtype=np.int64)
+        sign = np.where(c & 0x80, -1.0, 1.0)
+        E, M = (c >> 3) & 0xF, (c & 0x7).astype(np.float64)
+        normal = (1.0 + M / 8.0) * 2.0 ** (E - float(bias))
+        mag = normal if subnormal_as_normal else np.where(E == 0, M * 2.0 ** (1 - bias - 3), normal)
+        return sign * np.where((E == 15) & (M == 7), np.nan, mag)
+    return decode
+
+
+def _e4m3_encode(ties="even", saturate=True):
+    def encode(x):
+        x = _f64(x)
+        grid = om.e4m3_decode(np.arange(127))
+        a = np.abs(x) if not saturate else np.minimum(np.abs(x), 448.0)
+        hi = np.clip(np.searchsorted(grid, a, side="left"), 0, 126)
+        lo = np.maximum(hi - 1, 0)
+        dlo, dhi = a - grid[lo], grid[hi] - a
+        tie = hi if ties == "up" else lo
+        pick = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, tie))
+        code = pick.astype(np.int64) | np.where(np.signbit(x), 0x80, 0)
+        code = np.where(a > 448.0, 0x7F, code)
+        return np.where(np.isnan(x), 0x7F, code).astype(np.uint8)
+    return encode
+
+
 MUTANTS = {
     "rope_negative_angle": {"rope_interleave": _rope("even_odd", "halves", 2.0, -1.0)},
     "rope_half_split_pairs": {"rope_interleave": _rope("halves", "halves", 2.0, 1.0)},
@@ -229,6 +256,11 @@ MUTANTS = {
     "page_row_div_mod_swapped": {"page_row": _page_row_swapped},
     "page_row_ignores_table": {"page_row": _page_row_unmapped},
     "o_proj_rows_reversed": {"o_proj": _o_proj_untransposed_rows},
+    "e4m3_bias_8": {"e4m3_decode": _e4m3_decode(bias=8)},
+    "e4m3_subnormals_as_normals": {"e4m3_decode": _e4m3_decode(subnormal_as_normal=True)},
+    "e4m3_ties_away_from_zero": {"e4m3_encode": _e4m3_encode(ties="up")},
+    "e4m3_ties_towards_zero": {"e4m3_encode": _e4m3_encode(ties="down")},
+    "e4m3_no_saturation": {"e4m3_encode": _e4m3_encode(saturate=False)},
 }
 
 

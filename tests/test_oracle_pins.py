@@ -469,3 +469,70 @@ def test_o_proj_hand_values_and_one_hot():
         e = np.zeros((1, 7))
         e[0, k] = 1.0
         assert np.array_equal(oracle.o_proj(e, r)[0], r[:, k])
+
+
+# ------------------------------------------------------------- FP8 latent cache
+def test_e4m3_textbook_values():
+    """Values fixed by the format: bias 7, three mantissa bits, subnormals
+    M * 2^-9, no infinities, S.1111.111 is NaN."""
+    table = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x30: 0.5, 0x38: 1.0,
+             0x39: 1.125, 0x3F: 1.875, 0x40: 2.0, 0x70: 128.0, 0x78: 256.0, 0x7E: 448.0, 0xB8: -1.0, 0xFE: -448.0}
+    for code, val in table.items():
+        assert oracle.e4m3_decode(code) == val, hex(code)
+    assert np.isnan(oracle.e4m3_decode(0x7F)) and np.isnan(oracle.e4m3_decode(0xFF))
+    assert np.signbit(oracle.e4m3_decode(0x80)) and oracle.e4m3_decode(0x80) == 0.0
+    pos = oracle.e4m3_decode(np.arange(127))
+    assert np.all(np.diff(pos) > 0)                                    # monotone in the code
+    np.testing.assert_array_equal(oracle.e4m3_decode(np.arange(128, 255)), -pos)
+
+
+def test_e4m3_matches_torch_float8():
+    """All 256 codes, and a spread of values inside the finite range, against
+    torch's float8_e4m3fn (a library routine of the same format)."""
+    torch = pytest.importorskip("torch")
+    codes = np.arange(256)
+    ref = torch.tensor(codes, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    got = oracle.e4m3_decode(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(got[~np.isnan(got)], ref[~np.isnan(ref)])
+    r = _rng(11)
+    x = np.clip(r.standard_normal(50000) * np.exp(r.uniform(-12, 7, 50000)), -448, 448)
+    x = np.concatenate([x, oracle.e4m3_decode(np.arange(126)) * 1.0000001, [0.0, -0.0, 448.0]])
+    ref = torch.tensor(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(oracle.e4m3_encode(x), ref)
+
+
+def test_e4m3_rounding_by_hand():
+    """Halfway cases go to the even code; past 448 saturates; NaN stays NaN."""
+    cases = {1.0625: 0x38,        # halfway 1.0 (0x38) / 1.125 (0x39) -> even 0x38
+             1.1875: 0x3A,        # halfway 1.125 (0x39) / 1.25 (0x3A) -> even 0x3A
+             1.07: 0x39, 1.05: 0x38,
+             2.0 ** -10: 0x00,    # halfway 0 / 2^-9 -> 0x00
+             3 * 2.0 ** -10: 0x02,  # halfway 2^-9 (0x01) / 2^-8 (0x02) -> 0x02
+             464.0: 0x7E, 1e6: 0x7E, -1e6: 0xFE, -1.0: 0xB8}
+    for x, code in cases.items():
+        assert int(oracle.e4m3_encode(x)) == code, x
+    assert int(oracle.e4m3_encode(float("nan"))) == 0x7F
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)])
+    np.testing.assert_array_equal(oracle.e4m3_encode(oracle.e4m3_decode(finite)), finite)
+
+
+def test_cache_append_fp8_codes_within_half_a_quantum():
+    """The codes decode to the normalised row over lat_scale to within half a
+    quantum of E4M3 (2^-4 relative for normal values, 2^-10 absolute below
+    2^-6); the rope part is cache_append's."""
+    r = _rng(12)
+    B, S, Dl, Dr = 2, 3, 32, 8
+    comp = r.standard_normal((B, S, Dl + Dr))
+    w = r.uniform(0.5, 1.5, Dl)
+    lat_scale = math.sqrt(Dl) * 1.5 / 448
+    codes, rc, pos = oracle.cache_append_fp8(comp, w, 1e-6, [5, 9], Dl, lat_scale)
+    lc, rc0, pos0 = oracle.cache_append(comp, w, 1e-6, [5, 9], Dl)
+    y = lc / lat_scale
+    d = oracle.e4m3_decode(codes)
+    bound = np.maximum(np.abs(y) * 2.0 ** -4, 2.0 ** -10)
+    assert np.all(np.abs(d - y) <= bound + 1e-12)
+    assert np.max(np.abs(y)) <= 448                       # the RMSNorm bound keeps the row in range
+    np.testing.assert_array_equal(rc, rc0)
+    np.testing.assert_array_equal(pos, pos0)
+    np.testing.assert_allclose(oracle.dequant_latent(codes, lat_scale), lat_scale * d)
