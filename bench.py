@@ -43,8 +43,10 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 ROW_WORKLOADS = ("glm_batched_b32_s1", "glm_batched_b32_s6", "glm_dsa_t65536", "glm_prefill_s2048",
-                 "glm_append_b32_s6", "glm_paged_b32_s1", "glm_dsa_t65536_l4", "glm_decode_oproj_t4096")
+                 "glm_append_b32_s6", "glm_paged_b32_s1", "glm_dsa_t65536_l4", "glm_decode_oproj_t4096",
+                 "glm_batched_b32_s1_fp8", "glm_decode_t4096_fp8")
 OPROJ_HIDDEN = 6144  # model width of the projection row: a size chosen here, the pages print none
+FP8_LAT_SCALE = 0.05  # scale of the synthetic FP8 latent cache (codes of magnitude 2^-3 .. 30)
 APPEND_RMS_EPS = 1e-6
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a
 # workload's dominant kernel, from one ncu capture of that kernel on this
@@ -74,6 +76,9 @@ def build_workload(name, device):
     import mla_latent_kv_06_gb300 as mla
     from workload import GLM, mla_inputs, workload_inputs, SEED_BASE
 
+    fp8 = name.endswith("_fp8")  # the same workload over the FP8 latent cache
+    if fp8:
+        name = name[:-len("_fp8")]
     if name.startswith("glm_decode_t"):
         T = int(name[len("glm_decode_t"):])
         if name == "glm_decode_t4096":
@@ -122,6 +127,12 @@ def build_workload(name, device):
     R = B * S
     T_list = x["T_list"]
     row = 2 * (d.kv_lora + d.qk_rope)                      # latent-cache bytes per key
+    if fp8:
+        from workload import fp8_latent_codes
+        assert kind == "decode" and "table" not in x
+        x["Lc8"] = fp8_latent_codes(B, T_list, x["T_cap"], d.kv_lora, SEED_BASE + 8, device)
+        del x["Lc"]
+        row = d.kv_lora + 2 * d.qk_rope                    # E4M3 latent, bf16 rope key
     w_uk = 2 * d.H * d.qk_nope * d.kv_lora
     w_uv = 2 * d.H * d.v_head * d.kv_lora
     q_bytes = 2 * R * d.H * d.qk_head
@@ -136,6 +147,11 @@ def build_workload(name, device):
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
         calls = [lambda: mla.decode_paged(x["q"], x["Lc"], x["Rc"], x["table"], x["T"], x["kv_b"], d, out=out,
                                           workspace=ws)]
+    elif kind == "decode" and fp8:
+        need = mla.lib().mla_decode_fp8_workspace_size(mla.ctypes.byref(mla.make_dims(d)), B, S, x["T_cap"])
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+        calls = [lambda: mla.decode_fp8(x["q"], x["Lc8"], x["Rc"], x["T"], x["kv_b"], d, FP8_LAT_SCALE, out=out,
+                                        workspace=ws)]
     elif kind == "decode":
         need = mla.decode_workspace_size(d, mla.MLA_BF16, B, S, x["T_cap"])
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
@@ -154,8 +170,12 @@ def build_workload(name, device):
                 "attention": ("tensor", attn_flops) if S > 1 else ("hbm", cache + qcat),
                 "combine": ("hbm", w_uv + out_bytes), "merge": ("hbm", clat),
                 "up_gemm": ("hbm", w_uv + clat + out_bytes)}
-        e2e = None if "table" in x else dict(inputs=[x["q"], x["T"]], run=lambda q, T: mla.decode_absorbed(
-            q, x["Lc"], x["Rc"], T, x["kv_b"], d, out=out, workspace=ws), out=out)
+        if fp8:
+            e2e = dict(inputs=[x["q"], x["T"]], run=lambda q, T: mla.decode_fp8(
+                q, x["Lc8"], x["Rc"], T, x["kv_b"], d, FP8_LAT_SCALE, out=out, workspace=ws), out=out)
+        else:
+            e2e = None if "table" in x else dict(inputs=[x["q"], x["T"]], run=lambda q, T: mla.decode_absorbed(
+                q, x["Lc"], x["Rc"], T, x["kv_b"], d, out=out, workspace=ws), out=out)
     elif kind == "dsa":
         k = x["topk"]
         T_cap = x["T_cap"]
@@ -580,6 +600,8 @@ def main():
                                                                        "kernels")}}
                     if "flops" in r["info"]:
                         rows[wl]["tflops"] = r["info"]["flops"] / t / 1e12
+                    if wl.endswith("_fp8"):
+                        rows[wl]["cache"] = "E4M3 latent codes (one scale), bf16 rope key"
                 line["rows"] = rows
             if not args.no_cpu:
                 tok_s, n, el = oracle_sample(args.workload)

@@ -218,6 +218,55 @@ int mla_sparse_decode_paged(const mla_dims* d, int dtype, int B, int S, const vo
                             void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * FP8 latent cache (a cache format of this library: the pages name FP8 only
+ * as a weight format)
+ *
+ * The latent part of each cached row is kv_lora E4M3 codes (1 sign, 4
+ * exponent bits with bias 7, 3 mantissa bits, no infinities, 0x7F/0xFF NaN,
+ * largest finite value 448) with one scale for the whole cache:
+ *   Lc[b,t,:] = lat_scale * e4m3(Lc8[b,t,:])
+ *   Lc8 [B, T_cap, kv_lora] uint8 (or the pool [num_pages, page_size, kv_lora])
+ *   Rc  [B, T_cap, qk_rope] bf16, unchanged
+ * Half the bytes of a bf16 row's latent part.  RMSNorm bounds every written
+ * value by sqrt(kv_lora) * max|kv_a_ln|, so lat_scale = that bound / 448
+ * never saturates.
+ *
+ * mla_decode_fp8 / mla_decode_fp8_paged compute the absorbed decode of
+ * mla_decode_absorbed (q, kv_b bf16; out float; T, pages as there) over the
+ * dequantised latent.  The tensor-core kernels read the codes directly
+ * (kind::f8f6f4 MMAs): each query row's absorbed latent query is rounded to
+ * E4M3 with its own scale (its largest magnitude / 448), and the softmax
+ * probabilities are rounded to E4M3 for the value product (row sums in
+ * fp32).  Both roundings carry the E4M3 unit roundoff 2^-4, so results match
+ * the exact attention over the dequantised cache to a few percent, not to
+ * bf16 accuracy.  Only the GLM-5.2 head geometry (64 heads, kv_lora 512,
+ * qk_rope 64) with 16-byte aligned tensors is served; page_size must be a
+ * multiple of 128; anything else returns MLA_ERR_UNSUPPORTED.  lat_scale must
+ * be positive and finite.  Workspace: mla_decode_fp8_workspace_size (the
+ * paged call takes T_cap = max_pages * page_size).
+ *
+ * mla_cache_append_fp8 / _paged write the new rows as mla_cache_append does
+ * (comp, kv_a_ln bf16), the latent values as E4M3 codes of
+ * RMSNorm(...) / lat_scale (fp32 arithmetic, round to nearest even,
+ * saturating at 448).  lat_scale must be positive, finite, with a finite
+ * inverse.
+ * ------------------------------------------------------------------------- */
+size_t mla_decode_fp8_workspace_size(const mla_dims* d, int B, int S, int T_cap);
+int mla_decode_fp8(const mla_dims* d, int B, int S, const void* q, const uint8_t* Lc8, const void* Rc,
+                   float lat_scale, int T_cap, const int32_t* T, const void* kv_b, float* out,
+                   void* workspace, size_t workspace_bytes, void* stream);
+int mla_decode_fp8_paged(const mla_dims* d, int B, int S, const void* q, const uint8_t* Lc8_pages,
+                         const void* Rc_pages, float lat_scale, int num_pages, int page_size,
+                         const int32_t* block_table, int max_pages, const int32_t* T, const void* kv_b,
+                         float* out, void* workspace, size_t workspace_bytes, void* stream);
+int mla_cache_append_fp8(const mla_dims* d, int B, int S, const void* comp, const void* kv_a_ln, float rms_eps,
+                         float lat_scale, int T_cap, const int32_t* T, uint8_t* Lc8, void* Rc, void* stream);
+int mla_cache_append_fp8_paged(const mla_dims* d, int B, int S, const void* comp, const void* kv_a_ln,
+                               float rms_eps, float lat_scale, uint8_t* Lc8_pages, void* Rc_pages, int num_pages,
+                               int page_size, const int32_t* block_table, int max_pages, const int32_t* T,
+                               void* stream);
+
+/* ---------------------------------------------------------------------------
  * Non-absorbed prefill ([MLA-KV] §2.3, non-absorbed path)
  *
  * Step 1: one kv_b product rebuilds, for every key t < Tk = pos_base + S,

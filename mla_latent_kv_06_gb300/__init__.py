@@ -31,6 +31,8 @@ EXPORTS = (
     "mla_decode_paged_workspace_size", "mla_decode_paged", "mla_sparse_decode_paged", "mla_cache_append_paged",
     "dsa_select_workspace_size", "dsa_select",
     "mla_o_proj_workspace_size", "mla_o_proj", "mla_decode_oproj_workspace_size", "mla_decode_oproj",
+    "mla_decode_fp8_workspace_size", "mla_decode_fp8", "mla_decode_fp8_paged", "mla_cache_append_fp8",
+    "mla_cache_append_fp8_paged",
 )
 
 
@@ -88,6 +90,13 @@ def _declare(lib: ctypes.CDLL) -> None:
         "mla_o_proj": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
         "mla_decode_oproj_workspace_size": (_SZ, [_DP, _I, _I, _I, _I, _I]),
         "mla_decode_oproj": (_I, [_DP, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _SZ, _P]),
+        "mla_decode_fp8_workspace_size": (_SZ, [_DP, _I, _I, _I]),
+        "mla_decode_fp8": (_I, [_DP, _I, _I, _P, _P, _P, ctypes.c_float, _I, _P, _P, _P, _P, _SZ, _P]),
+        "mla_decode_fp8_paged": (_I, [_DP, _I, _I, _P, _P, _P, ctypes.c_float, _I, _I, _P, _I, _P, _P, _P, _P,
+                                      _SZ, _P]),
+        "mla_cache_append_fp8": (_I, [_DP, _I, _I, _P, _P, ctypes.c_float, ctypes.c_float, _I, _P, _P, _P, _P]),
+        "mla_cache_append_fp8_paged": (_I, [_DP, _I, _I, _P, _P, ctypes.c_float, ctypes.c_float, _P, _P, _I, _I,
+                                            _P, _I, _P, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -424,3 +433,81 @@ def cache_append_paged(comp, kv_a_ln, block_table, T, Lc_pages, Rc_pages, dims, 
                                         _ptr(Lc_pages), _ptr(Rc_pages), num_pages, page_size, _ptr(block_table),
                                         block_table.shape[1], _ptr(T), _stream(stream)))
     return Lc_pages, Rc_pages
+
+
+# ------------------------------------------------------------- FP8 latent cache
+def _need_bf16(*ts):
+    torch = _torch()
+    for t in ts:
+        if t.dtype != torch.bfloat16:
+            raise TypeError("the FP8 cache entry points take bf16 q, Rc, kv_b and comp")
+
+
+def _need_u8(t):
+    torch = _torch()
+    if t.dtype != torch.uint8:
+        raise TypeError("the FP8 latent cache holds uint8 E4M3 codes")
+
+
+def decode_fp8(q, Lc8, Rc, T, kv_b, dims, lat_scale: float, out=None, workspace=None, stream=None):
+    """Absorbed decode over an FP8 latent cache: Lc8 [B, T_cap, kv_lora] uint8
+    E4M3 codes (latent = lat_scale * code), Rc [B, T_cap, qk_rope] bf16."""
+    torch = _torch()
+    _need_bf16(q, Rc, kv_b)
+    _need_u8(Lc8)
+    B, S, H = q.shape[0], q.shape[1], q.shape[2]
+    T_cap = Lc8.shape[1]
+    if out is None:
+        out = torch.empty(B, S, H, dims.v_head, dtype=torch.float32, device=q.device)
+    d = make_dims(dims)
+    need = lib().mla_decode_fp8_workspace_size(ctypes.byref(d), B, S, T_cap)
+    workspace, wsb = _workspace(need, q.device, workspace)
+    _check(lib().mla_decode_fp8(ctypes.byref(d), B, S, _ptr(q), _ptr(Lc8), _ptr(Rc), float(lat_scale), T_cap,
+                                _ptr(T), _ptr(kv_b), _ptr(out), _ptr(workspace), wsb, _stream(stream)))
+    return out
+
+
+def decode_fp8_paged(q, Lc8_pages, Rc_pages, block_table, T, kv_b, dims, lat_scale: float, out=None,
+                     workspace=None, stream=None):
+    """decode_fp8 over page pools: Lc8_pages [num_pages, page_size, kv_lora] uint8,
+    Rc_pages [num_pages, page_size, qk_rope] bf16, block_table [B, max_pages] int32."""
+    torch = _torch()
+    _need_bf16(q, Rc_pages, kv_b)
+    _need_u8(Lc8_pages)
+    B, S, H = q.shape[0], q.shape[1], q.shape[2]
+    num_pages, page_size = Lc8_pages.shape[0], Lc8_pages.shape[1]
+    max_pages = block_table.shape[1]
+    if out is None:
+        out = torch.empty(B, S, H, dims.v_head, dtype=torch.float32, device=q.device)
+    d = make_dims(dims)
+    need = lib().mla_decode_fp8_workspace_size(ctypes.byref(d), B, S, max_pages * page_size)
+    workspace, wsb = _workspace(need, q.device, workspace)
+    _check(lib().mla_decode_fp8_paged(ctypes.byref(d), B, S, _ptr(q), _ptr(Lc8_pages), _ptr(Rc_pages),
+                                      float(lat_scale), num_pages, page_size, _ptr(block_table), max_pages, _ptr(T),
+                                      _ptr(kv_b), _ptr(out), _ptr(workspace), wsb, _stream(stream)))
+    return out
+
+
+def cache_append_fp8(comp, kv_a_ln, T, Lc8, Rc, dims, rms_eps: float, lat_scale: float, stream=None):
+    """mla_cache_append into the FP8 cache (in place): Lc8 uint8 codes, Rc bf16."""
+    _need_bf16(comp, kv_a_ln, Rc)
+    _need_u8(Lc8)
+    B, S = comp.shape[0], comp.shape[1]
+    d = make_dims(dims)
+    _check(lib().mla_cache_append_fp8(ctypes.byref(d), B, S, _ptr(comp), _ptr(kv_a_ln), float(rms_eps),
+                                      float(lat_scale), Lc8.shape[1], _ptr(T), _ptr(Lc8), _ptr(Rc), _stream(stream)))
+    return Lc8, Rc
+
+
+def cache_append_fp8_paged(comp, kv_a_ln, block_table, T, Lc8_pages, Rc_pages, dims, rms_eps: float,
+                           lat_scale: float, stream=None):
+    """cache_append_fp8 into the page pools (in place)."""
+    _need_bf16(comp, kv_a_ln, Rc_pages)
+    _need_u8(Lc8_pages)
+    B, S = comp.shape[0], comp.shape[1]
+    num_pages, page_size = Lc8_pages.shape[0], Lc8_pages.shape[1]
+    d = make_dims(dims)
+    _check(lib().mla_cache_append_fp8_paged(ctypes.byref(d), B, S, _ptr(comp), _ptr(kv_a_ln), float(rms_eps),
+                                            float(lat_scale), _ptr(Lc8_pages), _ptr(Rc_pages), num_pages, page_size,
+                                            _ptr(block_table), block_table.shape[1], _ptr(T), _stream(stream)))
+    return Lc8_pages, Rc_pages

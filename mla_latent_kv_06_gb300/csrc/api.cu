@@ -263,6 +263,74 @@ MLA_EXPORT int mla_decode_paged(const mla_dims* d, int dtype, int B, int S, cons
   return run_decode(a, dtype, false, workspace, workspace_bytes, stream, "mla_decode_paged launch");
 }
 
+namespace {
+int run_decode_fp8(mla::DecodeArgs& a, float lat_scale, void* workspace, size_t workspace_bytes, void* stream,
+                   const char* what) {
+  if (!(lat_scale > 0.f) || !std::isfinite(lat_scale))
+    return fail(MLA_ERR_INVALID, "lat_scale must be positive and finite");
+  if (!tc_decode_ok(a.g, MLA_BF16, a.q, a.Lc, a.Rc, a.kv_b))
+    return fail(MLA_ERR_UNSUPPORTED, "the FP8 cache needs the 64-head, 512+64 latent geometry and 16-byte aligned "
+                                     "tensors");
+  if (a.pages.table && a.pages.page_size % 128 != 0)
+    return fail(MLA_ERR_UNSUPPORTED, "page_size=%d is not a multiple of 128", a.pages.page_size);
+  a.lat_fp8 = 1;
+  a.lat_scale = lat_scale;
+  return run_decode(a, MLA_BF16, false, workspace, workspace_bytes, stream, what);
+}
+}  // namespace
+
+MLA_EXPORT size_t mla_decode_fp8_workspace_size(const mla_dims* d, int B, int S, int T_cap) {
+  mla::Geometry g;
+  if (!resolve(d, &g) || B < 1 || S < 1 || T_cap < S || !mla::tc_decode_geometry_ok(g)) return 0;
+  return round256(mla::tc_decode_workspace_bytes(g, B, S, T_cap, /*sparse_topk=*/0));
+}
+
+MLA_EXPORT int mla_decode_fp8(const mla_dims* d, int B, int S, const void* q, const uint8_t* Lc8, const void* Rc,
+                              float lat_scale, int T_cap, const int32_t* T, const void* kv_b, float* out,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  mla::Geometry g;
+  int rc = check_common(d, MLA_BF16, B, S, &g);
+  if (rc) return rc;
+  if (T_cap < S) return fail(MLA_ERR_INVALID, "T_cap=%d < S=%d", T_cap, S);
+  if (!q || !Lc8 || !Rc || !T || !kv_b || !out) return fail(MLA_ERR_INVALID, "null tensor pointer");
+  mla::DecodeArgs a{};
+  a.g = g;
+  a.B = B;
+  a.S = S;
+  a.T_cap = T_cap;
+  a.q = q;
+  a.Lc = Lc8;
+  a.Rc = Rc;
+  a.T = T;
+  a.kv_b = kv_b;
+  a.out = out;
+  return run_decode_fp8(a, lat_scale, workspace, workspace_bytes, stream, "mla_decode_fp8 launch");
+}
+
+MLA_EXPORT int mla_decode_fp8_paged(const mla_dims* d, int B, int S, const void* q, const uint8_t* Lc8_pages,
+                                    const void* Rc_pages, float lat_scale, int num_pages, int page_size,
+                                    const int32_t* block_table, int max_pages, const int32_t* T, const void* kv_b,
+                                    float* out, void* workspace, size_t workspace_bytes, void* stream) {
+  mla::Geometry g;
+  int rc = check_common(d, MLA_BF16, B, S, &g);
+  if (rc) return rc;
+  mla::DecodeArgs a{};
+  rc = check_pages(S, num_pages, page_size, block_table, max_pages, &a.pages);
+  if (rc) return rc;
+  if (!q || !Lc8_pages || !Rc_pages || !T || !kv_b || !out) return fail(MLA_ERR_INVALID, "null tensor pointer");
+  a.g = g;
+  a.B = B;
+  a.S = S;
+  a.T_cap = max_pages * page_size;
+  a.q = q;
+  a.Lc = Lc8_pages;
+  a.Rc = Rc_pages;
+  a.T = T;
+  a.kv_b = kv_b;
+  a.out = out;
+  return run_decode_fp8(a, lat_scale, workspace, workspace_bytes, stream, "mla_decode_fp8_paged launch");
+}
+
 MLA_EXPORT int mla_decode_launch_count(const mla_dims* d, int dtype, int B, int S, int sparse) {
   mla::Geometry g;
   if (!resolve(d, &g) || B < 1 || S < 1) return 0;
@@ -593,7 +661,7 @@ MLA_EXPORT int mla_decode_oproj(const mla_dims* d, int dtype, int B, int S, cons
 namespace {
 int run_cache_append(const mla_dims* d, int dtype, int B, int S, const void* comp, const void* kv_a_ln,
                      float rms_eps, int T_cap, const int32_t* T, void* Lc, void* Rc, const mla::PageTable& pages,
-                     void* stream, const char* what) {
+                     void* stream, const char* what, float lat_scale = 0.f) {
   mla::Geometry g;
   int rc = check_common(d, dtype, B, S, &g);
   if (rc != MLA_OK) return rc;
@@ -606,6 +674,10 @@ int run_cache_append(const mla_dims* d, int dtype, int B, int S, const void* com
   if (!pages.table && (long long)B * T_cap >= (1ll << 31))
     return fail(MLA_ERR_UNSUPPORTED, "B*T_cap of 2^31 rows or more");
   mla::AppendArgs a{B, S, T_cap, g.Dl, g.Dr, comp, kv_a_ln, rms_eps, T, Lc, Rc, flags_ptr(), pages, {}};
+  if (lat_scale != 0.f) {  // the FP8 cache
+    a.lat_fp8 = 1;
+    a.lat_inv_scale = 1.f / lat_scale;
+  }
   for (int j = 0; j < g.Dr / 2; ++j) a.theta[j] = std::pow(g.rope_base, -2.0 * j / g.Dr);
   if (!a.flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -634,6 +706,28 @@ MLA_EXPORT int mla_cache_append_paged(const mla_dims* d, int dtype, int B, int S
   if (rc) return rc;
   return run_cache_append(d, dtype, B, S, comp, kv_a_ln, rms_eps, max_pages * page_size, T, Lc_pages, Rc_pages, pt,
                           stream, "mla_cache_append_paged launch");
+}
+
+MLA_EXPORT int mla_cache_append_fp8(const mla_dims* d, int B, int S, const void* comp, const void* kv_a_ln,
+                                    float rms_eps, float lat_scale, int T_cap, const int32_t* T, uint8_t* Lc8,
+                                    void* Rc, void* stream) {
+  if (!(lat_scale > 0.f) || !std::isfinite(lat_scale) || !std::isfinite(1.f / lat_scale))
+    return fail(MLA_ERR_INVALID, "lat_scale must be positive and finite with a finite inverse");
+  return run_cache_append(d, MLA_BF16, B, S, comp, kv_a_ln, rms_eps, T_cap, T, Lc8, Rc, mla::PageTable{}, stream,
+                          "mla_cache_append_fp8 launch", lat_scale);
+}
+
+MLA_EXPORT int mla_cache_append_fp8_paged(const mla_dims* d, int B, int S, const void* comp, const void* kv_a_ln,
+                                          float rms_eps, float lat_scale, uint8_t* Lc8_pages, void* Rc_pages,
+                                          int num_pages, int page_size, const int32_t* block_table, int max_pages,
+                                          const int32_t* T, void* stream) {
+  if (!(lat_scale > 0.f) || !std::isfinite(lat_scale) || !std::isfinite(1.f / lat_scale))
+    return fail(MLA_ERR_INVALID, "lat_scale must be positive and finite with a finite inverse");
+  mla::PageTable pt{};
+  int rc = check_pages(S, num_pages, page_size, block_table, max_pages, &pt);
+  if (rc) return rc;
+  return run_cache_append(d, MLA_BF16, B, S, comp, kv_a_ln, rms_eps, max_pages * page_size, T, Lc8_pages, Rc_pages,
+                          pt, stream, "mla_cache_append_fp8_paged launch", lat_scale);
 }
 
 MLA_EXPORT int dsa_index_key_append(int B, int S, int index_hd, int rope_dim, const float* k_idx,

@@ -6,12 +6,16 @@
 // shared by all heads into Rc.  §2.2: the indexer key goes through layernorm
 // (eps 1e-6) and RoPE into Ic (fp32, page "第 7 章 · 03 token 精确前向验证与
 // faithful DSA", §二).  The S new tokens of sequence b sit at rows
-// pos = T[b] - S + s.  One CTA per new token.  A row is a few KB, so the
+// pos = T[b] - S + s.  The FP8 cache stores the latent row as E4M3 codes of
+// the normalised values divided by the cache's scale (round to nearest even,
+// saturating at 448).  One CTA per new token.  A row is a few KB, so the
 // kernels are bound by latency, not bandwidth: every thread issues all of
 // its loads (the row's values, the norm weights, T[b]) before the first use,
 // so that each row costs one DRAM round trip, then one block reduction
 // (two for the LayerNorm) and the stores.  Both launch as programmatic
 // dependents: the launch overlaps the preceding kernel, the loads wait for it.
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -53,7 +57,8 @@ __device__ __forceinline__ int new_row(int Tb, int s, int S, int T_cap, unsigned
 }
 
 // kPer values of the latent part per thread (element tid + k * kAppThreads).
-template <typename Tv, int kPer>
+// kFp8: the latent row goes out as E4M3 codes.
+template <typename Tv, int kPer, bool kFp8 = false>
 __global__ void __launch_bounds__(kAppThreads) cache_append_kernel(AppendArgs a) {
   __shared__ float red[kAppThreads / 32];
   const int tid = threadIdx.x;
@@ -89,11 +94,21 @@ __global__ void __launch_bounds__(kAppThreads) cache_append_kernel(AppendArgs a)
     if (tid == 0) raise_flag(a.flags, MLA_DEV_BAD_INDEX);
     return;
   }
-  Tv* lc = static_cast<Tv*>(a.Lc) + (size_t)row * a.kv_lora;
+  if constexpr (kFp8) {
+    unsigned char* lc = static_cast<unsigned char*>(a.Lc) + (size_t)row * a.kv_lora;
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int i = tid + k * kAppThreads;
-    if (i < a.kv_lora) store(lc + i, xv[k] * inv * wv[k]);
+    for (int k = 0; k < kPer; ++k) {
+      const int i = tid + k * kAppThreads;
+      if (i < a.kv_lora)
+        lc[i] = (unsigned char)__nv_cvt_float_to_fp8(xv[k] * inv * wv[k] * a.lat_inv_scale, __NV_SATFINITE, __NV_E4M3);
+    }
+  } else {
+    Tv* lc = static_cast<Tv*>(a.Lc) + (size_t)row * a.kv_lora;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = tid + k * kAppThreads;
+      if (i < a.kv_lora) store(lc + i, xv[k] * inv * wv[k]);
+    }
   }
   if (tid < half) {
     Tv* rc = static_cast<Tv*>(a.Rc) + (size_t)row * a.qk_rope;
@@ -162,6 +177,10 @@ __global__ void __launch_bounds__(kAppThreads) key_append_kernel(KeyAppendArgs a
 template <typename Tv>
 cudaError_t launch_append_t(const AppendArgs& a, cudaStream_t st) {
   const dim3 grid(a.B * a.S), block(kAppThreads);
+  if (a.lat_fp8) {
+    if (a.kv_lora <= 4 * kAppThreads) return launch_pdl(cache_append_kernel<Tv, 4, true>, grid, block, 0, st, a);
+    return launch_pdl(cache_append_kernel<Tv, kMaxAppendPer, true>, grid, block, 0, st, a);
+  }
   if (a.kv_lora <= 4 * kAppThreads) return launch_pdl(cache_append_kernel<Tv, 4>, grid, block, 0, st, a);
   return launch_pdl(cache_append_kernel<Tv, kMaxAppendPer>, grid, block, 0, st, a);
 }
@@ -169,6 +188,7 @@ cudaError_t launch_append_t(const AppendArgs& a, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_cache_append(const AppendArgs& a, int dtype, cudaStream_t st) {
+  if (a.lat_fp8 && dtype != MLA_BF16) return cudaErrorInvalidValue;  // the FP8 cache keeps Rc in bf16
   return dtype == MLA_BF16 ? launch_append_t<__nv_bfloat16>(a, st) : launch_append_t<float>(a, st);
 }
 

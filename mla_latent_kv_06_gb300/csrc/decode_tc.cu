@@ -23,6 +23,8 @@
 // The sparse variant first gathers each query's selected [Lc | Rc] rows into
 // a contiguous staging buffer (row-major, 576 values per key, zero past nsel),
 // so that its attention pass uses the same 1024-byte-aligned tile loads.
+#include <cuda_fp8.h>
+
 #include <atomic>
 #include <cmath>
 
@@ -44,6 +46,15 @@ constexpr uint32_t kQAtomBytes = 8192;         // 64 rows x 64 bf16
 constexpr uint32_t kQBytes = 9 * kQAtomBytes;  // 73728
 constexpr uint32_t kKVBytes = 9 * kSlotBytes;  // 147456
 constexpr uint32_t kAttnDynSmem = kQBytes + kKVBytes + 1024;
+// FP8 latent cache: a key tile is four latent atoms of 128 keys x 128 E4M3
+// codes and the bf16 rope atom, 16 KB each; the query block holds the
+// quantised latent part (four 8 KB atoms of 64 rows x 128 codes) and the rope
+// part (bf16), built by the softmax warps from the bf16 qcat block, which
+// lands in a staging area of the bf16 layout.
+constexpr int kSlots8 = 5;
+constexpr uint32_t kQ8Bytes = 5 * kQAtomBytes;   // 40960
+constexpr uint32_t kKV8Bytes = 5 * kSlotBytes;   // 81920
+constexpr uint32_t kAttn8DynSmem = kQBytes + kQ8Bytes + kKV8Bytes + 1024;
 constexpr int kSoftWarps = 8;
 constexpr int kSoftThreads = 32 * kSoftWarps;
 constexpr int kAttnThreads = 64 + kSoftThreads;
@@ -71,6 +82,7 @@ struct AttnParams {
   int qsplit;     // CTAs per piece (1, 2 or 4): each repeats the score product and owns 4/qsplit
                   // of the four 128-row blocks of O^T (the value product and its partial)
   float c;        // softmax scale * log2(e)
+  float lat_scale;  // FP8 cache: latent row = lat_scale * E4M3 codes
   float* o_part;
   float* ml_part;
   unsigned int* flags;
@@ -234,6 +246,74 @@ __device__ __forceinline__ int tile_keys(const AttnParams& p, int row, int s, in
   return n < kTile ? n : kTile;
 }
 
+// Two E4M3 codes of (lo, hi), lo in the low byte (the lower address).
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+
+// FP8 cache: quantise a piece's query block.  Thread tsm (0..255) takes query
+// row r = tsm / 4 and quarter qq = tsm % 4: latent columns 128 qq .. 128 qq +
+// 127 become E4M3 codes with the row's scale sq = amax / 448 (one 128-byte row
+// of latent atom qq of sQ8), and rope values 16 qq .. 16 qq + 15 become bf16
+// divided by lat_scale * sq, so that one fp32 accumulator holds
+// (qabs . Lc + q_rot . Rc) / (lat_scale * sq).  fh[r] = c * lat_scale * sq
+// turns it back into the score in log2 units.  Staging and sQ8 use the same
+// 128-byte-swizzled K-major rows (16-byte chunk index XOR row % 8).
+__device__ __forceinline__ void quantise_q(const unsigned char* sQ, unsigned char* sQ8, float* fh, int tsm, float c,
+                                           float lat_scale) {
+  const int r = tsm >> 2, qq = tsm & 3, sw = r & 7;
+  // the 128 latent values of this thread: 16 chunks of 8 bf16 (chunk i: atom
+  // 2 qq + i / 8, chunk i % 8 of the row)
+  auto chunk = [&](int i) -> uint4 {
+    return *reinterpret_cast<const uint4*>(sQ + (2 * qq + (i >> 3)) * kQAtomBytes + r * 128 + (((i & 7) ^ sw) << 4));
+  };
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    uint4 v = chunk(i);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float2 f = __bfloat1622float2(b2[t]);
+      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  const float sq = amax > 0.f ? amax * (1.f / 448.f) : 1.f;
+  const float inv = amax > 0.f ? 448.f / amax : 1.f;
+  // 16 codes (one 16-byte chunk of the E4M3 row) from two bf16 chunks
+#pragma unroll
+  for (int cc = 0; cc < 8; ++cc) {
+    uint32_t code[4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint4 v = chunk(2 * cc + h);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+      const float2 f0 = __bfloat1622float2(b2[0]), f1 = __bfloat1622float2(b2[1]);
+      const float2 f2 = __bfloat1622float2(b2[2]), f3 = __bfloat1622float2(b2[3]);
+      code[2 * h] = e4m3x2(f0.x * inv, f0.y * inv) | (e4m3x2(f1.x * inv, f1.y * inv) << 16);
+      code[2 * h + 1] = e4m3x2(f2.x * inv, f2.y * inv) | (e4m3x2(f3.x * inv, f3.y * inv) << 16);
+    }
+    *reinterpret_cast<uint4*>(sQ8 + qq * kQAtomBytes + r * 128 + ((cc ^ sw) << 4)) =
+        make_uint4(code[0], code[1], code[2], code[3]);
+  }
+  const float rs = 1.f / (lat_scale * sq);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int cc = 2 * qq + h;
+    uint4 v = *reinterpret_cast<const uint4*>(sQ + 8 * kQAtomBytes + r * 128 + ((cc ^ sw) << 4));
+    __nv_bfloat162* b2 = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float2 f = __bfloat1622float2(b2[t]);
+      b2[t] = __floats2bfloat162_rn(f.x * rs, f.y * rs);
+    }
+    *reinterpret_cast<uint4*>(sQ8 + 4 * kQAtomBytes + r * 128 + ((cc ^ sw) << 4)) = v;
+  }
+  if (qq == 0) fh[r] = c * lat_scale * sq;
+}
+
 // ===========================================================================
 // Attention kernel
 //
@@ -247,16 +327,20 @@ __device__ __forceinline__ int tile_keys(const AttnParams& p, int row, int s, in
 // the next tile's loads start while it still runs, and the next score product
 // accumulates atom by atom as they land.
 // ===========================================================================
-template <bool kSparse>
+template <bool kSparse, bool kFp8 = false>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
+  static_assert(!(kSparse && kFp8), "the FP8 cache has no sparse path");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
-  unsigned char* sQ = smem;
-  unsigned char* sKV = smem + kQBytes;
+  unsigned char* sQ = smem;                // bf16 query block (FP8: its staging copy)
+  unsigned char* sQ8 = smem + kQBytes;     // FP8: quantised query block
+  unsigned char* sKV = smem + kQBytes + (kFp8 ? kQ8Bytes : 0);
+  constexpr int nslots = kFp8 ? kSlots8 : kSlots;
 
   __shared__ uint64_t full_bar[kSlots], empty_bar[kSlots];
-  __shared__ uint64_t q_full, q_empty, s_full, s_free, p_full, o_done, mma_done, o_blk[4];
+  __shared__ uint64_t q_full, q_empty, q8_full, s_full, s_free, p_full, o_done, mma_done, o_blk[4];
+  __shared__ __align__(16) float fh_sh[2][kH];  // FP8: per query row score factor, by piece parity
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ __align__(16) float red_max[4][kH];
@@ -280,7 +364,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       mbar_init(&empty_bar[i], 1);
     }
     mbar_init(&q_full, 1);
-    mbar_init(&q_empty, 1);
+    mbar_init(&q_empty, kFp8 ? kSoftThreads : 1);  // FP8: freed once the softmax warps quantised it
+    mbar_init(&q8_full, kSoftThreads);
     mbar_init(&s_full, 1);
     mbar_init(&s_free, kSoftThreads);
     mbar_init(&p_full, kSoftThreads);
@@ -363,12 +448,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           if (bad_page) raise_flag(p.flags, MLA_DEV_BAD_INDEX);
         }
         const uint32_t par = (it & 1) ^ 1;
-        for (int a = 0; a < kSlots && ok; ++a) {
+        for (int a = 0; a < nslots && ok; ++a) {
           ok = mbar_wait(&empty_bar[a], par, abort, p.flags, p.wait_ns);
           if (!ok) break;
           mbar_arrive_expect_tx(&full_bar[a], kSlotBytes);
-          const CUtensorMap* map = a < 8 ? &p.mL : &p.mR;
-          const int x = a < 8 ? 64 * a : 0;
+          const bool lat = a < nslots - 1;
+          const CUtensorMap* map = lat ? &p.mL : &p.mR;
+          const int x = lat ? (kFp8 ? 128 * a : 64 * a) : 0;
           if (p.read_once) tma_load_2d_hint(sKV + a * kSlotBytes, map, x, y, &full_bar[a], pol_once);
           else tma_load_2d(sKV + a * kSlotBytes, map, x, y, &full_bar[a]);
           last_it[a] = it;
@@ -401,7 +487,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     // ------------------------------------------------------------ MMA issuer (whole warp waits, lane 0 issues)
     const uint32_t idS = idesc_bf16_f32(128, 64, 0, 0);
     const uint32_t idO = idesc_bf16_f32(128, 64, 1, 1);
-    const uint32_t kv0 = smem_u32(sKV), q0 = smem_u32(sQ);
+    const uint32_t idS8 = idesc_e4m3_f32(128, 64, 0, 0);
+    const uint32_t idO8 = idesc_e4m3_f32(128, 64, 1, 0);
+    const uint32_t kv0 = smem_u32(sKV), q0 = smem_u32(kFp8 ? sQ8 : sQ);
     TileCursor<kSparse> c;
     c.start(p, ts, NR, N, g, s, row0);
     int it = 0, pc = -1;
@@ -413,24 +501,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     while (ok && c.live) {
       const bool first = c.first();
       // keys of this tile, read now so that the load overlaps the waits below
-      const int ksteps = (tile_keys<kSparse>(p, c.row, s, c.k) + 15) >> 4;
+      const int tkeys = tile_keys<kSparse>(p, c.row, s, c.k);
+      const int ksteps = kFp8 ? (tkeys + 31) >> 5 : (tkeys + 15) >> 4;
       if (first) {
         ++pc;
-        ok = wait(&q_full, pc & 1);
+        ok = wait(kFp8 ? &q8_full : &q_full, pc & 1);
       }
       ok = ok && wait(&s_free, (it & 1) ^ 1);
       if (!ok) break;
       tc_fence_after();
-      for (int a = 0; a < kSlots && ok; ++a) {
+      for (int a = 0; a < nslots && ok; ++a) {
         ok = wait(&full_bar[a], it & 1);
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
+          // 32 bytes of K per instruction: 16 bf16 or 32 E4M3 values
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t da = smem_desc_sw128(kv0 + a * kSlotBytes + kk * 32, 16, 1024);
             const uint64_t db = smem_desc_sw128(q0 + a * kQAtomBytes + kk * 32, 16, 1024);
-            mma_bf16(tmem + kTmemS, da, db, idS, (a | kk) != 0 ? 1u : 0u);
+            if (kFp8 && a < nslots - 1) mma_f8(tmem + kTmemS, da, db, idS8, (a | kk) != 0 ? 1u : 0u);
+            else mma_bf16(tmem + kTmemS, da, db, idS, (a | kk) != 0 ? 1u : 0u);
           }
         }
         __syncwarp();
@@ -439,13 +530,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       if (!ok) break;
       if (lane == 0) {
         mma_commit(&s_full);
-        if (c.last()) mma_commit(&q_empty);
+        if (!kFp8 && c.last()) mma_commit(&q_empty);
       }
       __syncwarp();
       ok = wait(&p_full, it & 1);
       if (!ok) break;
       tc_fence_after();
-      if (lane == 0) {
+      if (kFp8 && lane == 0) {
+        // O^T block m = latent atom m (MN-major, 32 keys = 4 KB per step) x P^T
+        // (K-major E4M3 in the rope atom's slot)
+        for (int m = 0; m < 4; ++m)
+          if (m < mb0 || m >= mb1) mma_commit(&empty_bar[m]);
+        for (int m = mb0; m < mb1; ++m) {
+          for (int kk = 0; kk < ksteps; ++kk) {
+            const uint64_t da = smem_desc_sw128(kv0 + m * kSlotBytes + kk * 4096, kSlotBytes, 1024);
+            const uint64_t db = smem_desc_sw128(kv0 + 4 * kSlotBytes + kk * 32, 16, 1024);
+            mma_f8(tmem + kTmemO + 64 * m, da, db, idO8, (kk > 0 || !first) ? 1u : 0u);
+          }
+          mma_commit(&empty_bar[m]);
+          mma_commit(&o_blk[m]);
+        }
+        mma_commit(&empty_bar[4]);
+        mma_commit(&o_done);
+      } else if (lane == 0) {
         // latent atoms of the blocks another part owns: free once the score product retired
         for (int m = 0; m < 4; ++m)
           if (m < mb0 || m >= mb1) {
@@ -487,7 +594,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     const float c = p.c;
     TileCursor<kSparse> cur;
     cur.start(p, ts, NR, N, g, s, row0);
-    int it = 0, slot = 0, pos = 0, nkeys = 0;
+    int it = 0, slot = 0, pos = 0, nkeys = 0, spc = -1;
     const int32_t* srow = nullptr;
     bool ok = true, bad_idx = false;
     float lp[32];
@@ -517,7 +624,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         const float l = red_sum[0][tsm] + red_sum[1][tsm] + red_sum[2][tsm] + red_sum[3][tsm];
         float* ml = p.ml_part + ((size_t)slot * kH + tsm) * 2;
         ml[0] = m_sh[tsm];
-        ml[1] = bad ? __int_as_float(0x7fc00000) : l;
+        // FP8: O^T summed codes; dividing l by lat_scale puts the scale back
+        ml[1] = bad ? __int_as_float(0x7fc00000) : (kFp8 ? l / p.lat_scale : l);
       }
       if (bad && tsm == 0 && part == 0) raise_flag(p.flags, MLA_DEV_BAD_INDEX);
       return true;
@@ -526,6 +634,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     while (ok && cur.live) {
       const bool first = cur.first();
       if (first) {
+        if constexpr (kFp8) {
+          // quantise the new piece's query block first, so that its score
+          // product can start while the previous piece's partial is written
+          ++spc;
+          const bool qfail = !mbar_wait(&q_full, spc & 1, abort, p.flags, p.wait_ns);
+          if (bar_red_or(1, kSoftThreads, qfail)) {
+            ok = false;
+            break;
+          }
+          quantise_q(sQ, sQ8, fh_sh[spc & 1], tsm, c, p.lat_scale);
+          fence_proxy_async_smem();
+          mbar_arrive(&q8_full);
+          mbar_arrive(&q_empty);
+        }
         if (it > 0 && !epilogue(it - 1)) {
           ok = false;
           break;
@@ -575,7 +697,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       bool need = false;
       if (tsm < kH) {
         const float tmax = fmaxf(fmaxf(red_max[0][tsm], red_max[1][tsm]), fmaxf(red_max[2][tsm], red_max[3][tsm]));
-        const float cand = tmax * c;
+        const float cand = tmax * (kFp8 ? fh_sh[spc & 1][tsm] : c);
         const float mo = first ? -INFINITY : m_sh[tsm];
         float mn = mo, al = 1.f;
         if (cand > mo + kTau) {
@@ -587,46 +709,88 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         need = !first && al != 1.f;
       }
       const bool rescale = bar_red_or(2, kSoftThreads, need);
-      // probabilities (bf16, the value-product operand) and their row sums
-      uint32_t pk[16];
+      if constexpr (kFp8) {
+        // probabilities: fp32 row sums, E4M3 codes for the value product.
+        // P^T is K-major in the rope atom's slot: query row n holds the codes
+        // of the tile's 128 keys in one 128-byte row (rows in 1 KB groups of
+        // 8, 16-byte chunks XOR-swizzled by n % 8); this thread writes byte
+        // trow of rows col0 .. col0 + 31.
+        if (rescale) {
 #pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        const float4 mu = *reinterpret_cast<const float4*>(&m_sh[col0 + i]);
-        pk[i / 2] = pack_bf16(exp2f(fmaf(v[i + 0], c, -mu.x)), exp2f(fmaf(v[i + 1], c, -mu.y)));
-        pk[i / 2 + 1] = pack_bf16(exp2f(fmaf(v[i + 2], c, -mu.z)), exp2f(fmaf(v[i + 3], c, -mu.w)));
-      }
-      if (rescale) {
+          for (int i = 0; i < 32; i += 4) {
+            const float4 al = *reinterpret_cast<const float4*>(&alpha_sh[col0 + i]);
+            lp[i + 0] *= al.x;
+            lp[i + 1] *= al.y;
+            lp[i + 2] *= al.z;
+            lp[i + 3] *= al.w;
+          }
+        }
+        const float* fh = fh_sh[spc & 1];
+        unsigned char* pt = sKV + 4 * kSlotBytes;
+        const int kc = trow >> 4, kb = trow & 15;
+        auto put = [&](int n, uint32_t code) {
+          pt[(n >> 3) * 1024 + (n & 7) * 128 + ((kc ^ (n & 7)) << 4) + kb] = (unsigned char)code;
+        };
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
-          const float4 al = *reinterpret_cast<const float4*>(&alpha_sh[col0 + i]);
-          lp[i + 0] *= al.x;
-          lp[i + 1] *= al.y;
-          lp[i + 2] *= al.z;
-          lp[i + 3] *= al.w;
+          const float4 mu = *reinterpret_cast<const float4*>(&m_sh[col0 + i]);
+          const float4 f = *reinterpret_cast<const float4*>(&fh[col0 + i]);
+          const float p0 = exp2f(fmaf(v[i], f.x, -mu.x)), p1 = exp2f(fmaf(v[i + 1], f.y, -mu.y));
+          const float p2 = exp2f(fmaf(v[i + 2], f.z, -mu.z)), p3 = exp2f(fmaf(v[i + 3], f.w, -mu.w));
+          lp[i] += p0;
+          lp[i + 1] += p1;
+          lp[i + 2] += p2;
+          lp[i + 3] += p3;
+          const uint32_t c01 = e4m3x2(p0, p1), c23 = e4m3x2(p2, p3);
+          put(col0 + i, c01 & 0xFFu);
+          put(col0 + i + 1, c01 >> 8);
+          put(col0 + i + 2, c23 & 0xFFu);
+          put(col0 + i + 3, c23 >> 8);
+        }
+      } else {
+        // probabilities (bf16, the value-product operand) and their row sums
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float4 mu = *reinterpret_cast<const float4*>(&m_sh[col0 + i]);
+          pk[i / 2] = pack_bf16(exp2f(fmaf(v[i + 0], c, -mu.x)), exp2f(fmaf(v[i + 1], c, -mu.y)));
+          pk[i / 2 + 1] = pack_bf16(exp2f(fmaf(v[i + 2], c, -mu.z)), exp2f(fmaf(v[i + 3], c, -mu.w)));
+        }
+        if (rescale) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 al = *reinterpret_cast<const float4*>(&alpha_sh[col0 + i]);
+            lp[i + 0] *= al.x;
+            lp[i + 1] *= al.y;
+            lp[i + 2] *= al.z;
+            lp[i + 3] *= al.w;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          __nv_bfloat162 t = *reinterpret_cast<__nv_bfloat162*>(&pk[i]);
+          const float2 f = __bfloat1622float2(t);
+          lp[2 * i] += f.x;
+          lp[2 * i + 1] += f.y;
+        }
+        // P^T row into the rope atom's slot (its score product is done): a
+        // 128-byte row per key, 16-byte chunks XOR-swizzled by row
+        unsigned char* prow = sKV + 8 * kSlotBytes + trow * 128;
+        const int cbase = col0 >> 3;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const uint4 val = make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+          *reinterpret_cast<uint4*>(prow + (((cbase + cc) ^ (trow & 7)) << 4)) = val;
         }
       }
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        __nv_bfloat162 t = *reinterpret_cast<__nv_bfloat162*>(&pk[i]);
-        const float2 f = __bfloat1622float2(t);
-        lp[2 * i] += f.x;
-        lp[2 * i + 1] += f.y;
-      }
-      // P^T row into the rope atom's slot (its score product is done): a
-      // 128-byte row per key, 16-byte chunks XOR-swizzled by row
-      unsigned char* prow = sKV + 8 * kSlotBytes + trow * 128;
-      const int cbase = col0 >> 3;
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        const uint4 val = make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-        *reinterpret_cast<uint4*>(prow + (((cbase + cc) ^ (trow & 7)) << 4)) = val;
-      }
-      // Masked key rows inside the value product's last 16-key step: their
-      // probability is 0, but the latent row must be finite too.
-      const int z1 = (cur.k * kTile + kTile <= nkeys) ? kTile : (((nkeys - cur.k * kTile) + 15) & ~15);
+      // Masked key rows inside the value product's last K step (16 keys, 32
+      // for E4M3): their probability is 0, but the latent row must be finite too.
+      constexpr int kStep = kFp8 ? 32 : 16;
+      const int z1 = (cur.k * kTile + kTile <= nkeys) ? kTile : (((nkeys - cur.k * kTile) + kStep - 1) & ~(kStep - 1));
       if (!valid && trow < z1) {
+        constexpr int kHalfAtoms = kFp8 ? 2 : 4;  // latent atoms of this thread's half of the row
 #pragma unroll
-        for (int a = 4 * half; a < 4 * half + 4; ++a) {
+        for (int a = kHalfAtoms * half; a < kHalfAtoms * half + kHalfAtoms; ++a) {
           unsigned char* lr = sKV + a * kSlotBytes + trow * 128;
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc) *reinterpret_cast<uint4*>(lr + 16 * cc) = make_uint4(0, 0, 0, 0);
@@ -697,8 +861,9 @@ struct AbsorbParams {
   int do_qabs;            // 0: plan and rotary part only (qabs comes from the GEMM kernel)
   // L2 prefetch (small batches): the latent cache rows [0, T[b]) of every
   // sequence and the W_UV rows this CTA's combine counterpart will read
-  const __nv_bfloat16* Lc;
+  const unsigned char* Lc;  // latent rows of lat_row_bytes bytes (bf16 or E4M3)
   const __nv_bfloat16* Rc;
+  int lat_row_bytes;
   int prefetch;
   double theta[kDr / 2];  // RoPE frequencies rope_base^(-2j/qk_rope), from the host
   unsigned int* flags;
@@ -834,17 +999,17 @@ __global__ void __launch_bounds__(kAbsThreads, 2) absorb_kernel(const AbsorbPara
         const long long row = cache_row(p.pages, b, p.T_cap, (u / 9) * kTile, &bad_page);
         if (bad_page) continue;
         const int part = u % 9;
-        if (part < 8) l2_prefetch(p.Lc + (size_t)(row + 16 * part) * kDl, 16 * kDl * 2);
+        if (part < 8) l2_prefetch(p.Lc + (size_t)(row + 16 * part) * p.lat_row_bytes, 16 * p.lat_row_bytes);
         else l2_prefetch(p.Rc + (size_t)row * kDr, kTile * kDr * 2);
       }
       base += units;
     }
     for (int b = 0; !p.pages.table && b < p.B; ++b) {
       const int Tb = min(max(p.T[b], 0), p.T_cap);
-      const size_t lb = (size_t)Tb * kDl * 2, rb = (size_t)Tb * kDr * 2;
+      const size_t lb = (size_t)Tb * p.lat_row_bytes, rb = (size_t)Tb * kDr * 2;
       const size_t l0 = (lb * me / nblk) & ~(size_t)15, l1 = (lb * (me + 1) / nblk) & ~(size_t)15;
       const size_t r0 = (rb * me / nblk) & ~(size_t)15, r1 = (rb * (me + 1) / nblk) & ~(size_t)15;
-      const unsigned char* lbase = reinterpret_cast<const unsigned char*>(p.Lc + (size_t)b * p.T_cap * kDl);
+      const unsigned char* lbase = p.Lc + (size_t)b * p.T_cap * p.lat_row_bytes;
       const unsigned char* rbase = reinterpret_cast<const unsigned char*>(p.Rc + (size_t)b * p.T_cap * kDr);
       if (l1 > l0) l2_prefetch(lbase + l0, (uint32_t)(l1 - l0));
       if (r1 > r0) l2_prefetch(rbase + r0, (uint32_t)(r1 - r0));
@@ -1315,7 +1480,7 @@ cudaError_t set_smem_once(Kern kern, int bytes, std::atomic<unsigned long long>*
   return e;
 }
 
-std::atomic<unsigned long long> g_abs_attr[4] = {{0}, {0}, {0}, {0}}, g_attn_attr[2] = {{0}, {0}}, g_cmb_attr{0};
+std::atomic<unsigned long long> g_abs_attr[4] = {{0}, {0}, {0}, {0}}, g_attn_attr[3] = {{0}, {0}, {0}}, g_cmb_attr{0};
 
 Plan make_plan(int B, int S, int T_cap, int sparse_topk) {
   Plan pl{};
@@ -1380,6 +1545,7 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
 
   // 0. sparse: gather the selected key rows (plain launch: the absorb kernel,
   //    launched next with programmatic serialization, starts once it retires)
+  if (sparse && a.lat_fp8) return cudaErrorInvalidValue;
   if (sparse) {
     GatherParams gp{};
     gp.Lc = static_cast<const __nv_bfloat16*>(a.Lc);
@@ -1419,10 +1585,12 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   ap.sparse = sparse ? 1 : 0;
   const bool big = pl.R > kSmallRows;
   ap.do_qabs = big ? 0 : 1;
-  ap.Lc = static_cast<const __nv_bfloat16*>(a.Lc);
+  ap.Lc = static_cast<const unsigned char*>(a.Lc);
   ap.Rc = static_cast<const __nv_bfloat16*>(a.Rc);
+  ap.lat_row_bytes = a.lat_fp8 ? kDl : kDl * 2;
   // L2 prefetch on the small-batch path while the cache stays well inside L2
-  ap.prefetch = (!big && !sparse && (long long)B * a.T_cap * (kDl + kDr) * 2 <= (48ll << 20)) ? 1 : 0;
+  ap.prefetch =
+      (!big && !sparse && (long long)B * a.T_cap * (ap.lat_row_bytes + kDr * 2) <= (48ll << 20)) ? 1 : 0;
   ap.pages = sparse ? PageTable{} : a.pages;
   for (int j = 0; j < kDr / 2; ++j) ap.theta[j] = std::pow(g.rope_base, -2.0 * j / kDr);
   ap.flags = a.flags;
@@ -1468,7 +1636,9 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   bool maps_ok = make_tmap_2d_bf16(&tp.mQ, qcat, (uint64_t)pl.R * kH, kDc, kDc, kH, 64);
   if (!sparse) {
     const uint64_t rows = (uint64_t)pool_rows;
-    maps_ok = maps_ok && make_tmap_2d_bf16(&tp.mL, a.Lc, rows, kDl, kDl, kTile, 64) &&
+    maps_ok = maps_ok &&
+              (a.lat_fp8 ? make_tmap_2d_u8(&tp.mL, a.Lc, rows, kDl, kDl, kTile, 128)
+                         : make_tmap_2d_bf16(&tp.mL, a.Lc, rows, kDl, kDl, kTile, 64)) &&
               make_tmap_2d_bf16(&tp.mR, a.Rc, rows, kDr, kDr, kTile, 64);
     tp.kv_rows = a.T_cap;
   } else {
@@ -1495,17 +1665,19 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   tp.qsplit = pieces * 4 <= sms ? 4 : pieces * 2 <= sms ? 2 : 1;
   tp.read_once = ((sparse || S == 1) && tp.qsplit == 1) ? 1 : 0;
   tp.c = g.scale * kLog2e;
+  tp.lat_scale = a.lat_fp8 ? a.lat_scale : 1.f;
   tp.o_part = o_part;
   tp.ml_part = ml_part;
   tp.flags = a.flags;
   tp.wait_ns = a.wait_limit_ns;
   tp.pages = sparse ? PageTable{} : a.pages;
-  auto kern = sparse ? attn_kernel<true> : attn_kernel<false>;
-  e = set_smem_once(kern, (int)kAttnDynSmem, &g_attn_attr[sparse ? 1 : 0]);
+  auto kern = sparse ? attn_kernel<true> : a.lat_fp8 ? attn_kernel<false, true> : attn_kernel<false>;
+  const uint32_t attn_smem = a.lat_fp8 ? kAttn8DynSmem : kAttnDynSmem;
+  e = set_smem_once(kern, (int)attn_smem, &g_attn_attr[sparse ? 1 : a.lat_fp8 ? 2 : 0]);
   if (e != cudaSuccess) return e;
   const int nblk = pieces * tp.qsplit;
   kernel_mark(st, "attention");
-  e = launch_pdl(kern, dim3(nblk), dim3(kAttnThreads), kAttnDynSmem, st, tp);
+  e = launch_pdl(kern, dim3(nblk), dim3(kAttnThreads), attn_smem, st, tp);
   if (e != cudaSuccess) return e;
 
   // 3. merge of the splits and the W_UV lift

@@ -50,6 +50,8 @@ struct DecodeArgs {
   unsigned int* flags;
   long long wait_limit_ns;
   PageTable pages;  // table == nullptr: contiguous [B, T_cap] caches
+  int lat_fp8;      // Lc holds E4M3 codes (the FP8 cache); latent = lat_scale * code
+  float lat_scale;
 };
 
 cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, bool sparse, cudaStream_t st);
@@ -132,6 +134,8 @@ struct AppendArgs {
   unsigned int* flags;
   PageTable pages;
   double theta[kMaxRopePairs];
+  int lat_fp8;          // Lc receives E4M3 codes of the normalised row * lat_inv_scale
+  float lat_inv_scale;
 };
 cudaError_t launch_cache_append(const AppendArgs& a, int dtype, cudaStream_t st);
 

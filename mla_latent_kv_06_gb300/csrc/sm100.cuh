@@ -187,6 +187,16 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f8f6f4 (8-bit float inputs, fp32 accumulate).
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Instruction descriptor for kind::tf32 with fp32 D, both operands K-major.
 __host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N) {
   return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
@@ -288,6 +298,18 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
   return (1u << 4)                        // D format: f32
          | (1u << 7)                      // A format: bf16
          | (1u << 10)                     // B format: bf16
+         | ((uint32_t)a_mn << 15)         // A major
+         | ((uint32_t)b_mn << 16)         // B major
+         | ((uint32_t)(N >> 3) << 17)     // N / 8
+         | ((uint32_t)(M >> 4) << 24);    // M / 16
+}
+
+// Instruction descriptor for kind::f8f6f4 with E4M3 A/B (format code 0) and
+// fp32 D.  a_mn / b_mn: operand stored MN-major (1) or K-major (0).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4)                        // D format: f32
+         | (0u << 7)                      // A format: E4M3
+         | (0u << 10)                     // B format: E4M3
          | ((uint32_t)a_mn << 15)         // A major
          | ((uint32_t)b_mn << 16)         // B major
          | ((uint32_t)(N >> 3) << 17)     // N / 8

@@ -44,6 +44,23 @@ inline bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows,
   return r == CUDA_SUCCESS;
 }
 
+// 2D row-major byte tensor [rows][cols] (row pitch `pitch_bytes`, a multiple
+// of 16), box [box_rows][box_cols] (box_cols <= 128 for the 128-byte swizzle):
+// the E4M3 codes of an FP8 cache.  Rows past `rows` read as zero.
+inline bool make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t pitch_bytes,
+                            uint32_t box_rows, uint32_t box_cols) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {pitch_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 2D row-major fp32 tensor [rows][cols] (row pitch `pitch_elems`), box
 // [box_rows][box_cols] (box_cols * 4 <= 128 for the 128-byte swizzle).
 inline bool make_tmap_2d_f32(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t pitch_elems,

@@ -92,6 +92,25 @@ def test_host_rejects_bad_arguments_without_a_gpu(lib):
                                       None) == mla.MLA_ERR_INVALID
     assert lib.mla_decode_paged_workspace_size(ctypes.byref(d), 1, 1, 1, 2, 64) == 0  # not a multiple of 128
     assert lib.mla_decode_paged_workspace_size(ctypes.byref(d), 1, 1, 1, 2, 128) > 0
+    # FP8 cache: scale not positive / not finite, other geometries, page sizes off 128
+    tiny = mla.MlaDims(4, 16, 8, 32, 16, 0.0, 0.0)
+    for sc in (0.0, -1.0, float("inf"), float("nan")):
+        assert lib.mla_decode_fp8(ctypes.byref(d), 1, 1, p, p, p, sc, 16, p, p, p, None, 0,
+                                  None) == mla.MLA_ERR_INVALID
+        assert lib.mla_cache_append_fp8(ctypes.byref(d), 1, 1, p, p, 1e-6, sc, 8, p, p, p,
+                                        None) == mla.MLA_ERR_INVALID
+    assert lib.mla_cache_append_fp8(ctypes.byref(d), 1, 1, p, p, 1e-6, 1e-39, 8, p, p, p,
+                                    None) == mla.MLA_ERR_INVALID  # 1 / lat_scale overflows
+    assert lib.mla_decode_fp8(ctypes.byref(tiny), 1, 1, p, p, p, 0.01, 16, p, p, p, None, 0,
+                              None) == mla.MLA_ERR_UNSUPPORTED
+    assert lib.mla_decode_fp8(ctypes.byref(d), 1, 1, None, p, p, 0.01, 16, p, p, p, None, 0,
+                              None) == mla.MLA_ERR_INVALID
+    assert lib.mla_decode_fp8_paged(ctypes.byref(d), 1, 1, p, p, p, 0.01, 4, 64, p, 2, p, p, p, None, 0,
+                                    None) == mla.MLA_ERR_UNSUPPORTED
+    assert lib.mla_cache_append_fp8_paged(ctypes.byref(d), 1, 1, p, p, 1e-6, 0.01, p, p, 4, 128, None, 2, p,
+                                          None) == mla.MLA_ERR_INVALID
+    assert lib.mla_decode_fp8_workspace_size(ctypes.byref(tiny), 1, 1, 16) == 0
+    assert lib.mla_decode_fp8_workspace_size(ctypes.byref(d), 1, 1, 16) > 0
 
 
 def test_workspace_sizes_are_host_only(lib):

@@ -127,6 +127,27 @@ def mla_inputs(dims: Dims, B: int, S: int, T: Sequence[int], T_cap: int, dtype: 
     return dict(q=q, Lc=Lc, Rc=Rc, kv_b=kv_b, T=Tt)
 
 
+E4M3_NAN = 0x7F  # the positive NaN code of the FP8 format
+
+
+def fp8_latent_codes(B: int, T: Sequence[int], T_cap: int, kv_lora: int, seed: int, device="cpu") -> torch.Tensor:
+    """A synthetic FP8 latent cache ``[B, T_cap, kv_lora]`` uint8: random E4M3
+    bit patterns (uniform sign, exponent field 4..11, uniform mantissa), i.e.
+    magnitudes 2^-3 .. 2^4 * 1.875 before the cache scale.  Rows at positions
+    >= T[b] hold the NaN code, so that a kernel reading past a sequence's end
+    is caught."""
+    g = _gen(seed + 0x3000, device)
+    shape = (B, T_cap, kv_lora)
+    sign = torch.randint(0, 2, shape, generator=g, device=device, dtype=torch.int32) << 7
+    expo = torch.randint(4, 12, shape, generator=g, device=device, dtype=torch.int32) << 3
+    mant = torch.randint(0, 8, shape, generator=g, device=device, dtype=torch.int32)
+    codes = (sign | expo | mant).to(torch.uint8)
+    for b, t in enumerate(T):
+        if t < T_cap:
+            codes[b, t:] = E4M3_NAN
+    return codes
+
+
 def dsa_inputs(B: int, S: int, T: Sequence[int], T_cap: int, n_ih: int, index_hd: int,
                seed: int, device="cpu") -> Dict[str, torch.Tensor]:
     """Indexer query ``q_idx [B,S,n_ih,index_hd]``, head weights ``w [B,S,n_ih]``
