@@ -46,15 +46,17 @@ constexpr uint32_t kQAtomBytes = 8192;         // 64 rows x 64 bf16
 constexpr uint32_t kQBytes = 9 * kQAtomBytes;  // 73728
 constexpr uint32_t kKVBytes = 9 * kSlotBytes;  // 147456
 constexpr uint32_t kAttnDynSmem = kQBytes + kKVBytes + 1024;
-// FP8 latent cache: a key tile is four latent atoms of 128 keys x 128 E4M3
-// codes and the bf16 rope atom, 16 KB each; the query block holds the
-// quantised latent part (four 8 KB atoms of 64 rows x 128 codes) and the rope
-// part (bf16), built by the softmax warps from the bf16 qcat block, which
-// lands in a staging area of the bf16 layout.
-constexpr int kSlots8 = 5;
-constexpr uint32_t kQ8Bytes = 5 * kQAtomBytes;   // 40960
-constexpr uint32_t kKV8Bytes = 5 * kSlotBytes;   // 81920
-constexpr uint32_t kAttn8DynSmem = kQBytes + kQ8Bytes + kKV8Bytes + 1024;
+// FP8 latent cache (attn8_kernel): a key tile is four latent atoms of 128
+// keys x 128 E4M3 codes and the bf16 rope atom, 16 KB each, and two tiles are
+// resident; the query block is four 8 KB atoms of 64 rows x 128 codes and the
+// bf16 rope atom, loaded from the quantised query rows (640 bytes each: 512
+// codes, then 64 bf16).
+constexpr int kAtoms8 = 5;
+constexpr uint32_t kQ8Bytes = 5 * kQAtomBytes;     // 40960
+constexpr uint32_t kTile8Bytes = 5 * kSlotBytes;   // 81920
+constexpr uint32_t kAttn8DynSmem = kQ8Bytes + 2 * kTile8Bytes + 1024;
+constexpr int kQ8Row = kDl + 2 * kDr;              // 640 bytes
+constexpr uint32_t kTmemO8 = 128;  // FP8: S^T double-buffered (cols 0..127), then O^T
 constexpr int kSoftWarps = 8;
 constexpr int kSoftThreads = 32 * kSoftWarps;
 constexpr int kAttnThreads = 64 + kSoftThreads;
@@ -83,6 +85,7 @@ struct AttnParams {
                   // of the four 128-row blocks of O^T (the value product and its partial)
   float c;        // softmax scale * log2(e)
   float lat_scale;  // FP8 cache: latent row = lat_scale * E4M3 codes
+  const float* fh;  // FP8 cache: per query row, c * lat_scale * the row's quantisation scale
   float* o_part;
   float* ml_part;
   unsigned int* flags;
@@ -251,69 +254,6 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
 }
 
-// FP8 cache: quantise a piece's query block.  Thread tsm (0..255) takes query
-// row r = tsm / 4 and quarter qq = tsm % 4: latent columns 128 qq .. 128 qq +
-// 127 become E4M3 codes with the row's scale sq = amax / 448 (one 128-byte row
-// of latent atom qq of sQ8), and rope values 16 qq .. 16 qq + 15 become bf16
-// divided by lat_scale * sq, so that one fp32 accumulator holds
-// (qabs . Lc + q_rot . Rc) / (lat_scale * sq).  fh[r] = c * lat_scale * sq
-// turns it back into the score in log2 units.  Staging and sQ8 use the same
-// 128-byte-swizzled K-major rows (16-byte chunk index XOR row % 8).
-__device__ __forceinline__ void quantise_q(const unsigned char* sQ, unsigned char* sQ8, float* fh, int tsm, float c,
-                                           float lat_scale) {
-  const int r = tsm >> 2, qq = tsm & 3, sw = r & 7;
-  // the 128 latent values of this thread: 16 chunks of 8 bf16 (chunk i: atom
-  // 2 qq + i / 8, chunk i % 8 of the row)
-  auto chunk = [&](int i) -> uint4 {
-    return *reinterpret_cast<const uint4*>(sQ + (2 * qq + (i >> 3)) * kQAtomBytes + r * 128 + (((i & 7) ^ sw) << 4));
-  };
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    uint4 v = chunk(i);
-    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const float2 f = __bfloat1622float2(b2[t]);
-      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-    }
-  }
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-  const float sq = amax > 0.f ? amax * (1.f / 448.f) : 1.f;
-  const float inv = amax > 0.f ? 448.f / amax : 1.f;
-  // 16 codes (one 16-byte chunk of the E4M3 row) from two bf16 chunks
-#pragma unroll
-  for (int cc = 0; cc < 8; ++cc) {
-    uint32_t code[4];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint4 v = chunk(2 * cc + h);
-      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&v);
-      const float2 f0 = __bfloat1622float2(b2[0]), f1 = __bfloat1622float2(b2[1]);
-      const float2 f2 = __bfloat1622float2(b2[2]), f3 = __bfloat1622float2(b2[3]);
-      code[2 * h] = e4m3x2(f0.x * inv, f0.y * inv) | (e4m3x2(f1.x * inv, f1.y * inv) << 16);
-      code[2 * h + 1] = e4m3x2(f2.x * inv, f2.y * inv) | (e4m3x2(f3.x * inv, f3.y * inv) << 16);
-    }
-    *reinterpret_cast<uint4*>(sQ8 + qq * kQAtomBytes + r * 128 + ((cc ^ sw) << 4)) =
-        make_uint4(code[0], code[1], code[2], code[3]);
-  }
-  const float rs = 1.f / (lat_scale * sq);
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int cc = 2 * qq + h;
-    uint4 v = *reinterpret_cast<const uint4*>(sQ + 8 * kQAtomBytes + r * 128 + ((cc ^ sw) << 4));
-    __nv_bfloat162* b2 = reinterpret_cast<__nv_bfloat162*>(&v);
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const float2 f = __bfloat1622float2(b2[t]);
-      b2[t] = __floats2bfloat162_rn(f.x * rs, f.y * rs);
-    }
-    *reinterpret_cast<uint4*>(sQ8 + 4 * kQAtomBytes + r * 128 + ((cc ^ sw) << 4)) = v;
-  }
-  if (qq == 0) fh[r] = c * lat_scale * sq;
-}
-
 // ===========================================================================
 // Attention kernel
 //
@@ -327,20 +267,16 @@ __device__ __forceinline__ void quantise_q(const unsigned char* sQ, unsigned cha
 // the next tile's loads start while it still runs, and the next score product
 // accumulates atom by atom as they land.
 // ===========================================================================
-template <bool kSparse, bool kFp8 = false>
+template <bool kSparse>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
-  static_assert(!(kSparse && kFp8), "the FP8 cache has no sparse path");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
-  unsigned char* sQ = smem;                // bf16 query block (FP8: its staging copy)
-  unsigned char* sQ8 = smem + kQBytes;     // FP8: quantised query block
-  unsigned char* sKV = smem + kQBytes + (kFp8 ? kQ8Bytes : 0);
-  constexpr int nslots = kFp8 ? kSlots8 : kSlots;
+  unsigned char* sQ = smem;
+  unsigned char* sKV = smem + kQBytes;
 
   __shared__ uint64_t full_bar[kSlots], empty_bar[kSlots];
-  __shared__ uint64_t q_full, q_empty, q8_full, s_full, s_free, p_full, o_done, mma_done, o_blk[4];
-  __shared__ __align__(16) float fh_sh[2][kH];  // FP8: per query row score factor, by piece parity
+  __shared__ uint64_t q_full, q_empty, s_full, s_free, p_full, o_done, mma_done, o_blk[4];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ __align__(16) float red_max[4][kH];
@@ -364,8 +300,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       mbar_init(&empty_bar[i], 1);
     }
     mbar_init(&q_full, 1);
-    mbar_init(&q_empty, kFp8 ? kSoftThreads : 1);  // FP8: freed once the softmax warps quantised it
-    mbar_init(&q8_full, kSoftThreads);
+    mbar_init(&q_empty, 1);
     mbar_init(&s_full, 1);
     mbar_init(&s_free, kSoftThreads);
     mbar_init(&p_full, kSoftThreads);
@@ -448,13 +383,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           if (bad_page) raise_flag(p.flags, MLA_DEV_BAD_INDEX);
         }
         const uint32_t par = (it & 1) ^ 1;
-        for (int a = 0; a < nslots && ok; ++a) {
+        for (int a = 0; a < kSlots && ok; ++a) {
           ok = mbar_wait(&empty_bar[a], par, abort, p.flags, p.wait_ns);
           if (!ok) break;
           mbar_arrive_expect_tx(&full_bar[a], kSlotBytes);
-          const bool lat = a < nslots - 1;
-          const CUtensorMap* map = lat ? &p.mL : &p.mR;
-          const int x = lat ? (kFp8 ? 128 * a : 64 * a) : 0;
+          const CUtensorMap* map = a < 8 ? &p.mL : &p.mR;
+          const int x = a < 8 ? 64 * a : 0;
           if (p.read_once) tma_load_2d_hint(sKV + a * kSlotBytes, map, x, y, &full_bar[a], pol_once);
           else tma_load_2d(sKV + a * kSlotBytes, map, x, y, &full_bar[a]);
           last_it[a] = it;
@@ -487,9 +421,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     // ------------------------------------------------------------ MMA issuer (whole warp waits, lane 0 issues)
     const uint32_t idS = idesc_bf16_f32(128, 64, 0, 0);
     const uint32_t idO = idesc_bf16_f32(128, 64, 1, 1);
-    const uint32_t idS8 = idesc_e4m3_f32(128, 64, 0, 0);
-    const uint32_t idO8 = idesc_e4m3_f32(128, 64, 1, 0);
-    const uint32_t kv0 = smem_u32(sKV), q0 = smem_u32(kFp8 ? sQ8 : sQ);
+    const uint32_t kv0 = smem_u32(sKV), q0 = smem_u32(sQ);
     TileCursor<kSparse> c;
     c.start(p, ts, NR, N, g, s, row0);
     int it = 0, pc = -1;
@@ -501,27 +433,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     while (ok && c.live) {
       const bool first = c.first();
       // keys of this tile, read now so that the load overlaps the waits below
-      const int tkeys = tile_keys<kSparse>(p, c.row, s, c.k);
-      const int ksteps = kFp8 ? (tkeys + 31) >> 5 : (tkeys + 15) >> 4;
+      const int ksteps = (tile_keys<kSparse>(p, c.row, s, c.k) + 15) >> 4;
       if (first) {
         ++pc;
-        ok = wait(kFp8 ? &q8_full : &q_full, pc & 1);
+        ok = wait(&q_full, pc & 1);
       }
       ok = ok && wait(&s_free, (it & 1) ^ 1);
       if (!ok) break;
       tc_fence_after();
-      for (int a = 0; a < nslots && ok; ++a) {
+      for (int a = 0; a < kSlots && ok; ++a) {
         ok = wait(&full_bar[a], it & 1);
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
-          // 32 bytes of K per instruction: 16 bf16 or 32 E4M3 values
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t da = smem_desc_sw128(kv0 + a * kSlotBytes + kk * 32, 16, 1024);
             const uint64_t db = smem_desc_sw128(q0 + a * kQAtomBytes + kk * 32, 16, 1024);
-            if (kFp8 && a < nslots - 1) mma_f8(tmem + kTmemS, da, db, idS8, (a | kk) != 0 ? 1u : 0u);
-            else mma_bf16(tmem + kTmemS, da, db, idS, (a | kk) != 0 ? 1u : 0u);
+            mma_bf16(tmem + kTmemS, da, db, idS, (a | kk) != 0 ? 1u : 0u);
           }
         }
         __syncwarp();
@@ -530,29 +459,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       if (!ok) break;
       if (lane == 0) {
         mma_commit(&s_full);
-        if (!kFp8 && c.last()) mma_commit(&q_empty);
+        if (c.last()) mma_commit(&q_empty);
       }
       __syncwarp();
       ok = wait(&p_full, it & 1);
       if (!ok) break;
       tc_fence_after();
-      if (kFp8 && lane == 0) {
-        // O^T block m = latent atom m (MN-major, 32 keys = 4 KB per step) x P^T
-        // (K-major E4M3 in the rope atom's slot)
-        for (int m = 0; m < 4; ++m)
-          if (m < mb0 || m >= mb1) mma_commit(&empty_bar[m]);
-        for (int m = mb0; m < mb1; ++m) {
-          for (int kk = 0; kk < ksteps; ++kk) {
-            const uint64_t da = smem_desc_sw128(kv0 + m * kSlotBytes + kk * 4096, kSlotBytes, 1024);
-            const uint64_t db = smem_desc_sw128(kv0 + 4 * kSlotBytes + kk * 32, 16, 1024);
-            mma_f8(tmem + kTmemO + 64 * m, da, db, idO8, (kk > 0 || !first) ? 1u : 0u);
-          }
-          mma_commit(&empty_bar[m]);
-          mma_commit(&o_blk[m]);
-        }
-        mma_commit(&empty_bar[4]);
-        mma_commit(&o_done);
-      } else if (lane == 0) {
+      if (lane == 0) {
         // latent atoms of the blocks another part owns: free once the score product retired
         for (int m = 0; m < 4; ++m)
           if (m < mb0 || m >= mb1) {
@@ -594,7 +507,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     const float c = p.c;
     TileCursor<kSparse> cur;
     cur.start(p, ts, NR, N, g, s, row0);
-    int it = 0, slot = 0, pos = 0, nkeys = 0, spc = -1;
+    int it = 0, slot = 0, pos = 0, nkeys = 0;
     const int32_t* srow = nullptr;
     bool ok = true, bad_idx = false;
     float lp[32];
@@ -624,8 +537,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         const float l = red_sum[0][tsm] + red_sum[1][tsm] + red_sum[2][tsm] + red_sum[3][tsm];
         float* ml = p.ml_part + ((size_t)slot * kH + tsm) * 2;
         ml[0] = m_sh[tsm];
-        // FP8: O^T summed codes; dividing l by lat_scale puts the scale back
-        ml[1] = bad ? __int_as_float(0x7fc00000) : (kFp8 ? l / p.lat_scale : l);
+        ml[1] = bad ? __int_as_float(0x7fc00000) : l;
       }
       if (bad && tsm == 0 && part == 0) raise_flag(p.flags, MLA_DEV_BAD_INDEX);
       return true;
@@ -634,20 +546,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     while (ok && cur.live) {
       const bool first = cur.first();
       if (first) {
-        if constexpr (kFp8) {
-          // quantise the new piece's query block first, so that its score
-          // product can start while the previous piece's partial is written
-          ++spc;
-          const bool qfail = !mbar_wait(&q_full, spc & 1, abort, p.flags, p.wait_ns);
-          if (bar_red_or(1, kSoftThreads, qfail)) {
-            ok = false;
-            break;
-          }
-          quantise_q(sQ, sQ8, fh_sh[spc & 1], tsm, c, p.lat_scale);
-          fence_proxy_async_smem();
-          mbar_arrive(&q8_full);
-          mbar_arrive(&q_empty);
-        }
         if (it > 0 && !epilogue(it - 1)) {
           ok = false;
           break;
@@ -697,7 +595,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       bool need = false;
       if (tsm < kH) {
         const float tmax = fmaxf(fmaxf(red_max[0][tsm], red_max[1][tsm]), fmaxf(red_max[2][tsm], red_max[3][tsm]));
-        const float cand = tmax * (kFp8 ? fh_sh[spc & 1][tsm] : c);
+        const float cand = tmax * c;
         const float mo = first ? -INFINITY : m_sh[tsm];
         float mn = mo, al = 1.f;
         if (cand > mo + kTau) {
@@ -709,88 +607,46 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         need = !first && al != 1.f;
       }
       const bool rescale = bar_red_or(2, kSoftThreads, need);
-      if constexpr (kFp8) {
-        // probabilities: fp32 row sums, E4M3 codes for the value product.
-        // P^T is K-major in the rope atom's slot: query row n holds the codes
-        // of the tile's 128 keys in one 128-byte row (rows in 1 KB groups of
-        // 8, 16-byte chunks XOR-swizzled by n % 8); this thread writes byte
-        // trow of rows col0 .. col0 + 31.
-        if (rescale) {
+      // probabilities (bf16, the value-product operand) and their row sums
+      uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const float4 al = *reinterpret_cast<const float4*>(&alpha_sh[col0 + i]);
-            lp[i + 0] *= al.x;
-            lp[i + 1] *= al.y;
-            lp[i + 2] *= al.z;
-            lp[i + 3] *= al.w;
-          }
-        }
-        const float* fh = fh_sh[spc & 1];
-        unsigned char* pt = sKV + 4 * kSlotBytes;
-        const int kc = trow >> 4, kb = trow & 15;
-        auto put = [&](int n, uint32_t code) {
-          pt[(n >> 3) * 1024 + (n & 7) * 128 + ((kc ^ (n & 7)) << 4) + kb] = (unsigned char)code;
-        };
+      for (int i = 0; i < 32; i += 4) {
+        const float4 mu = *reinterpret_cast<const float4*>(&m_sh[col0 + i]);
+        pk[i / 2] = pack_bf16(exp2f(fmaf(v[i + 0], c, -mu.x)), exp2f(fmaf(v[i + 1], c, -mu.y)));
+        pk[i / 2 + 1] = pack_bf16(exp2f(fmaf(v[i + 2], c, -mu.z)), exp2f(fmaf(v[i + 3], c, -mu.w)));
+      }
+      if (rescale) {
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
-          const float4 mu = *reinterpret_cast<const float4*>(&m_sh[col0 + i]);
-          const float4 f = *reinterpret_cast<const float4*>(&fh[col0 + i]);
-          const float p0 = exp2f(fmaf(v[i], f.x, -mu.x)), p1 = exp2f(fmaf(v[i + 1], f.y, -mu.y));
-          const float p2 = exp2f(fmaf(v[i + 2], f.z, -mu.z)), p3 = exp2f(fmaf(v[i + 3], f.w, -mu.w));
-          lp[i] += p0;
-          lp[i + 1] += p1;
-          lp[i + 2] += p2;
-          lp[i + 3] += p3;
-          const uint32_t c01 = e4m3x2(p0, p1), c23 = e4m3x2(p2, p3);
-          put(col0 + i, c01 & 0xFFu);
-          put(col0 + i + 1, c01 >> 8);
-          put(col0 + i + 2, c23 & 0xFFu);
-          put(col0 + i + 3, c23 >> 8);
-        }
-      } else {
-        // probabilities (bf16, the value-product operand) and their row sums
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 mu = *reinterpret_cast<const float4*>(&m_sh[col0 + i]);
-          pk[i / 2] = pack_bf16(exp2f(fmaf(v[i + 0], c, -mu.x)), exp2f(fmaf(v[i + 1], c, -mu.y)));
-          pk[i / 2 + 1] = pack_bf16(exp2f(fmaf(v[i + 2], c, -mu.z)), exp2f(fmaf(v[i + 3], c, -mu.w)));
-        }
-        if (rescale) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const float4 al = *reinterpret_cast<const float4*>(&alpha_sh[col0 + i]);
-            lp[i + 0] *= al.x;
-            lp[i + 1] *= al.y;
-            lp[i + 2] *= al.z;
-            lp[i + 3] *= al.w;
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          __nv_bfloat162 t = *reinterpret_cast<__nv_bfloat162*>(&pk[i]);
-          const float2 f = __bfloat1622float2(t);
-          lp[2 * i] += f.x;
-          lp[2 * i + 1] += f.y;
-        }
-        // P^T row into the rope atom's slot (its score product is done): a
-        // 128-byte row per key, 16-byte chunks XOR-swizzled by row
-        unsigned char* prow = sKV + 8 * kSlotBytes + trow * 128;
-        const int cbase = col0 >> 3;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const uint4 val = make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-          *reinterpret_cast<uint4*>(prow + (((cbase + cc) ^ (trow & 7)) << 4)) = val;
+          const float4 al = *reinterpret_cast<const float4*>(&alpha_sh[col0 + i]);
+          lp[i + 0] *= al.x;
+          lp[i + 1] *= al.y;
+          lp[i + 2] *= al.z;
+          lp[i + 3] *= al.w;
         }
       }
-      // Masked key rows inside the value product's last K step (16 keys, 32
-      // for E4M3): their probability is 0, but the latent row must be finite too.
-      constexpr int kStep = kFp8 ? 32 : 16;
-      const int z1 = (cur.k * kTile + kTile <= nkeys) ? kTile : (((nkeys - cur.k * kTile) + kStep - 1) & ~(kStep - 1));
-      if (!valid && trow < z1) {
-        constexpr int kHalfAtoms = kFp8 ? 2 : 4;  // latent atoms of this thread's half of the row
 #pragma unroll
-        for (int a = kHalfAtoms * half; a < kHalfAtoms * half + kHalfAtoms; ++a) {
+      for (int i = 0; i < 16; ++i) {
+        __nv_bfloat162 t = *reinterpret_cast<__nv_bfloat162*>(&pk[i]);
+        const float2 f = __bfloat1622float2(t);
+        lp[2 * i] += f.x;
+        lp[2 * i + 1] += f.y;
+      }
+      // P^T row into the rope atom's slot (its score product is done): a
+      // 128-byte row per key, 16-byte chunks XOR-swizzled by row
+      unsigned char* prow = sKV + 8 * kSlotBytes + trow * 128;
+      const int cbase = col0 >> 3;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const uint4 val = make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+        *reinterpret_cast<uint4*>(prow + (((cbase + cc) ^ (trow & 7)) << 4)) = val;
+      }
+      // Masked key rows inside the value product's last 16-key step: their
+      // probability is 0, but the latent row must be finite too.
+      const int z1 = (cur.k * kTile + kTile <= nkeys) ? kTile : (((nkeys - cur.k * kTile) + 15) & ~15);
+      if (!valid && trow < z1) {
+#pragma unroll
+        for (int a = 4 * half; a < 4 * half + 4; ++a) {
           unsigned char* lr = sKV + a * kSlotBytes + trow * 128;
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc) *reinterpret_cast<uint4*>(lr + 16 * cc) = make_uint4(0, 0, 0, 0);
@@ -819,6 +675,524 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
               w[i + 3] *= al.w;
             }
             tmem_st32(tmem + t_lane + kTmemO + 64 * m + col0, w);
+          }
+          tmem_wait_st();
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&p_full);
+      ++it;
+      cur.next(p, ts, NR, N, g, s);
+    }
+    if (ok && it > 0) epilogue(it - 1);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ===========================================================================
+// FP8 query quantiser: one warp per query row (r, h) of qcat.  The 512
+// absorbed values become E4M3 codes with the row's scale sq = amax / 448; the
+// 64 rope values become bf16 divided by lat_scale * sq, so that one fp32
+// accumulator of the FP8 attention holds (qabs . Lc + q_rot . Rc) / (lat_scale
+// * sq); fh[row] = c * lat_scale * sq turns it back into the score in log2
+// units.  Output rows of 640 bytes: the codes, then the rope values.
+// ===========================================================================
+struct QuantParams {
+  const __nv_bfloat16* qcat;  // [rows, 576]
+  unsigned char* q8;          // [rows, 640]
+  float* fh;                  // [rows]
+  int rows;
+  float c, lat_scale;
+};
+
+__global__ void __launch_bounds__(256) quant_q_kernel(const QuantParams p) {
+  grid_dep_wait();  // qcat comes from the absorb kernels
+  grid_dep_launch();
+  const int w = (int)((blockIdx.x * 256u + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+  if (w >= p.rows) return;
+  const __nv_bfloat16* src = p.qcat + (size_t)w * kDc;
+  uint4 raw[2];
+  raw[0] = *reinterpret_cast<const uint4*>(src + 16 * lane);
+  raw[1] = *reinterpret_cast<const uint4*>(src + 16 * lane + 8);
+  const uint32_t rp = *reinterpret_cast<const uint32_t*>(src + kDl + 2 * lane);
+  float v[16];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw[h]);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float2 f = __bfloat1622float2(b2[t]);
+      v[8 * h + 2 * t] = f.x;
+      v[8 * h + 2 * t + 1] = f.y;
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float sq = amax > 0.f ? amax * (1.f / 448.f) : 1.f;
+  const float inv = amax > 0.f ? 448.f / amax : 1.f;
+  uint32_t code[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    code[i] = e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv) | (e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv) << 16);
+  unsigned char* dst = p.q8 + (size_t)w * kQ8Row;
+  *reinterpret_cast<uint4*>(dst + 16 * lane) = make_uint4(code[0], code[1], code[2], code[3]);
+  const float rs = 1.f / (p.lat_scale * sq);
+  __nv_bfloat162 r2 = *reinterpret_cast<const __nv_bfloat162*>(&rp);
+  const float2 rf = __bfloat1622float2(r2);
+  r2 = __floats2bfloat162_rn(rf.x * rs, rf.y * rs);
+  *reinterpret_cast<__nv_bfloat162*>(dst + kDl + 4 * lane) = r2;  // bytes 512.. : the rope values
+  if (lane == 0) p.fh[w] = p.c * p.lat_scale * sq;
+}
+
+// ===========================================================================
+// FP8 attention kernel (latent cache of E4M3 codes with one cache scale).
+//
+// The products of attn_kernel on kind::f8f6f4 MMAs (32 codes of K per
+// instruction: half the instructions per tile):
+//   S^T[128 keys x 64 rows]  = [Lc codes | Rc] tile x q8^T   (K = 512 codes, then 64 bf16)
+//   O^T[512 x 64 rows]      += Lc codes^T x P^T                (K = keys, P as E4M3 codes)
+// Half-size tiles leave room for two key-tile buffers, and TMEM holds two score
+// accumulators: the MMA warp issues the score product of tile j before the
+// value product of tile j - 1, so the tensor pipe computes the next scores
+// while the softmax warps turn the current ones into probabilities, and tile
+// j + 1 loads while tile j is in use.  The row sum l stays fp32; the partial's
+// l is divided by lat_scale, which puts the cache scale back.
+// ===========================================================================
+__global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                         ~static_cast<uintptr_t>(1023));
+  unsigned char* sQ8 = smem;
+  unsigned char* sKV = smem + kQ8Bytes;  // buffer u at sKV + u * kTile8Bytes
+
+  __shared__ uint64_t full_bar[2][kAtoms8], empty_bar[2][kAtoms8];
+  __shared__ uint64_t q_full, q_empty, s_full[2], s_free[2], p_full, o_done, mma_done, o_blk[4];
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+  __shared__ __align__(16) float red_max[4][kH];
+  __shared__ __align__(16) float red_sum[4][kH];
+  __shared__ __align__(16) float m_sh[kH];
+  __shared__ __align__(16) float alpha_sh[kH];
+  __shared__ __align__(16) float fh_sh[2][kH];
+  __shared__ int plan_ts[kPlanMax + 1];
+  __shared__ int plan_wsum[kAttnThreads / 32];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = p.S;
+  const int part = (int)blockIdx.x % p.qsplit, brow = (int)blockIdx.x / p.qsplit;
+  const int g = brow / S, s = brow % S;
+  const int mb0 = part * (4 / p.qsplit), mb1 = mb0 + 4 / p.qsplit;
+
+  if (threadIdx.x == 0) {
+    for (int u = 0; u < 2; ++u)
+      for (int a = 0; a < kAtoms8; ++a) {
+        mbar_init(&full_bar[u][a], 1);
+        mbar_init(&empty_bar[u][a], 1);
+      }
+    mbar_init(&q_full, 1);
+    mbar_init(&q_empty, 1);
+    for (int u = 0; u < 2; ++u) {
+      mbar_init(&s_full[u], 1);
+      mbar_init(&s_free[u], kSoftThreads);
+    }
+    mbar_init(&p_full, kSoftThreads);
+    mbar_init(&o_done, 1);
+    for (int m = 0; m < 4; ++m) mbar_init(&o_blk[m], 1);
+    mbar_init(&mma_done, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&p.mQ);
+    prefetch_tensormap(&p.mL);
+    prefetch_tensormap(&p.mR);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  volatile int* abort = &abort_flag;
+  grid_dep_launch();
+
+  // Tile plan, as in attn_kernel.
+  const int NR = p.B;
+  const bool local_plan = NR <= kPlanMax;
+  const int32_t* ts = p.tile_start;
+  if (local_plan) {
+    int carry = 0;
+    for (int base = 0; base < NR; base += kAttnThreads) {
+      const int r = base + threadIdx.x;
+      int x = r < NR ? row_tiles<false>(p, r) : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) plan_wsum[warp] = x;
+      __syncthreads();
+      int off = carry;
+      for (int i = 0; i < warp; ++i) off += plan_wsum[i];
+      if (r < NR) plan_ts[r + 1] = off + x;
+      int tot = 0;
+      for (int i = 0; i < kAttnThreads / 32; ++i) tot += plan_wsum[i];
+      carry += tot;
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) plan_ts[0] = 0;
+    __syncthreads();
+    ts = plan_ts;
+  } else {
+    grid_dep_wait();
+  }
+  const long long N = ts[NR];
+  const long long c0 = chunk_begin(N, g, p.G);
+  const int row0 = first_row(ts, NR, c0);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_once = l2_policy_evict_first();
+      TileCursor<false> c;
+      c.start(p, ts, NR, N, g, s, row0);
+      int it = 0, pc = -1, last_it[2][kAtoms8], last_q = -1;
+      for (int u = 0; u < 2; ++u)
+        for (int a = 0; a < kAtoms8; ++a) last_it[u][a] = -1;
+      bool ok = true, dep_waited = !local_plan;
+      // First cache row of a tile (the tile's 128 rows lie in one page).
+      auto tile_y = [&](const TileCursor<false>& t, bool* bad_page) -> int {
+        *bad_page = false;
+        if (!p.pages.table) return t.row * p.kv_rows + t.k * kTile;
+        return (int)cache_row(p.pages, t.row, p.T_cap, t.k * kTile, bad_page);
+      };
+      while (ok && c.live) {
+        const bool first = c.first();
+        if (first) ++pc;
+        bool bad_page;
+        const int y = tile_y(c, &bad_page);
+        if (bad_page) raise_flag(p.flags, MLA_DEV_BAD_INDEX);
+        const int u = it & 1;
+        const uint32_t par = ((it >> 1) & 1) ^ 1;
+        unsigned char* tile = sKV + u * kTile8Bytes;
+        for (int a = 0; a < kAtoms8 && ok; ++a) {
+          ok = mbar_wait(&empty_bar[u][a], par, abort, p.flags, p.wait_ns);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&full_bar[u][a], kSlotBytes);
+          const CUtensorMap* map = a < 4 ? &p.mL : &p.mR;
+          const int x = a < 4 ? 128 * a : 0;
+          if (p.read_once) tma_load_2d_hint(tile + a * kSlotBytes, map, x, y, &full_bar[u][a], pol_once);
+          else tma_load_2d(tile + a * kSlotBytes, map, x, y, &full_bar[u][a]);
+          last_it[u][a] = it;
+        }
+        if (ok && first) {  // the piece's quantised query block
+          if (!dep_waited) {
+            grid_dep_wait();  // q8 comes from the quantiser
+            dep_waited = true;
+          }
+          ok = mbar_wait(&q_empty, (pc & 1) ^ 1, abort, p.flags, p.wait_ns);
+          if (ok) {
+            mbar_arrive_expect_tx(&q_full, kQ8Bytes);
+            const int qrow = c.row * S + s;
+            for (int a = 0; a < kAtoms8; ++a) tma_load_2d(sQ8 + a * kQAtomBytes, &p.mQ, 128 * a, qrow * kH, &q_full);
+            last_q = pc;
+          }
+        }
+        ++it;
+        c.next(p, ts, NR, N, g, s);
+      }
+      // Never leave with copies in flight: wait for the last load of each slot.
+      volatile int no_abort = 0;
+      const long long drain_ns = p.wait_ns > kDrainNs ? p.wait_ns : kDrainNs;
+      for (int u = 0; u < 2; ++u)
+        for (int a = 0; a < kAtoms8; ++a)
+          if (last_it[u][a] >= 0)
+            mbar_wait(&full_bar[u][a], (last_it[u][a] >> 1) & 1, &no_abort, p.flags, drain_ns);
+      if (last_q >= 0) mbar_wait(&q_full, last_q & 1, &no_abort, p.flags, drain_ns);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (whole warp waits, lane 0 issues)
+    const uint32_t idS = idesc_bf16_f32(128, 64, 0, 0);
+    const uint32_t idS8 = idesc_e4m3_f32(128, 64, 0, 0);
+    const uint32_t idO8 = idesc_e4m3_f32(128, 64, 1, 0);
+    const uint32_t kv0 = smem_u32(sKV), q0 = smem_u32(sQ8);
+    TileCursor<false> c;
+    c.start(p, ts, NR, N, g, s, row0);
+    int it = 0, pc = -1;
+    bool ok = true, issued = false;
+    auto wait = [&](uint64_t* bar, uint32_t par) -> bool {
+      const bool r = mbar_wait(bar, par, abort, p.flags, p.wait_ns);
+      return __all_sync(0xffffffffu, r);
+    };
+    // Value product of tile j: O^T block m = latent atom m (MN-major, 32 keys =
+    // 4 KB per step) x P^T (K-major codes in the tile's rope slot).
+    auto value = [&](int j, int ksteps, bool firstj) -> bool {
+      if (!wait(&p_full, j & 1)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        const int u = j & 1;
+        const uint32_t base = kv0 + u * kTile8Bytes;
+        for (int m = 0; m < 4; ++m)
+          if (m < mb0 || m >= mb1) mma_commit(&empty_bar[u][m]);  // another part's block: free now
+        for (int m = mb0; m < mb1; ++m) {
+          for (int kk = 0; kk < ksteps; ++kk) {
+            const uint64_t da = smem_desc_sw128(base + m * kSlotBytes + kk * 4096, kSlotBytes, 1024);
+            const uint64_t db = smem_desc_sw128(base + 4 * kSlotBytes + kk * 32, 16, 1024);
+            mma_f8(tmem + kTmemO8 + 64 * m, da, db, idO8, (kk > 0 || !firstj) ? 1u : 0u);
+          }
+          mma_commit(&empty_bar[u][m]);
+          mma_commit(&o_blk[m]);  // the epilogue may read this block while the next ones run
+        }
+        mma_commit(&empty_bar[u][4]);
+        mma_commit(&o_done);
+      }
+      __syncwarp();
+      return true;
+    };
+    bool pend = false, pend_first = false;
+    int pend_it = 0, pend_ks = 0;
+    while (ok && c.live) {
+      const bool first = c.first();
+      const int ksteps = (tile_keys<false>(p, c.row, s, c.k) + 31) >> 5;
+      const int u = it & 1;
+      if (first) {
+        ++pc;
+        ok = wait(&q_full, pc & 1);
+      }
+      ok = ok && wait(&s_free[u], ((it >> 1) & 1) ^ 1);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t base = kv0 + u * kTile8Bytes;
+      for (int a = 0; a < kAtoms8 && ok; ++a) {
+        ok = wait(&full_bar[u][a], (it >> 1) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          // 32 bytes of K per instruction: 32 codes, or 16 bf16 for the rope atom
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t da = smem_desc_sw128(base + a * kSlotBytes + kk * 32, 16, 1024);
+            const uint64_t db = smem_desc_sw128(q0 + a * kQAtomBytes + kk * 32, 16, 1024);
+            if (a < 4) mma_f8(tmem + kTmemS + 64 * u, da, db, idS8, (a | kk) != 0 ? 1u : 0u);
+            else mma_bf16(tmem + kTmemS + 64 * u, da, db, idS, 1u);
+          }
+        }
+        __syncwarp();
+        issued = true;
+      }
+      if (!ok) break;
+      if (lane == 0) {
+        mma_commit(&s_full[u]);
+        if (c.last()) mma_commit(&q_empty);
+      }
+      __syncwarp();
+      // the previous tile's value product, queued behind this tile's scores
+      if (pend && !(ok = value(pend_it, pend_ks, pend_first))) break;
+      pend = true;
+      pend_it = it;
+      pend_ks = ksteps;
+      pend_first = first;
+      ++it;
+      c.next(p, ts, NR, N, g, s);
+    }
+    if (ok && pend) value(pend_it, pend_ks, pend_first);
+    if (issued) {  // all MMAs retired before TMEM is released
+      if (lane == 0) mma_commit(&mma_done);
+      __syncwarp();
+      volatile int no_abort = 0;
+      mbar_wait(&mma_done, 0, &no_abort, p.flags, p.wait_ns > kDrainNs ? p.wait_ns : kDrainNs);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax warps 2..9
+    const int tsm = threadIdx.x - 64;         // 0..255
+    const int qd = warp & 3;                  // TMEM lane quadrant of this warp
+    const int half = (warp - 2) >> 2;         // which 32 of the 64 query rows this warp covers
+    const int col0 = 32 * half;
+    const int trow = 32 * qd + lane;          // key row of the tile / latent row of an O^T block
+    const uint32_t t_lane = (uint32_t)(32 * qd) << 16;
+    TileCursor<false> cur;
+    cur.start(p, ts, NR, N, g, s, row0);
+    int it = 0, slot = 0, nkeys = 0, spc = -1;
+    bool ok = true, dep_waited = false;
+    float lp[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) lp[i] = 0.f;
+
+    auto epilogue = [&](int j) -> bool {
+      float* op = p.o_part + (size_t)slot * kH * kDl;
+      // The softmax waits for a value product only before a rescale, so tile
+      // j - 1's may still run: wait for it first, which leaves tile j's as the
+      // one phase of o_blk that can be open.
+      if (j > 0) {
+        const bool fail = !mbar_wait(&o_done, (j - 1) & 1, abort, p.flags, p.wait_ns);
+        if (bar_red_or(1, kSoftThreads, fail)) return false;
+      }
+#pragma unroll 1
+      for (int m = mb0; m < mb1; ++m) {
+        const bool fail = !mbar_wait(&o_blk[m], j & 1, abort, p.flags, p.wait_ns);
+        if (bar_red_or(1, kSoftThreads, fail)) return false;
+        tc_fence_after();
+        float w[32];
+        tmem_ld32(tmem + t_lane + kTmemO8 + 64 * m + col0, w);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) op[(size_t)(col0 + i) * kDl + 128 * m + trow] = w[i];
+      }
+      tc_fence_before();
+      transpose_reduce32<false>(lp, lane);
+      red_sum[qd][col0 + lane] = lp[0];
+      named_barrier(1, kSoftThreads);
+      if (tsm < kH && part == 0) {  // every part holds the same m and l
+        const float l = red_sum[0][tsm] + red_sum[1][tsm] + red_sum[2][tsm] + red_sum[3][tsm];
+        float* ml = p.ml_part + ((size_t)slot * kH + tsm) * 2;
+        ml[0] = m_sh[tsm];
+        ml[1] = l / p.lat_scale;  // O^T sums codes: dividing l by lat_scale puts the scale back
+      }
+      return true;
+    };
+
+    while (ok && cur.live) {
+      const bool first = cur.first();
+      const int u = it & 1;
+      if (first) {
+        if (it > 0 && !epilogue(it - 1)) {
+          ok = false;
+          break;
+        }
+        ++spc;
+        nkeys = p.T[cur.row] - S + s + 1;
+        slot = (g + cur.row) * S + s;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) lp[i] = 0.f;
+        if (!dep_waited) {
+          grid_dep_wait();  // fh comes from the quantiser
+          dep_waited = true;
+        }
+        if (tsm < kH) fh_sh[spc & 1][tsm] = p.fh[(size_t)(cur.row * S + s) * kH + tsm];
+      }
+      bool fail = !mbar_wait(&s_full[u], (it >> 1) & 1, abort, p.flags, p.wait_ns);
+      if (bar_red_or(1, kSoftThreads, fail)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float v[32];
+      tmem_ld32(tmem + t_lane + kTmemS + 64 * u + col0, v);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&s_free[u]);
+      const int j = cur.k * kTile + trow;
+      const bool valid = j < nkeys;
+      if (!valid) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = -INFINITY;
+      }
+      float mx[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) mx[i] = v[i];
+      transpose_reduce32<true>(mx, lane);
+      red_max[qd][col0 + lane] = mx[0];
+      named_barrier(1, kSoftThreads);
+      const float* fh = fh_sh[spc & 1];
+      bool need = false;
+      if (tsm < kH) {
+        const float tmax = fmaxf(fmaxf(red_max[0][tsm], red_max[1][tsm]), fmaxf(red_max[2][tsm], red_max[3][tsm]));
+        const float cand = tmax * fh[tsm];
+        const float mo = first ? -INFINITY : m_sh[tsm];
+        float mn = mo, al = 1.f;
+        if (cand > mo + kTau) {
+          mn = cand;
+          al = exp2f(mo - mn);
+        }
+        m_sh[tsm] = mn;
+        alpha_sh[tsm] = al;
+        need = !first && al != 1.f;
+      }
+      const bool rescale = bar_red_or(2, kSoftThreads, need);
+      if (rescale) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float4 al = *reinterpret_cast<const float4*>(&alpha_sh[col0 + i]);
+          lp[i + 0] *= al.x;
+          lp[i + 1] *= al.y;
+          lp[i + 2] *= al.z;
+          lp[i + 3] *= al.w;
+        }
+      }
+      // probabilities: fp32 row sums, E4M3 codes for the value product.  P^T
+      // is K-major in the tile's rope slot: query row n holds the codes of
+      // the 128 keys in one 128-byte row (rows in 1 KB groups of 8, 16-byte
+      // chunks XOR-swizzled by n % 8); this thread writes byte trow of rows
+      // col0 .. col0 + 31.
+      unsigned char* tile = sKV + u * kTile8Bytes;
+      unsigned char* pt = tile + 4 * kSlotBytes;
+      const int kc = trow >> 4, kb = trow & 15;
+      auto put = [&](int n, uint32_t code) {
+        pt[(n >> 3) * 1024 + (n & 7) * 128 + ((kc ^ (n & 7)) << 4) + kb] = (unsigned char)code;
+      };
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        const float4 mu = *reinterpret_cast<const float4*>(&m_sh[col0 + i]);
+        const float4 f = *reinterpret_cast<const float4*>(&fh[col0 + i]);
+        const float p0 = exp2f(fmaf(v[i], f.x, -mu.x)), p1 = exp2f(fmaf(v[i + 1], f.y, -mu.y));
+        const float p2 = exp2f(fmaf(v[i + 2], f.z, -mu.z)), p3 = exp2f(fmaf(v[i + 3], f.w, -mu.w));
+        lp[i] += p0;
+        lp[i + 1] += p1;
+        lp[i + 2] += p2;
+        lp[i + 3] += p3;
+        const uint32_t c01 = e4m3x2(p0, p1), c23 = e4m3x2(p2, p3);
+        put(col0 + i, c01 & 0xFFu);
+        put(col0 + i + 1, c01 >> 8);
+        put(col0 + i + 2, c23 & 0xFFu);
+        put(col0 + i + 3, c23 >> 8);
+      }
+      // Masked key rows inside the value product's last 32-key step: their
+      // probability is 0, but the latent codes must be finite too.
+      const int z1 = (cur.k * kTile + kTile <= nkeys) ? kTile : (((nkeys - cur.k * kTile) + 31) & ~31);
+      if (!valid && trow < z1) {
+#pragma unroll
+        for (int a = 2 * half; a < 2 * half + 2; ++a) {
+          unsigned char* lr = tile + a * kSlotBytes + trow * 128;
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) *reinterpret_cast<uint4*>(lr + 16 * cc) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      if (rescale) {
+        // O^T is stable once the previous value product retired.  Without a
+        // rescale nothing here touches O^T, and the tensor pipe orders this
+        // tile's value product after the previous one by itself.
+        fail = !mbar_wait(&o_done, (it - 1) & 1, abort, p.flags, p.wait_ns);
+        if (bar_red_or(2, kSoftThreads, fail)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        {
+#pragma unroll 1
+          for (int m = mb0; m < mb1; ++m) {
+            float w[32];
+            tmem_ld32(tmem + t_lane + kTmemO8 + 64 * m + col0, w);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              const float4 al = *reinterpret_cast<const float4*>(&alpha_sh[col0 + i]);
+              w[i] *= al.x;
+              w[i + 1] *= al.y;
+              w[i + 2] *= al.z;
+              w[i + 3] *= al.w;
+            }
+            tmem_st32(tmem + t_lane + kTmemO8 + 64 * m + col0, w);
           }
           tmem_wait_st();
         }
@@ -1451,7 +1825,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const GatherParams p) {
 // ===========================================================================
 struct Plan {
   int G, NR, P, R, Kpad;
-  size_t off_q, off_ts, off_bad, off_o, off_ml, off_stage, off_clat, off_invl, total;
+  size_t off_q, off_ts, off_bad, off_o, off_ml, off_stage, off_clat, off_invl, off_q8, off_fh, total;
 };
 
 // Query rows above which the weight products run as tcgen05 GEMMs; below it
@@ -1522,6 +1896,11 @@ Plan make_plan(int B, int S, int T_cap, int sparse_topk) {
   off = align256(off + (pl.R > kSmallRows ? (size_t)pl.R * kH * kDl * 2 : 0));
   pl.off_invl = off;
   off = align256(off + (pl.R > kSmallRows ? (size_t)pl.R * kH * 4 : 0));
+  // FP8 cache (dense only): quantised query rows and their score factors
+  pl.off_q8 = off;
+  off = align256(off + (sparse_topk ? 0 : (size_t)pl.R * kH * kQ8Row));
+  pl.off_fh = off;
+  off = align256(off + (sparse_topk ? 0 : (size_t)pl.R * kH * 4));
   pl.total = off;
   return pl;
 }
@@ -1631,9 +2010,26 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
     if (e != cudaSuccess) return e;
   }
 
+  // 1b. FP8 cache: quantise the query rows
+  unsigned char* q8 = w + pl.off_q8;
+  float* fh = reinterpret_cast<float*>(w + pl.off_fh);
+  if (a.lat_fp8) {
+    QuantParams qp{};
+    qp.qcat = qcat;
+    qp.q8 = q8;
+    qp.fh = fh;
+    qp.rows = pl.R * kH;
+    qp.c = g.scale * kLog2e;
+    qp.lat_scale = a.lat_scale;
+    kernel_mark(st, "quant_q");
+    e = launch_pdl(quant_q_kernel, dim3((qp.rows * 32 + 255) / 256), dim3(256), 0, st, qp);
+    if (e != cudaSuccess) return e;
+  }
+
   // 2. attention
   AttnParams tp{};
-  bool maps_ok = make_tmap_2d_bf16(&tp.mQ, qcat, (uint64_t)pl.R * kH, kDc, kDc, kH, 64);
+  bool maps_ok = a.lat_fp8 ? make_tmap_2d_u8(&tp.mQ, q8, (uint64_t)pl.R * kH, kQ8Row, kQ8Row, kH, 128)
+                           : make_tmap_2d_bf16(&tp.mQ, qcat, (uint64_t)pl.R * kH, kDc, kDc, kH, 64);
   if (!sparse) {
     const uint64_t rows = (uint64_t)pool_rows;
     maps_ok = maps_ok &&
@@ -1666,12 +2062,13 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   tp.read_once = ((sparse || S == 1) && tp.qsplit == 1) ? 1 : 0;
   tp.c = g.scale * kLog2e;
   tp.lat_scale = a.lat_fp8 ? a.lat_scale : 1.f;
+  tp.fh = fh;
   tp.o_part = o_part;
   tp.ml_part = ml_part;
   tp.flags = a.flags;
   tp.wait_ns = a.wait_limit_ns;
   tp.pages = sparse ? PageTable{} : a.pages;
-  auto kern = sparse ? attn_kernel<true> : a.lat_fp8 ? attn_kernel<false, true> : attn_kernel<false>;
+  auto kern = sparse ? attn_kernel<true> : a.lat_fp8 ? attn8_kernel : attn_kernel<false>;
   const uint32_t attn_smem = a.lat_fp8 ? kAttn8DynSmem : kAttnDynSmem;
   e = set_smem_once(kern, (int)attn_smem, &g_attn_attr[sparse ? 1 : a.lat_fp8 ? 2 : 0]);
   if (e != cudaSuccess) return e;
