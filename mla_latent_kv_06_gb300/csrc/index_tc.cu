@@ -12,7 +12,10 @@
 // x_lo = x - tf32(x): the omitted Ic_lo*q_lo term and the rounding of the
 // split leave an error of a few fp32 ulps of the terms.  Integer-valued inputs
 // of magnitude below 2^11 have x_lo = 0 and fp32 partial sums below 2^24, so
-// their scores come out exact in any order.
+// their scores come out exact in any order.  A product whose low operand is
+// exactly zero adds exact zeros, so it is skipped: the query's low part when
+// the whole query is tf32-exact, a tile's low part (and its rewrite) when the
+// tile is -- the check reads the tile once and writes nothing.
 //
 // CTA = a run of 128-key tiles of one (b, s): warp 0 streams the tiles
 // (four 32-column atoms, 128-byte swizzle) into a 3-stage ring with TMA,
@@ -79,6 +82,7 @@ __global__ void __launch_bounds__(kIThreads, 1) index_tc_kernel(const __grid_con
   unsigned char* sQlo = sQ + kIQBytes;                  // q - tf32(q)
   __shared__ uint64_t full_bar[kIStages], empty_bar[kIStages], hi_done[kIStages], lo_ready[kIStages];
   __shared__ uint64_t acc_full[2], acc_free[2], mma_done;
+  __shared__ int lo_needed[kIStages];  // the tile of this stage has a nonzero low part
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ float w_s[kIHeads];
@@ -129,17 +133,20 @@ __global__ void __launch_bounds__(kIThreads, 1) index_tc_kernel(const __grid_con
   }
   // query block: stored value and low part, K-major with the 128-byte swizzle
   const float* qsrc = p.q + ((size_t)b * p.S + s) * kIHeads * kIHd;
+  bool qlo_nz = false;
   for (int e = threadIdx.x; e < kIHeads * kIHd; e += kIThreads) {
     const int h = e / kIHd, d = e % kIHd;
     const float x = qsrc[e];
     const uint32_t off = (uint32_t)(d / 32) * kIQAtomBytes + swz4(h, d % 32);
+    const float lo = tf32_lo(x);
     *reinterpret_cast<float*>(sQ + off) = x;
-    *reinterpret_cast<float*>(sQlo + off) = tf32_lo(x);
+    *reinterpret_cast<float*>(sQlo + off) = lo;
+    qlo_nz = qlo_nz || lo != 0.f;
   }
   if (threadIdx.x < kIHeads) w_s[threadIdx.x] = p.w[((size_t)b * p.S + s) * kIHeads + threadIdx.x];
   fence_proxy_async_smem();
   tc_fence_before();
-  __syncthreads();
+  const bool q_has_lo = __syncthreads_or(qlo_nz) != 0;
   tc_fence_after();
   const uint32_t tmem = tmem_base;
   volatile int* abort = &abort_flag;
@@ -180,7 +187,7 @@ __global__ void __launch_bounds__(kIThreads, 1) index_tc_kernel(const __grid_con
       tc_fence_after();
       if (lane == 0) {
         const uint32_t tile = t0 + st * kITileBytes;
-        for (int pass = 0; pass < 2; ++pass)
+        for (int pass = 0; pass < (q_has_lo ? 2 : 1); ++pass)
           for (int a = 0; a < 4; ++a)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
@@ -200,7 +207,7 @@ __global__ void __launch_bounds__(kIThreads, 1) index_tc_kernel(const __grid_con
       tc_fence_after();
       if (lane == 0) {
         const uint32_t tile = t0 + st * kITileBytes;
-        for (int a = 0; a < 4; ++a)
+        for (int a = 0; a < (lo_needed[st] ? 4 : 0); ++a)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t da = smem_desc_sw128(tile + a * kIAtomBytes + kk * 32, 16, 1024);
@@ -270,18 +277,30 @@ __global__ void __launch_bounds__(kIThreads, 1) index_tc_kernel(const __grid_con
           ok = false;
           break;
         }
-        // tile -> tile - tf32(tile), in place (the first two products have read it)
+        // Does the tile have low bits?  Read-only: a tf32-exact tile skips the
+        // rewrite and the third product.
         float4* tv = reinterpret_cast<float4*>(sTile + st * kITileBytes);
+        uint32_t bits = 0;
 #pragma unroll 8
         for (int u = e; u < (int)(kITileBytes / 16); u += 128) {
-          float4 x = tv[u];
-          x.x = tf32_lo(x.x);
-          x.y = tf32_lo(x.y);
-          x.z = tf32_lo(x.z);
-          x.w = tf32_lo(x.w);
-          tv[u] = x;
+          const uint4 x = reinterpret_cast<const uint4*>(tv)[u];
+          bits |= (x.x | x.y | x.z | x.w) & 0x1FFFu;
         }
-        fence_proxy_async_smem();
+        const bool has_lo = bar_red_or_n(1, 128, bits != 0);
+        if (has_lo) {
+          // tile -> tile - tf32(tile), in place (the first products have read it)
+#pragma unroll 8
+          for (int u = e; u < (int)(kITileBytes / 16); u += 128) {
+            float4 x = tv[u];
+            x.x = tf32_lo(x.x);
+            x.y = tf32_lo(x.y);
+            x.z = tf32_lo(x.z);
+            x.w = tf32_lo(x.w);
+            tv[u] = x;
+          }
+          fence_proxy_async_smem();
+        }
+        if (e == 0) lo_needed[st] = has_lo ? 1 : 0;
         mbar_arrive(&lo_ready[st]);
       }
       if (i > 0) ok = epilogue(i - 1);

@@ -152,6 +152,41 @@ def test_index_scores_general_floats(cuda_lib, T, S, nh, hd):
     assert cuda_lib.device_status() == 0
 
 
+@pytest.mark.parametrize("frac_q,frac_tiles", [(False, (3, 7)), (True, ()), (True, (0, 5))])
+def test_index_scores_mixed_exact_tiles(cuda_lib, frac_q, frac_tiles):
+    """Integer-valued keys except for the listed 128-key tiles, whose keys get a
+    fraction, and an integer or a fractional query: tiles without low bits skip
+    the third tf32 product, an exact query skips the second; every score stays
+    within 1e-5 (normwise) of the fp64 definition, and exactly equal where all
+    inputs are integers."""
+    r = np.random.default_rng(17)
+    T, S, nh, hd = [1100, 700], 1, 32, 128
+    B, T_cap = len(T), max(T) + 30
+    q = r.integers(-4, 5, (B, S, nh, hd)).astype(np.float32)
+    if frac_q:
+        q += (r.random(q.shape) * 0.5).astype(np.float32)
+    w = r.integers(-4, 5, (B, S, nh)).astype(np.float32)
+    Ic = r.integers(-4, 5, (B, T_cap, hd)).astype(np.float32)
+    for t in frac_tiles:
+        Ic[:, 128 * t:128 * (t + 1)] += np.float32(1.0 / 3.0)
+    for b, t in enumerate(T):
+        Ic[b, t:] = np.nan
+    Tt = torch.tensor(T, dtype=torch.int32, device=DEV)
+    sc = to_np(cuda_lib.index_scores(*(torch.from_numpy(x).to(DEV) for x in (q, w, Ic)), Tt))
+    ref = oracle.index_scores(q.astype(np.float64), w.astype(np.float64), Ic.astype(np.float64), T)
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isneginf(sc), np.isneginf(ref)) and np.all(np.isfinite(sc[fin]))
+    assert max_rel_err(sc[fin], ref[fin]) < 1e-5
+    if not frac_q:  # integer query: the integer tiles are exact
+        ints = np.ones(T_cap, dtype=bool)
+        for t in frac_tiles:
+            ints[128 * t:128 * (t + 1)] = False
+        for b, t in enumerate(T):
+            m = ints[:t]
+            assert np.array_equal(sc[b, 0, :t][m], ref[b, 0, :t][m])
+    assert cuda_lib.device_status() == 0
+
+
 def test_topk_ties_and_negative_zero(cuda_lib):
     """Many equal scores, +0.0 and -0.0 mixed: the lower index wins."""
     r = np.random.default_rng(3)
