@@ -439,11 +439,15 @@ __global__ void __launch_bounds__(kTopkThreads) topk_cluster_kernel(TopkArgs a, 
     // The indexer's per-CTA histograms of this row: CTA `rank` sums bins
     // 256*rank .. 256*rank+255 over them, the cluster gathers the slices.
     const uint32_t* hp = a.hpart + (size_t)row * a.hparts * 2048 + 256 * rank;
-    for (int i = tid; i < 256; i += kTopkThreads) {
-      int v = 0;
-      for (int c = 0; c < a.hparts; ++c) v += (int)__ldg(hp + (size_t)c * 2048 + i);
-      hist[0][256 * rank + i] = v;
-    }
+    // kTopkThreads / 256 threads per bin, each summing every such part with
+    // its loads in flight together; the sums meet in shared memory.
+    constexpr int kPerBin = kTopkThreads / 256;
+    static_assert(kTopkThreads % 256 == 0, "whole bins per thread group");
+    const int bin = tid & 255, grp = tid >> 8;
+    int v = 0;
+#pragma unroll 8
+    for (int c = grp; c < a.hparts; c += kPerBin) v += (int)__ldg(hp + (size_t)c * 2048 + bin);
+    atomicAdd(&hist[0][256 * rank + bin], v);
     cluster_sync_all();
     for (int i = tid; i < 2048; i += kTopkThreads) tot[i] = ld_cluster_int(&hist[0][i], (uint32_t)(i >> 8));
     __syncthreads();

@@ -132,18 +132,34 @@ __global__ void __launch_bounds__(kIThreads, 1) index_tc_kernel(const __grid_con
     tmem_relinquish();
   }
   // query block: stored value and low part, K-major with the 128-byte swizzle
-  const float* qsrc = p.q + ((size_t)b * p.S + s) * kIHeads * kIHd;
-  bool qlo_nz = false;
-  for (int e = threadIdx.x; e < kIHeads * kIHd; e += kIThreads) {
-    const int h = e / kIHd, d = e % kIHd;
-    const float x = qsrc[e];
-    const uint32_t off = (uint32_t)(d / 32) * kIQAtomBytes + swz4(h, d % 32);
-    const float lo = tf32_lo(x);
-    *reinterpret_cast<float*>(sQ + off) = x;
-    *reinterpret_cast<float*>(sQlo + off) = lo;
-    qlo_nz = qlo_nz || lo != 0.f;
+  // All of the thread's query loads are in flight before the first store
+  // (one memory round trip, not one per element).
+  const float4* qsrc = reinterpret_cast<const float4*>(p.q + ((size_t)b * p.S + s) * kIHeads * kIHd);
+  constexpr int kQVec = kIHeads * kIHd / 4, kQPer = (kQVec + kIThreads - 1) / kIThreads;
+  float4 qv[kQPer];
+#pragma unroll
+  for (int u = 0; u < kQPer; ++u) {
+    const int e4 = threadIdx.x + u * kIThreads;
+    if (e4 < kQVec) qv[u] = qsrc[e4];
   }
   if (threadIdx.x < kIHeads) w_s[threadIdx.x] = p.w[((size_t)b * p.S + s) * kIHeads + threadIdx.x];
+  bool qlo_nz = false;
+#pragma unroll
+  for (int u = 0; u < kQPer; ++u) {
+    const int e4 = threadIdx.x + u * kIThreads;
+    if (e4 < kQVec) {
+      const float xs[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int e = 4 * e4 + c, h = e / kIHd, d = e % kIHd;
+        const uint32_t off = (uint32_t)(d / 32) * kIQAtomBytes + swz4(h, d % 32);
+        const float lo = tf32_lo(xs[c]);
+        *reinterpret_cast<float*>(sQ + off) = xs[c];
+        *reinterpret_cast<float*>(sQlo + off) = lo;
+        qlo_nz = qlo_nz || lo != 0.f;
+      }
+    }
+  }
   fence_proxy_async_smem();
   tc_fence_before();
   const bool q_has_lo = __syncthreads_or(qlo_nz) != 0;
@@ -207,14 +223,16 @@ __global__ void __launch_bounds__(kIThreads, 1) index_tc_kernel(const __grid_con
       tc_fence_after();
       if (lane == 0) {
         const uint32_t tile = t0 + st * kITileBytes;
-        for (int a = 0; a < (lo_needed[st] ? 4 : 0); ++a)
+        if (lo_needed[st]) {  // an exact tile's stage was freed by the warps that checked it
+          for (int a = 0; a < 4; ++a)
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t da = smem_desc_sw128(tile + a * kIAtomBytes + kk * 32, 16, 1024);
-            const uint64_t db = smem_desc_sw128(q0 + a * kIQAtomBytes + kk * 32, 16, 1024);
-            mma_tf32(tmem + 32 * buf, da, db, idesc, 1u);
-          }
-        mma_commit(&empty_bar[st]);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t da = smem_desc_sw128(tile + a * kIAtomBytes + kk * 32, 16, 1024);
+              const uint64_t db = smem_desc_sw128(q0 + a * kIQAtomBytes + kk * 32, 16, 1024);
+              mma_tf32(tmem + 32 * buf, da, db, idesc, 1u);
+            }
+          mma_commit(&empty_bar[st]);
+        }
         mma_commit(&acc_full[buf]);
       }
       __syncwarp();
@@ -300,7 +318,12 @@ __global__ void __launch_bounds__(kIThreads, 1) index_tc_kernel(const __grid_con
           }
           fence_proxy_async_smem();
         }
-        if (e == 0) lo_needed[st] = has_lo ? 1 : 0;
+        if (e == 0) {
+          lo_needed[st] = has_lo ? 1 : 0;
+          // An exact tile is read for the last time: free its stage now rather
+          // than after the next tile's first products.
+          if (!has_lo) mbar_arrive(&empty_bar[st]);
+        }
         mbar_arrive(&lo_ready[st]);
       }
       if (i > 0) ok = epilogue(i - 1);
@@ -338,7 +361,9 @@ int index_tc_parts(int B, int S, int n_ih, int hd, int T_cap) {
 }
 
 cudaError_t launch_index_scores_tc(const IndexArgs& a, cudaStream_t st) {
-  if (a.n_ih != kIHeads || a.hd != kIHd || (reinterpret_cast<uintptr_t>(a.Ic) & 15u) != 0)
+  // 16-byte aligned Ic (TMA) and q_idx (vector loads); anything else takes the CUDA-core kernel
+  if (a.n_ih != kIHeads || a.hd != kIHd || (reinterpret_cast<uintptr_t>(a.Ic) & 15u) != 0 ||
+      (reinterpret_cast<uintptr_t>(a.q_idx) & 15u) != 0)
     return cudaErrorNotSupported;
   IdxTcParams p{};
   if (!make_tmap_2d_f32(&p.mI, a.Ic, (uint64_t)a.B * a.T_cap, kIHd, kIHd, kITile, 32)) return cudaErrorNotSupported;

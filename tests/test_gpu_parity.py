@@ -187,6 +187,22 @@ def test_index_scores_mixed_exact_tiles(cuda_lib, frac_q, frac_tiles):
     assert cuda_lib.device_status() == 0
 
 
+def test_index_scores_unaligned_query(cuda_lib):
+    """A query tensor that starts 4 bytes past a 16-byte boundary takes the
+    CUDA-core indexer (the tensor-core one loads it in 16-byte vectors): the
+    scores stay bit-exact on integer inputs."""
+    T, S = [700, 300], 1
+    d = dsa_inputs(2, S, T, max(T), 32, 128, 77, "cpu")
+    flat = torch.empty(d["q_idx"].numel() + 1, dtype=torch.float32, device=DEV)
+    q = flat[1:].view(d["q_idx"].shape)
+    q.copy_(d["q_idx"].to(DEV))
+    assert q.data_ptr() % 16 == 4
+    Tt = torch.tensor(T, dtype=torch.int32, device=DEV)
+    sc = cuda_lib.index_scores(q, d["w"].to(DEV), d["Ic"].to(DEV), Tt)
+    assert np.array_equal(to_np(sc), oracle.index_scores(to_np(d["q_idx"]), to_np(d["w"]), to_np(d["Ic"]), T))
+    assert cuda_lib.device_status() == 0
+
+
 def test_topk_ties_and_negative_zero(cuda_lib):
     """Many equal scores, +0.0 and -0.0 mixed: the lower index wins."""
     r = np.random.default_rng(3)
