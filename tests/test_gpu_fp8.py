@@ -83,6 +83,20 @@ def test_decode_fp8_glm_batched_b32_sampled(cuda_lib):
         assert max_rel_err(out[b, s], ref[b, s]) < U_E4M3, b
 
 
+def test_decode_fp8_more_sequences_than_the_in_kernel_plan(cuda_lib):
+    """1100 sequences (the attention CTAs read the absorb kernel's plan), 1..200 keys each."""
+    B = 1100
+    r = np.random.default_rng(31)
+    T = [int(t) for t in r.integers(1, 201, B)]
+    x = _inputs(T, 1, 32)
+    out = to_np(cuda_lib.decode_fp8(x["q"].to(DEV), x["Lc8"].to(DEV), x["Rc"].to(DEV), x["T"].to(DEV),
+                                    x["kv_b"].to(DEV), GLM, LAT_SCALE))
+    assert cuda_lib.device_status() == 0
+    for b in (0, 777, 1023, 1024, 1099):
+        one = {k: (v[b:b + 1] if k in ("q", "Lc8", "Rc") else v) for k, v in x.items()}
+        assert max_rel_err(out[b], _ref(one, [T[b]])[0]) < U_E4M3, b
+
+
 @pytest.mark.parametrize("page_size", [128, 256])
 @pytest.mark.parametrize("T,S", [([129, 300, 64], 1), ([130, 257, 6], 6)])
 def test_decode_fp8_paged(cuda_lib, page_size, T, S):

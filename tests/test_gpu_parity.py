@@ -344,6 +344,49 @@ def test_sparse_decode_keep_all_and_subset(cuda_lib, dtype, dims):
     assert max_rel_err(ref[0], dense[0]) < 1e-12
 
 
+def test_decode_more_sequences_than_the_in_kernel_plan(cuda_lib):
+    """1100 sequences (above the 1024 tile-list rows an attention CTA plans by
+    itself, so it reads the absorb kernel's plan), 1..200 keys each; a sample
+    of rows against the oracle."""
+    B = 1100
+    r = np.random.default_rng(21)
+    T = [int(t) for t in r.integers(1, 201, B)]
+    x = mla_inputs(GLM, B, 1, T, 200, "bf16", 22, "cpu")
+    g = _dev(x)
+    out = to_np(cuda_lib.decode_absorbed(g["q"], g["Lc"], g["Rc"], g["T"], g["kv_b"], GLM))
+    assert cuda_lib.device_status() == 0
+    kvb = to_np(x["kv_b"])
+    for b in (0, 1, 517, 1023, 1024, 1099):
+        ref = oracle.decode_absorbed(to_np(x["q"][b:b + 1]), to_np(x["Lc"][b:b + 1]), to_np(x["Rc"][b:b + 1]), [T[b]],
+                                     kvb, GLM.qk_nope, GLM.softmax_scale)
+        assert max_rel_err(out[b], ref[0]) < TOL["bf16"], b
+
+
+def test_sparse_decode_more_rows_than_the_in_kernel_plan(cuda_lib):
+    """520 sequences x 2 query tokens = 1040 selection rows (above 1024)."""
+    B, S, k = 520, 2, 16
+    r = np.random.default_rng(23)
+    T = [int(t) for t in r.integers(S, 61, B)]
+    x = mla_inputs(GLM, B, S, T, 60, "bf16", 24, "cpu")
+    g = _dev(x)
+    sel = np.full((B, S, k), -1, dtype=np.int32)
+    nsel = np.zeros((B, S), dtype=np.int32)
+    for b in range(B):
+        for s in range(S):
+            pos = T[b] - S + s
+            cnt = min(pos + 1, k)
+            sel[b, s, :cnt] = np.sort(r.choice(pos + 1, cnt, replace=False))
+            nsel[b, s] = cnt
+    out = to_np(cuda_lib.sparse_decode(g["q"], g["Lc"], g["Rc"], g["T"], g["kv_b"], torch.from_numpy(sel).to(DEV),
+                                       torch.from_numpy(nsel).to(DEV), GLM))
+    assert cuda_lib.device_status() == 0
+    kvb = to_np(x["kv_b"])
+    for b in (0, 300, 511, 512, 519):
+        ref = oracle.sparse_decode(to_np(x["q"][b:b + 1]), to_np(x["Lc"][b:b + 1]), to_np(x["Rc"][b:b + 1]), [T[b]],
+                                   kvb, sel[b:b + 1], nsel[b:b + 1], GLM.qk_nope, GLM.softmax_scale)
+        assert max_rel_err(out[b], ref[0]) < TOL["bf16"], b
+
+
 def test_sparse_decode_flags_future_index(cuda_lib):
     T = [100]
     x = mla_inputs(GLM, 1, 1, T, 100, "bf16", 8, "cpu")
