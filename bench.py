@@ -55,7 +55,8 @@ NCU_TRAFFIC = {
     ("glm_decode_t4096", "attention"): 4885760,
     ("glm_batched_b32_s1", "attention"): 583096064,
     ("glm_append_b32_s6", "cache_append"): 243456,
-    ("glm_dsa_t65536", "topk_select"): 2326528,
+    ("glm_dsa_t65536", "index_scores"): 139203584,
+    ("glm_dsa_t65536", "topk_select"): 2325760,
     ("glm_prefill_s2048", "flash_attention"): 795437312,
     ("glm_batched_b32_s1_fp8", "attention"): 325514752,
 }
