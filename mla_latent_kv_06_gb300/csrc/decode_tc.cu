@@ -1678,7 +1678,9 @@ struct MergeParams {
   int B, S, G, sparse;
 };
 
-__global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
+constexpr int kMergeBatch = 2;  // splits whose partials are loaded together
+
+__global__ void __launch_bounds__(256, 3) merge_kernel(const MergeParams p) {
   grid_dep_wait();
   grid_dep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1698,38 +1700,81 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
   }
   const long long a = p.tile_start[row], e = p.tile_start[row + 1];
   const int glo = chunk_of(a, N, p.G), ghi = chunk_of(e - 1, N, p.G);
-  float M = -INFINITY;
-  for (int gg = glo + lane; gg <= ghi; gg += 32) {
-    int lo, hi;
-    if (p.sparse) piece_range<true>(p.tile_start, p.T, p.S, s, row, gg, p.G, N, &lo, &hi);
-    else piece_range<false>(p.tile_start, p.T, p.S, s, row, gg, p.G, N, &lo, &hi);
-    if (lo < hi) {
-      const int slot = p.sparse ? gg + row : (gg + row) * p.S + s;
-      M = fmaxf(M, p.ml_part[((size_t)slot * kH + h) * 2]);
-    }
-  }
-  M = warp_max(M);
   float acc[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) acc[i] = 0.f;
   float L = 0.f;
-  for (int gg = glo; gg <= ghi; ++gg) {
+  auto slot_of = [&](int gg) -> int {  // the split of chunk gg, or -1 when the chunk has no tile of this row
     int lo, hi;
     if (p.sparse) piece_range<true>(p.tile_start, p.T, p.S, s, row, gg, p.G, N, &lo, &hi);
     else piece_range<false>(p.tile_start, p.T, p.S, s, row, gg, p.G, N, &lo, &hi);
-    if (lo >= hi) continue;
-    const int slot = p.sparse ? gg + row : (gg + row) * p.S + s;
-    const float2 ml = *reinterpret_cast<const float2*>(p.ml_part + ((size_t)slot * kH + h) * 2);
-    const float wgt = exp2f(ml.x - M);
-    L = fmaf(wgt, ml.y, L);
-    const float4* op = reinterpret_cast<const float4*>(p.o_part + ((size_t)slot * kH + h) * kDl + 16 * lane);
+    if (lo >= hi) return -1;
+    return p.sparse ? gg + row : (gg + row) * p.S + s;
+  };
+  auto add = [&](float wgt, const float4 (&o)[4]) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float4 o = op[i];
-      acc[4 * i] = fmaf(wgt, o.x, acc[4 * i]);
-      acc[4 * i + 1] = fmaf(wgt, o.y, acc[4 * i + 1]);
-      acc[4 * i + 2] = fmaf(wgt, o.z, acc[4 * i + 2]);
-      acc[4 * i + 3] = fmaf(wgt, o.w, acc[4 * i + 3]);
+      acc[4 * i] = fmaf(wgt, o[i].x, acc[4 * i]);
+      acc[4 * i + 1] = fmaf(wgt, o[i].y, acc[4 * i + 1]);
+      acc[4 * i + 2] = fmaf(wgt, o[i].z, acc[4 * i + 2]);
+      acc[4 * i + 3] = fmaf(wgt, o[i].w, acc[4 * i + 3]);
+    }
+  };
+  auto part_of = [&](int slot) -> const float4* {
+    return reinterpret_cast<const float4*>(p.o_part + ((size_t)slot * kH + h) * kDl + 16 * lane);
+  };
+  if (ghi - glo < 32) {
+    // One split per lane: each lane reads its split's (m, l), the warp forms
+    // the weights, then the partials are read two splits at a time with all
+    // their loads in flight (more would cost occupancy when rows are many).
+    const int myslot = glo + lane <= ghi ? slot_of(glo + lane) : -1;
+    float2 ml = make_float2(-INFINITY, 0.f);
+    if (myslot >= 0) ml = *reinterpret_cast<const float2*>(p.ml_part + ((size_t)myslot * kH + h) * 2);
+    const float M = warp_max(ml.x);
+    const float mw = myslot >= 0 ? exp2f(ml.x - M) : 0.f;
+    L = warp_sum(mw * ml.y);
+    unsigned live = __ballot_sync(0xffffffffu, myslot >= 0);
+    while (live) {
+      int src[kMergeBatch];
+      float wg[kMergeBatch];
+      float4 o[kMergeBatch][4];
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u) {
+        src[u] = live ? __ffs(live) - 1 : -1;
+        if (live) live &= live - 1;
+      }
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u) {
+        const int sl = __shfl_sync(0xffffffffu, myslot, src[u] < 0 ? 0 : src[u]);
+        wg[u] = __shfl_sync(0xffffffffu, mw, src[u] < 0 ? 0 : src[u]);
+        if (src[u] >= 0) {
+          const float4* op = part_of(sl);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[u][i] = op[i];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u)
+        if (src[u] >= 0) add(wg[u], o[u]);
+    }
+  } else {  // more than 32 splits: one at a time
+    float M = -INFINITY;
+    for (int gg = glo + lane; gg <= ghi; gg += 32) {
+      const int slot = slot_of(gg);
+      if (slot >= 0) M = fmaxf(M, p.ml_part[((size_t)slot * kH + h) * 2]);
+    }
+    M = warp_max(M);
+    for (int gg = glo; gg <= ghi; ++gg) {
+      const int slot = slot_of(gg);
+      if (slot < 0) continue;
+      const float2 ml = *reinterpret_cast<const float2*>(p.ml_part + ((size_t)slot * kH + h) * 2);
+      const float wgt = exp2f(ml.x - M);
+      L = fmaf(wgt, ml.y, L);
+      float4 o[4];
+      const float4* op = part_of(slot);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = op[i];
+      add(wgt, o);
     }
   }
   const float il = 1.f / L;
