@@ -1263,6 +1263,43 @@ __device__ __forceinline__ void rope_row(const AbsorbParams& p, int r, int h, in
   dst[kDr / 2 + j] = __float2bfloat16_rn(x1 * cs + x0 * sn);
 }
 
+// Rotary parts of rows x pairs e = tid, tid + nthr, ... (row e / 32, pair e % 32):
+// eight pairs per thread at a time, their loads (T[b] and the two bf16 values)
+// all in flight before the first rotation.
+__device__ __forceinline__ void rope_rows(const AbsorbParams& p, int h, int tid, int nthr) {
+  const int R = p.B * p.S, Dq = p.Dn + kDr, n = R * (kDr / 2);
+  for (int e0 = tid; e0 < n; e0 += 8 * nthr) {
+    uint32_t raw[8];
+    int Tb[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = e0 + u * nthr;
+      if (e < n) {
+        const int r = e / (kDr / 2), j = e % (kDr / 2);
+        raw[u] = *reinterpret_cast<const uint32_t*>(p.q + ((size_t)r * kH + h) * Dq + p.Dn + 2 * j);
+        Tb[u] = p.T[r / p.S];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = e0 + u * nthr;
+      if (e < n) {
+        const int r = e / (kDr / 2), j = e % (kDr / 2), s = r % p.S;
+        const int pos = (Tb[u] < p.S || Tb[u] > p.T_cap) ? 0 : Tb[u] - p.S + s;
+        const double ang = (double)pos * p.theta[j];  // reduced to [-pi, pi] before the float sincos
+        const double k = rint(ang * 0.15915494309189535);
+        const float red = (float)fma(-k, 6.283185307179586, ang);
+        float sn, cs;
+        sincosf(red, &sn, &cs);
+        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[u]));
+        __nv_bfloat16* dst = p.qcat + ((size_t)r * kH + h) * kDc + kDl;
+        dst[j] = __float2bfloat16_rn(x.x * cs - x.y * sn);
+        dst[kDr / 2 + j] = __float2bfloat16_rn(x.y * cs + x.x * sn);
+      }
+    }
+  }
+}
+
 // Partial products of every query row with the thread's W_UK registers
 // (rows grp + 16u, columns c8*8 .. c8*8+7), one row at a time.
 template <int NV>
@@ -1392,7 +1429,7 @@ __global__ void __launch_bounds__(kAbsThreads, 2) absorb_kernel(const AbsorbPara
     l2_prefetch(wuv, (uint32_t)(p.Dv / gridDim.x) * kDl * 2);
   }
   if (!p.do_qabs) {  // rotary part only, every (row, pair) in parallel
-    for (int e = tid; e < R * (kDr / 2); e += kAbsThreads) rope_row(p, e / (kDr / 2), h, e % (kDr / 2));
+    rope_rows(p, h, tid, kAbsThreads);
     return;
   }
   // R <= kAbsRows here (larger batches take the GEMM path)
