@@ -678,7 +678,7 @@ int run_cache_append(const mla_dims* d, int dtype, int B, int S, const void* com
     a.lat_fp8 = 1;
     a.lat_inv_scale = 1.f / lat_scale;
   }
-  for (int j = 0; j < g.Dr / 2; ++j) a.theta[j] = std::pow(g.rope_base, -2.0 * j / g.Dr);
+  for (int j = 0; j < g.Dr / 2; ++j) a.turn[j] = mla::rope_turns(std::pow(g.rope_base, -2.0 * j / g.Dr));
   if (!a.flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   mla::call_begin();
@@ -745,7 +745,7 @@ MLA_EXPORT int dsa_index_key_append(int B, int S, int index_hd, int rope_dim, co
     return fail(MLA_ERR_UNSUPPORTED, "rope_dim=%d above %d", rope_dim, 2 * mla::kMaxRopePairs);
   mla::KeyAppendArgs a{B, S, T_cap, index_hd, rope_dim, k_idx, ln_w, ln_b, ln_eps, T, Ic, flags_ptr(), {}};
   const double base = rope_base > 0.f ? (double)rope_base : 10000.0;
-  for (int j = 0; j < rope_dim / 2; ++j) a.theta[j] = std::pow(base, -2.0 * j / rope_dim);
+  for (int j = 0; j < rope_dim / 2; ++j) a.turn[j] = mla::rope_turns(std::pow(base, -2.0 * j / rope_dim));
   if (!a.flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   mla::call_begin();

@@ -40,9 +40,9 @@ __device__ __forceinline__ void store(float* p, float v) { *p = v; }
 __device__ __forceinline__ void store(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
 // Pair j of a rope segment at position pos: (x0, x1) -> (y_j, y_{d/2+j}).
-__device__ __forceinline__ void rope_pair(int pos, double theta, float x0, float x1, float* y0, float* y1) {
+__device__ __forceinline__ void rope_pair(int pos, uint64_t turn, float x0, float x1, float* y0, float* y1) {
   float cs, sn;
-  rope_cs_theta(pos, theta, &cs, &sn);
+  rope_cs_turns(pos, turn, &cs, &sn);
   *y0 = x0 * cs - x1 * sn;
   *y1 = x1 * cs + x0 * sn;
 }
@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(kAppThreads) cache_append_kernel(AppendArgs a)
   if (tid < half) {
     Tv* rc = static_cast<Tv*>(a.Rc) + (size_t)row * a.qk_rope;
     float y0, y1;
-    rope_pair(pos, a.theta[tid], r0, r1, &y0, &y1);
+    rope_pair(pos, a.turn[tid], r0, r1, &y0, &y1);
     store(rc + tid, y0);
     store(rc + half + tid, y1);
   }
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kAppThreads) key_append_kernel(KeyAppendArgs a
   __syncthreads();
   for (int j = tid; j < half; j += kAppThreads) {
     float y0, y1;
-    rope_pair(pos, a.theta[j], row[2 * j], row[2 * j + 1], &y0, &y1);
+    rope_pair(pos, a.turn[j], row[2 * j], row[2 * j + 1], &y0, &y1);
     ic[r0 + j] = y0;
     ic[r0 + half + j] = y1;
   }

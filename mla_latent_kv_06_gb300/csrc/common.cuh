@@ -40,14 +40,24 @@ __device__ __forceinline__ void rope_cos_sin(int pos, int j, int d, double base,
   *s = (float)sn;
 }
 
-// cos/sin of the rotary angle pos * theta, theta = base^(-2j/d) given in
-// double: the product is formed and reduced to [-pi, pi] in double, so only
-// the reduced angle is rounded to float before the float sincos.
-__device__ __forceinline__ void rope_cs_theta(int pos, double theta, float* c, float* s) {
-  const double ang = (double)pos * theta;
-  const double k = rint(ang * 0.15915494309189535);
-  const float red = (float)fma(-k, 6.283185307179586, ang);
-  sincosf(red, s, c);
+// Rotary frequencies as fixed-point fractions of a turn: turns = theta / (2 pi)
+// in 0.64 fixed point.  Then pos * turns (mod 2^64) is the angle pos * theta
+// modulo 2 pi, formed with one integer multiply: the reduction needs no
+// floating point, and its error is the rounding of `turns` times pos (about
+// 2^-39 turn at pos 2^17), far below the float sincos that follows.  (FP64,
+// which the product would otherwise need, runs at a small fraction of the
+// fp32 rate on this GPU.)
+inline uint64_t rope_turns(double theta) {
+  return (uint64_t)(theta * 0.15915494309189535 * 18446744073709551616.0);
+}
+
+// cos/sin of the rotary angle pos * theta, theta given as rope_turns(theta):
+// the top 32 bits of the product, read as a signed fraction of a turn, give
+// the angle reduced to [-pi, pi).
+__device__ __forceinline__ void rope_cs_turns(int pos, uint64_t turns, float* c, float* s) {
+  const uint64_t ph = (uint64_t)(uint32_t)pos * turns;
+  const float ang = (float)(int32_t)(uint32_t)(ph >> 32) * 1.4629180792671596e-09f;  // 2 pi / 2^32
+  sincosf(ang, s, c);
 }
 
 // Programmatic dependent launch: wait for the preceding kernel's results /

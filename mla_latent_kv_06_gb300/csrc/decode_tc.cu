@@ -1239,7 +1239,7 @@ struct AbsorbParams {
   const __nv_bfloat16* Rc;
   int lat_row_bytes;
   int prefetch;
-  double theta[kDr / 2];  // RoPE frequencies rope_base^(-2j/qk_rope), from the host
+  uint64_t turn[kDr / 2];  // rope_turns(rope_base^(-2j/qk_rope)), from the host
   unsigned int* flags;
   PageTable pages;
 };
@@ -1250,12 +1250,8 @@ __device__ __forceinline__ void rope_row(const AbsorbParams& p, int r, int h, in
   const int b = r / p.S, s = r % p.S;
   const int Tb = p.T[b];
   const int pos = (Tb < p.S || Tb > p.T_cap) ? 0 : Tb - p.S + s;
-  // angle in double, reduced to [-pi, pi] before the float sincos
-  const double ang = (double)pos * p.theta[j];
-  const double k = rint(ang * 0.15915494309189535);
-  const float red = (float)fma(-k, 6.283185307179586, ang);
   float sn, cs;
-  sincosf(red, &sn, &cs);
+  rope_cs_turns(pos, p.turn[j], &cs, &sn);
   const __nv_bfloat16* qr = p.q + ((size_t)r * kH + h) * Dq + p.Dn;
   const float x0 = __bfloat162float(qr[2 * j]), x1 = __bfloat162float(qr[2 * j + 1]);
   __nv_bfloat16* dst = p.qcat + ((size_t)r * kH + h) * kDc + kDl;
@@ -1286,11 +1282,8 @@ __device__ __forceinline__ void rope_rows(const AbsorbParams& p, int h, int tid,
       if (e < n) {
         const int r = e / (kDr / 2), j = e % (kDr / 2), s = r % p.S;
         const int pos = (Tb[u] < p.S || Tb[u] > p.T_cap) ? 0 : Tb[u] - p.S + s;
-        const double ang = (double)pos * p.theta[j];  // reduced to [-pi, pi] before the float sincos
-        const double k = rint(ang * 0.15915494309189535);
-        const float red = (float)fma(-k, 6.283185307179586, ang);
         float sn, cs;
-        sincosf(red, &sn, &cs);
+        rope_cs_turns(pos, p.turn[j], &cs, &sn);
         const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[u]));
         __nv_bfloat16* dst = p.qcat + ((size_t)r * kH + h) * kDc + kDl;
         dst[j] = __float2bfloat16_rn(x.x * cs - x.y * sn);
@@ -2053,7 +2046,7 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   ap.prefetch =
       (!big && !sparse && (long long)B * a.T_cap * (ap.lat_row_bytes + kDr * 2) <= (48ll << 20)) ? 1 : 0;
   ap.pages = sparse ? PageTable{} : a.pages;
-  for (int j = 0; j < kDr / 2; ++j) ap.theta[j] = std::pow(g.rope_base, -2.0 * j / kDr);
+  for (int j = 0; j < kDr / 2; ++j) ap.turn[j] = rope_turns(std::pow(g.rope_base, -2.0 * j / kDr));
   ap.flags = a.flags;
   const size_t abs_smem = (size_t)kAbsRows * g.Dn * 4 + (size_t)kAbsGroups * kAbsRows * kAbsCols * 4;
   auto akern = absorb_kernel<4>;

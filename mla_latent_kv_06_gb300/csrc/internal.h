@@ -133,7 +133,7 @@ struct AppendArgs {
   void* Rc;  // [B, T_cap, qk_rope] or the page pool
   unsigned int* flags;
   PageTable pages;
-  double theta[kMaxRopePairs];
+  uint64_t turn[kMaxRopePairs];  // rope_turns(rope_base^(-2j/qk_rope))
   int lat_fp8;          // Lc receives E4M3 codes of the normalised row * lat_inv_scale
   float lat_inv_scale;
 };
@@ -148,7 +148,7 @@ struct KeyAppendArgs {
   const int32_t* T;
   float* Ic;  // [B, T_cap, hd]
   unsigned int* flags;
-  double theta[kMaxRopePairs];
+  uint64_t turn[kMaxRopePairs];  // rope_turns(rope_base^(-2j/rope_dim))
 };
 cudaError_t launch_index_key_append(const KeyAppendArgs& a, cudaStream_t st);
 

@@ -66,7 +66,7 @@ struct FlashParams {
   float* out;
   int B, S, Tk, pos_base;
   float c;                // softmax scale * log2(e)
-  double theta[kDr / 2];  // RoPE frequencies
+  uint64_t turn[kDr / 2];  // rope_turns(rope_base^(-2j/qk_rope))
   unsigned int* flags;
   long long wait_ns;
 };
@@ -249,11 +249,8 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
 #pragma unroll
           for (int v2 = 0; v2 < 2; ++v2) {
             const int jj = 16 * half + u + v2;
-            const double ang = (double)pos * p.theta[jj];
-            const double kq = rint(ang * 0.15915494309189535);
-            const float red = (float)fma(-kq, 6.283185307179586, ang);
             float sn, cs;
-            sincosf(red, &sn, &cs);
+            rope_cs_turns(pos, p.turn[jj], &cs, &sn);
             const float x0 = __bfloat162float(qr[2 * jj]), x1 = __bfloat162float(qr[2 * jj + 1]);
             r0[v2] = x0 * cs - x1 * sn;   // -> y[jj]
             r1[v2] = x1 * cs + x0 * sn;   // -> y[32 + jj]
@@ -439,7 +436,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, unsigned int* flags, long lo
   fp.Tk = Tk;
   fp.pos_base = a.pos_base;
   fp.c = g.scale * kLog2e;
-  for (int j = 0; j < kDr / 2; ++j) fp.theta[j] = std::pow(g.rope_base, -2.0 * j / kDr);
+  for (int j = 0; j < kDr / 2; ++j) fp.turn[j] = rope_turns(std::pow(g.rope_base, -2.0 * j / kDr));
   fp.flags = flags;
   fp.wait_ns = wait_ns;
   int dev = 0;
