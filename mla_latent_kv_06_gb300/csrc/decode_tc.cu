@@ -1232,7 +1232,6 @@ struct AbsorbParams {
   int32_t* tile_start;  // [NR + 1]
   int32_t* bad;         // [NR]
   int B, S, T_cap, Dn, Dv, topk, sparse;
-  int do_qabs;            // 0: plan and rotary part only (qabs comes from the GEMM kernel)
   // L2 prefetch (small batches): the latent cache rows [0, T[b]) of every
   // sequence and the W_UV rows this CTA's combine counterpart will read
   const unsigned char* Lc;  // latent rows of lat_row_bytes bytes (bf16 or E4M3)
@@ -1319,8 +1318,10 @@ __device__ __forceinline__ void absorb_regs(const uint4 (&wv)[NV], const float* 
   }
 }
 
-// NV = qk_nope / 16: W_UK registers (16-byte vectors) per thread.
-template <int NV>
+// NV = qk_nope / 16: W_UK registers (16-byte vectors) per thread.  kQabs =
+// false: the plan and the rotary part only (the GEMM forms qabs); a separate
+// instantiation, so that the small-batch kernel carries only its own code.
+template <int NV, bool kQabs = true>
 __global__ void __launch_bounds__(kAbsThreads, 2) absorb_kernel(const AbsorbParams p) {
   // Under programmatic serialization this kernel may start before the
   // previous kernel of the stream retires (for example the combine of an
@@ -1383,7 +1384,7 @@ __global__ void __launch_bounds__(kAbsThreads, 2) absorb_kernel(const AbsorbPara
   // flight before anything else touches memory.
   const int c8 = tid % (kAbsCols / 8), grp = tid / (kAbsCols / 8);
   uint4 wv[NV];
-  if (p.do_qabs) {
+  if (kQabs) {
     const __nv_bfloat16* W = p.kv_b + (size_t)h * (Dn + p.Dv) * kDl + cb * kAbsCols + c8 * 8;
 #pragma unroll
     for (int u = 0; u < NV; ++u) wv[u] = __ldg(reinterpret_cast<const uint4*>(W + (size_t)(grp + kAbsGroups * u) * kDl));
@@ -1421,7 +1422,7 @@ __global__ void __launch_bounds__(kAbsThreads, 2) absorb_kernel(const AbsorbPara
     const __nv_bfloat16* wuv = p.kv_b + ((size_t)h * (p.Dn + p.Dv) + p.Dn + (size_t)cb * (p.Dv / gridDim.x)) * kDl;
     l2_prefetch(wuv, (uint32_t)(p.Dv / gridDim.x) * kDl * 2);
   }
-  if (!p.do_qabs) {  // rotary part only, every (row, pair) in parallel
+  if constexpr (!kQabs) {  // rotary part only, every (row, pair) in parallel
     rope_rows(p, h, tid, kAbsThreads);
     return;
   }
@@ -1929,7 +1930,7 @@ cudaError_t set_smem_once(Kern kern, int bytes, std::atomic<unsigned long long>*
   return e;
 }
 
-std::atomic<unsigned long long> g_abs_attr[4] = {{0}, {0}, {0}, {0}}, g_attn_attr[3] = {{0}, {0}, {0}}, g_cmb_attr{0};
+std::atomic<unsigned long long> g_abs_attr[5] = {{0}, {0}, {0}, {0}, {0}}, g_attn_attr[3] = {{0}, {0}, {0}}, g_cmb_attr{0};
 
 Plan make_plan(int B, int S, int T_cap, int sparse_topk) {
   Plan pl{};
@@ -2038,7 +2039,6 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   ap.topk = a.topk;
   ap.sparse = sparse ? 1 : 0;
   const bool big = pl.R > kSmallRows;
-  ap.do_qabs = big ? 0 : 1;
   ap.Lc = static_cast<const unsigned char*>(a.Lc);
   ap.Rc = static_cast<const __nv_bfloat16*>(a.Rc);
   ap.lat_row_bytes = a.lat_fp8 ? kDl : kDl * 2;
@@ -2049,10 +2049,10 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   for (int j = 0; j < kDr / 2; ++j) ap.turn[j] = rope_turns(std::pow(g.rope_base, -2.0 * j / kDr));
   ap.flags = a.flags;
   const size_t abs_smem = (size_t)kAbsRows * g.Dn * 4 + (size_t)kAbsGroups * kAbsRows * kAbsCols * 4;
-  auto akern = absorb_kernel<4>;
+  auto akern = absorb_kernel<4, false>;
   if (!big) akern = g.Dn == 64 ? absorb_kernel<4> : g.Dn == 128 ? absorb_kernel<8> : g.Dn == 192 ? absorb_kernel<12>
                                                                                                : absorb_kernel<16>;
-  e = set_smem_once(akern, (int)abs_smem, &g_abs_attr[big ? 0 : g.Dn / 64 - 1]);
+  e = set_smem_once(akern, (int)abs_smem, &g_abs_attr[big ? 4 : g.Dn / 64 - 1]);
   if (e != cudaSuccess) return e;
   kernel_mark(st, big ? "plan_rope" : "absorb");
   e = launch_pdl(akern, dim3(big ? 1 : kDl / kAbsCols, kH), dim3(kAbsThreads), abs_smem, st, ap);
