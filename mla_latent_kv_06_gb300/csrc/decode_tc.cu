@@ -267,7 +267,7 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 // the next tile's loads start while it still runs, and the next score product
 // accumulates atom by atom as they land.
 // ===========================================================================
-template <bool kSparse>
+template <bool kSparse, bool kPaged = false>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         const bool first = c.first();
         if (first) ++pc;
         int y = c.row * p.kv_rows + c.k * kTile;  // tile-list row = block of key-source rows
-        if (!kSparse && p.pages.table) {  // the tile's 128 rows lie in one page
+        if (kPaged) {  // the tile's 128 rows lie in one page
           bool bad_page = false;
           y = (int)cache_row(p.pages, c.row, p.T_cap, c.k * kTile, &bad_page);
           if (bad_page) raise_flag(p.flags, MLA_DEV_BAD_INDEX);
@@ -1321,7 +1321,7 @@ __device__ __forceinline__ void absorb_regs(const uint4 (&wv)[NV], const float* 
 // NV = qk_nope / 16: W_UK registers (16-byte vectors) per thread.  kQabs =
 // false: the plan and the rotary part only (the GEMM forms qabs); a separate
 // instantiation, so that the small-batch kernel carries only its own code.
-template <int NV, bool kQabs = true>
+template <int NV, bool kQabs = true, bool kPaged = false>
 __global__ void __launch_bounds__(kAbsThreads, 2) absorb_kernel(const AbsorbParams p) {
   // Under programmatic serialization this kernel may start before the
   // previous kernel of the stream retires (for example the combine of an
@@ -1396,7 +1396,7 @@ __global__ void __launch_bounds__(kAbsThreads, 2) absorb_kernel(const AbsorbPara
     const int nblk = gridDim.x * gridDim.y, me = h * gridDim.x + cb;
     // Paged caches: units of 16 KB, nine per key tile (eight 16-row blocks of
     // latent rows, then the tile's rope rows), dealt round-robin to the CTAs.
-    for (int b = 0, base = 0; p.pages.table && b < p.B; ++b) {
+    for (int b = 0, base = 0; kPaged && b < p.B; ++b) {
       const int Tb = min(max(p.T[b], 0), p.T_cap);
       const int units = (Tb + kTile - 1) / kTile * 9;
       for (int u = ((me - base) % nblk + nblk) % nblk; u < units; u += nblk) {
@@ -1409,7 +1409,7 @@ __global__ void __launch_bounds__(kAbsThreads, 2) absorb_kernel(const AbsorbPara
       }
       base += units;
     }
-    for (int b = 0; !p.pages.table && b < p.B; ++b) {
+    for (int b = 0; !kPaged && b < p.B; ++b) {
       const int Tb = min(max(p.T[b], 0), p.T_cap);
       const size_t lb = (size_t)Tb * p.lat_row_bytes, rb = (size_t)Tb * kDr * 2;
       const size_t l0 = (lb * me / nblk) & ~(size_t)15, l1 = (lb * (me + 1) / nblk) & ~(size_t)15;
@@ -1930,7 +1930,7 @@ cudaError_t set_smem_once(Kern kern, int bytes, std::atomic<unsigned long long>*
   return e;
 }
 
-std::atomic<unsigned long long> g_abs_attr[5] = {{0}, {0}, {0}, {0}, {0}}, g_attn_attr[3] = {{0}, {0}, {0}}, g_cmb_attr{0};
+std::atomic<unsigned long long> g_abs_attr[9] = {}, g_attn_attr[4] = {}, g_cmb_attr{0};
 
 Plan make_plan(int B, int S, int T_cap, int sparse_topk) {
   Plan pl{};
@@ -2049,10 +2049,15 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   for (int j = 0; j < kDr / 2; ++j) ap.turn[j] = rope_turns(std::pow(g.rope_base, -2.0 * j / kDr));
   ap.flags = a.flags;
   const size_t abs_smem = (size_t)kAbsRows * g.Dn * 4 + (size_t)kAbsGroups * kAbsRows * kAbsCols * 4;
-  auto akern = absorb_kernel<4, false>;
-  if (!big) akern = g.Dn == 64 ? absorb_kernel<4> : g.Dn == 128 ? absorb_kernel<8> : g.Dn == 192 ? absorb_kernel<12>
-                                                                                               : absorb_kernel<16>;
-  e = set_smem_once(akern, (int)abs_smem, &g_abs_attr[big ? 4 : g.Dn / 64 - 1]);
+  // one instantiation per case, so that each carries only its own code
+  using AbsKern = void (*)(const AbsorbParams);
+  static const AbsKern abs_kerns[2][4] = {
+      {absorb_kernel<4>, absorb_kernel<8>, absorb_kernel<12>, absorb_kernel<16>},
+      {absorb_kernel<4, true, true>, absorb_kernel<8, true, true>, absorb_kernel<12, true, true>,
+       absorb_kernel<16, true, true>}};
+  const bool paged_abs = ap.prefetch && ap.pages.table;
+  const AbsKern akern = big ? absorb_kernel<4, false> : abs_kerns[paged_abs ? 1 : 0][g.Dn / 64 - 1];
+  e = set_smem_once(akern, (int)abs_smem, &g_abs_attr[big ? 8 : (paged_abs ? 4 : 0) + g.Dn / 64 - 1]);
   if (e != cudaSuccess) return e;
   kernel_mark(st, big ? "plan_rope" : "absorb");
   e = launch_pdl(akern, dim3(big ? 1 : kDl / kAbsCols, kH), dim3(kAbsThreads), abs_smem, st, ap);
@@ -2143,9 +2148,9 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   tp.flags = a.flags;
   tp.wait_ns = a.wait_limit_ns;
   tp.pages = sparse ? PageTable{} : a.pages;
-  auto kern = sparse ? attn_kernel<true> : a.lat_fp8 ? attn8_kernel : attn_kernel<false>;
+  auto kern = sparse ? attn_kernel<true> : a.lat_fp8 ? attn8_kernel : paged ? attn_kernel<false, true> : attn_kernel<false>;
   const uint32_t attn_smem = a.lat_fp8 ? kAttn8DynSmem : kAttnDynSmem;
-  e = set_smem_once(kern, (int)attn_smem, &g_attn_attr[sparse ? 1 : a.lat_fp8 ? 2 : 0]);
+  e = set_smem_once(kern, (int)attn_smem, &g_attn_attr[sparse ? 1 : a.lat_fp8 ? 2 : paged ? 3 : 0]);
   if (e != cudaSuccess) return e;
   const int nblk = pieces * tp.qsplit;
   kernel_mark(st, "attention");
