@@ -1422,8 +1422,8 @@ __global__ void __launch_bounds__(kAbsThreads, 2) absorb_kernel(const AbsorbPara
     const __nv_bfloat16* wuv = p.kv_b + ((size_t)h * (p.Dn + p.Dv) + p.Dn + (size_t)cb * (p.Dv / gridDim.x)) * kDl;
     l2_prefetch(wuv, (uint32_t)(p.Dv / gridDim.x) * kDl * 2);
   }
-  if constexpr (!kQabs) {  // rotary part only, every (row, pair) in parallel
-    rope_rows(p, h, tid, kAbsThreads);
+  if constexpr (!kQabs) {  // rotary part only, every (row, pair) in parallel over the head's CTAs
+    rope_rows(p, h, cb * kAbsThreads + tid, gridDim.x * kAbsThreads);
     return;
   }
   // R <= kAbsRows here (larger batches take the GEMM path)
@@ -2057,10 +2057,12 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
        absorb_kernel<16, true, true>}};
   const bool paged_abs = ap.prefetch && ap.pages.table;
   const AbsKern akern = big ? absorb_kernel<4, false> : abs_kerns[paged_abs ? 1 : 0][g.Dn / 64 - 1];
+  // many rows: the rotary part of each head spread over up to four CTAs
+  const int abs_gx = big ? std::min(4, (pl.R * (kDr / 2) + 2047) / 2048) : kDl / kAbsCols;
   e = set_smem_once(akern, (int)abs_smem, &g_abs_attr[big ? 8 : (paged_abs ? 4 : 0) + g.Dn / 64 - 1]);
   if (e != cudaSuccess) return e;
   kernel_mark(st, big ? "plan_rope" : "absorb");
-  e = launch_pdl(akern, dim3(big ? 1 : kDl / kAbsCols, kH), dim3(kAbsThreads), abs_smem, st, ap);
+  e = launch_pdl(akern, dim3(abs_gx, kH), dim3(kAbsThreads), abs_smem, st, ap);
   if (e != cudaSuccess) return e;
   if (big) {  // qabs for many rows: per-head GEMM [R x qk_nope] x W_UK[h] on the tensor cores
     GemmArgs ga{};
