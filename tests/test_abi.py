@@ -113,6 +113,52 @@ def test_host_rejects_bad_arguments_without_a_gpu(lib):
     assert lib.mla_decode_fp8_workspace_size(ctypes.byref(d), 1, 1, 16) > 0
 
 
+def test_host_rejects_bad_arguments_of_the_fused_and_projection_calls(lib):
+    d = mla.MlaDims(64, 192, 64, 512, 256, 0.0, 0.0)
+    p = ctypes.c_void_p(256)
+    # fused selection: sizes, null tensors, a query block too large for one CTA, missing workspace
+    assert lib.dsa_select(0, 1, 32, 128, p, p, p, 16, p, 8, p, p, p, None, 0, None) == mla.MLA_ERR_INVALID
+    assert lib.dsa_select(1, 1, 32, 128, None, p, p, 16, p, 8, p, p, p, None, 0, None) == mla.MLA_ERR_INVALID
+    assert lib.dsa_select(1, 1, 512, 512, p, p, p, 16, p, 8, p, p, p, None, 0, None) == mla.MLA_ERR_UNSUPPORTED
+    assert lib.dsa_select(1, 1, 32, 128, p, p, p, 16, p, 8, p, p, p, None, 0, None) == mla.MLA_ERR_INVALID
+    assert b"workspace" in lib.mla_last_error()
+    # output projection: sizes, in_dim not a multiple of 8, dtype, null and misaligned pointers
+    assert lib.mla_o_proj(0, 64, 8, mla.MLA_BF16, p, p, p, None, 0, None) == mla.MLA_ERR_INVALID
+    assert lib.mla_o_proj(1, 60, 8, mla.MLA_BF16, p, p, p, None, 0, None) == mla.MLA_ERR_INVALID
+    assert lib.mla_o_proj(1, 64, 8, 7, p, p, p, None, 0, None) == mla.MLA_ERR_INVALID
+    assert lib.mla_o_proj(1, 64, 8, mla.MLA_BF16, None, p, p, None, 0, None) == mla.MLA_ERR_INVALID
+    assert lib.mla_o_proj(1, 64, 8, mla.MLA_BF16, ctypes.c_void_p(8), p, p, None, 0, None) == mla.MLA_ERR_INVALID
+    # decode + projection: S > T_cap, null workspace (the attention output lives there)
+    assert lib.mla_decode_oproj(ctypes.byref(d), 1, 1, 4, p, p, p, 2, p, p, p, 8, p, p, 1 << 30,
+                                None) == mla.MLA_ERR_INVALID
+    assert lib.mla_decode_oproj(ctypes.byref(d), 1, 1, 1, p, p, p, 16, p, p, p, 8, p, None, 0,
+                                None) == mla.MLA_ERR_INVALID
+    # prefill without caller workspace: negative pos_base, rebuilt KV above the static scratch
+    assert lib.mla_prefill_naive_noalloc(ctypes.byref(d), 1, 1, 4, -1, p, p, p, p, p, None) == mla.MLA_ERR_INVALID
+    assert lib.mla_prefill_naive_noalloc(ctypes.byref(d), 1, 1, 2048, 8192, p, p, p, p, p,
+                                         None) == mla.MLA_ERR_INVALID
+
+
+def test_host_only_sizes_and_counts(lib):
+    d = mla.MlaDims(64, 192, 64, 512, 256, 0.0, 0.0)
+    tiny = mla.MlaDims(4, 16, 8, 32, 16, 0.0, 0.0)
+    assert lib.dsa_select_workspace_size(0, 1, 32, 128, 16, 8) == 0
+    assert lib.dsa_select_workspace_size(1, 1, 32, 128, 1024, 64) > 0      # tensor-core indexer histograms
+    assert lib.dsa_select_workspace_size(1, 1, 4, 32, 1024, 64) == 0       # CUDA-core indexer: none
+    assert lib.dsa_topk_select_workspace_size(1, 1, 16, 0) == 0
+    assert lib.mla_sparse_decode_workspace_size(ctypes.byref(d), mla.MLA_BF16, 1, 1, 0) == 0
+    assert lib.mla_sparse_decode_workspace_size(ctypes.byref(d), mla.MLA_BF16, 1, 1, 2048) > 0
+    assert lib.mla_o_proj_workspace_size(0, 64, 8, mla.MLA_BF16) == 0
+    assert lib.mla_decode_oproj_workspace_size(ctypes.byref(d), mla.MLA_BF16, 1, 1, 4096, 6144) > 0
+    assert lib.mla_decode_oproj_workspace_size(ctypes.byref(d), mla.MLA_BF16, 1, 2, 1, 6144) == 0
+    # kernels per tensor-core decode call: absorb, attention, combine; five for more than 8 rows;
+    # one more (the gather) for the sparse path; one kernel on the CUDA cores
+    assert lib.mla_decode_launch_count(ctypes.byref(d), mla.MLA_BF16, 1, 1, 0) == 3
+    assert lib.mla_decode_launch_count(ctypes.byref(d), mla.MLA_BF16, 32, 1, 0) == 5
+    assert lib.mla_decode_launch_count(ctypes.byref(d), mla.MLA_BF16, 4, 1, 1) == 4
+    assert lib.mla_decode_launch_count(ctypes.byref(tiny), mla.MLA_F32, 1, 1, 0) == 1
+
+
 def test_workspace_sizes_are_host_only(lib):
     d = mla.MlaDims(4, 16, 8, 32, 16, 0.0, 0.0)
     assert lib.mla_decode_absorbed_workspace_size(ctypes.byref(d), mla.MLA_F32, 1, 1, 64) == 0
