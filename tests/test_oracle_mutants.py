@@ -100,6 +100,31 @@ def _prefill_exclusive(q, Lc, Rc, kv_b, qk_nope, scale, pos_base, rope_base=1000
     return out
 
 
+def _prefill(kind):
+    """The two-step prefill with one slip: key and value rows swapped, the query
+    one position late, or the rotation at the row index instead of the position."""
+    def prefill(q, Lc, Rc, kv_b, qk_nope, scale, pos_base, rope_base=10000.0, queries=None, heads=None):
+        q, kvb = _f64(q), _f64(kv_b)
+        S, H = q.shape[0], q.shape[1]
+        Tk = pos_base + S
+        L, R = _f64(Lc)[:Tk], _f64(Rc)[:Tk]
+        KV = np.einsum("hjl,tl->thj", kvb, L)
+        v_head = kvb.shape[1] - qk_nope
+        if kind == "swap":
+            kn, val = KV[..., v_head:], KV[..., :v_head]
+        else:
+            kn, val = KV[..., :qk_nope], KV[..., qk_nope:]
+        out = np.full((S, H, v_head), np.nan)
+        for s in range(S) if queries is None else queries:
+            pos = pos_base + s + (1 if kind == "late" else 0)
+            n = min(pos + 1, Tk)
+            q_rot = om.rope_interleave(q[s, :, qk_nope:], s if kind == "rope_at_row" else pos, rope_base)
+            sc = scale * (np.einsum("hi,thi->ht", q[s, :, :qk_nope], kn[:n]) + q_rot @ R[:n].T)
+            out[s] = np.einsum("ht,thj->hj", om.softmax_probs(sc), val[:n])
+        return out
+    return prefill
+
+
 # ---------------------------------------------------------------- indexer slips
 def _index(variant):
     def index_scores(q_idx, w, Ic, T, S_positions=None):
@@ -238,6 +263,9 @@ MUTANTS = {
     "query_position_plus_one": {"query_positions": _positions(1)},
     "query_position_minus_one": {"query_positions": _positions(-1)},
     "prefill_excludes_self": {"prefill_nonabsorbed": _prefill_exclusive},
+    "prefill_key_value_rows_swapped": {"prefill_nonabsorbed": _prefill("swap")},
+    "prefill_query_one_late": {"prefill_nonabsorbed": _prefill("late")},
+    "prefill_rope_at_row_index": {"prefill_nonabsorbed": _prefill("rope_at_row")},
     "indexer_no_relu": {"index_scores": _index("no_relu")},
     "indexer_no_head_weights": {"index_scores": _index("no_weights")},
     "indexer_relu_after_sum": {"index_scores": _index("relu_after_sum")},
