@@ -196,6 +196,40 @@ def _layer(variant):
     return layer_norm
 
 
+def _sparse_ignores_nsel(q, Lc, Rc, T, kv_b, sel, nsel, qk_nope, scale, rope_base=10000.0, rows=None):
+    """Attends to all k entries of the selection, the -1 padding included."""
+    q = np.asarray(q)
+    B, S, H = q.shape[0], q.shape[1], q.shape[2]
+    out = np.full((B, S, H, np.asarray(kv_b).shape[1] - qk_nope), np.nan)
+    for b in range(B):
+        for s, pos in enumerate(om.query_positions(int(T[b]), S)):
+            idx = np.asarray(sel[b, s], dtype=np.int64)
+            out[b, s] = om.attend_absorbed(q[b, s], np.asarray(Lc)[b, idx], np.asarray(Rc)[b, idx], kv_b, qk_nope,
+                                           pos, scale, rope_base)
+    return out
+
+
+def _unpage_shifted(pool, block_table, T):
+    """Reads token t from the row of token t + 1."""
+    pool = _f64(pool)
+    ps, D = pool.shape[1], pool.shape[2]
+    rows = pool.reshape(-1, D)
+    out = np.full((len(T), max(T), D), np.nan)
+    for b, n in enumerate(T):
+        for t in range(n):
+            out[b, t] = rows[om.page_row(block_table, b, min(t + 1, n - 1), ps)]
+    return out
+
+
+def _dequant_without_scale(codes, lat_scale):
+    return om.e4m3_decode(codes)
+
+
+def _append_fp8_without_scale(comp, kv_a_ln, eps, T, kv_lora, lat_scale, base=10000.0):
+    lc, rc, pos = om.cache_append(comp, kv_a_ln, eps, T, kv_lora, base)
+    return om.e4m3_encode(lc), rc, pos
+
+
 def _page_row_swapped(block_table, b, t, page_size):
     return int(block_table[b][t % page_size]) * page_size + t // page_size
 
@@ -281,6 +315,10 @@ MUTANTS = {
     "layer_norm_drops_bias": {"layer_norm": _layer("no_bias")},
     "index_key_not_rotated": {"index_key_append": _key_append_no_rope},
     "index_key_rotates_head": {"index_key_append": _key_append_head_rope},
+    "sparse_ignores_nsel": {"sparse_decode": _sparse_ignores_nsel},
+    "unpage_reads_the_next_token": {"unpage": _unpage_shifted},
+    "dequant_drops_the_scale": {"dequant_latent": _dequant_without_scale},
+    "fp8_append_drops_the_scale": {"cache_append_fp8": _append_fp8_without_scale},
     "page_row_div_mod_swapped": {"page_row": _page_row_swapped},
     "page_row_ignores_table": {"page_row": _page_row_unmapped},
     "o_proj_rows_reversed": {"o_proj": _o_proj_untransposed_rows},
