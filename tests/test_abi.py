@@ -173,3 +173,31 @@ def test_product_path_does_not_use_the_oracle():
             if fn.endswith((".py", ".cu", ".cuh", ".h")):
                 src = open(os.path.join(dirpath, fn)).read()
                 assert "import oracle" not in src and "from oracle" not in src, fn
+
+
+def test_header_is_c_and_the_library_links_from_c(tmp_path, lib):
+    """include/mla.h compiles as C99 with warnings as errors, and a C program
+    linked against libmla.so calls host-only entry points (no GPU needed)."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    prog = tmp_path / "abi.c"
+    prog.write_text(r"""
+#include <stdio.h>
+#include "mla.h"
+int main(void) {
+  mla_dims d = {64, 192, 64, 512, 256, 0.0f, 0.0f};
+  size_t ws = mla_decode_absorbed_workspace_size(&d, MLA_BF16, 1, 1, 4096);
+  int bad = mla_decode_absorbed(&d, MLA_BF16, 1, 1, NULL, NULL, NULL, 16, NULL, NULL, NULL, NULL, 0, NULL);
+  printf("%d %zu %d %d\n", mla_abi_version(), ws, bad, mla_last_error()[0] != 0);
+  return 0;
+}
+""")
+    libdir = os.path.dirname(mla.LIB_PATH)
+    exe = tmp_path / "abi"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(prog), "-o",
+                    str(exe), "-L", libdir, "-lmla", "-Wl,-rpath," + libdir], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    assert out[0] == "1" and int(out[1]) > 0 and int(out[2]) == mla.MLA_ERR_INVALID and out[3] == "1"
+
