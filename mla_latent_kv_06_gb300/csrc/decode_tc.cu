@@ -20,9 +20,14 @@
 //                (one key row and 32 heads per thread) and write the
 //                per-split (m, l, O) partials.
 //  3. combine  : log-sum-exp merge of the splits, then out = W_UV clat / l.
+// More than 8 query rows: the absorb and the W_UV lift run as tcgen05 GEMMs
+// (gemm_tc.cu) and merge_kernel replaces the combine's merge.
 // The sparse variant first gathers each query's selected [Lc | Rc] rows into
 // a contiguous staging buffer (row-major, 576 values per key, zero past nsel),
 // so that its attention pass uses the same 1024-byte-aligned tile loads.
+// The FP8 latent cache (E4M3 codes, one scale) adds quant_q_kernel, which
+// quantises the query rows, and attn8_kernel, the attention on kind::f8f6f4
+// MMAs with two resident key tiles.
 #include <cuda_fp8.h>
 
 #include <atomic>
