@@ -44,17 +44,6 @@ struct GemmParams {
   long long wait_ns;
 };
 
-// OR of x over the 128 epilogue threads (named barrier 1).
-__device__ __forceinline__ bool epi_any(bool x) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)x)
-      : "memory");
-  return r != 0;
-}
-
 template <int BN, bool kBMN>
 __global__ void __launch_bounds__(kGThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
   using Cfg = GemmCfg<BN>;
@@ -187,7 +176,7 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_kernel(const __grid_constan
       const int m = m0 + 32 * wq + lane;
       // a failed wait is decided jointly by the 128 epilogue threads
       const bool fail = !mbar_wait(&acc_full[buf], (i >> 1) & 1, abort, p.flags, p.wait_ns);
-      if (epi_any(fail)) break;
+      if (bar_red_or(1, 128, fail)) break;
       tc_fence_after();
       float scale = 1.f;
       if (p.out_kind == kGemmOutF32Scaled && m < p.M) scale = p.scale[(size_t)m * p.Z + z];

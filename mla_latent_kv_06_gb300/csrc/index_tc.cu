@@ -60,16 +60,6 @@ __device__ __forceinline__ uint32_t swz4(int r, int k) {
   return (uint32_t)(r * 128 + ((((k * 4) >> 4) ^ (r & 7)) << 4) + ((k * 4) & 15));
 }
 
-__device__ __forceinline__ bool bar_red_or_n(int id, int n, bool x) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)x), "r"(id), "r"(n)
-      : "memory");
-  return r != 0;
-}
-
 // x - tf32(x): the part the tensor core drops
 __device__ __forceinline__ float tf32_lo(float x) { return x - __uint_as_float(__float_as_uint(x) & 0xFFFFE000u); }
 
@@ -264,7 +254,7 @@ __global__ void __launch_bounds__(kIThreads, 1) index_tc_kernel(const __grid_con
     auto epilogue = [&](int j) -> bool {
       const int buf = j & 1;
       const bool fail = !mbar_wait(&acc_full[buf], (j >> 1) & 1, abort, p.flags, p.wait_ns);
-      if (bar_red_or_n(1, 128, fail)) return false;
+      if (bar_red_or(1, 128, fail)) return false;
       tc_fence_after();
       float v[32];
       tmem_ld32(tmem + t_lane + 32 * buf, v);
@@ -291,7 +281,7 @@ __global__ void __launch_bounds__(kIThreads, 1) index_tc_kernel(const __grid_con
       if (i < na) {
         const int st = i % kIStages;
         const bool fail = !mbar_wait(&hi_done[st], (i / kIStages) & 1, abort, p.flags, p.wait_ns);
-        if (bar_red_or_n(1, 128, fail)) {
+        if (bar_red_or(1, 128, fail)) {
           ok = false;
           break;
         }
@@ -304,7 +294,7 @@ __global__ void __launch_bounds__(kIThreads, 1) index_tc_kernel(const __grid_con
           const uint4 x = reinterpret_cast<const uint4*>(tv)[u];
           bits |= (x.x | x.y | x.z | x.w) & 0x1FFFu;
         }
-        const bool has_lo = bar_red_or_n(1, 128, bits != 0);
+        const bool has_lo = bar_red_or(1, 128, bits != 0);
         if (has_lo) {
           // tile -> tile - tf32(tile), in place (the first products have read it)
 #pragma unroll 8

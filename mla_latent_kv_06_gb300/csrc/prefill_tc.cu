@@ -71,16 +71,6 @@ struct FlashParams {
   long long wait_ns;
 };
 
-__device__ __forceinline__ bool bar_red_or(int id, int n, bool x) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)x), "r"(id), "r"(n)
-      : "memory");
-  return r != 0;
-}
-
 __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_constant__ FlashParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &

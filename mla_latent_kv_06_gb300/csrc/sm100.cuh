@@ -140,7 +140,24 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// OR of x over the n threads (whole warps) arriving at named barrier `id`.
+// bar.red is the aligned form: the warp reconverges first.
+__device__ __forceinline__ bool bar_red_or(int id, int n, bool x) {
+  __syncwarp();
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)x), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+// bar.sync is the aligned form: every thread of each arriving warp must reach
+// it together, so the warp reconverges first (the compiler does not see the
+// inline barrier and may leave a warp split after a lane-dependent branch).
 __device__ __forceinline__ void named_barrier(int id, int nthreads) {
+  __syncwarp();
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
