@@ -3,12 +3,20 @@
 Headline workload: GLM-5.2-shaped single-sequence absorbed decode, B=1, S=1,
 T=4096 (bf16 cache, fp32 accumulate).  One step = one mla_decode_absorbed
 call (query RoPE, absorb through W_UK, scores over Lc/Rc, softmax, latent
-context, W_UV lift).  L2 is flushed (256 MiB write) before every timed step,
-outside the timed interval, because the step's inputs fit in L2.  The timed
-steps replay a CUDA graph of the API call; a second, instrumented replay
-records CUDA events between the library's kernels (mla_set_kernel_events) to
-attribute time per kernel, and the roofline object describes the dominant
-kernel.
+context, W_UV lift).
+
+Timing protocol: one step's inputs (34 MB at T=4096) fit in the 129 MB L2,
+so the bench keeps C copies of every input, C * step bytes >= 4 x L2, and
+step i reads copy i mod C: each step's cache, weights and query come from
+HBM, as in a decode that runs layer after layer with each layer's own
+weights and cache.  The K timed steps are one CUDA graph replayed once
+between two CUDA events (per step = total / K).  Two more figures come with
+every line: each step timed alone after a 256 MiB L2 flush write (which also
+evicts the kernels' instructions, and adds the graph-launch overhead to every
+step), and K back-to-back steps on one copy (warm L2).  A second,
+instrumented replay records CUDA events between the library's kernels
+(mla_set_kernel_events) to attribute time per kernel, and the roofline object
+describes the dominant kernel.
 
 The default run also measures the other workloads of the hot path ("rows"):
 batched decode B=32 with S=1 and S=6, DSA (indexer + top-2048 + sparse
@@ -42,6 +50,8 @@ METRIC = "MLA decode tokens/s and latent-cache HBM GB/s (% roofline) at T=4k–6
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
+L2_BYTES = 129 << 20
+ROTATE_BYTES = 4 * L2_BYTES  # input copies cycled so that a step never finds its inputs in L2
 ROW_WORKLOADS = ("glm_batched_b32_s1", "glm_batched_b32_s6", "glm_dsa_t65536", "glm_prefill_s2048",
                  "glm_append_b32_s6", "glm_paged_b32_s1", "glm_dsa_t65536_l4", "glm_decode_oproj_t4096",
                  "glm_batched_b32_s1_fp8", "glm_decode_t4096_fp8")
@@ -50,16 +60,31 @@ FP8_LAT_SCALE = 0.05  # scale of the synthetic FP8 latent cache (codes of magnit
 APPEND_RMS_EPS = 1e-6
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a
 # workload's dominant kernel, from one ncu capture of that kernel on this
-# workload; an entry is dropped as soon as its kernel changes.
-NCU_TRAFFIC = {
-    ("glm_decode_t4096", "attention"): 4885760,
-    ("glm_batched_b32_s1", "attention"): 583096064,
-    ("glm_append_b32_s6", "cache_append"): 243456,
-    ("glm_dsa_t65536", "index_scores"): 139203584,
-    ("glm_dsa_t65536", "topk_select"): 2325760,
-    ("glm_prefill_s2048", "flash_attention"): 795437312,
-    ("glm_batched_b32_s1_fp8", "attention"): 325514752,
-}
+# workload.  NCU_TRAFFIC_SOURCES is the digest of the library sources the
+# captures ran on (source_digest()); when the sources differ, every entry is
+# stale and the roofline reports traffic as null.
+NCU_TRAFFIC_SOURCES = "none"
+NCU_TRAFFIC = {}
+
+
+def source_digest():
+    """sha256 (first 16 hex digits) of the library's CUDA sources and headers."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mla_latent_kv_06_gb300", "csrc")
+    for f in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))
+                    + glob.glob(os.path.join(csrc, "*.h"))):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(name, kernel):
+    if NCU_TRAFFIC_SOURCES != source_digest():
+        return None
+    return NCU_TRAFFIC.get((name, kernel))
 
 
 def peaks():
@@ -170,7 +195,9 @@ def build_workload(name, device):
                 "plan_rope": ("hbm", q_bytes),
                 "attention": ("tensor", attn_flops) if S > 1 else ("hbm", cache + qcat),
                 "combine": ("hbm", w_uv + out_bytes), "merge": ("hbm", clat),
-                "up_gemm": ("hbm", w_uv + clat + out_bytes)}
+                "up_gemm": ("hbm", w_uv + clat + out_bytes),
+                # the single-launch path: every byte of the step
+                "fused_decode": ("tensor", attn_flops) if S > 1 else ("hbm", info["alg_bytes"])}
         if fp8:
             e2e = dict(inputs=[x["q"], x["T"]], run=lambda q, T: mla.decode_fp8(
                 q, x["Lc8"], x["Rc"], T, x["kv_b"], d, FP8_LAT_SCALE, out=out, workspace=ws), out=out)
@@ -218,7 +245,8 @@ def build_workload(name, device):
         w_o = 2 * OPROJ_HIDDEN * d.H * d.v_head
         info.update(cache_bytes=cache, alg_bytes=cache + w_uk + w_uv + w_o + q_bytes + out_bytes + 4 * R * OPROJ_HIDDEN)
         work = {"absorb": ("hbm", w_uk + q_bytes), "attention": ("hbm", cache + qcat),
-                "combine": ("hbm", w_uv + out_bytes), "oproj_gemv": ("hbm", w_o + out_bytes + 4 * R * OPROJ_HIDDEN)}
+                "combine": ("hbm", w_uv + out_bytes), "oproj_gemv": ("hbm", w_o + out_bytes + 4 * R * OPROJ_HIDDEN),
+                "fused_decode": ("hbm", cache + w_uk + w_uv + q_bytes + out_bytes)}
         e2e = None
     elif kind == "append":
         from workload import append_inputs
@@ -317,7 +345,7 @@ def capture(calls, stream):
 
 
 def time_steps(step, K, W, flush, stream):
-    """Device time (ms) of K steps, each after an L2 flush that is not timed."""
+    """Device time (ms) of K steps, each timed alone after an L2 flush that is not timed."""
     import torch
     for _ in range(W):
         flush.zero_()
@@ -334,10 +362,29 @@ def time_steps(step, K, W, flush, stream):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
-def kernel_times(calls, K, flush, stream):
-    """Per-kernel device time (us) from events the library records around its launches."""
+def time_graph(steps, W, stream):
+    """Device time (ms) of one replay of a CUDA graph holding the given steps
+    back to back, after W untimed steps (a graph of the first W)."""
+    import torch
+    warm = capture([c for st in steps[:W] for c in st], stream)
+    timed = capture([c for st in steps for c in st], stream)
+    warm.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    timed.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def kernel_times(steps, K, stream):
+    """Per-kernel device time (us, mean per launch) from events the library
+    records around its launches, over K replays of a graph of `steps` (which
+    cycle through the input copies), and launches per step."""
     import torch
     import mla_latent_kv_06_gb300 as mla
+    calls = [c for st in steps for c in st]
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in calls]
     for ev in evs:  # create the CUDA events before the capture
         for e in ev:
@@ -354,7 +401,6 @@ def kernel_times(calls, K, flush, stream):
     torch.cuda.synchronize()
     acc = {}
     for _ in range(K):
-        flush.zero_()
         g.replay()
         torch.cuda.synchronize()
         for nm, ev in zip(names, evs):
@@ -364,14 +410,18 @@ def kernel_times(calls, K, flush, stream):
     for nm in names:
         for n in nm:
             counts[n] = counts.get(n, 0) + 1
+    counts = {n: v // len(steps) for n, v in counts.items()}
     return {n: statistics.mean(v) for n, v in acc.items()}, counts
 
 
-def time_e2e(e2e, K, W, flush, stream):
-    """Public-API call with host buffers: the step's inputs from pinned host memory (one
-    staging buffer, each input at a 256-byte offset, so one host-to-device copy), the call,
-    and the output copied back."""
+def time_e2e(e2e_sets, K, W, stream):
+    """Public-API call with host buffers, K steps back to back in one graph:
+    every step copies its inputs from pinned host memory (one staging buffer,
+    each input at a 256-byte offset, so one host-to-device copy), calls the
+    library on input copy i mod C, and copies the output back to pinned host
+    memory."""
     import torch
+    e2e = e2e_sets[0]
     ins = [t.detach().cpu().contiguous() for t in e2e["inputs"]]
     offs, total = [], 0
     for t in ins:
@@ -387,12 +437,15 @@ def time_e2e(e2e, K, W, flush, stream):
     host_out = torch.empty(e2e["out"].shape, dtype=e2e["out"].dtype).pin_memory()
     d2h = host_out.numel() * host_out.element_size()
 
-    def one():
-        dev.copy_(host, non_blocking=True)
-        e2e["run"](*dev_in)
-        host_out.copy_(e2e["out"], non_blocking=True)
+    def one(es):
+        def f():
+            dev.copy_(host, non_blocking=True)
+            es["run"](*dev_in)
+            host_out.copy_(es["out"], non_blocking=True)
+        return [f]
 
-    return time_steps(one, K, W, flush, stream), total, d2h
+    steps = [one(e2e_sets[i % len(e2e_sets)]) for i in range(K)]
+    return time_graph(steps, W, stream), total, d2h
 
 
 def roofline(name, work, ktimes, counts, pk, pk_kind):
@@ -409,27 +462,46 @@ def roofline(name, work, ktimes, counts, pk, pk_kind):
     total = sum(share_us.values())
     return {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
             "frac": achieved / peak, "peak_source": pk_kind, "algorithmic_per_launch": amount,
-            "kernel_us": ktimes[dom], "traffic": NCU_TRAFFIC.get((name, dom)),
+            "kernel_us": ktimes[dom], "traffic": ncu_traffic(name, dom),
             "kernels": {n: {"us": round(v, 2), "launches": counts.get(n, 1), "share": round(share_us[n] / total, 3)}
                         for n, v in ktimes.items()}}
 
 
-def measure(name, dev, stream, flush, K, W, pk, pk_kind, want_e2e):
+def rotation_copies(step_bytes):
+    """Input copies to cycle through so that the bytes read between two uses of
+    one copy exceed 4 x L2."""
+    return max(1, -(-ROTATE_BYTES // max(1, int(step_bytes))))
+
+
+def measure(name, dev, stream, flush, K, W, pk, pk_kind, want_e2e, extra=True):
+    """K steps cycling through C input copies in one graph (the headline
+    protocol); with `extra`, also one copy flushed before each step and one
+    copy back to back (warm L2)."""
     import torch
     import mla_latent_kv_06_gb300 as mla
-    x, calls, info, work, e2e = build_workload(name, dev)
-    for c in calls:
-        c()
+    sets = [build_workload(name, dev)]
+    info, work = sets[0][2], sets[0][3]
+    C = rotation_copies(info["alg_bytes"])
+    for _ in range(C - 1):
+        sets.append(build_workload(name, dev))
+    for st in sets:
+        for c in st[1]:
+            c()
     torch.cuda.synchronize()
     assert mla.device_status() == 0, "device flags raised while warming up"
-    g = capture(calls, stream)
-    ms = time_steps(g.replay, K, W, flush, stream)
-    kt, counts = kernel_times(calls, max(3, min(K, 20)), flush, stream)
-    res = {"ms": ms, "info": info, "ktimes": kt, "counts": counts,
+    total_ms = time_graph([sets[i % C][1] for i in range(K)], W, stream)
+    kt, counts = kernel_times([sets[i % C][1] for i in range(max(C, 4))], 5, stream)
+    assert mla.device_status() == 0, "device flags raised while timing"
+    res = {"total_ms": total_ms, "copies": C, "info": info, "ktimes": kt, "counts": counts,
            "roof": roofline(name, work, kt, counts, pk, pk_kind)}
-    if want_e2e and e2e is not None:
-        res["e2e"] = time_e2e(e2e, K, W, flush, stream)
-    del x, calls, g
+    if extra:
+        g = capture(sets[0][1], stream)
+        res["flushed_ms"] = statistics.median(time_steps(g.replay, min(K, 20), W, flush, stream))
+        res["warm_ms"] = time_graph([sets[0][1]] * K, W, stream) / K
+        del g
+    if want_e2e and sets[0][4] is not None:
+        res["e2e"] = time_e2e([st[4] for st in sets], K, W, stream)
+    del sets
     torch.cuda.empty_cache()
     return res
 
@@ -491,6 +563,7 @@ def oracle_sample(name, budget_s=12.0):
 
 
 def host_threads():
+    """Threads the oracle's BLAS runs on (all host cores unless limited)."""
     try:
         from threadpoolctl import threadpool_info
         import numpy  # noqa: F401  (loads BLAS)
@@ -499,7 +572,37 @@ def host_threads():
             return int(n[0])
     except Exception:
         pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
     return os.cpu_count() or 1
+
+
+def host_cpu():
+    """Host CPU model (lscpu, else /proc/cpuinfo) and core count (nproc)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name:"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                fields = dict(ln.split(":", 1) for ln in f if ":" in ln)
+            fields = {k.strip(): v.strip() for k, v in fields.items()}
+            model = fields.get("model name") or " ".join(
+                f"{k} {fields[k]}" for k in ("CPU implementer", "CPU part") if k in fields) or None
+        except OSError:
+            pass
+    try:
+        nproc = int(subprocess.run(["nproc"], capture_output=True, text=True, timeout=10).stdout.strip())
+    except (OSError, ValueError, subprocess.SubprocessError):
+        nproc = os.cpu_count() or 1
+    return {"cpu_model": model, "nproc": nproc}
 
 
 # ------------------------------------------------------------------ main
@@ -526,11 +629,13 @@ def main():
             return
         tok_s, n, el = oracle_sample(args.workload, budget_s=min(60.0, max(5.0, 2.0 * K)))
         cores = host_threads()
+        hc = host_cpu()
         line = {"impl": "reference", "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": args.gpus,
                 "steps": K, "warmup": W, "ms_per_step": 1e3 / tok_s, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {"workload": args.workload},
                 "cpu_baseline": {"value": tok_s, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                 "cpu_model": hc["cpu_model"], "nproc": hc["nproc"],
                                  "sample": f"{n} query tokens x 64 heads of {args.workload} in {el:.1f} s"},
                 "e2e": {"value": tok_s, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
@@ -558,7 +663,7 @@ def main():
         res = measure(args.workload, dev, stream, flush, K, W, pk, pk_kind, want_e2e=True)
         t_wall = time.perf_counter() - t_wall
         clk = clocks.stop()
-        total_ms = slowest_rank_ms(sum(res["ms"]), dev)
+        total_ms = slowest_rank_ms(res["total_ms"], dev)
         info = res["info"]
         ms_per_step = total_ms / K
         value = job_throughput(info["tokens"], K, world, total_ms)
@@ -572,28 +677,31 @@ def main():
                                "T": T_list if len(T_list) <= 4 else f"sum {sum(T_list)}",
                                "heads": 64, "kv_lora": 512, "qk_rope": 64, "qk_nope": 192, "v_head": 256,
                                "parallelism": f"replicas x{world}",
-                               "l2": "256 MiB flush write before every timed step (outside the timed interval)",
-                               "launch": "CUDA graph replay of one API call"},
+                               "l2": (f"inputs larger than L2: {res['copies']} copies of every input, "
+                                      f"step i reads copy i mod {res['copies']} (>= 4 x 129 MB between reuses)"),
+                               "launch": f"one CUDA graph of the {K} timed steps back to back"},
                     "latent_cache_gbs": info["cache_bytes"] / step_s / 1e9,
                     "hbm_gbs_algorithmic": info["alg_bytes"] / step_s / 1e9,
                     "step_frac_of_measured_hbm": info["alg_bytes"] / step_s / 1e9 / pk["hbm_gbs"],
                     "step_frac_of_8tbs": info["alg_bytes"] / step_s / 8e12,
                     "roofline": res["roof"], "clocks": clk,
                     "gpu_launches": sum(res["counts"].values()) * K,
-                    "step_ms_min": min(res["ms"]), "step_ms_median": statistics.median(res["ms"]),
+                    "flushed_single_step_ms": res["flushed_ms"], "warm_l2_step_ms": res["warm_ms"],
                     "wall_s_timed_region": t_wall}
             if "e2e" in res:
                 ems, h2d, d2h = res["e2e"]
-                line["e2e"] = {"value": info["tokens"] * K / (sum(ems) / 1e3) * world, "unit": "tokens/s",
-                               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": sum(ems) / K}
+                line["e2e"] = {"value": info["tokens"] * K / (ems / 1e3) * world, "unit": "tokens/s",
+                               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems / K}
             else:
                 line["e2e"] = None
             if args.workload == "glm_decode_t4096" and not args.no_sweep:
                 sweep = {}
                 for T in (4096, 8192, 16384, 32768, 65536):
-                    r = measure(f"glm_decode_t{T}", dev, stream, flush, 20, 3, pk, pk_kind, want_e2e=False)
-                    t = statistics.median(r["ms"]) / 1e3
-                    sweep[str(T)] = {"tokens_s": 1 / t, "us": t * 1e6,
+                    r = measure(f"glm_decode_t{T}", dev, stream, flush, 100, 5, pk, pk_kind, want_e2e=False)
+                    t = r["total_ms"] / 100 / 1e3
+                    sweep[str(T)] = {"tokens_s": 1 / t, "us": t * 1e6, "copies": r["copies"],
+                                     "flushed_single_step_us": r["flushed_ms"] * 1e3,
+                                     "warm_l2_us": r["warm_ms"] * 1e3,
                                      "latent_cache_gbs": r["info"]["cache_bytes"] / t / 1e9,
                                      "hbm_gbs_algorithmic": r["info"]["alg_bytes"] / t / 1e9,
                                      "frac_of_measured_hbm": r["info"]["alg_bytes"] / t / 1e9 / pk["hbm_gbs"],
@@ -602,9 +710,10 @@ def main():
             if args.workload == "glm_decode_t4096" and not args.no_rows:
                 rows = {}
                 for wl in ROW_WORKLOADS:
-                    r = measure(wl, dev, stream, flush, 10, 3, pk, pk_kind, want_e2e=False)
-                    t = statistics.median(r["ms"]) / 1e3
-                    rows[wl] = {"us_per_step": t * 1e6, "tokens_s": r["info"]["tokens"] / t,
+                    r = measure(wl, dev, stream, flush, 20, 3, pk, pk_kind, want_e2e=False)
+                    t = r["total_ms"] / 20 / 1e3
+                    rows[wl] = {"us_per_step": t * 1e6, "tokens_s": r["info"]["tokens"] / t, "copies": r["copies"],
+                                "flushed_single_step_us": r["flushed_ms"] * 1e3, "warm_l2_us": r["warm_ms"] * 1e3,
                                 "hbm_gbs_algorithmic": r["info"]["alg_bytes"] / t / 1e9,
                                 "roofline": {k: r["roof"][k] for k in ("kernel", "bound", "achieved", "unit", "frac",
                                                                        "traffic", "algorithmic_per_launch",
@@ -616,8 +725,9 @@ def main():
                 line["rows"] = rows
             if not args.no_cpu:
                 tok_s, n, el = oracle_sample(args.workload)
+                hc = host_cpu()
                 line["cpu_baseline"] = {"value": tok_s, "unit": "tokens/s", "cores": host_threads(),
-                                        "kind": "oracle",
+                                        "kind": "oracle", "cpu_model": hc["cpu_model"], "nproc": hc["nproc"],
                                         "sample": f"{n} query tokens x 64 heads of {args.workload} in {el:.1f} s"}
             print(json.dumps(line), flush=True)
     if world > 1:
