@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle
-from tests._np import max_rel_err, to_np
+from tests._np import check_close, max_rel_err, to_np
 from workload import GLM, TINY, append_inputs, mla_inputs, paged_layout, to_pages
 
 pytestmark = pytest.mark.gpu
@@ -41,7 +41,7 @@ def test_decode_paged(cuda_lib, dtype, dims, page_size, T, S):
                                  T, to_np(x["kv_b"]), dims.qk_nope, dims.softmax_scale)
     got = to_np(out)
     assert np.all(np.isfinite(got))
-    assert max_rel_err(got, ref) < TOL[dtype]
+    check_close(got, ref, TOL[dtype])
 
 
 def test_decode_paged_glm_b32_sampled(cuda_lib):
@@ -62,7 +62,7 @@ def test_decode_paged_glm_b32_sampled(cuda_lib):
         Lb = to_np(Lp.view(-1, GLM.kv_lora)[rows])
         Rb = to_np(Rp.view(-1, GLM.qk_rope)[rows])
         ref = oracle.attend_absorbed(to_np(x["q"][b, 0]), Lb, Rb, kvb, GLM.qk_nope, pos, GLM.softmax_scale)
-        assert max_rel_err(out[b, 0], ref) < TOL["bf16"], b
+        check_close(out[b, 0], ref, TOL["bf16"], b)
 
 
 @pytest.mark.parametrize("dtype,dims,page_size", [("f32", TINY, 8), ("bf16", GLM, 128)])
@@ -86,7 +86,7 @@ def test_sparse_decode_paged(cuda_lib, dtype, dims, page_size):
     tbl = table.tolist()
     ref = oracle.sparse_decode(to_np(x["q"]), oracle.unpage(to_np(Lp), tbl, T), oracle.unpage(to_np(Rp), tbl, T), T,
                                to_np(x["kv_b"]), sel.numpy(), nsel.numpy(), dims.qk_nope, dims.softmax_scale)
-    assert max_rel_err(to_np(out), ref) < TOL[dtype]
+    check_close(to_np(out), ref, TOL[dtype])
 
 
 def test_decode_paged_flags_bad_page(cuda_lib):

@@ -18,7 +18,7 @@ import pytest
 import torch
 
 import mla_latent_kv_06_gb300 as mla
-from tests._np import max_rel_err, to_np
+from tests._np import check_close, max_rel_err, to_np
 from workload import GLM, TINY, mla_inputs
 
 pytestmark = pytest.mark.gpu
@@ -55,7 +55,7 @@ def test_noalloc_matches_prefill_on_two_calls_in_a_row(cuda_lib):
         torch.cuda.synchronize()
         g, r = to_np(got), to_np(ref)
         assert np.all(np.isfinite(g))
-        assert max_rel_err(g, r) < TOL[dtype]
+        check_close(g, r, TOL[dtype])
 
 
 def test_noalloc_repeated_call_same_inputs(cuda_lib):
@@ -69,7 +69,7 @@ def test_noalloc_repeated_call_same_inputs(cuda_lib):
     ref = cuda_lib.prefill_naive(x["q"], x["Lc"], x["Rc"], x["kv_b"], GLM, 120)
     torch.cuda.synchronize()
     for o in outs:
-        assert max_rel_err(to_np(o), to_np(ref)) < TOL["bf16"]
+        check_close(to_np(o), to_np(ref), TOL["bf16"])
 
 
 def test_noalloc_refuses_requests_beyond_its_scratch(cuda_lib):
