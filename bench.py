@@ -52,6 +52,7 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 L2_FLUSH_BYTES = 256 << 20
 L2_BYTES = 129 << 20
 ROTATE_BYTES = 4 * L2_BYTES  # input copies cycled so that a step never finds its inputs in L2
+COPIES_MEM_BYTES = 24 << 30  # device memory the input copies of one workload may take
 ROW_WORKLOADS = ("glm_batched_b32_s1", "glm_batched_b32_s6", "glm_dsa_t65536", "glm_prefill_s2048",
                  "glm_append_b32_s6", "glm_paged_b32_s1", "glm_dsa_t65536_l4", "glm_decode_oproj_t4096",
                  "glm_batched_b32_s1_fp8", "glm_decode_t4096_fp8")
@@ -467,10 +468,12 @@ def roofline(name, work, ktimes, counts, pk, pk_kind):
                         for n, v in ktimes.items()}}
 
 
-def rotation_copies(step_bytes):
+def rotation_copies(step_bytes, copy_bytes):
     """Input copies to cycle through so that the bytes read between two uses of
-    one copy exceed 4 x L2."""
-    return max(1, -(-ROTATE_BYTES // max(1, int(step_bytes))))
+    one copy exceed 4 x L2, capped so that the copies (copy_bytes of device
+    memory each) fit in COPIES_MEM_BYTES."""
+    want = max(1, -(-ROTATE_BYTES // max(1, int(step_bytes))))
+    return max(1, min(want, COPIES_MEM_BYTES // max(1, int(copy_bytes))))
 
 
 def measure(name, dev, stream, flush, K, W, pk, pk_kind, want_e2e, extra=True):
@@ -479,9 +482,10 @@ def measure(name, dev, stream, flush, K, W, pk, pk_kind, want_e2e, extra=True):
     copy back to back (warm L2)."""
     import torch
     import mla_latent_kv_06_gb300 as mla
+    m0 = torch.cuda.memory_allocated(dev)
     sets = [build_workload(name, dev)]
     info, work = sets[0][2], sets[0][3]
-    C = rotation_copies(info["alg_bytes"])
+    C = rotation_copies(info["alg_bytes"], torch.cuda.memory_allocated(dev) - m0)
     for _ in range(C - 1):
         sets.append(build_workload(name, dev))
     for st in sets:
@@ -492,7 +496,8 @@ def measure(name, dev, stream, flush, K, W, pk, pk_kind, want_e2e, extra=True):
     total_ms = time_graph([sets[i % C][1] for i in range(K)], W, stream)
     kt, counts = kernel_times([sets[i % C][1] for i in range(max(C, 4))], 5, stream)
     assert mla.device_status() == 0, "device flags raised while timing"
-    res = {"total_ms": total_ms, "copies": C, "info": info, "ktimes": kt, "counts": counts,
+    res = {"total_ms": total_ms, "copies": C, "rotation_bytes": C * info["alg_bytes"], "info": info,
+           "ktimes": kt, "counts": counts,
            "roof": roofline(name, work, kt, counts, pk, pk_kind)}
     if extra:
         g = capture(sets[0][1], stream)
@@ -677,8 +682,9 @@ def main():
                                "T": T_list if len(T_list) <= 4 else f"sum {sum(T_list)}",
                                "heads": 64, "kv_lora": 512, "qk_rope": 64, "qk_nope": 192, "v_head": 256,
                                "parallelism": f"replicas x{world}",
-                               "l2": (f"inputs larger than L2: {res['copies']} copies of every input, "
-                                      f"step i reads copy i mod {res['copies']} (>= 4 x 129 MB between reuses)"),
+                               "l2": (f"inputs larger than L2: {res['copies']} copies of every input, step i reads "
+                                      f"copy i mod {res['copies']} ({res['rotation_bytes'] / 1e6:.0f} MB read between "
+                                      f"two uses of a copy, L2 129 MB)"),
                                "launch": f"one CUDA graph of the {K} timed steps back to back"},
                     "latent_cache_gbs": info["cache_bytes"] / step_s / 1e9,
                     "hbm_gbs_algorithmic": info["alg_bytes"] / step_s / 1e9,
@@ -700,6 +706,7 @@ def main():
                     r = measure(f"glm_decode_t{T}", dev, stream, flush, 100, 5, pk, pk_kind, want_e2e=False)
                     t = r["total_ms"] / 100 / 1e3
                     sweep[str(T)] = {"tokens_s": 1 / t, "us": t * 1e6, "copies": r["copies"],
+                                     "bytes_between_reuses": r["rotation_bytes"],
                                      "flushed_single_step_us": r["flushed_ms"] * 1e3,
                                      "warm_l2_us": r["warm_ms"] * 1e3,
                                      "latent_cache_gbs": r["info"]["cache_bytes"] / t / 1e9,
@@ -713,6 +720,7 @@ def main():
                     r = measure(wl, dev, stream, flush, 20, 3, pk, pk_kind, want_e2e=False)
                     t = r["total_ms"] / 20 / 1e3
                     rows[wl] = {"us_per_step": t * 1e6, "tokens_s": r["info"]["tokens"] / t, "copies": r["copies"],
+                                "bytes_between_reuses": r["rotation_bytes"],
                                 "flushed_single_step_us": r["flushed_ms"] * 1e3, "warm_l2_us": r["warm_ms"] * 1e3,
                                 "hbm_gbs_algorithmic": r["info"]["alg_bytes"] / t / 1e9,
                                 "roofline": {k: r["roof"][k] for k in ("kernel", "bound", "achieved", "unit", "frac",
