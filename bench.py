@@ -196,9 +196,7 @@ def build_workload(name, device):
                 "plan_rope": ("hbm", q_bytes),
                 "attention": ("tensor", attn_flops) if S > 1 else ("hbm", cache + qcat),
                 "combine": ("hbm", w_uv + out_bytes), "merge": ("hbm", clat),
-                "up_gemm": ("hbm", w_uv + clat + out_bytes),
-                # the single-launch path: every byte of the step
-                "fused_decode": ("tensor", attn_flops) if S > 1 else ("hbm", info["alg_bytes"])}
+                "up_gemm": ("hbm", w_uv + clat + out_bytes)}
         if fp8:
             e2e = dict(inputs=[x["q"], x["T"]], run=lambda q, T: mla.decode_fp8(
                 q, x["Lc8"], x["Rc"], T, x["kv_b"], d, FP8_LAT_SCALE, out=out, workspace=ws), out=out)
@@ -246,8 +244,7 @@ def build_workload(name, device):
         w_o = 2 * OPROJ_HIDDEN * d.H * d.v_head
         info.update(cache_bytes=cache, alg_bytes=cache + w_uk + w_uv + w_o + q_bytes + out_bytes + 4 * R * OPROJ_HIDDEN)
         work = {"absorb": ("hbm", w_uk + q_bytes), "attention": ("hbm", cache + qcat),
-                "combine": ("hbm", w_uv + out_bytes), "oproj_gemv": ("hbm", w_o + out_bytes + 4 * R * OPROJ_HIDDEN),
-                "fused_decode": ("hbm", cache + w_uk + w_uv + q_bytes + out_bytes)}
+                "combine": ("hbm", w_uv + out_bytes), "oproj_gemv": ("hbm", w_o + out_bytes + 4 * R * OPROJ_HIDDEN)}
         e2e = None
     elif kind == "append":
         from workload import append_inputs

@@ -334,7 +334,7 @@ MLA_EXPORT int mla_decode_fp8_paged(const mla_dims* d, int B, int S, const void*
 MLA_EXPORT int mla_decode_launch_count(const mla_dims* d, int dtype, int B, int S, int sparse) {
   mla::Geometry g;
   if (!resolve(d, &g) || B < 1 || S < 1) return 0;
-  if (dtype == MLA_BF16 && mla::tc_decode_geometry_ok(g)) return mla::tc_decode_launch_count(g, sparse != 0, B, S);
+  if (dtype == MLA_BF16 && mla::tc_decode_geometry_ok(g)) return mla::tc_decode_launch_count(sparse != 0, B, S);
   return 1;
 }
 

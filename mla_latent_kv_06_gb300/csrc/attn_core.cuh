@@ -1,7 +1,6 @@
 // attn_core.cuh -- the absorbed-attention pass over the latent cache on the
 // tensor cores (page "MLA 注意力与 KV 缓存", §2.3: scores qabs . Lc + q_rot . Rc,
-// softmax, latent context sum p Lc), shared by the stand-alone attention
-// kernel and the fused single-launch decode.
+// softmax, latent context sum p Lc), as used by the attention kernel.
 //
 // Per key tile the tensor pipe runs two products,
 //   S^T[128 keys x 64 rows]   = [Lc | Rc] tile x qcat^T              (K = 576)

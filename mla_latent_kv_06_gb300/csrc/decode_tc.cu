@@ -1671,19 +1671,15 @@ bool tc_decode_geometry_ok(const Geometry& g) {
          g.Dv >= kCmbJ && g.Dv % kCmbJ == 0;
 }
 
-int tc_decode_launch_count(const Geometry& g, bool sparse, int B, int S) {
-  if (!sparse && fused_decode_workspace_bytes(g, B, S, S) > 0) return 1;
+int tc_decode_launch_count(bool sparse, int B, int S) {
   return (sparse ? 1 : 0) + ((long long)B * S > kSmallRows ? 5 : 3);
 }
 
-size_t tc_decode_workspace_bytes(const Geometry& g, int B, int S, int T_cap, int sparse_topk) {
-  const size_t chain = make_plan(B, S, T_cap, sparse_topk).total;
-  const size_t fused = sparse_topk ? 0 : fused_decode_workspace_bytes(g, B, S, T_cap);
-  return chain > fused ? chain : fused;
+size_t tc_decode_workspace_bytes(const Geometry&, int B, int S, int T_cap, int sparse_topk) {
+  return make_plan(B, S, T_cap, sparse_topk).total;
 }
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, void* ws, size_t, cudaStream_t st) {
-  if (fused_decode_ok(a, false)) return launch_decode_fused(a, ws, st);
   return run(a, ws, false, st);
 }
 

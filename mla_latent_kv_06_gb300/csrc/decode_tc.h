@@ -17,17 +17,10 @@ bool tc_decode_geometry_ok(const Geometry& g);
 size_t tc_decode_workspace_bytes(const Geometry& g, int B, int S, int T_cap, int sparse_topk);
 
 // Kernels launched by one tensor-core decode call.
-int tc_decode_launch_count(const Geometry& g, bool sparse, int B, int S);
+int tc_decode_launch_count(bool sparse, int B, int S);
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);
 
-// Single-launch absorbed decode of a few query rows (decode_fused.cu): true
-// when the request takes it (bf16 contiguous cache, B*S <= 4, a device with
-// enough SMs for one persistent CTA per SM).
-bool fused_decode_ok(const DecodeArgs& a, bool sparse);
-// Workspace of the single-launch path, 0 when it does not take the shape.
-size_t fused_decode_workspace_bytes(const Geometry& g, int B, int S, int T_cap);
-cudaError_t launch_decode_fused(const DecodeArgs& a, void* ws, cudaStream_t st);
 cudaError_t launch_sparse_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);
 
 }  // namespace mla
