@@ -47,23 +47,46 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase of `bar` with the given parity.  Gives up after
-// `limit_ns` of %globaltimer, or once *abort is set by another thread; in
-// both cases it sets *abort, raises MLA_DEV_TIMEOUT and returns false.
+// Non-blocking test of the phase of `bar` with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// try_wait that suspends the thread for at most about hint_ns.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase of `bar` with the given parity.  Gives up once
+// `limit_ns` of %globaltimer have passed since the first test failed (each
+// suspension is capped at the time left, at most 1 us, so the bound holds for
+// any limit), or once *abort is set by another thread; in both cases it sets
+// *abort, raises MLA_DEV_TIMEOUT (on a timeout) and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           unsigned int* flags, long long limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0) {
-      if (*abort) return false;
-      if ((long long)(global_ns() - t0) > limit_ns) {
-        *abort = 1;
-        raise_flag(flags, MLA_DEV_TIMEOUT);
-        return false;
-      }
+  for (;;) {
+    const long long left = limit_ns - (long long)(global_ns() - t0);
+    if (left <= 0) {
+      *abort = 1;
+      raise_flag(flags, MLA_DEV_TIMEOUT);
+      return false;
     }
+    if (mbar_try_wait_hint(bar, parity, (uint32_t)(left < 1000 ? left : 1000))) return true;
+    if (*abort) return false;
   }
 }
 
