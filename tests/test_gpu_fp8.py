@@ -23,6 +23,7 @@ import pytest
 import torch
 
 import oracle
+from tests._fp8_model import fp8_row_model
 from tests._np import max_rel_err, to_np
 from workload import GLM, append_inputs, fp8_latent_codes, mla_inputs, paged_layout, seq_lengths, to_pages
 
@@ -41,6 +42,27 @@ def _inputs(T, S, seed, device="cpu"):
     return x
 
 
+def _check_rows_against_model(got, x, T, S, lat_scale=LAT_SCALE, rows=None):
+    """Each checked (b, s) row: the kernel's normwise error against the exact
+    attention over the dequantised cache stays within 1.5x the error of the CPU
+    rounding model on the same row (and at least 2e-3, for rows the roundings
+    barely touch), and within the stated E4M3 bound."""
+    codes = x["Lc8"].cpu().numpy()
+    kvb = to_np(x["kv_b"])
+    for b in range(len(T)):
+        for s in range(S):
+            if rows is not None and (b, s) not in rows:
+                continue
+            pos = T[b] - S + s
+            q = to_np(x["q"][b, s])
+            x8 = oracle.e4m3_decode(codes[b, :pos + 1])
+            R = to_np(x["Rc"][b, :pos + 1])
+            ref = oracle.attend_absorbed(q, lat_scale * x8, R, kvb, GLM.qk_nope, pos, GLM.softmax_scale)
+            e_model = max_rel_err(fp8_row_model(q, x8, R, kvb, pos + 1, lat_scale), ref)
+            e_gpu = max_rel_err(got[b, s], ref)
+            assert e_gpu < U_E4M3 and e_gpu <= max(1.5 * e_model, 2e-3), (b, s, e_gpu, e_model)
+
+
 def _ref(x, T, lat_scale=LAT_SCALE, rows=None):
     return oracle.decode_absorbed(to_np(x["q"]), oracle.dequant_latent(x["Lc8"].cpu().numpy(), lat_scale),
                                   to_np(x["Rc"]), T, to_np(x["kv_b"]), GLM.qk_nope, GLM.softmax_scale, rows=rows)
@@ -56,6 +78,7 @@ def test_decode_fp8(cuda_lib, T, S):
     got = to_np(out)
     assert np.all(np.isfinite(got))
     assert max_rel_err(got, _ref(x, T)) < U_E4M3
+    _check_rows_against_model(got, x, T, S)
 
 
 @pytest.mark.parametrize("lat_scale", [1.0 / 64, 0.3])
@@ -67,6 +90,7 @@ def test_decode_fp8_scale_enters_linearly(cuda_lib, lat_scale):
                               GLM, lat_scale)
     assert cuda_lib.device_status() == 0
     assert max_rel_err(to_np(out), _ref(x, T, lat_scale)) < U_E4M3
+    _check_rows_against_model(to_np(out), x, T, S, lat_scale)
 
 
 def test_decode_fp8_glm_batched_b32_sampled(cuda_lib):
@@ -79,6 +103,8 @@ def test_decode_fp8_glm_batched_b32_sampled(cuda_lib):
     for b in (0, 13, 31):
         one = {k: (v[b:b + 1].cpu() if k in ("q", "Lc8", "Rc") else v.cpu()) for k, v in x.items()}
         assert max_rel_err(out[b], _ref(one, [T[b]])[0]) < U_E4M3, b
+    xc = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    _check_rows_against_model(out, xc, T, 1, rows={(0, 0), (13, 0), (31, 0)})
 
 
 def test_decode_fp8_more_sequences_than_the_in_kernel_plan(cuda_lib):
