@@ -296,17 +296,20 @@ int mla_prefill_naive(const mla_dims* d, int dtype, int B, int S, int pos_base,
  * cannot afford the device-wide synchronisation cudaMalloc/cudaFree may
  * cause, and plain C callers with no allocator at hand.
  *
- * Same arguments and results as mla_prefill_naive minus the workspace: the
- * rebuilt KV lives in a 32 MiB static device array of the library, held by
- * every GPU that loads it until the process exits.  Calls needing more
- * (B * (pos_base+S) * H * (qk_nope+v_head) * sizeof(input dtype) > 32 MiB)
- * return MLA_ERR_INVALID with the sizes in mla_last_error().  The first call
- * on a device looks up the array's device address (cudaGetSymbolAddress, with
- * that device current); make that first call before any stream capture.
- * The call allocates nothing.  All calls share the one array, which keeps the
- * last call's contents (every entry is rewritten before it is read, so
- * nothing needs clearing); calls whose executions overlap on the GPU race on
- * it, so order them on one stream.
+ * Same arguments, results and kernels as mla_prefill_naive (the tensor-core
+ * kernels for bf16 GLM-shaped heads with 16-byte aligned tensors, the
+ * CUDA-core ones otherwise) minus the workspace: the rebuilt KV lives in a
+ * 32 MiB static device array of the library, held by every GPU that loads it
+ * until the process exits.  Calls needing more (B * (pos_base+S) * H *
+ * (qk_nope+v_head) * sizeof(input dtype) > 32 MiB, for GLM-shaped bf16 heads
+ * 585 keys) return MLA_ERR_INVALID with the sizes in mla_last_error().  The
+ * stream must belong to the current device (MLA_ERR_INVALID otherwise): the
+ * array's address is looked up per device.  The first call on a device looks
+ * up that address (cudaGetSymbolAddress, with that device current); make that
+ * first call before any stream capture.  The call allocates nothing.  All
+ * calls share the one array, which keeps the last call's contents (every
+ * entry is rewritten before it is read, so nothing needs clearing); calls
+ * whose executions overlap on the GPU race on it, so order them on one stream.
  * ------------------------------------------------------------------------- */
 int mla_prefill_naive_noalloc(const mla_dims* d, int dtype, int B, int S, int pos_base,
                               const void* q, const void* Lc, const void* Rc, const void* kv_b,

@@ -92,6 +92,8 @@ bool tc_decode_ok(const mla::Geometry& g, int dtype, const void* q, const void* 
 }  // namespace
 
 void mla::set_last_error(const char* msg) { g_err = msg ? msg : ""; }
+unsigned int* mla::device_flags() { return flags_ptr(); }
+long long mla::wait_limit_ns() { return g_wait_limit_ns.load(); }
 
 namespace {
 // Inside a stream capture a plain record only orders the graph; the external

@@ -155,6 +155,12 @@ cudaError_t launch_index_key_append(const KeyAppendArgs& a, cudaStream_t st);
 // Sets the thread-local message returned by mla_last_error().
 void set_last_error(const char* msg);
 
+// Device address of the library's status word on the current device (null
+// when it cannot be resolved), and the bound of every wait inside a kernel
+// (mla_set_wait_limit_ns).
+unsigned int* device_flags();
+long long wait_limit_ns();
+
 // Per-call launch bookkeeping behind mla_set_kernel_events / mla_last_launch_names:
 // call_begin() at the start of each API call, kernel_mark() right before each
 // kernel launch, call_end() after the last one.

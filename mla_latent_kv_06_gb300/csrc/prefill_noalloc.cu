@@ -14,6 +14,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "prefill_tc.h"
 
 #define MLA_EXPORT extern "C" __attribute__((visibility("default")))
 
@@ -54,6 +55,8 @@ cudaError_t scratch_ptr(unsigned char** out) {
   return cudaSuccess;
 }
 
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
 }  // namespace
 
 MLA_EXPORT int mla_prefill_naive_noalloc(const mla_dims* d, int dtype, int B, int S, int pos_base,
@@ -65,13 +68,29 @@ MLA_EXPORT int mla_prefill_naive_noalloc(const mla_dims* d, int dtype, int B, in
   if (dtype != MLA_F32 && dtype != MLA_BF16) return fail(MLA_ERR_INVALID, "unknown dtype");
   if (B < 1 || S < 1 || pos_base < 0) return fail(MLA_ERR_INVALID, "B, S must be >= 1 and pos_base >= 0");
   if (!q || !Lc || !Rc || !kv_b || !out) return fail(MLA_ERR_INVALID, "null tensor pointer");
+  // Rebuilt KV bytes, B * (pos_base + S) * H * (qk_nope + v_head) * element size, each
+  // product checked: a request whose size does not fit in 64 bits is refused too.
   const size_t el = dtype == MLA_F32 ? 4 : 2;
-  const size_t need = (size_t)B * ((size_t)pos_base + S) * d->H * (d->qk_nope + d->v_head) * el;
-  if (need > kScratchBytes)
-    return fail(MLA_ERR_INVALID, "rebuilt KV needs " + std::to_string(need) + " bytes, more than the " +
-                                     std::to_string(kScratchBytes) + "-byte static scratch of this entry point");
+  const long long Tk = (long long)pos_base + S;
+  size_t need = 0;
+  const bool fits = Tk <= 0x7fffffffLL && (long long)B * Tk <= 0x7fffffffLL &&
+                    !__builtin_mul_overflow((size_t)B * (size_t)Tk, (size_t)d->H, &need) &&
+                    !__builtin_mul_overflow(need, (size_t)d->qk_nope + (size_t)d->v_head, &need) &&
+                    !__builtin_mul_overflow(need, el, &need);
+  if (!fits || need > kScratchBytes)
+    return fail(MLA_ERR_INVALID, "rebuilt KV needs " + (fits ? std::to_string(need) : std::string("over 2^64")) +
+                                     " bytes, more than the " + std::to_string(kScratchBytes) +
+                                     "-byte static scratch of this entry point");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int cur = 0, sdev = 0;
+  cudaError_t e = cudaGetDevice(&cur);
+  if (e == cudaSuccess) e = cudaStreamGetDevice(st, &sdev);
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, std::string("device lookup: ") + cudaGetErrorString(e));
+  if (sdev != cur)
+    return fail(MLA_ERR_INVALID, "the stream belongs to device " + std::to_string(sdev) +
+                                     ", not the current device " + std::to_string(cur));
   unsigned char* scratch = nullptr;
-  cudaError_t e = scratch_ptr(&scratch);
+  e = scratch_ptr(&scratch);
   if (e != cudaSuccess)
     return fail(MLA_ERR_CUDA, std::string("scratch address lookup: ") + cudaGetErrorString(e));
   mla::PrefillArgs a{};
@@ -89,9 +108,21 @@ MLA_EXPORT int mla_prefill_naive_noalloc(const mla_dims* d, int dtype, int B, in
   a.Lc = Lc;
   a.Rc = Rc;
   a.kv_b = kv_b;
-  a.kv = scratch;  // every entry is written by the rebuild kernel before it is read
+  a.kv = scratch;  // every entry is written by the rebuild before it is read
   a.out = out;
-  e = mla::launch_prefill_simt(a, dtype, static_cast<cudaStream_t>(stream));
+  // the same dispatch as mla_prefill_naive: the tensor-core kernels for bf16
+  // GLM-shaped heads with 16-byte aligned tensors, the CUDA-core ones otherwise
+  mla::call_begin();
+  if (dtype == MLA_BF16 && mla::tc_prefill_geometry_ok(a.g) && aligned16(q) && aligned16(Lc) && aligned16(Rc) &&
+      aligned16(kv_b)) {
+    unsigned int* flags = mla::device_flags();
+    if (!flags) return fail(MLA_ERR_CUDA, "cannot resolve the device status word");
+    e = mla::launch_prefill_tc(a, flags, mla::wait_limit_ns(), st);
+  } else {
+    mla::kernel_mark(st, "prefill_simt");
+    e = mla::launch_prefill_simt(a, dtype, st);
+  }
+  mla::call_end(st);
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, std::string("launch: ") + cudaGetErrorString(e));
   return MLA_OK;
 }
