@@ -547,28 +547,46 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, AttnShared& sh
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = -INFINITY;
     }
-    float mx[32];
+    // The running max of a head moves only when the tile's max exceeds it by
+    // more than kTau (lazy rescale).  Past a piece's first tile that is rare,
+    // and one OR over the threads tells whether any head's does: only then is
+    // the tile max reduced and the running max updated.
+    bool slow = first;
+    if (!first) {
+      bool ex = false;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) mx[i] = v[i];
-    transpose_reduce32<true>(mx, lane);
-    sh.red_max[qd][col0 + lane] = mx[0];
-    named_barrier(1, kSoftThreads);
-    bool need = false;
-    if (tsm < kH) {
-      const float tmax =
-          fmaxf(fmaxf(sh.red_max[0][tsm], sh.red_max[1][tsm]), fmaxf(sh.red_max[2][tsm], sh.red_max[3][tsm]));
-      const float cand = tmax * c;
-      const float mo = first ? -INFINITY : sh.m_sh[tsm];
-      float mn = mo, al = 1.f;
-      if (cand > mo + kTau) {
-        mn = cand;
-        al = exp2f(mo - mn);
+      for (int i = 0; i < 32; i += 4) {
+        const float4 mo = *reinterpret_cast<const float4*>(&sh.m_sh[col0 + i]);
+        ex = ex || v[i] * c > mo.x + kTau || v[i + 1] * c > mo.y + kTau || v[i + 2] * c > mo.z + kTau ||
+             v[i + 3] * c > mo.w + kTau;
       }
-      sh.m_sh[tsm] = mn;
-      sh.alpha_sh[tsm] = al;
-      need = !first && al != 1.f;
+      slow = bar_red_or(2, kSoftThreads, ex);
     }
-    const bool rescale = bar_red_or(2, kSoftThreads, need);
+    bool rescale = false;
+    if (slow) {
+      float mx[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) mx[i] = v[i];
+      transpose_reduce32<true>(mx, lane);
+      sh.red_max[qd][col0 + lane] = mx[0];
+      named_barrier(1, kSoftThreads);
+      bool need = false;
+      if (tsm < kH) {
+        const float tmax =
+            fmaxf(fmaxf(sh.red_max[0][tsm], sh.red_max[1][tsm]), fmaxf(sh.red_max[2][tsm], sh.red_max[3][tsm]));
+        const float cand = tmax * c;
+        const float mo = first ? -INFINITY : sh.m_sh[tsm];
+        float mn = mo, al = 1.f;
+        if (cand > mo + kTau) {
+          mn = cand;
+          al = exp2f(mo - mn);
+        }
+        sh.m_sh[tsm] = mn;
+        sh.alpha_sh[tsm] = al;
+        need = !first && al != 1.f;
+      }
+      rescale = bar_red_or(2, kSoftThreads, need);
+    }
     // probabilities (bf16, the value-product operand) and their row sums
     uint32_t pk[16];
 #pragma unroll

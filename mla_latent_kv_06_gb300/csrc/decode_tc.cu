@@ -536,28 +536,46 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_con
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = -INFINITY;
       }
-      float mx[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) mx[i] = v[i];
-      transpose_reduce32<true>(mx, lane);
-      red_max[qd][col0 + lane] = mx[0];
-      named_barrier(1, kSoftThreads);
       const float* fh = fh_sh[spc & 1];
-      bool need = false;
-      if (tsm < kH) {
-        const float tmax = fmaxf(fmaxf(red_max[0][tsm], red_max[1][tsm]), fmaxf(red_max[2][tsm], red_max[3][tsm]));
-        const float cand = tmax * fh[tsm];
-        const float mo = first ? -INFINITY : m_sh[tsm];
-        float mn = mo, al = 1.f;
-        if (cand > mo + kTau) {
-          mn = cand;
-          al = exp2f(mo - mn);
+      // lazy rescale: past a piece's first tile, the tile max is reduced only
+      // when some head's scores exceed its running max by more than kTau
+      bool slow = first;
+      if (!first) {
+        bool ex = false;
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float4 mo = *reinterpret_cast<const float4*>(&m_sh[col0 + i]);
+          const float4 f = *reinterpret_cast<const float4*>(&fh[col0 + i]);
+          ex = ex || v[i] * f.x > mo.x + kTau || v[i + 1] * f.y > mo.y + kTau || v[i + 2] * f.z > mo.z + kTau ||
+               v[i + 3] * f.w > mo.w + kTau;
         }
-        m_sh[tsm] = mn;
-        alpha_sh[tsm] = al;
-        need = !first && al != 1.f;
+        slow = bar_red_or(2, kSoftThreads, ex);
       }
-      const bool rescale = bar_red_or(2, kSoftThreads, need);
+      bool rescale = false;
+      if (slow) {
+        float mx[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mx[i] = v[i];
+        transpose_reduce32<true>(mx, lane);
+        red_max[qd][col0 + lane] = mx[0];
+        named_barrier(1, kSoftThreads);
+        bool need = false;
+        if (tsm < kH) {
+          const float tmax =
+              fmaxf(fmaxf(red_max[0][tsm], red_max[1][tsm]), fmaxf(red_max[2][tsm], red_max[3][tsm]));
+          const float cand = tmax * fh[tsm];
+          const float mo = first ? -INFINITY : m_sh[tsm];
+          float mn = mo, al = 1.f;
+          if (cand > mo + kTau) {
+            mn = cand;
+            al = exp2f(mo - mn);
+          }
+          m_sh[tsm] = mn;
+          alpha_sh[tsm] = al;
+          need = !first && al != 1.f;
+        }
+        rescale = bar_red_or(2, kSoftThreads, need);
+      }
       if (rescale) {
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
@@ -761,15 +779,25 @@ __device__ __forceinline__ void absorb_regs(const uint4 (&wv)[NV], const float* 
 // instantiation, so that the small-batch kernel carries only its own code.
 template <int NV, bool kQabs = true, bool kPaged = false>
 __global__ void __launch_bounds__(kAbsThreads, 2) absorb_kernel(const AbsorbParams p) {
-  // Under programmatic serialization this kernel may start before the
-  // previous kernel of the stream retires (for example the combine of an
-  // earlier call that still reads the workspace): wait before touching memory.
-  grid_dep_wait();
-  grid_dep_launch();
   extern __shared__ __align__(128) unsigned char sm[];
   const int cb = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   const int Dn = p.Dn, Dq = Dn + kDr;
   const int R = p.B * p.S;
+  // W_UK[h][:, cb*128 : cb*128+128] straight into registers: thread (grp, c8)
+  // holds rows grp, grp+16, ... of columns c8*8 .. c8*8+7.  Under programmatic
+  // serialization this kernel may start before the previous kernel of the
+  // stream retires (for example the combine of an earlier call): the weights
+  // are an input no kernel of this library writes, so their loads go out
+  // first; everything else waits for that kernel.
+  const int c8 = tid % (kAbsCols / 8), grp = tid / (kAbsCols / 8);
+  uint4 wv[NV];
+  if (kQabs) {
+    const __nv_bfloat16* W = p.kv_b + (size_t)h * (Dn + p.Dv) * kDl + cb * kAbsCols + c8 * 8;
+#pragma unroll
+    for (int u = 0; u < NV; ++u) wv[u] = __ldg(reinterpret_cast<const uint4*>(W + (size_t)(grp + kAbsGroups * u) * kDl));
+  }
+  grid_dep_wait();
+  grid_dep_launch();
 
   float* qn = reinterpret_cast<float*>(sm);      // [kAbsRows][Dn]
   float* part = qn + kAbsRows * Dn;               // [kAbsGroups][kAbsRows][kAbsCols]
@@ -817,16 +845,6 @@ __global__ void __launch_bounds__(kAbsThreads, 2) absorb_kernel(const AbsorbPara
     if (tid == 0) p.tile_start[0] = 0;
   }
 
-  // W_UK[h][:, cb*128 : cb*128+128] straight into registers: thread (grp, c8)
-  // holds rows grp, grp+16, ... of columns c8*8 .. c8*8+7.  All loads are in
-  // flight before anything else touches memory.
-  const int c8 = tid % (kAbsCols / 8), grp = tid / (kAbsCols / 8);
-  uint4 wv[NV];
-  if (kQabs) {
-    const __nv_bfloat16* W = p.kv_b + (size_t)h * (Dn + p.Dv) * kDl + cb * kAbsCols + c8 * 8;
-#pragma unroll
-    for (int u = 0; u < NV; ++u) wv[u] = __ldg(reinterpret_cast<const uint4*>(W + (size_t)(grp + kAbsGroups * u) * kDl));
-  }
   if (p.prefetch && tid == 0) {
     // Everything the later kernels of this call read streams from HBM now,
     // behind W_UK, in the order it is needed: 1/nblk of every sequence's
