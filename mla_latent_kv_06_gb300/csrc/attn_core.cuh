@@ -77,6 +77,7 @@ struct AttnParams {
   float c;        // softmax scale * log2(e)
   float lat_scale;  // FP8 cache: latent row = lat_scale * E4M3 codes
   const float* fh;  // FP8 cache: per query row, c * lat_scale * the row's quantisation scale
+  const __nv_bfloat16* qcat;  // FP8 cache, few rows: the unquantised query rows [R*64, 576]
   float* o_part;
   float* ml_part;
   unsigned int* flags;

@@ -205,6 +205,64 @@ __global__ void __launch_bounds__(256) quant_q_kernel(const QuantParams p) {
 // j + 1 loads while tile j is in use.  The row sum l stays fp32; the partial's
 // l is divided by lat_scale, which puts the cache scale back.
 // ===========================================================================
+// Query rows row0 .. row0 + 63 of qcat (one piece: 64 heads) into the FP8
+// query atoms: softmax warp w (0..7) takes heads 8w .. 8w + 7, lane L the 16
+// absorbed values 16L .. 16L + 15 and the rope pair 2L, 2L + 1 of each.  The
+// arithmetic is quant_q_kernel's; the bytes land where a 128-byte-swizzled TMA
+// load of the 640-byte quantised rows puts them (16-byte chunk c of row r at
+// chunk c ^ (r & 7)).
+__device__ __forceinline__ void quantise_query_rows(const AttnParams& p, size_t row0, int w, int lane,
+                                                    unsigned char* sQ8, float* fh) {
+  for (int hh = 0; hh < 8; ++hh) {
+    const int h = 8 * w + hh;
+    const __nv_bfloat16* src = p.qcat + (row0 + h) * kDc;
+    uint4 raw[2];
+    raw[0] = *reinterpret_cast<const uint4*>(src + 16 * lane);
+    raw[1] = *reinterpret_cast<const uint4*>(src + 16 * lane + 8);
+    const uint32_t rp = *reinterpret_cast<const uint32_t*>(src + kDl + 2 * lane);
+    float v[16];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw[k]);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float2 f = __bfloat1622float2(b2[t]);
+        v[8 * k + 2 * t] = f.x;
+        v[8 * k + 2 * t + 1] = f.y;
+      }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float sq = amax > 0.f ? amax * (1.f / 448.f) : 1.f;
+    const float inv = amax > 0.f ? 448.f / amax : 1.f;
+    uint32_t code[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      code[i] = e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv) | (e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv) << 16);
+    // codes 16L .. 16L+15: atom L / 8, chunk L % 8 of row h
+    const int c = lane & 7;
+    *reinterpret_cast<uint4*>(sQ8 + (lane >> 3) * kQAtomBytes + h * 128 + ((c ^ (h & 7)) << 4)) =
+        make_uint4(code[0], code[1], code[2], code[3]);
+    // rope pair: bytes 4L .. 4L+3 of row h of the bf16 atom (chunk L / 4)
+    const float rs = 1.f / (p.lat_scale * sq);
+    __nv_bfloat162 r2 = *reinterpret_cast<const __nv_bfloat162*>(&rp);
+    const float2 rf = __bfloat1622float2(r2);
+    r2 = __floats2bfloat162_rn(rf.x * rs, rf.y * rs);
+    const int rc = lane >> 2;
+    *reinterpret_cast<__nv_bfloat162*>(sQ8 + 4 * kQAtomBytes + h * 128 + ((rc ^ (h & 7)) << 4) + 4 * (lane & 3)) = r2;
+    if (lane == 0) fh[h] = p.c * p.lat_scale * sq;
+  }
+}
+
+// kQuantIn: the softmax warps quantise each piece's query rows from qcat
+// themselves (as quant_q_kernel does, one warp per head) and write the codes
+// and rope values into the query atoms, in the layout a 128-byte-swizzled TMA
+// load of the quantised rows would give; the few-row path takes this form,
+// which saves the quantiser's launch and hand-over.
+template <bool kQuantIn>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -236,7 +294,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_con
         mbar_init(&full_bar[u][a], 1);
         mbar_init(&empty_bar[u][a], 1);
       }
-    mbar_init(&q_full, 1);
+    mbar_init(&q_full, kQuantIn ? kSoftThreads : 1);
     mbar_init(&q_empty, 1);
     for (int u = 0; u < 2; ++u) {
       mbar_init(&s_full[u], 1);
@@ -248,7 +306,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_con
     mbar_init(&mma_done, 1);
     abort_flag = 0;
     fence_mbar_init();
-    prefetch_tensormap(&p.mQ);
+    if (!kQuantIn) prefetch_tensormap(&p.mQ);
     prefetch_tensormap(&p.mL);
     prefetch_tensormap(&p.mR);
   }
@@ -332,7 +390,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_con
           else tma_load_2d(tile + a * kSlotBytes, map, x, y, &full_bar[u][a]);
           last_it[u][a] = it;
         }
-        if (ok && first) {  // the piece's quantised query block
+        if (!kQuantIn && ok && first) {  // the piece's quantised query block
           if (!dep_waited) {
             grid_dep_wait();  // q8 comes from the quantiser
             dep_waited = true;
@@ -504,20 +562,37 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_con
       const bool first = cur.first();
       const int u = it & 1;
       if (first) {
+        ++spc;
+        if (kQuantIn) {
+          // the piece's query block, once the previous piece's score products are done
+          if (!dep_waited) {
+            grid_dep_wait();  // qcat comes from the absorb kernel
+            dep_waited = true;
+          }
+          const bool qfail = !mbar_wait(&q_empty, (spc & 1) ^ 1, abort, p.flags, p.wait_ns);
+          if (bar_red_or(1, kSoftThreads, qfail)) {
+            ok = false;
+            break;
+          }
+          quantise_query_rows(p, (size_t)(cur.row * S + s) * kH, warp - 2, lane, sQ8, fh_sh[spc & 1]);
+          fence_proxy_async_smem();
+          mbar_arrive(&q_full);
+        }
         if (it > 0 && !epilogue(it - 1)) {
           ok = false;
           break;
         }
-        ++spc;
         nkeys = p.T[cur.row] - S + s + 1;
         slot = (g + cur.row) * S + s;
 #pragma unroll
         for (int i = 0; i < 32; ++i) lp[i] = 0.f;
-        if (!dep_waited) {
-          grid_dep_wait();  // fh comes from the quantiser
-          dep_waited = true;
+        if (!kQuantIn) {
+          if (!dep_waited) {
+            grid_dep_wait();  // fh comes from the quantiser
+            dep_waited = true;
+          }
+          if (tsm < kH) fh_sh[spc & 1][tsm] = p.fh[(size_t)(cur.row * S + s) * kH + tsm];
         }
-        if (tsm < kH) fh_sh[spc & 1][tsm] = p.fh[(size_t)(cur.row * S + s) * kH + tsm];
       }
       bool fail = !mbar_wait(&s_full[u], (it >> 1) & 1, abort, p.flags, p.wait_ns);
       if (bar_red_or(1, kSoftThreads, fail)) {
@@ -1386,7 +1461,7 @@ cudaError_t set_smem_once(Kern kern, int bytes, std::atomic<unsigned long long>*
   return e;
 }
 
-std::atomic<unsigned long long> g_abs_attr[9] = {}, g_attn_attr[4] = {}, g_cmb_attr{0};
+std::atomic<unsigned long long> g_abs_attr[9] = {}, g_attn_attr[5] = {}, g_cmb_attr{0};
 
 Plan make_plan(int B, int S, int T_cap, int sparse_topk) {
   Plan pl{};
@@ -1551,7 +1626,7 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   // 1b. FP8 cache: quantise the query rows
   unsigned char* q8 = w + pl.off_q8;
   float* fh = reinterpret_cast<float*>(w + pl.off_fh);
-  if (a.lat_fp8) {
+  if (a.lat_fp8 && big) {  // few rows: the attention kernel quantises them itself
     QuantParams qp{};
     qp.qcat = qcat;
     qp.q8 = q8;
@@ -1601,14 +1676,18 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   tp.c = g.scale * kLog2e;
   tp.lat_scale = a.lat_fp8 ? a.lat_scale : 1.f;
   tp.fh = fh;
+  tp.qcat = qcat;
   tp.o_part = o_part;
   tp.ml_part = ml_part;
   tp.flags = a.flags;
   tp.wait_ns = a.wait_limit_ns;
   tp.pages = sparse ? PageTable{} : a.pages;
-  auto kern = sparse ? attn_kernel<true> : a.lat_fp8 ? attn8_kernel : paged ? attn_kernel<false, true> : attn_kernel<false>;
+  auto kern = sparse     ? attn_kernel<true>
+              : a.lat_fp8 ? (big ? attn8_kernel<false> : attn8_kernel<true>)
+              : paged     ? attn_kernel<false, true>
+                          : attn_kernel<false>;
   const uint32_t attn_smem = a.lat_fp8 ? kAttn8DynSmem : kAttnDynSmem;
-  e = set_smem_once(kern, (int)attn_smem, &g_attn_attr[sparse ? 1 : a.lat_fp8 ? 2 : paged ? 3 : 0]);
+  e = set_smem_once(kern, (int)attn_smem, &g_attn_attr[sparse ? 1 : a.lat_fp8 ? (big ? 2 : 4) : paged ? 3 : 0]);
   if (e != cudaSuccess) return e;
   const int nblk = pieces * tp.qsplit;
   kernel_mark(st, "attention");
