@@ -217,9 +217,12 @@ def build_workload(name, device):
                                                                   T_cap, k), 1), dtype=torch.uint8, device=device)
         calls = [lambda: mla.select(x["q_idx"], x["w"], x["Ic"], x["T"], k, scores=sc, sel=sel, nsel=nsel,
                                     workspace=sws)]
-        for y, o in zip(x["layers"], outs):
-            calls.append(lambda y=y, o=o: mla.sparse_decode(y["q"], y["Lc"], y["Rc"], x["T"], y["kv_b"], sel, nsel, d,
-                                                            out=o, workspace=ws))
+        if L == 1:
+            calls.append(lambda: mla.sparse_decode(x["q"], x["Lc"], x["Rc"], x["T"], x["kv_b"], sel, nsel, d, out=out,
+                                                   workspace=ws))
+        else:  # one call for the layers that share the selection
+            layers = [(y["q"], y["Lc"], y["Rc"], y["kv_b"]) for y in x["layers"]]
+            calls.append(lambda: mla.sparse_decode_layers(layers, x["T"], sel, nsel, d, outs=outs, workspace=ws))
         info["tokens"] = R * L  # one query token per layer
         ic = 4 * x["Ic"].shape[2] * sum(T_list)
         scores = 4 * R * T_cap
@@ -383,7 +386,7 @@ def kernel_times(steps, K, stream):
     import torch
     import mla_latent_kv_06_gb300 as mla
     calls = [c for st in steps for c in st]
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in calls]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(40)] for _ in calls]  # up to 39 launches a call
     for ev in evs:  # create the CUDA events before the capture
         for e in ev:
             e.record(stream)

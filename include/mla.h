@@ -143,6 +143,30 @@ int mla_sparse_decode(const mla_dims* d, int dtype, int B, int S,
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Sparse decode of L layers that share one DSA selection ([MLA-KV] §2.2: the
+ * shared layers reuse the indexer's top-k instead of running their own)
+ *
+ * Runs mla_sparse_decode for layers 0..L-1 in order on `stream`, all with the
+ * same T, sel, nsel and topk:
+ *   out[l] = mla_sparse_decode(q[l], Lc[l], Rc[l], kv_b[l], sel, nsel)
+ * q, Lc, Rc, kv_b and out are HOST arrays of L device pointers (one layer
+ * each; the caller keeps them alive for the call only); every layer has the
+ * shapes and dtype mla_sparse_decode documents, with one T_cap.  Layer l
+ * starts once layer l-1 has finished, as in a model whose query for layer l
+ * comes from layer l-1's output.  The arguments of all layers are checked
+ * before the first launch.
+ *   workspace: mla_sparse_decode_workspace_size(d, dtype, B, S, topk) bytes,
+ *              shared by the layers in stream order
+ * Errors: as mla_sparse_decode; L < 1, a null array or a null entry returns
+ * MLA_ERR_INVALID before anything is enqueued.  A launch error in layer l
+ * returns at once, with layers 0..l-1 enqueued.
+ * ------------------------------------------------------------------------- */
+int mla_sparse_decode_layers(const mla_dims* d, int dtype, int L, int B, int S, const void* const* q,
+                             const void* const* Lc, const void* const* Rc, int T_cap, const int32_t* T,
+                             const void* const* kv_b, const int32_t* sel, const int32_t* nsel, int topk,
+                             float* const* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Output projection ([MLA-KV] §2.3: both attention paths end with the o
  * output projection)
  *

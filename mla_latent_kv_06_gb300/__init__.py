@@ -24,7 +24,7 @@ EXPORTS = (
     "mla_last_error", "mla_abi_version", "mla_device_status", "mla_set_wait_limit_ns",
     "mla_set_kernel_events", "mla_last_launch_names",
     "mla_decode_absorbed_workspace_size", "mla_decode_absorbed", "mla_decode_launch_count",
-    "mla_sparse_decode_workspace_size", "mla_sparse_decode",
+    "mla_sparse_decode_workspace_size", "mla_sparse_decode", "mla_sparse_decode_layers",
     "mla_prefill_naive_workspace_size", "mla_prefill_naive", "mla_prefill_naive_noalloc",
     "dsa_index_scores", "dsa_topk_select_workspace_size", "dsa_topk_select",
     "mla_cache_append", "dsa_index_key_append",
@@ -54,6 +54,7 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 _SZ = ctypes.c_size_t
 _DP = ctypes.POINTER(MlaDims)
+_PP = ctypes.POINTER(ctypes.c_void_p)  # host array of device pointers
 
 
 def _declare(lib: ctypes.CDLL) -> None:
@@ -70,6 +71,8 @@ def _declare(lib: ctypes.CDLL) -> None:
         "mla_sparse_decode_workspace_size": (_SZ, [_DP, _I, _I, _I, _I]),
         "mla_sparse_decode": (_I, [_DP, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _P, _I, _P, _P,
                                    _SZ, _P]),
+        "mla_sparse_decode_layers": (_I, [_DP, _I, _I, _I, _I, _PP, _PP, _PP, _I, _P, _PP, _P, _P, _I, _PP, _P,
+                                          _SZ, _P]),
         "mla_prefill_naive_workspace_size": (_SZ, [_DP, _I, _I, _I, _I]),
         "mla_prefill_naive": (_I, [_DP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
         "mla_prefill_naive_noalloc": (_I, [_DP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
@@ -254,6 +257,35 @@ def sparse_decode(q, Lc, Rc, T, kv_b, sel, nsel, dims, out=None, workspace=None,
                                    _ptr(T), _ptr(kv_b), _ptr(sel), _ptr(nsel), topk, _ptr(out),
                                    _ptr(workspace), wsb, _stream(stream)))
     return out
+
+
+def sparse_decode_layers(layers, T, sel, nsel, dims, outs=None, workspace=None, stream=None):
+    """Sparse decode of L layers over one selection: layers is a list of
+    (q, Lc, Rc, kv_b) per layer; returns the list of L outputs [B,S,H,v_head]."""
+    torch = _torch()
+    L = len(layers)
+    q0, Lc0 = layers[0][0], layers[0][1]
+    B, S, H = q0.shape[0], q0.shape[1], q0.shape[2]
+    T_cap = Lc0.shape[1]
+    topk = sel.shape[2]
+    code = _dtype_code(q0)
+    for q, Lc, Rc, kv_b in layers:
+        if q.shape != q0.shape or Lc.shape != Lc0.shape or q.dtype != q0.dtype:
+            raise ValueError("every layer needs the shapes and dtype of layer 0")
+    if outs is None:
+        outs = [torch.empty(B, S, H, dims.v_head, dtype=torch.float32, device=q0.device) for _ in range(L)]
+    d = make_dims(dims)
+    need = lib().mla_sparse_decode_workspace_size(ctypes.byref(d), code, B, S, topk)
+    workspace, wsb = _workspace(need, q0.device, workspace)
+
+    def arr(i):
+        return (ctypes.c_void_p * L)(*[_ptr(layer[i]) for layer in layers])
+
+    _check(lib().mla_sparse_decode_layers(ctypes.byref(d), code, L, B, S, arr(0), arr(1), arr(2), T_cap, _ptr(T),
+                                          arr(3), _ptr(sel), _ptr(nsel), topk,
+                                          (ctypes.c_void_p * L)(*[_ptr(o) for o in outs]), _ptr(workspace), wsb,
+                                          _stream(stream)))
+    return outs
 
 
 def prefill_naive(q, Lc, Rc, kv_b, dims, pos_base: int, out=None, workspace=None, stream=None):

@@ -408,6 +408,45 @@ MLA_EXPORT int mla_sparse_decode_paged(const mla_dims* d, int dtype, int B, int 
   return run_decode(a, dtype, true, workspace, workspace_bytes, stream, "mla_sparse_decode_paged launch");
 }
 
+MLA_EXPORT int mla_sparse_decode_layers(const mla_dims* d, int dtype, int L, int B, int S, const void* const* q,
+                                        const void* const* Lc, const void* const* Rc, int T_cap, const int32_t* T,
+                                        const void* const* kv_b, const int32_t* sel, const int32_t* nsel, int topk,
+                                        float* const* out, void* workspace, size_t workspace_bytes, void* stream) {
+  mla::Geometry g;
+  int rc = check_common(d, dtype, B, S, &g);
+  if (rc) return rc;
+  if (L < 1) return fail(MLA_ERR_INVALID, "L=%d must be >= 1", L);
+  if (T_cap < S) return fail(MLA_ERR_INVALID, "T_cap=%d < S=%d", T_cap, S);
+  if (topk < 1) return fail(MLA_ERR_INVALID, "topk=%d must be >= 1", topk);
+  if (!q || !Lc || !Rc || !kv_b || !out) return fail(MLA_ERR_INVALID, "null per-layer pointer array");
+  if (!T || !sel || !nsel) return fail(MLA_ERR_INVALID, "null tensor pointer");
+  for (int l = 0; l < L; ++l)
+    if (!q[l] || !Lc[l] || !Rc[l] || !kv_b[l] || !out[l])
+      return fail(MLA_ERR_INVALID, "null tensor pointer for layer %d", l);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  mla::call_begin();
+  for (int l = 0; l < L; ++l) {
+    mla::DecodeArgs a{};
+    a.g = g;
+    a.B = B;
+    a.S = S;
+    a.T_cap = T_cap;
+    a.q = q[l];
+    a.Lc = Lc[l];
+    a.Rc = Rc[l];
+    a.T = T;
+    a.kv_b = kv_b[l];
+    a.out = out[l];
+    a.sel = sel;
+    a.nsel = nsel;
+    a.topk = topk;
+    rc = run_decode(a, dtype, true, workspace, workspace_bytes, stream, "mla_sparse_decode_layers launch", false);
+    if (rc) break;
+  }
+  mla::call_end(st);
+  return rc;
+}
+
 // ---------------------------------------------------------------- prefill
 MLA_EXPORT size_t mla_prefill_naive_workspace_size(const mla_dims* d, int dtype, int B, int S,
                                                     int pos_base) {

@@ -527,13 +527,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_con
 
     auto epilogue = [&](int j) -> bool {
       float* op = p.o_part + (size_t)slot * kH * kDl;
-      // The softmax waits for a value product only before a rescale, so tile
-      // j - 1's may still run: wait for it first, which leaves tile j's as the
-      // one phase of o_blk that can be open.
-      if (j > 0) {
-        const bool fail = !mbar_wait(&o_done, (j - 1) & 1, abort, p.flags, p.wait_ns);
-        if (bar_red_or(1, kSoftThreads, fail)) return false;
-      }
+      // Tile j - 1's value product is known retired here (the previous
+      // piece's epilogue, a rescale or the last-tile wait below saw it), so
+      // tile j's is the one phase of o_blk that can be open.
 #pragma unroll 1
       for (int m = mb0; m < mb1; ++m) {
         const bool fail = !mbar_wait(&o_blk[m], j & 1, abort, p.flags, p.wait_ns);
@@ -726,6 +722,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_con
             tmem_st32(tmem + t_lane + kTmemO8 + 64 * m + col0, w);
           }
           tmem_wait_st();
+        }
+      }
+      if (!first && !rescale && cur.last()) {
+        // The piece's epilogue reads O^T once this tile's value product
+        // retires.  The previous tile's must be seen retired before this P
+        // lets this tile's start: otherwise both could complete unseen, and
+        // a parity wait cannot tell phase k of o_done or o_blk from k + 2.
+        fail = !mbar_wait(&o_done, (it - 1) & 1, abort, p.flags, p.wait_ns);
+        if (bar_red_or(2, kSoftThreads, fail)) {
+          ok = false;
+          break;
         }
       }
       fence_proxy_async_smem();

@@ -109,16 +109,6 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
-// Four rows y0..y3 of a 2D tensor (box one row high) into consecutive smem rows.
-__device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* map, int x, int y0, int y1,
-                                            int y2, int y3, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(
-          smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // L2 policy that marks lines for early eviction (data read once).
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t pol;
@@ -136,20 +126,7 @@ __device__ __forceinline__ void tma_load_2d_hint(void* smem_dst, const CUtensorM
       : "memory");
 }
 
-// Pull one box of a 2D tensor into L2 (no shared memory involved).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-
 // Pull a contiguous global range (16-byte aligned, size a multiple of 16) into L2.
-// One 128-byte line into L2 through the load/store unit (never blocks the issuing thread).
-__device__ __forceinline__ void l2_prefetch_line(const void* gaddr) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(gaddr));
-}
-
 __device__ __forceinline__ void l2_prefetch(const void* gaddr, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gaddr), "r"(bytes) : "memory");
 }

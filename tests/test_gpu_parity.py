@@ -319,6 +319,31 @@ def test_dsa_selection_shared_by_later_layers(cuda_lib):
             check_close(out[b, 0], ref, TOL["bf16"], (layer, b))
 
 
+@pytest.mark.parametrize("dtype,dims,T,k", [("bf16", GLM, [9000, 20000], 2048), ("f32", TINY, [300, 41], 64)])
+def test_sparse_decode_layers_over_one_selection(cuda_lib, dtype, dims, T, k):
+    """One call runs L layers' sparse decodes over one selection ([MLA-KV]
+    §2.2): every layer equals the oracle over the selected keys, and equals a
+    separate mla_sparse_decode of that layer bit for bit (the next layer's
+    weights and rows pulled into L2 change no value)."""
+    S, L = 1, 3
+    d = dsa_inputs(2, S, T, max(T), 32, 128, 63, DEV)
+    Tt = torch.tensor(T, dtype=torch.int32, device=DEV)
+    sel, nsel = cuda_lib.topk_select(cuda_lib.index_scores(d["q_idx"], d["w"], d["Ic"], Tt), Tt, k)
+    rsel, rn = sel.cpu().numpy(), nsel.cpu().numpy()
+    xs = [mla_inputs(dims, 2, S, T, max(T), dtype, 80 + layer, DEV) for layer in range(L)]
+    outs = cuda_lib.sparse_decode_layers([(x["q"], x["Lc"], x["Rc"], x["kv_b"]) for x in xs], Tt, sel, nsel, dims)
+    assert cuda_lib.device_status() == 0
+    for layer, (x, out) in enumerate(zip(xs, outs)):
+        one = cuda_lib.sparse_decode(x["q"], x["Lc"], x["Rc"], Tt, x["kv_b"], sel, nsel, dims)
+        assert torch.equal(out, one), layer
+        kvb, o = to_np(x["kv_b"]), to_np(out)
+        for b in range(2):
+            idx = rsel[b, 0, :rn[b, 0]]
+            ref = oracle.attend_absorbed(to_np(x["q"][b, 0]), to_np(x["Lc"][b, idx]), to_np(x["Rc"][b, idx]),
+                                         kvb, dims.qk_nope, T[b] - 1, dims.softmax_scale)
+            check_close(o[b, 0], ref, TOL[dtype], (layer, b))
+
+
 @pytest.mark.parametrize("dtype,dims", [("f32", TINY), ("bf16", GLM)])
 def test_sparse_decode_keep_all_and_subset(cuda_lib, dtype, dims):
     T = [50, 300]
@@ -387,6 +412,27 @@ def test_sparse_decode_more_rows_than_the_in_kernel_plan(cuda_lib):
         ref = oracle.sparse_decode(to_np(x["q"][b:b + 1]), to_np(x["Lc"][b:b + 1]), to_np(x["Rc"][b:b + 1]), [T[b]],
                                    kvb, sel[b:b + 1], nsel[b:b + 1], GLM.qk_nope, GLM.softmax_scale)
         check_close(out[b], ref[0], TOL["bf16"], b)
+
+
+def test_sparse_decode_unsorted_ragged_selection(cuda_lib):
+    """Selections in any order, with repeated keys, and counts that end
+    mid-tile and mid-gather-group (301, 129, 3 of topk 512): each selected
+    entry is one key of the softmax, as in the oracle."""
+    T, k = [5000, 700, 3], 512
+    x = mla_inputs(GLM, 3, 1, T, max(T), "bf16", 90, "cpu")
+    g = _dev(x)
+    r = np.random.default_rng(91)
+    sel = np.zeros((3, 1, k), dtype=np.int32)
+    nsel = np.array([[301], [129], [3]], dtype=np.int32)
+    for b in range(3):
+        n = int(nsel[b, 0])
+        sel[b, 0, :n] = r.integers(0, T[b], n)  # unsorted, repeats allowed
+    out = to_np(cuda_lib.sparse_decode(g["q"], g["Lc"], g["Rc"], g["T"], g["kv_b"], torch.from_numpy(sel).to(DEV),
+                                       torch.from_numpy(nsel).to(DEV), GLM))
+    assert cuda_lib.device_status() == 0
+    ref = oracle.sparse_decode(to_np(x["q"]), to_np(x["Lc"]), to_np(x["Rc"]), T, to_np(x["kv_b"]), sel, nsel,
+                               GLM.qk_nope, GLM.softmax_scale)
+    check_close(out, ref, TOL["bf16"])
 
 
 def test_sparse_decode_flags_future_index(cuda_lib):
