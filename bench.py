@@ -55,37 +55,47 @@ ROTATE_BYTES = 4 * L2_BYTES  # input copies cycled so that a step never finds it
 COPIES_MEM_BYTES = 24 << 30  # device memory the input copies of one workload may take
 ROW_WORKLOADS = ("glm_batched_b32_s1", "glm_batched_b32_s6", "glm_dsa_t65536", "glm_prefill_s2048",
                  "glm_append_b32_s6", "glm_paged_b32_s1", "glm_dsa_t65536_l4", "glm_decode_oproj_t4096",
-                 "glm_batched_b32_s1_fp8", "glm_decode_t4096_fp8")
+                 "glm_batched_b32_s1_fp8", "glm_decode_t4096_fp8", "glm_decode_t65536_fp8", "glm_dsa_t65536_l4_oproj")
 OPROJ_HIDDEN = 6144  # model width of the projection row: a size chosen here, the pages print none
 FP8_LAT_SCALE = 0.05  # scale of the synthetic FP8 latent cache (codes of magnitude 2^-3 .. 30)
 APPEND_RMS_EPS = 1e-6
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a
 # workload's dominant kernel, from one ncu capture of that kernel on this
-# workload.  NCU_TRAFFIC_SOURCES is the digest of the library sources the
-# captures ran on (source_digest()); when the sources differ, every entry is
-# stale and the roofline reports traffic as null.
-NCU_TRAFFIC_SOURCES = "none"
+# workload, with the digest (kernel_digest()) of the sources that kernel was
+# built from.  An entry whose sources have changed since is stale, and the
+# roofline reports its traffic as null.
 NCU_TRAFFIC = {}
+# Library sources each timed kernel is built from, besides the shared headers.
+KERNEL_SOURCES = {
+    "attention": ("decode_tc.cu", "attn_core.cuh"), "absorb": ("decode_tc.cu",), "combine": ("decode_tc.cu",),
+    "merge": ("decode_tc.cu",), "plan_rope": ("decode_tc.cu",), "quant_q": ("decode_tc.cu",),
+    "gather": ("decode_tc.cu",), "absorb_gemm": ("gemm_tc.cu",), "up_gemm": ("gemm_tc.cu",),
+    "index_scores": ("index_tc.cu", "dsa.cu"), "topk_select": ("dsa.cu",), "kv_gemm": ("gemm_tc.cu",),
+    "flash_attention": ("prefill_tc.cu",), "cache_append": ("cache_append.cu",),
+    "index_key_append": ("cache_append.cu",), "oproj_gemv": ("oproj.cu",),
+}
+SHARED_SOURCES = ("common.cuh", "sm100.cuh", "internal.h", "tmap.h", "decode_tc.h", "gemm_tc.h")
 
 
-def source_digest():
-    """sha256 (first 16 hex digits) of the library's CUDA sources and headers."""
-    import glob
+def kernel_digest(kernel):
+    """sha256 (first 16 hex digits) of the library sources a kernel is built from."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_latent_kv_06_gb300", "csrc")
-    for f in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))
-                    + glob.glob(os.path.join(csrc, "*.h"))):
-        h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+    for f in sorted(set(SHARED_SOURCES + KERNEL_SOURCES.get(kernel, ()))):
+        path = os.path.join(csrc, f)
+        if os.path.exists(path):
+            h.update(f.encode())
+            with open(path, "rb") as fh:
+                h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(name, kernel):
-    if NCU_TRAFFIC_SOURCES != source_digest():
+    entry = NCU_TRAFFIC.get((name, kernel))
+    if entry is None or kernel not in KERNEL_SOURCES or entry[1] != kernel_digest(kernel):
         return None
-    return NCU_TRAFFIC.get((name, kernel))
+    return entry[0]
 
 
 def peaks():
@@ -117,10 +127,15 @@ def build_workload(name, device):
     elif name.startswith("glm_batched_b32_s"):
         x = workload_inputs("glm_batched_b32", device, S=int(name[len("glm_batched_b32_s"):]))
         kind = "decode"
-    elif name in ("glm_dsa_t65536", "glm_dsa_t65536_l4"):
+    elif name in ("glm_dsa_t65536", "glm_dsa_t65536_l4", "glm_dsa_t65536_l4_oproj"):
         x = workload_inputs("glm_dsa_t65536", device)
         x["layers"] = [x]
-        if name.endswith("_l4"):  # three more layers reuse the first layer's selection
+        if name.endswith("_oproj"):  # each layer's output projection too
+            g = torch.Generator(device=device)
+            g.manual_seed(SEED_BASE + 9)
+            x["w_o"] = [(torch.randn(OPROJ_HIDDEN, 64 * 256, generator=g, device=device) * 0.02).to(torch.bfloat16)
+                        for _ in range(4)]
+        if "_l4" in name:  # three more layers reuse the first layer's selection
             for layer in range(1, 4):
                 y = mla_inputs(x["dims"], x["B"], x["S"], x["T_list"], x["T_cap"], "bf16", SEED_BASE + 10 + layer,
                                device)
@@ -209,7 +224,9 @@ def build_workload(name, device):
         sc = torch.empty(B, S, T_cap, dtype=torch.float32, device=device)
         sel = torch.empty(B, S, k, dtype=torch.int32, device=device)
         nsel = torch.empty(B, S, dtype=torch.int32, device=device)
-        need = mla.lib().mla_sparse_decode_workspace_size(mla.ctypes.byref(mla.make_dims(d)), mla.MLA_BF16, B, S, k)
+        hidden = OPROJ_HIDDEN if "w_o" in x else 0
+        need = mla.lib().mla_sparse_decode_layers_workspace_size(mla.ctypes.byref(mla.make_dims(d)), mla.MLA_BF16,
+                                                                 B, S, k, hidden)
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
         L = len(x["layers"])
         outs = [out] + [torch.empty_like(out) for _ in range(L - 1)]
@@ -222,19 +239,22 @@ def build_workload(name, device):
                                                    workspace=ws))
         else:  # one call for the layers that share the selection
             layers = [(y["q"], y["Lc"], y["Rc"], y["kv_b"]) for y in x["layers"]]
-            calls.append(lambda: mla.sparse_decode_layers(layers, x["T"], sel, nsel, d, outs=outs, workspace=ws))
+            ys = [torch.empty(R, hidden, dtype=torch.float32, device=device) for _ in range(L)] if hidden else None
+            calls.append(lambda: mla.sparse_decode_layers(layers, x["T"], sel, nsel, d, outs=outs, w_o=x.get("w_o"),
+                                                          ys=ys, workspace=ws))
         info["tokens"] = R * L  # one query token per layer
         ic = 4 * x["Ic"].shape[2] * sum(T_list)
         scores = 4 * R * T_cap
         gathered = row * R * k
         clat = 2 * R * d.H * d.kv_lora
+        proj = (2 * hidden * d.H * d.v_head + out_bytes + 4 * R * hidden) if hidden else 0  # W_O, x, y per layer
         info.update(cache_bytes=gathered * L,
-                    alg_bytes=ic + 2 * scores + L * (gathered + w_uk + w_uv + q_bytes + out_bytes))
+                    alg_bytes=ic + 2 * scores + L * (gathered + w_uk + w_uv + q_bytes + out_bytes + proj))
         work = {"index_scores": ("hbm", ic + scores), "topk_select": ("hbm", scores + 4 * R * k),
                 "gather": ("hbm", 2 * gathered), "absorb": ("hbm", w_uk + q_bytes),
                 "attention": ("hbm", gathered + qcat), "combine": ("hbm", w_uv + out_bytes),
                 "absorb_gemm": ("hbm", w_uk + q_bytes + qcat), "plan_rope": ("hbm", q_bytes),
-                "merge": ("hbm", clat), "up_gemm": ("hbm", w_uv + clat + out_bytes)}
+                "merge": ("hbm", clat), "up_gemm": ("hbm", w_uv + clat + out_bytes), "oproj_gemv": ("hbm", proj)}
         e2e = None
     elif kind == "decode_oproj":
         need = mla.lib().mla_decode_oproj_workspace_size(mla.ctypes.byref(mla.make_dims(d)), mla.MLA_BF16, B, S,
@@ -614,7 +634,7 @@ def host_cpu():
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["mla", "reference"], default="mla")
     ap.add_argument("--workload", default="glm_decode_t4096")

@@ -144,27 +144,36 @@ int mla_sparse_decode(const mla_dims* d, int dtype, int B, int S,
 
 /* ---------------------------------------------------------------------------
  * Sparse decode of L layers that share one DSA selection ([MLA-KV] §2.2: the
- * shared layers reuse the indexer's top-k instead of running their own)
+ * shared layers reuse the indexer's top-k instead of running their own;
+ * §2.3: each attention ends with its o projection)
  *
- * Runs mla_sparse_decode for layers 0..L-1 in order on `stream`, all with the
- * same T, sel, nsel and topk:
+ * For layers l = 0..L-1 in order on `stream`, all with the same T, sel, nsel
+ * and topk:
  *   out[l] = mla_sparse_decode(q[l], Lc[l], Rc[l], kv_b[l], sel, nsel)
- * q, Lc, Rc, kv_b and out are HOST arrays of L device pointers (one layer
- * each; the caller keeps them alive for the call only); every layer has the
- * shapes and dtype mla_sparse_decode documents, with one T_cap.  Layer l
+ *   y[l]   = mla_o_proj(w_o[l], out[l])            (only when w_o != NULL)
+ * q, Lc, Rc, kv_b, out, w_o and y are HOST arrays of L device pointers (one
+ * layer each; the caller keeps them alive for the call only).  Every layer
+ * has the shapes and dtype mla_sparse_decode documents, with one T_cap;
+ *   w_o[l] [hidden, H*v_head] dtype, y[l] [B*S, hidden] float, out[l] 16-byte
+ *   aligned when projected.
+ * w_o == NULL skips the projections (hidden and y are then ignored).  Layer l
  * starts once layer l-1 has finished, as in a model whose query for layer l
- * comes from layer l-1's output.  The arguments of all layers are checked
+ * comes from layer l-1's output; a layer's projection is a programmatic
+ * dependent of its attention.  The arguments of all layers are checked
  * before the first launch.
- *   workspace: mla_sparse_decode_workspace_size(d, dtype, B, S, topk) bytes,
- *              shared by the layers in stream order
- * Errors: as mla_sparse_decode; L < 1, a null array or a null entry returns
- * MLA_ERR_INVALID before anything is enqueued.  A launch error in layer l
- * returns at once, with layers 0..l-1 enqueued.
+ *   workspace: mla_sparse_decode_layers_workspace_size(d, dtype, B, S, topk,
+ *              hidden) bytes (hidden = 0 without projection), 256-byte
+ *              aligned, shared by the layers in stream order
+ * Errors: as mla_sparse_decode and mla_o_proj; L < 1, a null array or a null
+ * entry returns MLA_ERR_INVALID before anything is enqueued.  A launch error
+ * in layer l returns at once, with layers 0..l-1 enqueued.
  * ------------------------------------------------------------------------- */
+size_t mla_sparse_decode_layers_workspace_size(const mla_dims* d, int dtype, int B, int S, int topk, int hidden);
 int mla_sparse_decode_layers(const mla_dims* d, int dtype, int L, int B, int S, const void* const* q,
                              const void* const* Lc, const void* const* Rc, int T_cap, const int32_t* T,
                              const void* const* kv_b, const int32_t* sel, const int32_t* nsel, int topk,
-                             float* const* out, void* workspace, size_t workspace_bytes, void* stream);
+                             float* const* out, const void* const* w_o, int hidden, float* const* y,
+                             void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Output projection ([MLA-KV] §2.3: both attention paths end with the o

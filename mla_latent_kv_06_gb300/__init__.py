@@ -24,7 +24,8 @@ EXPORTS = (
     "mla_last_error", "mla_abi_version", "mla_device_status", "mla_set_wait_limit_ns",
     "mla_set_kernel_events", "mla_last_launch_names",
     "mla_decode_absorbed_workspace_size", "mla_decode_absorbed", "mla_decode_launch_count",
-    "mla_sparse_decode_workspace_size", "mla_sparse_decode", "mla_sparse_decode_layers",
+    "mla_sparse_decode_workspace_size", "mla_sparse_decode", "mla_sparse_decode_layers_workspace_size",
+    "mla_sparse_decode_layers",
     "mla_prefill_naive_workspace_size", "mla_prefill_naive", "mla_prefill_naive_noalloc",
     "dsa_index_scores", "dsa_topk_select_workspace_size", "dsa_topk_select",
     "mla_cache_append", "dsa_index_key_append",
@@ -71,8 +72,9 @@ def _declare(lib: ctypes.CDLL) -> None:
         "mla_sparse_decode_workspace_size": (_SZ, [_DP, _I, _I, _I, _I]),
         "mla_sparse_decode": (_I, [_DP, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _P, _I, _P, _P,
                                    _SZ, _P]),
-        "mla_sparse_decode_layers": (_I, [_DP, _I, _I, _I, _I, _PP, _PP, _PP, _I, _P, _PP, _P, _P, _I, _PP, _P,
-                                          _SZ, _P]),
+        "mla_sparse_decode_layers_workspace_size": (_SZ, [_DP, _I, _I, _I, _I, _I]),
+        "mla_sparse_decode_layers": (_I, [_DP, _I, _I, _I, _I, _PP, _PP, _PP, _I, _P, _PP, _P, _P, _I, _PP, _PP, _I,
+                                          _PP, _P, _SZ, _P]),
         "mla_prefill_naive_workspace_size": (_SZ, [_DP, _I, _I, _I, _I]),
         "mla_prefill_naive": (_I, [_DP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
         "mla_prefill_naive_noalloc": (_I, [_DP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
@@ -259,9 +261,12 @@ def sparse_decode(q, Lc, Rc, T, kv_b, sel, nsel, dims, out=None, workspace=None,
     return out
 
 
-def sparse_decode_layers(layers, T, sel, nsel, dims, outs=None, workspace=None, stream=None):
+def sparse_decode_layers(layers, T, sel, nsel, dims, outs=None, w_o=None, ys=None, workspace=None, stream=None):
     """Sparse decode of L layers over one selection: layers is a list of
-    (q, Lc, Rc, kv_b) per layer; returns the list of L outputs [B,S,H,v_head]."""
+    (q, Lc, Rc, kv_b) per layer.  With w_o (a list of L [hidden, H*v_head]
+    weights) each layer's output is also projected.  Returns the list of L
+    outputs [B,S,H,v_head], and with w_o also the list of L projections
+    [B*S, hidden]."""
     torch = _torch()
     L = len(layers)
     q0, Lc0 = layers[0][0], layers[0][1]
@@ -274,18 +279,26 @@ def sparse_decode_layers(layers, T, sel, nsel, dims, outs=None, workspace=None, 
             raise ValueError("every layer needs the shapes and dtype of layer 0")
     if outs is None:
         outs = [torch.empty(B, S, H, dims.v_head, dtype=torch.float32, device=q0.device) for _ in range(L)]
+    hidden = 0
+    if w_o is not None:
+        if len(w_o) != L:
+            raise ValueError("one projection weight per layer")
+        hidden = w_o[0].shape[0]
+        if ys is None:
+            ys = [torch.empty(B * S, hidden, dtype=torch.float32, device=q0.device) for _ in range(L)]
     d = make_dims(dims)
-    need = lib().mla_sparse_decode_workspace_size(ctypes.byref(d), code, B, S, topk)
+    need = lib().mla_sparse_decode_layers_workspace_size(ctypes.byref(d), code, B, S, topk, hidden)
     workspace, wsb = _workspace(need, q0.device, workspace)
 
-    def arr(i):
-        return (ctypes.c_void_p * L)(*[_ptr(layer[i]) for layer in layers])
+    def arr(ts):
+        return (ctypes.c_void_p * L)(*[_ptr(t) for t in ts])
 
-    _check(lib().mla_sparse_decode_layers(ctypes.byref(d), code, L, B, S, arr(0), arr(1), arr(2), T_cap, _ptr(T),
-                                          arr(3), _ptr(sel), _ptr(nsel), topk,
-                                          (ctypes.c_void_p * L)(*[_ptr(o) for o in outs]), _ptr(workspace), wsb,
-                                          _stream(stream)))
-    return outs
+    _check(lib().mla_sparse_decode_layers(
+        ctypes.byref(d), code, L, B, S, arr([x[0] for x in layers]), arr([x[1] for x in layers]),
+        arr([x[2] for x in layers]), T_cap, _ptr(T), arr([x[3] for x in layers]), _ptr(sel), _ptr(nsel), topk,
+        arr(outs), arr(w_o) if w_o is not None else None, hidden, arr(ys) if w_o is not None else None,
+        _ptr(workspace), wsb, _stream(stream)))
+    return (outs, ys) if w_o is not None else outs
 
 
 def prefill_naive(q, Lc, Rc, kv_b, dims, pos_base: int, out=None, workspace=None, stream=None):

@@ -408,45 +408,6 @@ MLA_EXPORT int mla_sparse_decode_paged(const mla_dims* d, int dtype, int B, int 
   return run_decode(a, dtype, true, workspace, workspace_bytes, stream, "mla_sparse_decode_paged launch");
 }
 
-MLA_EXPORT int mla_sparse_decode_layers(const mla_dims* d, int dtype, int L, int B, int S, const void* const* q,
-                                        const void* const* Lc, const void* const* Rc, int T_cap, const int32_t* T,
-                                        const void* const* kv_b, const int32_t* sel, const int32_t* nsel, int topk,
-                                        float* const* out, void* workspace, size_t workspace_bytes, void* stream) {
-  mla::Geometry g;
-  int rc = check_common(d, dtype, B, S, &g);
-  if (rc) return rc;
-  if (L < 1) return fail(MLA_ERR_INVALID, "L=%d must be >= 1", L);
-  if (T_cap < S) return fail(MLA_ERR_INVALID, "T_cap=%d < S=%d", T_cap, S);
-  if (topk < 1) return fail(MLA_ERR_INVALID, "topk=%d must be >= 1", topk);
-  if (!q || !Lc || !Rc || !kv_b || !out) return fail(MLA_ERR_INVALID, "null per-layer pointer array");
-  if (!T || !sel || !nsel) return fail(MLA_ERR_INVALID, "null tensor pointer");
-  for (int l = 0; l < L; ++l)
-    if (!q[l] || !Lc[l] || !Rc[l] || !kv_b[l] || !out[l])
-      return fail(MLA_ERR_INVALID, "null tensor pointer for layer %d", l);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  mla::call_begin();
-  for (int l = 0; l < L; ++l) {
-    mla::DecodeArgs a{};
-    a.g = g;
-    a.B = B;
-    a.S = S;
-    a.T_cap = T_cap;
-    a.q = q[l];
-    a.Lc = Lc[l];
-    a.Rc = Rc[l];
-    a.T = T;
-    a.kv_b = kv_b[l];
-    a.out = out[l];
-    a.sel = sel;
-    a.nsel = nsel;
-    a.topk = topk;
-    rc = run_decode(a, dtype, true, workspace, workspace_bytes, stream, "mla_sparse_decode_layers launch", false);
-    if (rc) break;
-  }
-  mla::call_end(st);
-  return rc;
-}
-
 // ---------------------------------------------------------------- prefill
 MLA_EXPORT size_t mla_prefill_naive_workspace_size(const mla_dims* d, int dtype, int B, int S,
                                                     int pos_base) {
@@ -696,6 +657,86 @@ MLA_EXPORT int mla_decode_oproj(const mla_dims* d, int dtype, int B, int S, cons
   mla::call_end(st);
   if (e != cudaSuccess) return cuda_fail(e, "mla_decode_oproj projection launch");
   return MLA_OK;
+}
+
+// Layers sharing one DSA selection: workspace = the sparse decode's, then the
+// projection's (bf16 rows of x for its GEMM path).
+namespace {
+struct LayersPlan {
+  size_t dec, op_off, total;
+};
+LayersPlan layers_plan(const mla::Geometry& g, int dtype, int B, int S, int topk, int hidden) {
+  LayersPlan p{};
+  p.dec = (dtype == MLA_BF16 && mla::tc_decode_geometry_ok(g))
+              ? round256(mla::tc_decode_workspace_bytes(g, B, S, topk, topk))
+              : 0;
+  p.op_off = p.dec;
+  p.total = p.op_off + (hidden > 0 ? round256(mla::oproj_workspace_bytes(B * S, g.H * g.Dv, hidden, dtype)) : 0);
+  return p;
+}
+}  // namespace
+
+MLA_EXPORT size_t mla_sparse_decode_layers_workspace_size(const mla_dims* d, int dtype, int B, int S, int topk,
+                                                          int hidden) {
+  mla::Geometry g;
+  if (!resolve(d, &g) || B < 1 || S < 1 || topk < 1 || hidden < 0) return 0;
+  return layers_plan(g, dtype, B, S, topk, hidden).total;
+}
+
+MLA_EXPORT int mla_sparse_decode_layers(const mla_dims* d, int dtype, int L, int B, int S, const void* const* q,
+                                        const void* const* Lc, const void* const* Rc, int T_cap, const int32_t* T,
+                                        const void* const* kv_b, const int32_t* sel, const int32_t* nsel, int topk,
+                                        float* const* out, const void* const* w_o, int hidden, float* const* y,
+                                        void* workspace, size_t workspace_bytes, void* stream) {
+  mla::Geometry g;
+  int rc = check_common(d, dtype, B, S, &g);
+  if (rc) return rc;
+  if (L < 1) return fail(MLA_ERR_INVALID, "L=%d must be >= 1", L);
+  if (T_cap < S) return fail(MLA_ERR_INVALID, "T_cap=%d < S=%d", T_cap, S);
+  if (topk < 1) return fail(MLA_ERR_INVALID, "topk=%d must be >= 1", topk);
+  if (!q || !Lc || !Rc || !kv_b || !out) return fail(MLA_ERR_INVALID, "null per-layer pointer array");
+  if (!T || !sel || !nsel) return fail(MLA_ERR_INVALID, "null tensor pointer");
+  if (w_o && !y) return fail(MLA_ERR_INVALID, "null per-layer pointer array");
+  for (int l = 0; l < L; ++l)
+    if (!q[l] || !Lc[l] || !Rc[l] || !kv_b[l] || !out[l])
+      return fail(MLA_ERR_INVALID, "null tensor pointer for layer %d", l);
+  const int in_dim = g.H * g.Dv;
+  if (w_o)
+    for (int l = 0; l < L; ++l) {
+      rc = check_oproj(B * S, in_dim, hidden, dtype, w_o[l], out[l], y[l]);
+      if (rc) return rc;
+    }
+  const LayersPlan pl = layers_plan(g, dtype, B, S, topk, w_o ? hidden : 0);
+  if (pl.total && (!workspace || workspace_bytes < pl.total))
+    return fail(MLA_ERR_INVALID, "workspace of %zu bytes < %zu required", workspace_bytes, pl.total);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(MLA_ERR_INVALID, "workspace must be 256-byte aligned");
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  mla::call_begin();
+  for (int l = 0; l < L && rc == MLA_OK; ++l) {
+    mla::DecodeArgs a{};
+    a.g = g;
+    a.B = B;
+    a.S = S;
+    a.T_cap = T_cap;
+    a.q = q[l];
+    a.Lc = Lc[l];
+    a.Rc = Rc[l];
+    a.T = T;
+    a.kv_b = kv_b[l];
+    a.out = out[l];
+    a.sel = sel;
+    a.nsel = nsel;
+    a.topk = topk;
+    rc = run_decode(a, dtype, true, pl.dec ? ws : nullptr, pl.dec, stream, "mla_sparse_decode_layers launch", false);
+    if (rc == MLA_OK && w_o) {  // the layer's projection, a programmatic dependent of its attention
+      mla::OprojArgs o{B * S, in_dim, hidden, dtype, w_o[l], out[l], y[l], ws + pl.op_off};
+      cudaError_t e = mla::launch_oproj(o, true, a.flags, a.wait_limit_ns, st);
+      if (e != cudaSuccess) rc = cuda_fail(e, "mla_sparse_decode_layers projection launch");
+    }
+  }
+  mla::call_end(st);
+  return rc;
 }
 
 // ---------------------------------------------------------------- cache append

@@ -878,6 +878,45 @@ __global__ void __launch_bounds__(kAbsThreads, 2) absorb_kernel(const AbsorbPara
 #pragma unroll
     for (int u = 0; u < NV; ++u) wv[u] = __ldg(reinterpret_cast<const uint4*>(W + (size_t)(grp + kAbsGroups * u) * kDl));
   }
+  if (p.prefetch && tid == 0) {
+    // Everything the later kernels of this call read streams from HBM now,
+    // behind W_UK, in the order it is needed: 1/nblk of every sequence's
+    // cache rows (the attention kernel), then W_UV rows (the combine).  It is
+    // issued before the dependency wait: the kernel completes only once its
+    // prefetches have landed, and the wait is time they can use.  A
+    // prefetch changes no data; T and the page table are read here only to
+    // place it (lengths clamped to [0, T_cap], pages checked against the
+    // pool), so values an earlier kernel is still writing can at worst
+    // prefetch the wrong rows.
+    const int nblk = gridDim.x * gridDim.y, me = h * gridDim.x + cb;
+    // Paged caches: units of 16 KB, nine per key tile (eight 16-row blocks of
+    // latent rows, then the tile's rope rows), dealt round-robin to the CTAs.
+    for (int b = 0, base = 0; kPaged && b < p.B; ++b) {
+      const int Tb = min(max(p.T[b], 0), p.T_cap);
+      const int units = (Tb + kTile - 1) / kTile * 9;
+      for (int u = ((me - base) % nblk + nblk) % nblk; u < units; u += nblk) {
+        bool bad_page = false;
+        const long long row = cache_row(p.pages, b, p.T_cap, (u / 9) * kTile, &bad_page);
+        if (bad_page) continue;
+        const int part = u % 9;
+        if (part < 8) l2_prefetch(p.Lc + (size_t)(row + 16 * part) * p.lat_row_bytes, 16 * p.lat_row_bytes);
+        else l2_prefetch(p.Rc + (size_t)row * kDr, kTile * kDr * 2);
+      }
+      base += units;
+    }
+    for (int b = 0; !kPaged && b < p.B; ++b) {
+      const int Tb = min(max(p.T[b], 0), p.T_cap);
+      const size_t lb = (size_t)Tb * p.lat_row_bytes, rb = (size_t)Tb * kDr * 2;
+      const size_t l0 = (lb * me / nblk) & ~(size_t)15, l1 = (lb * (me + 1) / nblk) & ~(size_t)15;
+      const size_t r0 = (rb * me / nblk) & ~(size_t)15, r1 = (rb * (me + 1) / nblk) & ~(size_t)15;
+      const unsigned char* lbase = p.Lc + (size_t)b * p.T_cap * p.lat_row_bytes;
+      const unsigned char* rbase = reinterpret_cast<const unsigned char*>(p.Rc + (size_t)b * p.T_cap * kDr);
+      if (l1 > l0) l2_prefetch(lbase + l0, (uint32_t)(l1 - l0));
+      if (r1 > r0) l2_prefetch(rbase + r0, (uint32_t)(r1 - r0));
+    }
+    const __nv_bfloat16* wuv = p.kv_b + ((size_t)h * (p.Dn + p.Dv) + p.Dn + (size_t)cb * (p.Dv / gridDim.x)) * kDl;
+    l2_prefetch(wuv, (uint32_t)(p.Dv / gridDim.x) * kDl * 2);
+  }
   grid_dep_wait();
   grid_dep_launch();
 
@@ -927,39 +966,6 @@ __global__ void __launch_bounds__(kAbsThreads, 2) absorb_kernel(const AbsorbPara
     if (tid == 0) p.tile_start[0] = 0;
   }
 
-  if (p.prefetch && tid == 0) {
-    // Everything the later kernels of this call read streams from HBM now,
-    // behind W_UK, in the order it is needed: 1/nblk of every sequence's
-    // cache rows (the attention kernel), then W_UV rows (the combine).
-    const int nblk = gridDim.x * gridDim.y, me = h * gridDim.x + cb;
-    // Paged caches: units of 16 KB, nine per key tile (eight 16-row blocks of
-    // latent rows, then the tile's rope rows), dealt round-robin to the CTAs.
-    for (int b = 0, base = 0; kPaged && b < p.B; ++b) {
-      const int Tb = min(max(p.T[b], 0), p.T_cap);
-      const int units = (Tb + kTile - 1) / kTile * 9;
-      for (int u = ((me - base) % nblk + nblk) % nblk; u < units; u += nblk) {
-        bool bad_page = false;
-        const long long row = cache_row(p.pages, b, p.T_cap, (u / 9) * kTile, &bad_page);
-        if (bad_page) continue;
-        const int part = u % 9;
-        if (part < 8) l2_prefetch(p.Lc + (size_t)(row + 16 * part) * p.lat_row_bytes, 16 * p.lat_row_bytes);
-        else l2_prefetch(p.Rc + (size_t)row * kDr, kTile * kDr * 2);
-      }
-      base += units;
-    }
-    for (int b = 0; !kPaged && b < p.B; ++b) {
-      const int Tb = min(max(p.T[b], 0), p.T_cap);
-      const size_t lb = (size_t)Tb * p.lat_row_bytes, rb = (size_t)Tb * kDr * 2;
-      const size_t l0 = (lb * me / nblk) & ~(size_t)15, l1 = (lb * (me + 1) / nblk) & ~(size_t)15;
-      const size_t r0 = (rb * me / nblk) & ~(size_t)15, r1 = (rb * (me + 1) / nblk) & ~(size_t)15;
-      const unsigned char* lbase = p.Lc + (size_t)b * p.T_cap * p.lat_row_bytes;
-      const unsigned char* rbase = reinterpret_cast<const unsigned char*>(p.Rc + (size_t)b * p.T_cap * kDr);
-      if (l1 > l0) l2_prefetch(lbase + l0, (uint32_t)(l1 - l0));
-      if (r1 > r0) l2_prefetch(rbase + r0, (uint32_t)(r1 - r0));
-    }
-    const __nv_bfloat16* wuv = p.kv_b + ((size_t)h * (p.Dn + p.Dv) + p.Dn + (size_t)cb * (p.Dv / gridDim.x)) * kDl;
-    l2_prefetch(wuv, (uint32_t)(p.Dv / gridDim.x) * kDl * 2);
-  }
   if constexpr (!kQabs) {  // rotary part only, every (row, pair) in parallel over the head's CTAs
     rope_rows(p, h, cb * kAbsThreads + tid, gridDim.x * kAbsThreads);
     return;

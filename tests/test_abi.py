@@ -133,16 +133,22 @@ def test_host_rejects_bad_arguments_of_the_fused_and_projection_calls(lib):
                                 None) == mla.MLA_ERR_INVALID
     assert lib.mla_decode_oproj(ctypes.byref(d), 1, 1, 1, p, p, p, 16, p, p, p, 8, p, None, 0,
                                 None) == mla.MLA_ERR_INVALID
-    # sparse decode of several layers: L < 1, null pointer arrays, a null entry in one
+    # sparse decode of several layers: L < 1, null pointer arrays, a null entry in one,
+    # projection weights without outputs, a misaligned projection weight
     arr = (ctypes.c_void_p * 2)(256, 256)
     hole = (ctypes.c_void_p * 2)(256, None)
-    assert lib.mla_sparse_decode_layers(ctypes.byref(d), 1, 0, 1, 1, arr, arr, arr, 16, p, arr, p, p, 8, arr, p,
-                                        1 << 30, None) == mla.MLA_ERR_INVALID
-    assert lib.mla_sparse_decode_layers(ctypes.byref(d), 1, 2, 1, 1, None, arr, arr, 16, p, arr, p, p, 8, arr, p,
-                                        1 << 30, None) == mla.MLA_ERR_INVALID
-    assert lib.mla_sparse_decode_layers(ctypes.byref(d), 1, 2, 1, 1, arr, arr, hole, 16, p, arr, p, p, 8, arr, p,
-                                        1 << 30, None) == mla.MLA_ERR_INVALID
+    odd = (ctypes.c_void_p * 2)(256, 8)
+
+    def layers(L, q, rc, w_o, y):
+        return lib.mla_sparse_decode_layers(ctypes.byref(d), 1, L, 1, 1, q, arr, rc, 16, p, arr, p, p, 8, arr, w_o,
+                                            64, y, p, 1 << 30, None)
+    assert layers(0, arr, arr, None, None) == mla.MLA_ERR_INVALID
+    assert layers(2, None, arr, None, None) == mla.MLA_ERR_INVALID
+    assert layers(2, arr, hole, None, None) == mla.MLA_ERR_INVALID
     assert b"layer 1" in lib.mla_last_error()
+    assert layers(2, arr, arr, arr, None) == mla.MLA_ERR_INVALID
+    assert layers(2, arr, arr, odd, arr) == mla.MLA_ERR_INVALID
+    assert b"aligned" in lib.mla_last_error()
     # prefill without caller workspace: negative pos_base, rebuilt KV above the static scratch
     assert lib.mla_prefill_naive_noalloc(ctypes.byref(d), 1, 1, 4, -1, p, p, p, p, p, None) == mla.MLA_ERR_INVALID
     assert lib.mla_prefill_naive_noalloc(ctypes.byref(d), 1, 1, 2048, 8192, p, p, p, p, p,

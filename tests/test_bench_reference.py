@@ -20,3 +20,20 @@ def test_reference_arm_prints_one_contract_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_ncu_traffic_goes_stale_with_its_kernel_sources(monkeypatch):
+    """A stored ncu traffic figure is reported only while the sources of its
+    kernel are the ones it was captured on."""
+    sys.path.insert(0, ROOT)
+    import bench
+    key = ("glm_decode_t4096", "attention")
+    monkeypatch.setattr(bench, "NCU_TRAFFIC", {key: (4887552, bench.kernel_digest("attention"))})
+    assert bench.ncu_traffic(*key) == 4887552
+    monkeypatch.setattr(bench, "NCU_TRAFFIC", {key: (4887552, "0" * 16)})
+    assert bench.ncu_traffic(*key) is None
+    assert bench.ncu_traffic("glm_decode_t4096", "no_such_kernel") is None
+    # every kernel the bench times has its sources listed, and they exist
+    for k, files in bench.KERNEL_SOURCES.items():
+        for f in files + bench.SHARED_SOURCES:
+            assert os.path.exists(os.path.join(ROOT, "mla_latent_kv_06_gb300", "csrc", f)), (k, f)

@@ -331,7 +331,8 @@ def test_sparse_decode_layers_over_one_selection(cuda_lib, dtype, dims, T, k):
     sel, nsel = cuda_lib.topk_select(cuda_lib.index_scores(d["q_idx"], d["w"], d["Ic"], Tt), Tt, k)
     rsel, rn = sel.cpu().numpy(), nsel.cpu().numpy()
     xs = [mla_inputs(dims, 2, S, T, max(T), dtype, 80 + layer, DEV) for layer in range(L)]
-    outs = cuda_lib.sparse_decode_layers([(x["q"], x["Lc"], x["Rc"], x["kv_b"]) for x in xs], Tt, sel, nsel, dims)
+    layers = [(x["q"], x["Lc"], x["Rc"], x["kv_b"]) for x in xs]
+    outs = cuda_lib.sparse_decode_layers(layers, Tt, sel, nsel, dims)
     assert cuda_lib.device_status() == 0
     for layer, (x, out) in enumerate(zip(xs, outs)):
         one = cuda_lib.sparse_decode(x["q"], x["Lc"], x["Rc"], Tt, x["kv_b"], sel, nsel, dims)
@@ -342,6 +343,19 @@ def test_sparse_decode_layers_over_one_selection(cuda_lib, dtype, dims, T, k):
             ref = oracle.attend_absorbed(to_np(x["q"][b, 0]), to_np(x["Lc"][b, idx]), to_np(x["Rc"][b, idx]),
                                          kvb, dims.qk_nope, T[b] - 1, dims.softmax_scale)
             check_close(o[b, 0], ref, TOL[dtype], (layer, b))
+    # with each layer's output projection ([MLA-KV] §2.3): o_proj of the oracle's sparse decode
+    hidden = 640
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    g = torch.Generator(device="cpu").manual_seed(64)
+    w_o = [(torch.randn(hidden, dims.H * dims.v_head, generator=g) * 0.02).to(tdt).to(DEV) for _ in range(L)]
+    outs2, ys = cuda_lib.sparse_decode_layers(layers, Tt, sel, nsel, dims, w_o=w_o)
+    assert cuda_lib.device_status() == 0
+    for layer, (x, out2, y) in enumerate(zip(xs, outs2, ys)):
+        assert torch.equal(out2, outs[layer]), layer
+        att = oracle.sparse_decode(to_np(x["q"]), to_np(x["Lc"]), to_np(x["Rc"]), T, to_np(x["kv_b"]), rsel, rn,
+                                   dims.qk_nope, dims.softmax_scale)
+        ref = oracle.o_proj(att.reshape(2 * S, -1), to_np(w_o[layer]))
+        assert max_rel_err(to_np(y), ref) < (2e-2 if dtype == "bf16" else 1e-5), layer
 
 
 @pytest.mark.parametrize("dtype,dims", [("f32", TINY), ("bf16", GLM)])
