@@ -1013,12 +1013,6 @@ struct CombineParams {
   unsigned int* flags;
 };
 
-__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_u32(dst)),
-               "l"(src), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
-}
 
 __global__ void __launch_bounds__(kCmbThreads) combine_kernel(const CombineParams p) {
   extern __shared__ __align__(128) unsigned char sm[];

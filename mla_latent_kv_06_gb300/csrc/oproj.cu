@@ -5,16 +5,22 @@
 // y[r, :] = W_O vec(out[r, :, :]).  Its weight is the largest tensor of the
 // layer's attention (hidden x 64*256 values), so the projection is a stream
 // of W_O from HBM:
-//   * up to kOprojGemvRows rows: a GEMV, one warp per output row n, 16-byte
+//   * one or two rows of bf16 weights, in_dim a multiple of 2048 up to 16384:
+//     a ring of whole W_O rows per SM (bulk copies into six 32 KB stages, one
+//     producer thread), eight consumer warps against x held in registers;
+//   * otherwise up to kOprojGemvRows rows: a GEMV, one warp per output row n, 16-byte
 //     loads of W_O[n, :] (read once, marked evict-first in L2) against the
 //     rows of x held in L1; fp32 accumulation, a warp butterfly at the end;
 //   * more rows with bf16 weights: x rounded to bf16, then the batched
 //     tcgen05 GEMM (W_O read once per 128 rows of x).
 // Launched as a programmatic dependent, the GEMV issues its first W_O loads
 // before it waits for the kernel that writes x.
+#include <atomic>
+
 #include "common.cuh"
 #include "gemm_tc.h"
 #include "internal.h"
+#include "sm100.cuh"
 
 namespace mla {
 namespace {
@@ -150,6 +156,162 @@ cudaError_t launch_gemv(const OprojArgs& b, bool pdl, cudaStream_t st) {
   }
 }
 
+// ---------------------------------------------------------------- ring GEMV
+// CTA c owns the output rows [c*hidden/G, (c+1)*hidden/G): one contiguous
+// range of W_O.  Warp 8's lane 0 streams the rows through kRingStages
+// shared-memory stages with bulk copies (contiguous 32 KB reads, the form
+// that keeps HBM busiest); consumer thread t holds x[r, 8(t + 256j) + e] in
+// registers and, per row, dots its 8*per weights with them, reduces over its
+// warp and frees the stage.  The warps' sums meet in shared memory at the
+// end.  W_O is an input no kernel of this library writes, so the ring fills
+// before the dependency wait that x needs.
+constexpr int kRingWarps = 8;
+constexpr int kRingThreads = 32 * (kRingWarps + 1);
+constexpr int kRingStages = 6;
+constexpr int kRingRowMax = 16384;              // weights of one W_O row a stage holds
+constexpr uint32_t kRingStageBytes = kRingRowMax * 2;
+constexpr int kRingRowsMax = 256;               // output rows of one CTA
+constexpr int kRingPer = kRingRowMax / 8 / (32 * kRingWarps);  // 16-byte chunks per thread and row, at most
+
+struct RingArgs {
+  OprojArgs a;
+  unsigned int* flags;
+  long long wait_ns;
+};
+
+template <int R>
+constexpr size_t ring_smem_bytes() {
+  return (size_t)kRingStages * kRingStageBytes + (size_t)kRingWarps * kRingRowsMax * R * sizeof(float);
+}
+
+template <int R>
+__global__ void __launch_bounds__(kRingThreads, 1) oproj_ring_kernel(const RingArgs ra) {
+  using namespace sm100;
+  const OprojArgs& a = ra.a;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  float* part = reinterpret_cast<float*>(smem + (size_t)kRingStages * kRingStageBytes);  // [warp][row][R]
+  __shared__ uint64_t full[kRingStages], empty[kRingStages];
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int r0 = (int)((long long)a.hidden * c / G), n = (int)((long long)a.hidden * (c + 1) / G) - r0;
+  const uint32_t row_bytes = (uint32_t)a.in_dim * 2;
+  volatile int* abort = &abort_flag;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRingStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kRingWarps);
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  grid_dep_launch();
+  if (warp == kRingWarps) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      const unsigned char* W = static_cast<const unsigned char*>(a.w_o) + (size_t)r0 * row_bytes;
+      int last[kRingStages];
+      for (int st = 0; st < kRingStages; ++st) last[st] = -1;
+      for (int i = 0; i < n; ++i) {
+        const int st = i % kRingStages;
+        if (!mbar_wait(&empty[st], ((i / kRingStages) & 1) ^ 1, abort, ra.flags, ra.wait_ns)) break;
+        mbar_arrive_expect_tx(&full[st], row_bytes);
+        bulk_copy_g2s(smem + (size_t)st * kRingStageBytes, W + (size_t)i * row_bytes, row_bytes, &full[st]);
+        last[st] = i;
+      }
+      // never leave with copies in flight
+      volatile int no_abort = 0;
+      const long long drain_ns = ra.wait_ns > 1000000000LL ? ra.wait_ns : 1000000000LL;
+      for (int st = 0; st < kRingStages; ++st)
+        if (last[st] >= 0) mbar_wait(&full[st], (last[st] / kRingStages) & 1, &no_abort, ra.flags, drain_ns);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- consumers
+    const int t = threadIdx.x, per = a.in_dim / (8 * 32 * kRingWarps);
+    grid_dep_wait();  // x comes from the preceding kernel
+    float xr[R][kRingPer * 8];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int j = 0; j < kRingPer; ++j) {
+        if (j >= per) break;
+        const float4* xp = reinterpret_cast<const float4*>(a.x + (size_t)r * a.in_dim + (size_t)(t + 256 * j) * 8);
+        const float4 lo = __ldg(xp), hi = __ldg(xp + 1);
+        xr[r][8 * j + 0] = lo.x;
+        xr[r][8 * j + 1] = lo.y;
+        xr[r][8 * j + 2] = lo.z;
+        xr[r][8 * j + 3] = lo.w;
+        xr[r][8 * j + 4] = hi.x;
+        xr[r][8 * j + 5] = hi.y;
+        xr[r][8 * j + 6] = hi.z;
+        xr[r][8 * j + 7] = hi.w;
+      }
+    for (int i = 0; i < n; ++i) {
+      const int st = i % kRingStages;
+      int okl = 1;
+      if (lane == 0) okl = mbar_wait(&full[st], (i / kRingStages) & 1, abort, ra.flags, ra.wait_ns) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, okl, 0)) break;
+      const uint4* row = reinterpret_cast<const uint4*>(smem + (size_t)st * kRingStageBytes);
+      float acc[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) acc[r] = 0.f;
+#pragma unroll
+      for (int j = 0; j < kRingPer; ++j) {
+        if (j >= per) break;
+        float w[8];
+        WChunk<__nv_bfloat16>::unpack(row[t + 256 * j], w);
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[r] = fmaf(w[e], xr[r][8 * j + e], acc[r]);
+      }
+      __syncwarp();  // every lane has read the stage
+      if (lane == 0) mbar_arrive(&empty[st]);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float v = warp_sum(acc[r]);
+        if (lane == 0) part[((size_t)warp * kRingRowsMax + i) * R + r] = v;
+      }
+    }
+  }
+  __syncthreads();
+  if (*abort) return;  // a wait gave up (MLA_DEV_TIMEOUT is raised): leave y unwritten
+  for (int e = threadIdx.x; e < n * R; e += kRingThreads) {
+    const int i = e / R, r = e % R;
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < kRingWarps; ++w) v += part[((size_t)w * kRingRowsMax + i) * R + r];
+    a.y[(size_t)r * a.hidden + r0 + i] = v;
+  }
+}
+
+bool use_ring(const OprojArgs& a) {
+  return a.dtype == MLA_BF16 && a.R >= 1 && a.R <= 2 && a.in_dim % (8 * 32 * kRingWarps) == 0 &&
+         a.in_dim <= kRingRowMax;
+}
+
+template <int R>
+cudaError_t launch_ring_r(const RingArgs& ra, bool pdl, cudaStream_t st) {
+  static std::atomic<int> attr_set{0};
+  const size_t smem = ring_smem_bytes<R>();
+  if (!attr_set.load()) {
+    cudaError_t e = cudaFuncSetAttribute(oproj_ring_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set.store(1);
+  }
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  long long G = sms;
+  const long long need = ((long long)ra.a.hidden + kRingRowsMax - 1) / kRingRowsMax;  // rows per CTA <= kRingRowsMax
+  if (G < need) G = need;
+  if (G > ra.a.hidden) G = ra.a.hidden;
+  return launch_pdl(oproj_ring_kernel<R>, dim3((unsigned)G), dim3(kRingThreads), smem, st, ra, pdl);
+}
+
 // x (fp32) -> bf16 rows for the GEMM path (n even: in_dim is a multiple of 64 there).
 struct XCast {
   const float* x;
@@ -209,6 +371,10 @@ cudaError_t launch_oproj(const OprojArgs& a, bool pdl, unsigned int* flags, long
     return launch_gemm_tc(g, true, st);
   }
   kernel_mark(st, "oproj_gemv");
+  if (use_ring(a)) {
+    const RingArgs ra{a, flags, wait_ns};
+    return a.R == 1 ? launch_ring_r<1>(ra, pdl, st) : launch_ring_r<2>(ra, pdl, st);
+  }
   cudaError_t e = cudaSuccess;
   for (int r0 = 0; r0 < a.R && e == cudaSuccess; r0 += kOprojGemvRows) {
     OprojArgs b = a;

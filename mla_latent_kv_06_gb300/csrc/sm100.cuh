@@ -126,6 +126,15 @@ __device__ __forceinline__ void tma_load_2d_hint(void* smem_dst, const CUtensorM
       : "memory");
 }
 
+// Contiguous global -> shared bulk copy (both addresses 16-byte aligned, size
+// a multiple of 16), completing `bytes` transactions on `bar`.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 // Pull a contiguous global range (16-byte aligned, size a multiple of 16) into L2.
 __device__ __forceinline__ void l2_prefetch(const void* gaddr, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gaddr), "r"(bytes) : "memory");

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import oracle
-from tests._np import check_close, to_np
+from tests._np import check_close, max_rel_err, to_np
 from workload import GLM, dsa_inputs, fp8_latent_codes, mla_inputs
 
 pytestmark = pytest.mark.gpu
@@ -97,3 +97,19 @@ def test_fp8_decode_timeout_then_recovers(cuda_lib):
     ref = oracle.decode_absorbed(to_np(x["q"]), oracle.dequant_latent(L8.numpy(), 0.05), to_np(x["Rc"]), T,
                                  to_np(x["kv_b"]), GLM.qk_nope, GLM.softmax_scale)
     check_close(to_np(out), ref, 2.0 ** -4)
+
+
+def test_decode_oproj_timeout_then_recovers(cuda_lib):
+    """Decode, then the projection's ring of W_O rows (bulk copies into shared memory)."""
+    T, hidden = [700], 640
+    x = mla_inputs(GLM, 1, 1, T, 700, "bf16", 49, "cpu")
+    g = _dev(x)
+    gen = torch.Generator().manual_seed(50)
+    w = (torch.randn(hidden, GLM.H * GLM.v_head, generator=gen) * 0.02).to(torch.bfloat16)
+    wd = w.to(DEV)
+    y = _timed_out_then_recovers(
+        cuda_lib, lambda: cuda_lib.decode_oproj(g["q"], g["Lc"], g["Rc"], g["T"], g["kv_b"], wd, GLM))
+    att = oracle.decode_absorbed(to_np(x["q"]), to_np(x["Lc"]), to_np(x["Rc"]), T, to_np(x["kv_b"]), GLM.qk_nope,
+                                 GLM.softmax_scale)
+    ref = oracle.o_proj(att.reshape(1, -1), to_np(w)).reshape(1, 1, hidden)
+    assert max_rel_err(to_np(y), ref) < TOL_BF16
