@@ -728,6 +728,8 @@ MLA_EXPORT int mla_sparse_decode_layers(const mla_dims* d, int dtype, int L, int
     a.sel = sel;
     a.nsel = nsel;
     a.topk = topk;
+    a.stage_parity = l & 1;
+    a.gather_pdl = l > 0 ? 1 : 0;
     rc = run_decode(a, dtype, true, pl.dec ? ws : nullptr, pl.dec, stream, "mla_sparse_decode_layers launch", false);
     if (rc == MLA_OK && w_o) {  // the layer's projection, a programmatic dependent of its attention
       mla::OprojArgs o{B * S, in_dim, hidden, dtype, w_o[l], out[l], y[l], ws + pl.op_off};

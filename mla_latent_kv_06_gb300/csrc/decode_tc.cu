@@ -1432,6 +1432,10 @@ __global__ void __launch_bounds__(256) gather_kernel(const GatherParams p) {
       if (c < kDc / 8) dst[c] = v[kk][u];
     }
   }
+  // Launched as a programmatic dependent, this kernel reads only inputs that
+  // no kernel of the call writes; waiting here, after the stores, keeps the
+  // chain's order: its completion implies the previous kernel's.
+  grid_dep_wait();
 }
 
 // ===========================================================================
@@ -1504,8 +1508,8 @@ Plan make_plan(int B, int S, int T_cap, int sparse_topk) {
   pl.off_ml = off;
   off = align256(off + (size_t)pl.P * kH * 2 * 4);
   pl.Kpad = sparse_topk ? (sparse_topk + kTile - 1) / kTile * kTile : 0;
-  pl.off_stage = off;
-  off = align256(off + (size_t)pl.R * pl.Kpad * kDc * 2);
+  pl.off_stage = off;  // two staging buffers: consecutive layers of one call alternate
+  off = align256(off + 2 * (size_t)pl.R * pl.Kpad * kDc * 2);
   pl.off_clat = off;
   off = align256(off + (pl.R > kSmallRows ? (size_t)pl.R * kH * kDl * 2 : 0));
   pl.off_invl = off;
@@ -1533,11 +1537,17 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   int32_t* bad = reinterpret_cast<int32_t*>(w + pl.off_bad);
   float* o_part = reinterpret_cast<float*>(w + pl.off_o);
   float* ml_part = reinterpret_cast<float*>(w + pl.off_ml);
-  __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(w + pl.off_stage);
+  __nv_bfloat16* stage =
+      reinterpret_cast<__nv_bfloat16*>(w + pl.off_stage) + (a.stage_parity & 1) * (size_t)pl.R * pl.Kpad * kDc;
   cudaError_t e;
 
-  // 0. sparse: gather the selected key rows (plain launch: the absorb kernel,
-  //    launched next with programmatic serialization, starts once it retires)
+  // 0. sparse: gather the selected key rows.  A plain launch, except for the
+  //    later layers of one mla_sparse_decode_layers call: those alternate
+  //    between two staging buffers and launch as programmatic dependents of
+  //    the previous layer's last kernel, so their row loads overlap its tail
+  //    (the buffer they write was last read two layers back).  The absorb
+  //    kernel, launched next with programmatic serialization, starts once
+  //    the gather retires.
   if (sparse && a.lat_fp8) return cudaErrorInvalidValue;
   if (sparse) {
     GatherParams gp{};
@@ -1555,8 +1565,7 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
     gp.flags = a.flags;
     gp.pages = a.pages;
     kernel_mark(st, "gather");
-    gather_kernel<<<dim3(pl.Kpad / 32, pl.R), 256, 0, st>>>(gp);
-    e = cudaGetLastError();
+    e = launch_pdl(gather_kernel, dim3(pl.Kpad / 32, pl.R), dim3(256), 0, st, gp, a.gather_pdl != 0);
     if (e != cudaSuccess) return e;
   }
 

@@ -52,6 +52,11 @@ struct DecodeArgs {
   PageTable pages;  // table == nullptr: contiguous [B, T_cap] caches
   int lat_fp8;      // Lc holds E4M3 codes (the FP8 cache); latent = lat_scale * code
   float lat_scale;
+  // Sparse decode inside a multi-layer call: staging buffer 0 or 1, and
+  // whether the gather may launch as a programmatic dependent of the
+  // previous kernel (true only when that buffer was last read two layers back)
+  int stage_parity;
+  int gather_pdl;
 };
 
 cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, bool sparse, cudaStream_t st);
