@@ -25,10 +25,12 @@ def _w(hidden, in_dim, dtype, seed):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-# (1 | 2 rows, in_dim a multiple of 2048, bf16) take the ring of whole W_O rows; the 70000-row case needs
-# more CTAs than there are SMs
+# (1 | 2 rows, in_dim a multiple of 2048, bf16) take the ring of whole W_O rows, other shapes the register
+# GEMV; the 70000-row cases need more CTAs than there are SMs
 @pytest.mark.parametrize("R,in_dim,hidden", [(1, 16384, 6144), (2, 16384, 777), (1, 4096, 100), (2, 2048, 70000),
-                                             (3, 16384, 1000), (8, 64, 77), (5, 200, 64), (1, 8, 1), (2, 64, 30000)])
+                                             (3, 16384, 1000), (4, 16384, 6144), (8, 16384, 777), (5, 8192, 300),
+                                             (6, 4096, 50), (7, 32768, 129), (4, 4096, 70000),
+                                             (8, 64, 77), (5, 200, 64), (1, 8, 1), (2, 64, 30000)])
 def test_o_proj_streaming(cuda_lib, dtype, R, in_dim, hidden):
     g = torch.Generator().manual_seed(R + in_dim + hidden)
     x = torch.randn(R, in_dim, generator=g)

@@ -99,10 +99,12 @@ def test_fp8_decode_timeout_then_recovers(cuda_lib):
     check_close(to_np(out), ref, 2.0 ** -4)
 
 
-def test_decode_oproj_timeout_then_recovers(cuda_lib):
-    """Decode, then the projection's ring of W_O rows (bulk copies into shared memory)."""
-    T, hidden = [700], 640
-    x = mla_inputs(GLM, 1, 1, T, 700, "bf16", 49, "cpu")
+@pytest.mark.parametrize("B", [1, 4])
+def test_decode_oproj_timeout_then_recovers(cuda_lib, B):
+    """Decode, then the projection: the ring of W_O rows (bulk copies into shared memory) for B=1, the
+    register GEMV after the many-row decode chain for B=4."""
+    T, hidden = [700, 300, 129, 512][:B], 640
+    x = mla_inputs(GLM, B, 1, T, 700, "bf16", 49, "cpu")
     g = _dev(x)
     gen = torch.Generator().manual_seed(50)
     w = (torch.randn(hidden, GLM.H * GLM.v_head, generator=gen) * 0.02).to(torch.bfloat16)
@@ -111,5 +113,5 @@ def test_decode_oproj_timeout_then_recovers(cuda_lib):
         cuda_lib, lambda: cuda_lib.decode_oproj(g["q"], g["Lc"], g["Rc"], g["T"], g["kv_b"], wd, GLM))
     att = oracle.decode_absorbed(to_np(x["q"]), to_np(x["Lc"]), to_np(x["Rc"]), T, to_np(x["kv_b"]), GLM.qk_nope,
                                  GLM.softmax_scale)
-    ref = oracle.o_proj(att.reshape(1, -1), to_np(w)).reshape(1, 1, hidden)
+    ref = oracle.o_proj(att.reshape(B, -1), to_np(w)).reshape(B, 1, hidden)
     assert max_rel_err(to_np(y), ref) < TOL_BF16
