@@ -1383,6 +1383,7 @@ struct GatherParams {
 // trips instead of one per 16-byte chunk.
 __global__ void __launch_bounds__(256) gather_kernel(const GatherParams p) {
   constexpr int kKeys = 4, kChunks = (kDc / 8 + 31) / 32;  // 72 chunks of 16 B per row: 3 per lane
+  grid_dep_launch();  // the absorb kernel may start: it loads W_UK, then waits for this grid
   const int r = blockIdx.y, b = r / p.S, s = r % p.S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Tb = p.T[b];

@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(kOpThreads) oproj_gemv_kernel(OprojArgs a) {
       dst[i] = (i < nrows && k < a.in_dim) ? ld_stream(W + (size_t)i * a.in_dim + k) : make_uint4(0, 0, 0, 0);
   };
   if (s0 < s1) load(cur, s0);
+  grid_dep_launch();  // a dependent may start; whatever it reads of ours, it waits for this grid first
   grid_dep_wait();  // x comes from the preceding kernel; the first weights are already on their way
   for (int st = s0; st < s1; ++st) {
     if (st + 1 < s1) load(nxt, st + 1);
