@@ -65,21 +65,22 @@ APPEND_RMS_EPS = 1e-6
 # built from.  An entry whose sources have changed since is stale, and the
 # roofline reports its traffic as null.
 NCU_TRAFFIC = {
-    ("glm_decode_t4096", "attention"): (4892672, "b114adce053c55a6"),
-    ("glm_decode_t16384", "attention"): (19048448, "b114adce053c55a6"),
-    ("glm_decode_t65536", "attention"): (78042880, "b114adce053c55a6"),
-    ("glm_batched_b32_s1", "attention"): (582921728, "b114adce053c55a6"),
-    ("glm_batched_b32_s6", "attention"): (622723072, "b114adce053c55a6"),
-    ("glm_paged_b32_s1", "attention"): (582946048, "b114adce053c55a6"),
-    ("glm_dsa_t65536", "index_scores"): (139144192, "b648fe7b4abb50a3"),
-    ("glm_dsa_t65536_l4", "attention"): (9866752, "b114adce053c55a6"),
-    ("glm_prefill_s2048", "flash_attention"): (790936576, "bec8bd62051f0c5c"),
+    ("glm_decode_t4096", "attention"): (4892928, "d148b18d41b8e5ec"),
+    ("glm_decode_t16384", "attention"): (19048448, "d148b18d41b8e5ec"),
+    ("glm_decode_t65536", "attention"): (77837568, "d148b18d41b8e5ec"),
+    ("glm_batched_b32_s1", "attention"): (583025664, "d148b18d41b8e5ec"),
+    ("glm_batched_b32_s6", "attention"): (622339072, "d148b18d41b8e5ec"),
+    ("glm_paged_b32_s1", "attention"): (582912000, "d148b18d41b8e5ec"),
+    ("glm_dsa_t65536", "index_scores"): (138481408, "b648fe7b4abb50a3"),
+    ("glm_dsa_t65536_l4", "attention"): (9865984, "d148b18d41b8e5ec"),
+    ("glm_prefill_s2048", "flash_attention"): (790831616, "bec8bd62051f0c5c"),
     ("glm_append_b32_s6", "cache_append"): (243200, "917f89d7fe02c7ec"),
-    ("glm_batched_b32_s1_fp8", "attention"): (325418752, "b114adce053c55a6"),
-    ("glm_decode_t4096_fp8", "attention"): (2820352, "b114adce053c55a6"),
-    ("glm_decode_t65536_fp8", "attention"): (42211840, "b114adce053c55a6"),
-    ("glm_decode_oproj_t4096", "oproj_gemv"): (204809472, "e122d10ab32326e4"),
-    ("glm_dsa_t65536_l4_oproj", "oproj_gemv"): (204539648, "e122d10ab32326e4"),
+    ("glm_append_b32_s6", "index_key_append"): (114944, "917f89d7fe02c7ec"),
+    ("glm_batched_b32_s1_fp8", "attention"): (325578752, "d148b18d41b8e5ec"),
+    ("glm_decode_t4096_fp8", "attention"): (2812160, "d148b18d41b8e5ec"),
+    ("glm_decode_t65536_fp8", "attention"): (42193152, "d148b18d41b8e5ec"),
+    ("glm_decode_oproj_t4096", "oproj_gemv"): (205214720, "deda320adf90ae64"),
+    ("glm_dsa_t65536_l4_oproj", "oproj_gemv"): (204561920, "deda320adf90ae64"),
 }
 # Library sources each timed kernel is built from, besides the shared headers.
 KERNEL_SOURCES = {
