@@ -13,12 +13,15 @@
 // rescale stay in registers but for one shared-memory exchange.  Per
 // 128-key tile j:
 //   S(j)  = Q K(j)^T       M=128, N=128, K=256  (Q and K K-major)
-//   O    += P(j-1) V(j-1)  M=128, N=256, K=128  (P K-major, V MN-major)
+//   O    += P(j-1) V(j-1)  M=128, N=256, K=128  (P from TMEM, V MN-major)
 // A 128-key tile halves the score product's instructions and its re-reads of
-// the query block against 64-key tiles; shared memory then holds one K, one V
-// and one P buffer (K released by the score product, V by the value product,
-// P rewritten once the previous value product retired), S is double-buffered
-// in TMEM.
+// the query block against 64-key tiles; shared memory then holds one K and
+// one V buffer (K released by the score product, V by the value product).
+// S is double-buffered in TMEM, and P(j) is written as bf16 over the columns
+// of S(j) that the writing thread has read: the value product takes its A
+// operand from TMEM, so the softmax of tile j never waits for the value
+// product of tile j - 1 (only a rescale of O does), and the S buffer is
+// released by the value product's commit.
 #include <atomic>
 #include <cmath>
 
@@ -43,16 +46,14 @@ constexpr uint32_t kAtom = 128 * 128;       // 16 KB: 128 rows x 64 bf16 (one 12
 constexpr uint32_t kQBytes = 4 * kAtom;     // 64 KB: 256 query dims
 constexpr uint32_t kKBytes = 4 * kAtom;     // 64 KB: 192 k_nope + 64 k_rot dims of 128 keys
 constexpr uint32_t kVBytes = 4 * kAtom;     // 64 KB: 256 value dims of 128 keys (MN-major atoms)
-constexpr uint32_t kPBytes = 2 * kAtom;     // 32 KB: 128 queries x 128 keys bf16 (two K-major atoms)
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kQBytes;
 constexpr uint32_t kOffV = kOffK + kKBytes;
-constexpr uint32_t kOffP = kOffV + kVBytes;
-constexpr uint32_t kPrefillSmem = kOffP + kPBytes + 1024;
+constexpr uint32_t kPrefillSmem = kOffV + kVBytes + 1024;
 constexpr int kSoftThreads = 256;  // eight softmax warps
 constexpr int kPThreads = 64 + kSoftThreads;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 0;    // two S buffers of 128 columns
+constexpr uint32_t kTmemS = 0;    // two S buffers of 128 columns; P(j) over S(j): keys 64h.. at column 64h
 constexpr uint32_t kTmemO = 256;  // O: 256 columns
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kTau = 8.f;
@@ -78,11 +79,11 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
   unsigned char* sQ = smem + kOffQ;
   unsigned char* sK = smem + kOffK;
   unsigned char* sV = smem + kOffV;
-  unsigned char* sP = smem + kOffP;
-  // Single K, V and P buffers: a barrier completes once per tile (phase j for
-  // tile j); S is double-buffered (s_full/s_free[j & 1], phase j >> 1).  No
+  // Single K and V buffers: a barrier completes once per tile (phase j for
+  // tile j); S/P is double-buffered (s_full/s_free[j & 1], phase j >> 1).  No
   // wait can alias: the producer of phase j + 1 of any barrier depends on the
-  // waiter having passed phase j.
+  // waiter having passed phase j (the softmax waits for o_done only before a
+  // rescale, when the value product of the tile has not been issued yet).
   __shared__ uint64_t q_full, q_rope, k_full, k_empty, v_full, v_empty, s_full[2], s_free[2], p_full, o_done,
       mma_done;
   __shared__ uint32_t tmem_base;
@@ -106,7 +107,7 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
     mbar_init(&v_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], kSoftThreads);
+      mbar_init(&s_free[i], 1);  // the value product that read P from the buffer
     }
     mbar_init(&p_full, kSoftThreads);
     mbar_init(&o_done, 1);
@@ -171,21 +172,22 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
     if (lane == 0) {
       const uint32_t idesc_s = idesc_bf16_f32(128, kKT, 0, 0);
       const uint32_t idesc_o = idesc_bf16_f32(128, kDv, 0, 1);
-      const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), v0 = smem_u32(sV), p0 = smem_u32(sP);
+      const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), v0 = smem_u32(sV);
       bool ok = mbar_wait(&q_full, 0, abort, p.flags, p.wait_ns) && mbar_wait(&q_rope, 0, abort, p.flags, p.wait_ns);
       bool issued = false;
       auto pv = [&](int j) -> bool {  // O += P(j) V(j)
         if (!mbar_wait(&p_full, j & 1, abort, p.flags, p.wait_ns)) return false;
         if (!mbar_wait(&v_full, j & 1, abort, p.flags, p.wait_ns)) return false;
         tc_fence_after();
+        const uint32_t pj = tmem + kTmemS + kKT * (j & 1);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // 16 keys per step: P atom kk / 4, V rows 16 kk ..
-          const uint64_t da = smem_desc_sw128(p0 + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
+        for (int kk = 0; kk < 8; ++kk) {  // 16 keys per step: 8 columns of P, V rows 16 kk ..
           const uint64_t db = smem_desc_sw128(v0 + kk * 2048, kAtom, 1024);
-          mma_bf16(tmem + kTmemO, da, db, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + kTmemO, pj + (kk >> 2) * 64 + (kk & 3) * 8, db, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&v_empty);
         mma_commit(&o_done);
+        mma_commit(&s_free[j & 1]);
         return true;
       };
       for (int j = 0; j < nkt && ok; ++j) {
@@ -278,8 +280,6 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
       float v[64];
       tmem_ld64(tmem + t_lane + kTmemS + kKT * st + 64 * half, v);
       tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&s_free[st]);
       const int t0 = j * kKT + 64 * half;
       const int nvalid = row_ok ? max(0, min(64, pos - t0 + 1)) : 0;  // keys t0..t0+nvalid-1 are visible
       float mx = -INFINITY;
@@ -311,13 +311,13 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
         psum += f.x + f.y;
       }
       l = l * alpha + psum;
-      // P(j) overwrites P(j - 1), and a rescale rewrites O: both wait until
-      // O += P(j - 1) V(j - 1) retired (tcgen05.ld/st are warp-wide).
+      // A rescale rewrites O: it waits until O += P(j - 1) V(j - 1) retired
+      // (tcgen05.ld/st are warp-wide, so the warp decides together).
       fail = false;
-      if (j > 0) fail = !__all_sync(0xffffffffu, mbar_wait(&o_done, (j - 1) & 1, abort, p.flags, p.wait_ns));
-      if (!fail) {
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f && j > 0)) {
+      if (__any_sync(0xffffffffu, alpha != 1.f && j > 0)) {
+        fail = !__all_sync(0xffffffffu, mbar_wait(&o_done, (j - 1) & 1, abort, p.flags, p.wait_ns));
+        if (!fail) {
+          tc_fence_after();
 #pragma unroll 1
           for (int cb = 128 * half; cb < 128 * half + 128; cb += 64) {
             float w[64];
@@ -327,20 +327,19 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
             for (int i = 0; i < 64; ++i) w[i] *= alpha;
             tmem_st64(tmem + t_lane + kTmemO + cb, w);
           }
-          tmem_wait_st();
         }
-        // this thread's 64 keys are one 128-byte row of P atom `half`
-        unsigned char* prow = sP + half * kAtom + m * 128;
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
-          *reinterpret_cast<uint4*>(prow + ((cc ^ (m & 7)) << 4)) =
-              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+      }
+      if (!fail) {
+        // P(j): this thread's 64 keys as 32 bf16 pairs, over the first half of
+        // the 64 columns of S(j) it read (the other thread of the row writes
+        // its own columns)
+        tmem_st32(tmem + t_lane + kTmemS + kKT * st + 64 * half, reinterpret_cast<const float*>(pk));
+        tmem_wait_st();
       }
       if (bar_red_or(2, kSoftThreads, fail)) {
         ok = false;
         break;
       }
-      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&p_full);
     }
