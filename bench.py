@@ -65,22 +65,22 @@ APPEND_RMS_EPS = 1e-6
 # built from.  An entry whose sources have changed since is stale, and the
 # roofline reports its traffic as null.
 NCU_TRAFFIC = {
-    ("glm_decode_t4096", "attention"): (4892928, "d148b18d41b8e5ec"),
-    ("glm_decode_t16384", "attention"): (19048448, "d148b18d41b8e5ec"),
-    ("glm_decode_t65536", "attention"): (77837568, "d148b18d41b8e5ec"),
-    ("glm_batched_b32_s1", "attention"): (583025664, "d148b18d41b8e5ec"),
-    ("glm_batched_b32_s6", "attention"): (622339072, "d148b18d41b8e5ec"),
-    ("glm_paged_b32_s1", "attention"): (582912000, "d148b18d41b8e5ec"),
-    ("glm_dsa_t65536", "index_scores"): (138481408, "b648fe7b4abb50a3"),
-    ("glm_dsa_t65536_l4", "attention"): (9865984, "d148b18d41b8e5ec"),
-    ("glm_prefill_s2048", "flash_attention"): (790831616, "bec8bd62051f0c5c"),
-    ("glm_append_b32_s6", "cache_append"): (243200, "917f89d7fe02c7ec"),
-    ("glm_append_b32_s6", "index_key_append"): (114944, "917f89d7fe02c7ec"),
-    ("glm_batched_b32_s1_fp8", "attention"): (325578752, "d148b18d41b8e5ec"),
-    ("glm_decode_t4096_fp8", "attention"): (2812160, "d148b18d41b8e5ec"),
-    ("glm_decode_t65536_fp8", "attention"): (42193152, "d148b18d41b8e5ec"),
-    ("glm_decode_oproj_t4096", "oproj_gemv"): (205214720, "deda320adf90ae64"),
-    ("glm_dsa_t65536_l4_oproj", "oproj_gemv"): (204561920, "deda320adf90ae64"),
+    ("glm_decode_t4096", "attention"): (4892416, "856d4e4a5bcb31a5"),
+    ("glm_decode_t16384", "attention"): (19048192, "856d4e4a5bcb31a5"),
+    ("glm_decode_t65536", "attention"): (77968384, "856d4e4a5bcb31a5"),
+    ("glm_batched_b32_s1", "attention"): (583041024, "856d4e4a5bcb31a5"),
+    ("glm_batched_b32_s6", "attention"): (622261248, "856d4e4a5bcb31a5"),
+    ("glm_paged_b32_s1", "attention"): (582642944, "856d4e4a5bcb31a5"),
+    ("glm_dsa_t65536", "index_scores"): (138837248, "b77f6e9cbb7e9188"),
+    ("glm_dsa_t65536_l4", "attention"): (9866496, "856d4e4a5bcb31a5"),
+    ("glm_prefill_s2048", "flash_attention"): (795747072, "4cd35ca72f3b5a88"),
+    ("glm_append_b32_s6", "cache_append"): (243200, "cce2f582d5b0591c"),
+    ("glm_append_b32_s6", "index_key_append"): (115968, "cce2f582d5b0591c"),
+    ("glm_batched_b32_s1_fp8", "attention"): (325122560, "856d4e4a5bcb31a5"),
+    ("glm_decode_t4096_fp8", "attention"): (2807552, "856d4e4a5bcb31a5"),
+    ("glm_decode_t65536_fp8", "attention"): (42189312, "856d4e4a5bcb31a5"),
+    ("glm_decode_oproj_t4096", "oproj_gemv"): (205005312, "1888d6993a2c0d56"),
+    ("glm_dsa_t65536_l4_oproj", "oproj_gemv"): (204694528, "1888d6993a2c0d56"),
 }
 # Library sources each timed kernel is built from, besides the shared headers.
 KERNEL_SOURCES = {
