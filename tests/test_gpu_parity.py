@@ -319,13 +319,15 @@ def test_dsa_selection_shared_by_later_layers(cuda_lib):
             check_close(out[b, 0], ref, TOL["bf16"], (layer, b))
 
 
-@pytest.mark.parametrize("dtype,dims,T,k", [("bf16", GLM, [9000, 20000], 2048), ("f32", TINY, [300, 41], 64)])
-def test_sparse_decode_layers_over_one_selection(cuda_lib, dtype, dims, T, k):
+@pytest.mark.parametrize("dtype,dims,T,k,L", [("bf16", GLM, [9000, 20000], 2048, 3), ("bf16", GLM, [3000, 129], 512, 1),
+                                               ("f32", TINY, [300, 41], 64, 3)])
+def test_sparse_decode_layers_over_one_selection(cuda_lib, dtype, dims, T, k, L):
     """One call runs L layers' sparse decodes over one selection ([MLA-KV]
     §2.2): every layer equals the oracle over the selected keys, and equals a
-    separate mla_sparse_decode of that layer bit for bit (the next layer's
-    weights and rows pulled into L2 change no value)."""
-    S, L = 1, 3
+    separate mla_sparse_decode of that layer bit for bit (later layers'
+    gathers, launched early into alternating staging buffers, change no
+    value)."""
+    S = 1
     d = dsa_inputs(2, S, T, max(T), 32, 128, 63, DEV)
     Tt = torch.tensor(T, dtype=torch.int32, device=DEV)
     sel, nsel = cuda_lib.topk_select(cuda_lib.index_scores(d["q_idx"], d["w"], d["Ic"], Tt), Tt, k)
