@@ -83,6 +83,28 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_kernel(const __grid_constan
     prefetch_tensormap(&p.mA);
     prefetch_tensormap(&p.mB);
   }
+  // B is a weight no kernel of this library writes: the B halves of the first
+  // ring stages load before the dependency wait that A needs (thread 0 is the
+  // producer lane; each stage expects its A and B bytes together).
+  int npre = 0;
+  if (threadIdx.x == 0) {
+    for (int t = blockIdx.x; t < ntiles && npre < Cfg::kStages; t += gridDim.x) {
+      int n0, m0, z;
+      tile_of(t, &n0, &m0, &z);
+      const int brow = (int)(p.b_row0 + (long long)z * p.b_rows_per_z);
+      for (int kb = 0; kb < nk && npre < Cfg::kStages; ++kb, ++npre) {
+        unsigned char* sB = smem + npre * Cfg::kStage + Cfg::kA;
+        mbar_arrive_expect_tx(&full_bar[npre], Cfg::kStage);
+        if (!kBMN) {
+          tma_load_2d(sB, &p.mB, (int)p.b_col0 + kb * 64, brow + n0, &full_bar[npre]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j)
+            tma_load_2d(sB + j * 8192, &p.mB, (int)p.b_col0 + n0 + 64 * j, brow + kb * 64, &full_bar[npre]);
+        }
+      }
+    }
+  }
   if (warp == 1) {
     tmem_alloc(&tmem_base, 2 * BN);
     tmem_relinquish();
@@ -105,10 +127,15 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_kernel(const __grid_constan
         const int brow = (int)(p.b_row0 + (long long)z * p.b_rows_per_z);
         for (int kb = 0; kb < nk && ok; ++kb, ++g) {
           const int st = g % Cfg::kStages, u = g / Cfg::kStages;
-          ok = mbar_wait(&empty_bar[st], (u & 1) ^ 1, abort, p.flags, p.wait_ns);
-          if (!ok) break;
           unsigned char* sA = smem + st * Cfg::kStage;
           unsigned char* sB = sA + Cfg::kA;
+          if (g < npre) {  // B already on its way: the stage's A half
+            tma_load_3d(sA, &p.mA, kb * 64, z, m0, &full_bar[st]);
+            last = g;
+            continue;
+          }
+          ok = mbar_wait(&empty_bar[st], (u & 1) ^ 1, abort, p.flags, p.wait_ns);
+          if (!ok) break;
           mbar_arrive_expect_tx(&full_bar[st], Cfg::kStage);
           tma_load_3d(sA, &p.mA, kb * 64, z, m0, &full_bar[st]);
           if (!kBMN) {
