@@ -71,7 +71,7 @@ NCU_TRAFFIC = {
     ("glm_batched_b32_s1", "attention"): (583041024, "856d4e4a5bcb31a5"),
     ("glm_batched_b32_s6", "attention"): (622261248, "856d4e4a5bcb31a5"),
     ("glm_paged_b32_s1", "attention"): (582642944, "856d4e4a5bcb31a5"),
-    ("glm_dsa_t65536", "index_scores"): (138837248, "b77f6e9cbb7e9188"),
+    ("glm_dsa_t65536", "index_scores"): (139196928, "d8d0b28c3c50688c"),
     ("glm_dsa_t65536_l4", "attention"): (9866496, "856d4e4a5bcb31a5"),
     ("glm_prefill_s2048", "flash_attention"): (795747072, "4cd35ca72f3b5a88"),
     ("glm_append_b32_s6", "cache_append"): (243200, "cce2f582d5b0591c"),

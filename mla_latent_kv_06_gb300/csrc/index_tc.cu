@@ -116,6 +116,14 @@ __global__ void __launch_bounds__(kIThreads, 1) index_tc_kernel(const __grid_con
     abort_flag = 0;
     fence_mbar_init();
     prefetch_tensormap(&p.mI);
+    // the first tiles stream in while the query block is formed (thread 0 is
+    // the producer lane; the ring's stages are free at the start)
+    const int y0 = b * p.T_cap + tb * kITile;
+    for (int i = 0; i < na && i < kIStages; ++i) {
+      mbar_arrive_expect_tx(&full_bar[i], kITileBytes);
+      for (int a = 0; a < 4; ++a)
+        tma_load_2d(sTile + i * kITileBytes + a * kIAtomBytes, &p.mI, 32 * a, y0 + i * kITile, &full_bar[i]);
+    }
   }
   if (warp == 1) {
     tmem_alloc(&tmem_base, 64);
@@ -161,8 +169,9 @@ __global__ void __launch_bounds__(kIThreads, 1) index_tc_kernel(const __grid_con
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const int y0 = b * p.T_cap + tb * kITile;
-      int last = -1;
-      for (int i = 0; i < na; ++i) {
+      const int i0 = na < kIStages ? na : kIStages;  // issued before the query block
+      int last = i0 - 1;
+      for (int i = i0; i < na; ++i) {
         const int st = i % kIStages;
         if (!mbar_wait(&empty_bar[st], ((i / kIStages) & 1) ^ 1, abort, p.flags, p.wait_ns)) break;
         mbar_arrive_expect_tx(&full_bar[st], kITileBytes);
