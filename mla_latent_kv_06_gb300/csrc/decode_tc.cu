@@ -211,19 +211,28 @@ __global__ void __launch_bounds__(256) quant_q_kernel(const QuantParams p) {
 // arithmetic is quant_q_kernel's; the bytes land where a 128-byte-swizzled TMA
 // load of the 640-byte quantised rows puts them (16-byte chunk c of row r at
 // chunk c ^ (r & 7)).
+// All eight rows are loaded before the first store: the stores go through
+// generic pointers, which the compiler cannot separate from the loads, so
+// loads placed after them would each wait a full L2 round trip.
 __device__ __forceinline__ void quantise_query_rows(const AttnParams& p, size_t row0, int w, int lane,
                                                     unsigned char* sQ8, float* fh) {
+  uint4 raw8[8][2];
+  uint32_t rp8[8];
+#pragma unroll
+  for (int hh = 0; hh < 8; ++hh) {
+    const __nv_bfloat16* src = p.qcat + (row0 + 8 * w + hh) * kDc;
+    raw8[hh][0] = *reinterpret_cast<const uint4*>(src + 16 * lane);
+    raw8[hh][1] = *reinterpret_cast<const uint4*>(src + 16 * lane + 8);
+    rp8[hh] = *reinterpret_cast<const uint32_t*>(src + kDl + 2 * lane);
+  }
+#pragma unroll
   for (int hh = 0; hh < 8; ++hh) {
     const int h = 8 * w + hh;
-    const __nv_bfloat16* src = p.qcat + (row0 + h) * kDc;
-    uint4 raw[2];
-    raw[0] = *reinterpret_cast<const uint4*>(src + 16 * lane);
-    raw[1] = *reinterpret_cast<const uint4*>(src + 16 * lane + 8);
-    const uint32_t rp = *reinterpret_cast<const uint32_t*>(src + kDl + 2 * lane);
+    const uint32_t rp = rp8[hh];
     float v[16];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw[k]);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw8[hh][k]);
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         const float2 f = __bfloat1622float2(b2[t]);
@@ -1001,6 +1010,7 @@ constexpr int kCmbRows = 8;
 constexpr int kCPitch = kDl + 4;   // floats per clat row in smem
 constexpr int kMaxPieces = 256;    // splits per row (<= CTAs of the attention grid)
 constexpr uint32_t kCmbWBytes = kCmbJ * kDl * 2;
+constexpr int kCmbPre = 4;         // splits per warp whose partials load before the weights are formed
 
 struct CombineParams {
   const __nv_bfloat16* kv_b;
@@ -1090,10 +1100,31 @@ __global__ void __launch_bounds__(kCmbThreads) combine_kernel(const CombineParam
       inv_l[warp] = (cbad[row] || N <= 0) ? __int_as_float(0x7fc00000) : 1.f;
     }
   }
-  grid_dep_wait();  // partials come from the attention kernel
+  __syncthreads();  // every warp reads the lists below
+  grid_dep_wait();   // partials come from the attention kernel
   bool w_ready = false;
+  // (b) deals the 8 warps to the rows (wpr each); warp k takes every wpr-th
+  // split of its row.  The partials of its first kCmbPre splits are loaded
+  // now, so that they are in flight together with the (m, l) loads of (a)
+  // instead of waiting for the weights.
+  const int wpr = (kCmbThreads / 32) / nr;  // nr <= kCmbRows = 8
+  const int bw = warp / wpr, sk = warp % wpr;
+  float4 pre[kCmbPre][4];
+  if (bw < nr) {
+    const int cnt = pcnt[bw];
+#pragma unroll
+    for (int u = 0; u < kCmbPre; ++u) {
+      const int i = sk + u * wpr;
+      if (i < cnt) {
+        const float4* src =
+            reinterpret_cast<const float4*>(p.o_part + ((size_t)pslot[bw * kMaxPieces + i] * kH + h) * kDl);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) pre[u][q] = src[lane + 32 * q];
+      }
+    }
+  }
   {
-    // ... then, with the partials complete, their normalised weights
+    // (a) with the partials complete, their normalised weights
     if (warp < nr) {
       __syncwarp();  // entries were listed by other lanes
       const int cnt = pcnt[warp];
@@ -1115,20 +1146,32 @@ __global__ void __launch_bounds__(kCmbThreads) combine_kernel(const CombineParam
       for (int i = lane; i < cnt; i += 32) pm[warp * kMaxPieces + i] /= L;
     }
     __syncthreads();
-    // (b) clat[w][l] = sum_i weight_i * O_i[h][l] for every row at once: the
-    //     8 warps are dealt to the rows (wpr each); warp k takes every wpr-th
-    //     split of its row (all of their loads in flight together), lane
-    //     covers latents 4*lane + 128*q; the warp sums meet in shared memory.
+    // (b) clat[w][l] = sum_i weight_i * O_i[h][l] for every row at once:
+    //     lane covers latents 4*lane + 128*q; the warp sums meet in shared
+    //     memory.
     {
-      const int wpr = (kCmbThreads / 32) / nr;  // nr <= kCmbRows = 8
-      const int w = warp / wpr, sk = warp % wpr;
+      const int w = bw;
       if (w < nr) {
         const int cnt = pcnt[w];
         float4 acc[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < kCmbPre; ++u) {
+          const int i = sk + u * wpr;
+          if (i < cnt) {
+            const float wg = pm[w * kMaxPieces + i];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              acc[q].x = fmaf(wg, pre[u][q].x, acc[q].x);
+              acc[q].y = fmaf(wg, pre[u][q].y, acc[q].y);
+              acc[q].z = fmaf(wg, pre[u][q].z, acc[q].z);
+              acc[q].w = fmaf(wg, pre[u][q].w, acc[q].w);
+            }
+          }
+        }
 #pragma unroll 4
-        for (int i = sk; i < cnt; i += wpr) {
+        for (int i = sk + kCmbPre * wpr; i < cnt; i += wpr) {
           const float wg = pm[w * kMaxPieces + i];
           const float4* src =
               reinterpret_cast<const float4*>(p.o_part + ((size_t)pslot[w * kMaxPieces + i] * kH + h) * kDl);
