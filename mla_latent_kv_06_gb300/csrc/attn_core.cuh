@@ -633,32 +633,32 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, AttnShared& sh
         for (int cc = 0; cc < 8; ++cc) *reinterpret_cast<uint4*>(lr + 16 * cc) = make_uint4(0, 0, 0, 0);
       }
     }
-    if (!first) {
-      // O^T is stable once the previous value product retired
+    if (rescale) {  // (never on a piece's first tile)
+      // O^T is stable once the previous value product retired.  Without a
+      // rescale the softmax leaves O^T alone and needs no wait: the value
+      // product of this tile is queued behind the previous one anyway.
       fail = !mbar_wait(&sh.o_done, (it - 1) & 1, abort, p.flags, p.wait_ns);
       if (bar_red_or(2, kSoftThreads, fail)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      if (rescale) {
 #pragma unroll 1
-        for (int m = mb0; m < mb1; ++m) {
-          float w[32];
-          tmem_ld32(tmem + t_lane + kTmemO + 64 * m + col0, w);
-          tmem_wait_ld();
+      for (int m = mb0; m < mb1; ++m) {
+        float w[32];
+        tmem_ld32(tmem + t_lane + kTmemO + 64 * m + col0, w);
+        tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const float4 al = *reinterpret_cast<const float4*>(&sh.alpha_sh[col0 + i]);
-            w[i] *= al.x;
-            w[i + 1] *= al.y;
-            w[i + 2] *= al.z;
-            w[i + 3] *= al.w;
-          }
-          tmem_st32(tmem + t_lane + kTmemO + 64 * m + col0, w);
+        for (int i = 0; i < 32; i += 4) {
+          const float4 al = *reinterpret_cast<const float4*>(&sh.alpha_sh[col0 + i]);
+          w[i] *= al.x;
+          w[i + 1] *= al.y;
+          w[i + 2] *= al.z;
+          w[i + 3] *= al.w;
         }
-        tmem_wait_st();
+        tmem_st32(tmem + t_lane + kTmemO + 64 * m + col0, w);
       }
+      tmem_wait_st();
     }
     fence_proxy_async_smem();
     tc_fence_before();
