@@ -375,6 +375,14 @@ __device__ __forceinline__ void attn_mma(const AttnParams& p, AttnShared& sh, co
   const uint32_t idS = idesc_bf16_f32(128, 64, 0, 0);
   const uint32_t idO = idesc_bf16_f32(128, 64, 1, 1);
   const uint32_t kv0 = smem_u32(cx.sKV), q0 = smem_u32(cx.sQ);
+  // Operand descriptors of the first K step; a later step or atom adds its
+  // byte offset / 16 to the start-address field (shared-memory addresses stay
+  // below 256 KB, so the 14-bit field never carries).  The issuing thread then
+  // spends a few instructions per MMA.
+  const uint64_t dS0 = smem_desc_sw128(kv0, 16, 1024);                     // score A: key atoms, K-major
+  const uint64_t dQ0 = smem_desc_sw128(q0, 16, 1024);                      // score B: query atoms
+  const uint64_t dO0 = smem_desc_sw128(kv0, kSlotBytes, 1024);             // value A: latent atoms, MN-major
+  const uint64_t dP0 = smem_desc_sw128(kv0 + 8 * kSlotBytes, kSlotBytes, 1024);  // value B: P^T, MN-major
   TileCursor<kSparse> c;
   c.start(p, cx.ts, cx.NR, cx.N, cx.g, cx.s, cx.row0);
   int it = 0, pc = -1;
@@ -399,12 +407,10 @@ __device__ __forceinline__ void attn_mma(const AttnParams& p, AttnShared& sh, co
       if (!ok) break;
       tc_fence_after();
       if (lane == 0) {
+        const uint64_t da = dS0 + (uint64_t)(a * (kSlotBytes >> 4));
+        const uint64_t db = dQ0 + (uint64_t)(a * (kQAtomBytes >> 4));
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t da = smem_desc_sw128(kv0 + a * kSlotBytes + kk * 32, 16, 1024);
-          const uint64_t db = smem_desc_sw128(q0 + a * kQAtomBytes + kk * 32, 16, 1024);
-          mma_bf16(tmem + kTmemS, da, db, idS, (a | kk) != 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 4; ++kk) mma_bf16(tmem + kTmemS, da + 2 * kk, db + 2 * kk, idS, (a | kk) != 0 ? 1u : 0u);
       }
       __syncwarp();
       issued = true;
@@ -426,10 +432,15 @@ __device__ __forceinline__ void attn_mma(const AttnParams& p, AttnShared& sh, co
           mma_commit(&sh.empty_bar[2 * m + 1]);
         }
       for (int m = mb0; m < mb1; ++m) {
-        for (int kk = 0; kk < ksteps; ++kk) {
-          const uint64_t da = smem_desc_sw128(kv0 + (2 * m) * kSlotBytes + kk * 2048, kSlotBytes, 1024);
-          const uint64_t db = smem_desc_sw128(kv0 + 8 * kSlotBytes + kk * 2048, kSlotBytes, 1024);
-          mma_bf16(tmem + kTmemO + 64 * m, da, db, idO, (kk > 0 || !first) ? 1u : 0u);
+        const uint64_t da = dO0 + (uint64_t)(2 * m * (kSlotBytes >> 4));
+        const uint32_t dt = tmem + kTmemO + 64 * m;
+        if (ksteps == kTile / 16) {  // a full tile: the issue loop unrolled
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_bf16(dt, da + 128 * kk, dP0 + 128 * kk, idO, (kk > 0 || !first) ? 1u : 0u);
+        } else {
+          for (int kk = 0; kk < ksteps; ++kk)
+            mma_bf16(dt, da + 128 * kk, dP0 + 128 * kk, idO, (kk > 0 || !first) ? 1u : 0u);
         }
         mma_commit(&sh.empty_bar[2 * m]);
         mma_commit(&sh.empty_bar[2 * m + 1]);

@@ -431,6 +431,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_con
     const uint32_t idS8 = idesc_e4m3_f32(128, 64, 0, 0);
     const uint32_t idO8 = idesc_e4m3_f32(128, 64, 1, 0);
     const uint32_t kv0 = smem_u32(sKV), q0 = smem_u32(sQ8);
+    // First-step operand descriptors; a later step, atom or buffer adds its
+    // byte offset / 16 (addresses stay below 256 KB: no carry out of the field).
+    const uint64_t dS0 = smem_desc_sw128(kv0, 16, 1024);                    // score A, K-major
+    const uint64_t dQ0 = smem_desc_sw128(q0, 16, 1024);                     // score B
+    const uint64_t dV0 = smem_desc_sw128(kv0, kSlotBytes, 1024);            // value A, MN-major codes
+    const uint64_t dP0 = smem_desc_sw128(kv0 + 4 * kSlotBytes, 16, 1024);   // value B: P^T codes, K-major
     TileCursor<false> c;
     c.start(p, ts, NR, N, g, s, row0);
     int it = 0, pc = -1;
@@ -446,14 +452,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_con
       tc_fence_after();
       if (lane == 0) {
         const int u = j & 1;
-        const uint32_t base = kv0 + u * kTile8Bytes;
+        const uint64_t ub = (uint64_t)(u * (kTile8Bytes >> 4));
         for (int m = 0; m < 4; ++m)
           if (m < mb0 || m >= mb1) mma_commit(&empty_bar[u][m]);  // another part's block: free now
         for (int m = mb0; m < mb1; ++m) {
-          for (int kk = 0; kk < ksteps; ++kk) {
-            const uint64_t da = smem_desc_sw128(base + m * kSlotBytes + kk * 4096, kSlotBytes, 1024);
-            const uint64_t db = smem_desc_sw128(base + 4 * kSlotBytes + kk * 32, 16, 1024);
-            mma_f8(tmem + kTmemO8 + 64 * m, da, db, idO8, (kk > 0 || !firstj) ? 1u : 0u);
+          const uint64_t da = dV0 + ub + (uint64_t)(m * (kSlotBytes >> 4));
+          const uint64_t db = dP0 + ub;
+          const uint32_t dt = tmem + kTmemO8 + 64 * m;
+          if (ksteps == kTile / 32) {  // a full tile: the issue loop unrolled
+#pragma unroll
+            for (int kk = 0; kk < kTile / 32; ++kk)
+              mma_f8(dt, da + 256 * kk, db + 2 * kk, idO8, (kk > 0 || !firstj) ? 1u : 0u);
+          } else {
+            for (int kk = 0; kk < ksteps; ++kk) mma_f8(dt, da + 256 * kk, db + 2 * kk, idO8, (kk > 0 || !firstj) ? 1u : 0u);
           }
           mma_commit(&empty_bar[u][m]);
           mma_commit(&o_blk[m]);  // the epilogue may read this block while the next ones run
@@ -477,19 +488,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_con
       ok = ok && wait(&s_free[u], ((it >> 1) & 1) ^ 1);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t base = kv0 + u * kTile8Bytes;
+      const uint64_t ub = (uint64_t)(u * (kTile8Bytes >> 4));
       for (int a = 0; a < kAtoms8 && ok; ++a) {
         ok = wait(&full_bar[u][a], (it >> 1) & 1);
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
           // 32 bytes of K per instruction: 32 codes, or 16 bf16 for the rope atom
+          const uint64_t da = dS0 + ub + (uint64_t)(a * (kSlotBytes >> 4));
+          const uint64_t db = dQ0 + (uint64_t)(a * (kQAtomBytes >> 4));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t da = smem_desc_sw128(base + a * kSlotBytes + kk * 32, 16, 1024);
-            const uint64_t db = smem_desc_sw128(q0 + a * kQAtomBytes + kk * 32, 16, 1024);
-            if (a < 4) mma_f8(tmem + kTmemS + 64 * u, da, db, idS8, (a | kk) != 0 ? 1u : 0u);
-            else mma_bf16(tmem + kTmemS + 64 * u, da, db, idS, 1u);
+            if (a < 4) mma_f8(tmem + kTmemS + 64 * u, da + 2 * kk, db + 2 * kk, idS8, (a | kk) != 0 ? 1u : 0u);
+            else mma_bf16(tmem + kTmemS + 64 * u, da + 2 * kk, db + 2 * kk, idS, 1u);
           }
         }
         __syncwarp();
