@@ -85,6 +85,15 @@ struct AttnParams {
   PageTable pages;  // dense path: key tiles come from pages (page_size a multiple of kTile)
 };
 
+// One arrival per warp on a barrier initialised with the number of arriving
+// warps: after the warp syncs, lane 0's release-arrive publishes what every
+// lane wrote before it (ordered by the fences each lane issued first).  All
+// 32 lanes call it.
+__device__ __forceinline__ void mbar_arrive_warp(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // Reduce 64 per-lane values over the 32 lanes of a warp; afterwards lane L
 // holds the results for entries 2L and 2L+1 in v[0], v[1].
 template <bool kMax>
@@ -266,8 +275,8 @@ __device__ __forceinline__ void attn_init_barriers(AttnShared& sh) {
   mbar_init(&sh.q_full, 1);
   mbar_init(&sh.q_empty, 1);
   mbar_init(&sh.s_full, 1);
-  mbar_init(&sh.s_free, kSoftThreads);
-  mbar_init(&sh.p_full, kSoftThreads);
+  mbar_init(&sh.s_free, kSoftWarps);
+  mbar_init(&sh.p_full, kSoftWarps);
   mbar_init(&sh.o_done, 1);
   for (int m = 0; m < 4; ++m) mbar_init(&sh.o_blk[m], 1);
   mbar_init(&sh.mma_done, 1);
@@ -545,7 +554,7 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, AttnShared& sh
     tmem_ld32(tmem + t_lane + kTmemS + col0, v);
     tmem_wait_ld();
     tc_fence_before();
-    mbar_arrive(&sh.s_free);
+    mbar_arrive_warp(&sh.s_free);
     const int j = cur.k * kTile + trow;
     bool valid = j < nkeys;
     if (kSparse && valid) {
@@ -673,7 +682,7 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, AttnShared& sh
     }
     fence_proxy_async_smem();
     tc_fence_before();
-    mbar_arrive(&sh.p_full);
+    mbar_arrive_warp(&sh.p_full);
     ++it;
     cur.next(p, cx.ts, cx.NR, cx.N, g, s);
   }

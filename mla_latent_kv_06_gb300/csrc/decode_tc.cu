@@ -303,13 +303,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_con
         mbar_init(&full_bar[u][a], 1);
         mbar_init(&empty_bar[u][a], 1);
       }
-    mbar_init(&q_full, kQuantIn ? kSoftThreads : 1);
+    mbar_init(&q_full, kQuantIn ? kSoftWarps : 1);
     mbar_init(&q_empty, 1);
     for (int u = 0; u < 2; ++u) {
       mbar_init(&s_full[u], 1);
-      mbar_init(&s_free[u], kSoftThreads);
+      mbar_init(&s_free[u], kSoftWarps);
     }
-    mbar_init(&p_full, kSoftThreads);
+    mbar_init(&p_full, kSoftWarps);
     mbar_init(&o_done, 1);
     for (int m = 0; m < 4; ++m) mbar_init(&o_blk[m], 1);
     mbar_init(&mma_done, 1);
@@ -592,7 +592,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_con
           }
           quantise_query_rows(p, (size_t)(cur.row * S + s) * kH, warp - 2, lane, sQ8, fh_sh[spc & 1]);
           fence_proxy_async_smem();
-          mbar_arrive(&q_full);
+          mbar_arrive_warp(&q_full);
         }
         if (it > 0 && !epilogue(it - 1)) {
           ok = false;
@@ -620,7 +620,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_con
       tmem_ld32(tmem + t_lane + kTmemS + 64 * u + col0, v);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&s_free[u]);
+      mbar_arrive_warp(&s_free[u]);
       const int j = cur.k * kTile + trow;
       const bool valid = j < nkeys;
       if (!valid) {
@@ -757,7 +757,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_con
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&p_full);
+      mbar_arrive_warp(&p_full);
       ++it;
       cur.next(p, ts, NR, N, g, s);
     }
