@@ -244,7 +244,7 @@ __device__ __forceinline__ int tile_keys(const AttnParams& p, int row, int s, in
 // and the key tile live in dynamic shared memory).
 struct AttnShared {
   uint64_t full_bar[kSlots], empty_bar[kSlots];
-  uint64_t q_full, q_empty, s_full, s_free, p_full, o_done, mma_done, o_blk[4];
+  uint64_t q_full, q_empty, s_full, s_free, p_full, mma_done, o_blk[4];
   uint32_t tmem_base;
   int abort_flag;
   __align__(16) float red_max[4][kH];
@@ -277,7 +277,6 @@ __device__ __forceinline__ void attn_init_barriers(AttnShared& sh) {
   mbar_init(&sh.s_full, 1);
   mbar_init(&sh.s_free, kSoftWarps);
   mbar_init(&sh.p_full, kSoftWarps);
-  mbar_init(&sh.o_done, 1);
   for (int m = 0; m < 4; ++m) mbar_init(&sh.o_blk[m], 1);
   mbar_init(&sh.mma_done, 1);
   sh.abort_flag = 0;
@@ -337,7 +336,9 @@ __device__ __forceinline__ void attn_producer(const AttnParams& p, AttnShared& s
     }
     const uint32_t par = (it & 1) ^ 1;
     for (int a = 0; a < kSlots && ok; ++a) {
-      ok = mbar_wait(&sh.empty_bar[a], par, abort, p.flags, p.wait_ns);
+      // latent atoms 2m and 2m + 1 are released together (empty_bar[2m]),
+      // the rope slot on its own
+      if (a == 8 || (a & 1) == 0) ok = mbar_wait(&sh.empty_bar[a], par, abort, p.flags, p.wait_ns);
       if (!ok) break;
       mbar_arrive_expect_tx(&sh.full_bar[a], kSlotBytes);
       const CUtensorMap* map = a < 8 ? &p.mL : &p.mR;
@@ -436,10 +437,7 @@ __device__ __forceinline__ void attn_mma(const AttnParams& p, AttnShared& sh, co
     if (lane == 0) {
       // latent atoms of the blocks another part owns: free once the score product retired
       for (int m = 0; m < 4; ++m)
-        if (m < mb0 || m >= mb1) {
-          mma_commit(&sh.empty_bar[2 * m]);
-          mma_commit(&sh.empty_bar[2 * m + 1]);
-        }
+        if (m < mb0 || m >= mb1) mma_commit(&sh.empty_bar[2 * m]);
       for (int m = mb0; m < mb1; ++m) {
         const uint64_t da = dO0 + (uint64_t)(2 * m * (kSlotBytes >> 4));
         const uint32_t dt = tmem + kTmemO + 64 * m;
@@ -451,12 +449,11 @@ __device__ __forceinline__ void attn_mma(const AttnParams& p, AttnShared& sh, co
           for (int kk = 0; kk < ksteps; ++kk)
             mma_bf16(dt, da + 128 * kk, dP0 + 128 * kk, idO, (kk > 0 || !first) ? 1u : 0u);
         }
-        mma_commit(&sh.empty_bar[2 * m]);
-        mma_commit(&sh.empty_bar[2 * m + 1]);
-        mma_commit(&sh.o_blk[m]);  // the epilogue may read this block while the next ones run
+        mma_commit(&sh.empty_bar[2 * m]);  // latent atoms 2m, 2m + 1
+        // a piece's last tile: the epilogue may read this block while the next ones run
+        if (c.last()) mma_commit(&sh.o_blk[m]);
       }
       mma_commit(&sh.empty_bar[8]);
-      mma_commit(&sh.o_done);
     }
     __syncwarp();
     ++it;
@@ -496,13 +493,16 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, AttnShared& sh
 #pragma unroll
   for (int i = 0; i < 32; ++i) lp[i] = 0.f;
 
-  // Partials of a finished piece: each 128-row block of O^T as soon as its
-  // part of the last value product (tile j) retired.
-  auto epilogue = [&](int j) -> bool {
+  // Partials of the CTA's piece number `pcs`: each 128-row block of O^T as
+  // soon as its part of the piece's last value product retired (o_blk[m]
+  // completes once per piece).
+  int pcs = 0;
+  auto epilogue = [&]() -> bool {
     float* op = p.o_part + (size_t)slot * kH * kDl;
+    const uint32_t par = (uint32_t)(pcs++ & 1);
 #pragma unroll 1
     for (int m = mb0; m < mb1; ++m) {
-      const bool fail = !mbar_wait(&sh.o_blk[m], j & 1, abort, p.flags, p.wait_ns);
+      const bool fail = !mbar_wait(&sh.o_blk[m], par, abort, p.flags, p.wait_ns);
       if (bar_red_or(1, kSoftThreads, fail)) return false;
       tc_fence_after();
       float w[32];
@@ -528,7 +528,7 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, AttnShared& sh
   while (ok && cur.live) {
     const bool first = cur.first();
     if (first) {
-      if (it > 0 && !epilogue(it - 1)) {
+      if (it > 0 && !epilogue()) {
         ok = false;
         break;
       }
@@ -654,15 +654,10 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, AttnShared& sh
       }
     }
     if (rescale) {  // (never on a piece's first tile)
-      // O^T is stable once the previous value product retired.  Without a
-      // rescale the softmax leaves O^T alone and needs no wait: the value
-      // product of this tile is queued behind the previous one anyway.
-      fail = !mbar_wait(&sh.o_done, (it - 1) & 1, abort, p.flags, p.wait_ns);
-      if (bar_red_or(2, kSoftThreads, fail)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
+      // O^T is stable here: the MMA thread committed s_full for this tile
+      // after it issued the previous value product, and a commit tracks every
+      // MMA that thread issued before it; this tile's value product waits for
+      // p_full.
 #pragma unroll 1
       for (int m = mb0; m < mb1; ++m) {
         float w[32];
@@ -686,7 +681,7 @@ __device__ __forceinline__ void attn_softmax(const AttnParams& p, AttnShared& sh
     ++it;
     cur.next(p, cx.ts, cx.NR, cx.N, g, s);
   }
-  if (ok && it > 0) epilogue(it - 1);
+  if (ok && it > 0) epilogue();
 }
 
 }  // namespace
