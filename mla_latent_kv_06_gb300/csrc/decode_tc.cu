@@ -447,7 +447,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_con
     };
     // Value product of tile j: O^T block m = latent atom m (MN-major, 32 keys =
     // 4 KB per step) x P^T (K-major codes in the tile's rope slot).
-    auto value = [&](int j, int ksteps, bool firstj) -> bool {
+    auto value = [&](int j, int ksteps, bool firstj, bool lastj) -> bool {
       if (!wait(&p_full, j & 1)) return false;
       tc_fence_after();
       if (lane == 0) {
@@ -467,7 +467,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_con
             for (int kk = 0; kk < ksteps; ++kk) mma_f8(dt, da + 256 * kk, db + 2 * kk, idO8, (kk > 0 || !firstj) ? 1u : 0u);
           }
           mma_commit(&empty_bar[u][m]);
-          mma_commit(&o_blk[m]);  // the epilogue may read this block while the next ones run
+          // a piece's last tile: the epilogue may read this block while the next ones run
+          if (lastj) mma_commit(&o_blk[m]);
         }
         mma_commit(&empty_bar[u][4]);
         mma_commit(&o_done);
@@ -475,7 +476,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_con
       __syncwarp();
       return true;
     };
-    bool pend = false, pend_first = false;
+    bool pend = false, pend_first = false, pend_last = false;
     int pend_it = 0, pend_ks = 0;
     while (ok && c.live) {
       const bool first = c.first();
@@ -513,15 +514,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_con
       }
       __syncwarp();
       // the previous tile's value product, queued behind this tile's scores
-      if (pend && !(ok = value(pend_it, pend_ks, pend_first))) break;
+      if (pend && !(ok = value(pend_it, pend_ks, pend_first, pend_last))) break;
       pend = true;
       pend_it = it;
       pend_ks = ksteps;
       pend_first = first;
+      pend_last = c.last();
       ++it;
       c.next(p, ts, NR, N, g, s);
     }
-    if (ok && pend) value(pend_it, pend_ks, pend_first);
+    if (ok && pend) value(pend_it, pend_ks, pend_first, pend_last);
     if (issued) {  // all MMAs retired before TMEM is released
       if (lane == 0) mma_commit(&mma_done);
       __syncwarp();
@@ -545,14 +547,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_con
 #pragma unroll
     for (int i = 0; i < 32; ++i) lp[i] = 0.f;
 
-    auto epilogue = [&](int j) -> bool {
+    // o_blk[m] completes once per piece, with the piece's last value product:
+    // the epilogue of piece pcs waits for phase pcs.  The next piece's cannot
+    // complete before this epilogue ends (its value products wait for P).
+    int pcs = 0;
+    auto epilogue = [&]() -> bool {
       float* op = p.o_part + (size_t)slot * kH * kDl;
-      // Tile j - 1's value product is known retired here (the previous
-      // piece's epilogue, a rescale or the last-tile wait below saw it), so
-      // tile j's is the one phase of o_blk that can be open.
+      const uint32_t par = (uint32_t)(pcs++ & 1);
 #pragma unroll 1
       for (int m = mb0; m < mb1; ++m) {
-        const bool fail = !mbar_wait(&o_blk[m], j & 1, abort, p.flags, p.wait_ns);
+        const bool fail = !mbar_wait(&o_blk[m], par, abort, p.flags, p.wait_ns);
         if (bar_red_or(1, kSoftThreads, fail)) return false;
         tc_fence_after();
         float w[32];
@@ -594,7 +598,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_con
           fence_proxy_async_smem();
           mbar_arrive_warp(&q_full);
         }
-        if (it > 0 && !epilogue(it - 1)) {
+        if (it > 0 && !epilogue()) {
           ok = false;
           break;
         }
@@ -744,24 +748,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_con
           tmem_wait_st();
         }
       }
-      if (!first && !rescale && cur.last()) {
-        // The piece's epilogue reads O^T once this tile's value product
-        // retires.  The previous tile's must be seen retired before this P
-        // lets this tile's start: otherwise both could complete unseen, and
-        // a parity wait cannot tell phase k of o_done or o_blk from k + 2.
-        fail = !mbar_wait(&o_done, (it - 1) & 1, abort, p.flags, p.wait_ns);
-        if (bar_red_or(2, kSoftThreads, fail)) {
-          ok = false;
-          break;
-        }
-      }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive_warp(&p_full);
       ++it;
       cur.next(p, ts, NR, N, g, s);
     }
-    if (ok && it > 0) epilogue(it - 1);
+    if (ok && it > 0) epilogue();
   }
   tc_fence_before();
   __syncthreads();
