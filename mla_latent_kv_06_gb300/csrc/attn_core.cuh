@@ -376,7 +376,10 @@ __device__ __forceinline__ void attn_producer(const AttnParams& p, AttnShared& s
 }
 
 // ------------------------------------------------------------ MMA issuer (warp 1; lane 0 issues)
-template <bool kSparse>
+// kStream: the CTA streams several tiles; the score product then runs from one
+// lane's unrolled loop (less per-atom overhead), else from a compact
+// warp-wide loop whose smaller code costs less in a launch that runs it once.
+template <bool kSparse, bool kStream>
 __device__ __forceinline__ void attn_mma(const AttnParams& p, AttnShared& sh, const AttnCtx& cx) {
   volatile int* abort = &sh.abort_flag;
   const int lane = threadIdx.x & 31;
@@ -412,18 +415,47 @@ __device__ __forceinline__ void attn_mma(const AttnParams& p, AttnShared& sh, co
     ok = ok && wait(&sh.s_free, (it & 1) ^ 1);
     if (!ok) break;
     tc_fence_after();
-    for (int a = 0; a < kSlots && ok; ++a) {
-      ok = wait(&sh.full_bar[a], it & 1);
-      if (!ok) break;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint64_t da = dS0 + (uint64_t)(a * (kSlotBytes >> 4));
-        const uint64_t db = dQ0 + (uint64_t)(a * (kQAtomBytes >> 4));
+    // The score product.
+    if constexpr (!kStream) {  // the whole warp waits for each atom, lane 0 issues
+      for (int a = 0; a < kSlots && ok; ++a) {
+        ok = wait(&sh.full_bar[a], it & 1);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint64_t da = dS0 + (uint64_t)(a * (kSlotBytes >> 4));
+          const uint64_t db = dQ0 + (uint64_t)(a * (kQAtomBytes >> 4));
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_bf16(tmem + kTmemS, da + 2 * kk, db + 2 * kk, idS, (a | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk) mma_bf16(tmem + kTmemS, da + 2 * kk, db + 2 * kk, idS, (a | kk) != 0 ? 1u : 0u);
+        }
+        __syncwarp();
+        issued = true;
       }
-      __syncwarp();
-      issued = true;
+    } else {
+      // Lane 0 alone waits for each atom and issues its MMAs (the other lanes
+      // wait at the warp sync), then shares the outcome.  The atom loop is
+      // unrolled; the descriptors advance atom by atom from a base the
+      // compiler cannot see through, so that it does not keep all nine atoms'
+      // descriptors live (in registers or spilled) across tiles.
+      int sok = 1;
+      if (lane == 0) {
+        uint64_t da = dS0, db = dQ0;
+        asm volatile("" : "+l"(da), "+l"(db));
+#pragma unroll
+        for (int a = 0; a < kSlots; ++a) {
+          if (!mbar_wait(&sh.full_bar[a], it & 1, abort, p.flags, p.wait_ns)) {
+            sok = 0;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) mma_bf16(tmem + kTmemS, da + 2 * kk, db + 2 * kk, idS, (a | kk) != 0 ? 1u : 0u);
+          da += kSlotBytes >> 4;
+          db += kQAtomBytes >> 4;
+          issued = true;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, sok, 0) != 0;
+      issued = __shfl_sync(0xffffffffu, issued ? 1 : 0, 0) != 0;
     }
     if (!ok) break;
     if (lane == 0) {

@@ -55,7 +55,7 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 // programmatic dependent launch behind the absorb kernel (only the query-block
 // loads wait for it; the key tiles stream in meanwhile).
 // ===========================================================================
-template <bool kSparse, bool kPaged = false>
+template <bool kSparse, bool kPaged = false, bool kStream = false>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       });
     __syncwarp();
   } else if (warp == 1) {
-    attn_mma<kSparse>(p, sh, cx);
+    attn_mma<kSparse, kStream>(p, sh, cx);
   } else {
     attn_softmax<kSparse>(p, sh, cx);
   }
@@ -271,7 +271,7 @@ __device__ __forceinline__ void quantise_query_rows(const AttnParams& p, size_t 
 // and rope values into the query atoms, in the layout a 128-byte-swizzled TMA
 // load of the quantised rows would give; the few-row path takes this form,
 // which saves the quantiser's launch and hand-over.
-template <bool kQuantIn>
+template <bool kQuantIn, bool kStream = false>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -490,22 +490,51 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn8_kernel(const __grid_con
       if (!ok) break;
       tc_fence_after();
       const uint64_t ub = (uint64_t)(u * (kTile8Bytes >> 4));
-      for (int a = 0; a < kAtoms8 && ok; ++a) {
-        ok = wait(&full_bar[u][a], (it >> 1) & 1);
-        if (!ok) break;
-        tc_fence_after();
-        if (lane == 0) {
-          // 32 bytes of K per instruction: 32 codes, or 16 bf16 for the rope atom
-          const uint64_t da = dS0 + ub + (uint64_t)(a * (kSlotBytes >> 4));
-          const uint64_t db = dQ0 + (uint64_t)(a * (kQAtomBytes >> 4));
+      if constexpr (!kStream) {  // the whole warp waits for each atom, lane 0 issues
+        for (int a = 0; a < kAtoms8 && ok; ++a) {
+          ok = wait(&full_bar[u][a], (it >> 1) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            // 32 bytes of K per instruction: 32 codes, or 16 bf16 for the rope atom
+            const uint64_t da = dS0 + ub + (uint64_t)(a * (kSlotBytes >> 4));
+            const uint64_t db = dQ0 + (uint64_t)(a * (kQAtomBytes >> 4));
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            if (a < 4) mma_f8(tmem + kTmemS + 64 * u, da + 2 * kk, db + 2 * kk, idS8, (a | kk) != 0 ? 1u : 0u);
-            else mma_bf16(tmem + kTmemS + 64 * u, da + 2 * kk, db + 2 * kk, idS, 1u);
+            for (int kk = 0; kk < 4; ++kk) {
+              if (a < 4) mma_f8(tmem + kTmemS + 64 * u, da + 2 * kk, db + 2 * kk, idS8, (a | kk) != 0 ? 1u : 0u);
+              else mma_bf16(tmem + kTmemS + 64 * u, da + 2 * kk, db + 2 * kk, idS, 1u);
+            }
+          }
+          __syncwarp();
+          issued = true;
+        }
+      } else {
+        // Streaming CTAs: lane 0 alone waits for each atom and issues its MMAs
+        // from an unrolled loop, then shares the outcome; the descriptors
+        // advance from a base the compiler cannot see through.
+        int sok = 1;
+        if (lane == 0) {
+          uint64_t da = dS0 + ub, db = dQ0;
+          asm volatile("" : "+l"(da), "+l"(db));
+#pragma unroll
+          for (int a = 0; a < kAtoms8; ++a) {
+            if (!mbar_wait(&full_bar[u][a], (it >> 1) & 1, abort, p.flags, p.wait_ns)) {
+              sok = 0;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              if (a < 4) mma_f8(tmem + kTmemS + 64 * u, da + 2 * kk, db + 2 * kk, idS8, (a | kk) != 0 ? 1u : 0u);
+              else mma_bf16(tmem + kTmemS + 64 * u, da + 2 * kk, db + 2 * kk, idS, 1u);
+            }
+            da += kSlotBytes >> 4;
+            db += kQAtomBytes >> 4;
+            issued = true;
           }
         }
-        __syncwarp();
-        issued = true;
+        ok = __shfl_sync(0xffffffffu, sok, 0) != 0;
+        issued = __shfl_sync(0xffffffffu, issued ? 1 : 0, 0) != 0;
       }
       if (!ok) break;
       if (lane == 0) {
@@ -1520,7 +1549,7 @@ cudaError_t set_smem_once(Kern kern, int bytes, std::atomic<unsigned long long>*
   return e;
 }
 
-std::atomic<unsigned long long> g_abs_attr[9] = {}, g_attn_attr[5] = {}, g_cmb_attr{0};
+std::atomic<unsigned long long> g_abs_attr[9] = {}, g_attn_attr[10] = {}, g_cmb_attr{0};
 
 Plan make_plan(int B, int S, int T_cap, int sparse_topk) {
   Plan pl{};
@@ -1746,12 +1775,18 @@ cudaError_t run(const DecodeArgs& a, void* ws, bool sparse, cudaStream_t st) {
   tp.flags = a.flags;
   tp.wait_ns = a.wait_limit_ns;
   tp.pages = sparse ? PageTable{} : a.pages;
+  // Streaming launches (one CTA per piece, at least two tiles a CTA by the
+  // T_cap bound) take the instantiation with the single-lane score loop.
+  const long long tiles_cap = (long long)B * ((a.T_cap + kTile - 1) / kTile);
+  const bool stream = !sparse && tp.qsplit == 1 && tiles_cap >= 2LL * pl.G;
   auto kern = sparse     ? attn_kernel<true>
-              : a.lat_fp8 ? (big ? attn8_kernel<false> : attn8_kernel<true>)
-              : paged     ? attn_kernel<false, true>
-                          : attn_kernel<false>;
+              : a.lat_fp8 ? (big ? (stream ? attn8_kernel<false, true> : attn8_kernel<false>)
+                                 : (stream ? attn8_kernel<true, true> : attn8_kernel<true>))
+              : paged     ? (stream ? attn_kernel<false, true, true> : attn_kernel<false, true>)
+                          : (stream ? attn_kernel<false, false, true> : attn_kernel<false>);
   const uint32_t attn_smem = a.lat_fp8 ? kAttn8DynSmem : kAttnDynSmem;
-  e = set_smem_once(kern, (int)attn_smem, &g_attn_attr[sparse ? 1 : a.lat_fp8 ? (big ? 2 : 4) : paged ? 3 : 0]);
+  const int attr_slot = (sparse ? 1 : a.lat_fp8 ? (big ? 2 : 4) : paged ? 3 : 0) + (stream ? 5 : 0);
+  e = set_smem_once(kern, (int)attn_smem, &g_attn_attr[attr_slot]);
   if (e != cudaSuccess) return e;
   const int nblk = pieces * tp.qsplit;
   kernel_mark(st, "attention");

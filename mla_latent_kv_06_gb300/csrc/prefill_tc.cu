@@ -79,13 +79,17 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
   unsigned char* sQ = smem + kOffQ;
   unsigned char* sK = smem + kOffK;
   unsigned char* sV = smem + kOffV;
-  // Single K and V buffers: a barrier completes once per tile (phase j for
-  // tile j); S/P is double-buffered (s_full/s_free[j & 1], phase j >> 1).  No
-  // wait can alias: the producer of phase j + 1 of any barrier depends on the
-  // waiter having passed phase j (the softmax waits for o_done only before a
-  // rescale, when the value product of the tile has not been issued yet).
-  __shared__ uint64_t q_full, q_rope, k_full, k_empty, v_full, v_empty, s_full[2], s_free[2], p_full, o_done,
-      mma_done;
+  // Single K and V buffers (k_full / v_full complete once per tile, phase j
+  // for tile j); S/P is double-buffered.  Two commits per tile signal the
+  // MMA side: s_full[j & 1] once S(j) = Q K(j)^T retired (the softmax reads
+  // S(j); the producer may reload K), pv_done[j & 1] once O += P(j) V(j)
+  // retired (the producer may reload V, the MMA warp may reuse the S/P
+  // buffer, a rescale or the final read may touch O); both are in phase
+  // j >> 1 for tile j.  No waiter can fall two phases behind: the MMA order
+  // is S(0), S(1), PV(0), S(2), PV(1), ..., so S(j) retired implies PV(j - 2)
+  // retired, and the next phase of each barrier needs the waiter's own next
+  // step (a K or V load, a P, or the MMA warp's issue).
+  __shared__ uint64_t q_full, q_rope, k_full, v_full, s_full[2], pv_done[2], p_full, mma_done;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   // [half][row]: the halves' maxima, after the loop their row sums.  A thread
@@ -102,15 +106,12 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
     mbar_init(&q_full, 1);
     mbar_init(&q_rope, kSoftThreads);
     mbar_init(&k_full, 1);
-    mbar_init(&k_empty, 1);
     mbar_init(&v_full, 1);
-    mbar_init(&v_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 1);  // the value product that read P from the buffer
+      mbar_init(&pv_done[i], 1);
     }
     mbar_init(&p_full, kSoftThreads);
-    mbar_init(&o_done, 1);
     mbar_init(&mma_done, 1);
     abort_flag = 0;
     fence_mbar_init();
@@ -139,7 +140,7 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
       // product of tile j - 1: the key half of the stream runs one tile ahead.
       int last_k = -1, last_v = -1;
       auto load_k = [&](int j) -> bool {
-        if (j > 0 && !mbar_wait(&k_empty, (j - 1) & 1, abort, p.flags, p.wait_ns)) return false;
+        if (j > 0 && !mbar_wait(&s_full[(j - 1) & 1], ((j - 1) >> 1) & 1, abort, p.flags, p.wait_ns)) return false;
         const int y = b * p.Tk + j * kKT;
         mbar_arrive_expect_tx(&k_full, kKBytes);
         for (int a = 0; a < 3; ++a) tma_load_2d(sK + a * kAtom, &p.mKV, h * kDkv + 64 * a, y, &k_full);
@@ -148,7 +149,7 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
         return true;
       };
       auto load_v = [&](int j) -> bool {
-        if (j > 0 && !mbar_wait(&v_empty, (j - 1) & 1, abort, p.flags, p.wait_ns)) return false;
+        if (j > 0 && !mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort, p.flags, p.wait_ns)) return false;
         const int y = b * p.Tk + j * kKT;
         mbar_arrive_expect_tx(&v_full, kVBytes);
         for (int a = 0; a < 4; ++a) tma_load_2d(sV + a * kAtom, &p.mKV, h * kDkv + kDn + 64 * a, y, &v_full);
@@ -185,14 +186,12 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
           const uint64_t db = smem_desc_sw128(v0 + kk * 2048, kAtom, 1024);
           mma_bf16_ts(tmem + kTmemO, pj + (kk >> 2) * 64 + (kk & 3) * 8, db, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&v_empty);
-        mma_commit(&o_done);
-        mma_commit(&s_free[j & 1]);
+        mma_commit(&pv_done[j & 1]);
         return true;
       };
       for (int j = 0; j < nkt && ok; ++j) {
         const int st = j & 1, n = j >> 1;
-        ok = mbar_wait(&s_free[st], (n & 1) ^ 1, abort, p.flags, p.wait_ns) &&
+        ok = mbar_wait(&pv_done[st], (n & 1) ^ 1, abort, p.flags, p.wait_ns) &&  // PV(j - 2) read P from it
              mbar_wait(&k_full, j & 1, abort, p.flags, p.wait_ns);
         if (!ok) break;
         tc_fence_after();
@@ -205,7 +204,6 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
             mma_bf16(tmem + kTmemS + kKT * st, da, db, idesc_s, (a | kk) != 0);
           }
         mma_commit(&s_full[st]);
-        mma_commit(&k_empty);
         issued = true;
         if (j > 0) ok = pv(j - 1);
       }
@@ -315,7 +313,7 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
       // (tcgen05.ld/st are warp-wide, so the warp decides together).
       fail = false;
       if (__any_sync(0xffffffffu, alpha != 1.f && j > 0)) {
-        fail = !__all_sync(0xffffffffu, mbar_wait(&o_done, (j - 1) & 1, abort, p.flags, p.wait_ns));
+        fail = !__all_sync(0xffffffffu, mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort, p.flags, p.wait_ns));
         if (!fail) {
           tc_fence_after();
 #pragma unroll 1
@@ -346,7 +344,7 @@ __global__ void __launch_bounds__(kPThreads, 1) flash_kernel(const __grid_consta
     // row sums: the two halves of a row
     red_row[half][m] = l;
     bool fail = !ok;
-    if (!fail && nkt > 0) fail = !mbar_wait(&o_done, (nkt - 1) & 1, abort, p.flags, p.wait_ns);
+    if (!fail && nkt > 0) fail = !mbar_wait(&pv_done[(nkt - 1) & 1], ((nkt - 1) >> 1) & 1, abort, p.flags, p.wait_ns);
     if (!bar_red_or(2, kSoftThreads, fail) && nkt > 0) {
       tc_fence_after();
       float* orow = p.out + (((size_t)b * p.S + s) * kH + h) * kDv;
