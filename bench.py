@@ -65,20 +65,20 @@ APPEND_RMS_EPS = 1e-6
 # built from.  An entry whose sources have changed since is stale, and the
 # roofline reports its traffic as null.
 NCU_TRAFFIC = {
-    ("glm_decode_t4096", "attention"): (4892416, "856d4e4a5bcb31a5"),
-    ("glm_decode_t16384", "attention"): (19048192, "856d4e4a5bcb31a5"),
-    ("glm_decode_t65536", "attention"): (77968384, "856d4e4a5bcb31a5"),
-    ("glm_batched_b32_s1", "attention"): (583041024, "856d4e4a5bcb31a5"),
-    ("glm_batched_b32_s6", "attention"): (622261248, "856d4e4a5bcb31a5"),
-    ("glm_paged_b32_s1", "attention"): (582642944, "856d4e4a5bcb31a5"),
+    ("glm_decode_t4096", "attention"): (4891904, "b5c89e90e54c811b"),
+    ("glm_decode_t16384", "attention"): (19051264, "b5c89e90e54c811b"),
+    ("glm_decode_t65536", "attention"): (77918720, "b5c89e90e54c811b"),
+    ("glm_batched_b32_s1", "attention"): (582998784, "b5c89e90e54c811b"),
+    ("glm_batched_b32_s6", "attention"): (622450176, "b5c89e90e54c811b"),
+    ("glm_paged_b32_s1", "attention"): (582960640, "b5c89e90e54c811b"),
     ("glm_dsa_t65536", "index_scores"): (139196928, "d8d0b28c3c50688c"),
-    ("glm_dsa_t65536_l4", "attention"): (9866496, "856d4e4a5bcb31a5"),
-    ("glm_prefill_s2048", "flash_attention"): (795747072, "4cd35ca72f3b5a88"),
+    ("glm_dsa_t65536_l4", "attention"): (9864448, "b5c89e90e54c811b"),
+    ("glm_prefill_s2048", "flash_attention"): (797446912, "f81080760d23a01a"),
     ("glm_append_b32_s6", "cache_append"): (243200, "cce2f582d5b0591c"),
     ("glm_append_b32_s6", "index_key_append"): (115968, "cce2f582d5b0591c"),
-    ("glm_batched_b32_s1_fp8", "attention"): (325122560, "856d4e4a5bcb31a5"),
-    ("glm_decode_t4096_fp8", "attention"): (2807552, "856d4e4a5bcb31a5"),
-    ("glm_decode_t65536_fp8", "attention"): (42189312, "856d4e4a5bcb31a5"),
+    ("glm_batched_b32_s1_fp8", "attention"): (325867520, "b5c89e90e54c811b"),
+    ("glm_decode_t4096_fp8", "attention"): (2937088, "b5c89e90e54c811b"),
+    ("glm_decode_t65536_fp8", "attention"): (42172416, "b5c89e90e54c811b"),
     ("glm_decode_oproj_t4096", "oproj_gemv"): (205005312, "1888d6993a2c0d56"),
     ("glm_dsa_t65536_l4_oproj", "oproj_gemv"): (204694528, "1888d6993a2c0d56"),
 }
