@@ -81,6 +81,21 @@ def test_decode_fp8(cuda_lib, T, S):
     _check_rows_against_model(got, x, T, S)
 
 
+@pytest.mark.parametrize("T,S", [([40000], 1), ([40000, 39001], 2)])
+def test_decode_fp8_streaming_few_rows(cuda_lib, T, S):
+    """Few query rows over long caches: every CTA runs two or more key tiles,
+    which the streaming form of the FP8 attention serves, with the query rows
+    quantised inside the kernel; ragged last tiles and a second sequence."""
+    x = _inputs(T, S, 900 + sum(T) + S)
+    out = cuda_lib.decode_fp8(x["q"].to(DEV), x["Lc8"].to(DEV), x["Rc"].to(DEV), x["T"].to(DEV), x["kv_b"].to(DEV),
+                              GLM, LAT_SCALE)
+    assert cuda_lib.device_status() == 0
+    got = to_np(out)
+    assert np.all(np.isfinite(got))
+    assert max_rel_err(got, _ref(x, T)) < U_E4M3
+    _check_rows_against_model(got, x, T, S)
+
+
 @pytest.mark.parametrize("lat_scale", [1.0 / 64, 0.3])
 def test_decode_fp8_scale_enters_linearly(cuda_lib, lat_scale):
     """Other cache scales: the same codes describe a cache lat_scale times the codes."""
